@@ -1,0 +1,333 @@
+/*
+ * Oracle for the state-cached causal short convolution.
+ *
+ * TEST INFRASTRUCTURE ONLY. Nothing on the product path may link, load or call
+ * this file: only the tests, the smoke check and the CPU-baseline leg of the
+ * benchmark use it. It shares no code, header or constant with the CUDA
+ * library; it is plain C loops, written from the definitions on the pages:
+ *
+ *   [Z]  "vllm.model_executor.models.zaya" (ZayaCCA: __init__, project,
+ *        _mix_with_state, _cca_state_shapes)
+ *   [G]  "vllm.model_executor.layers.mamba.ops.cpu.gdn_attention"
+ *        (_conv_buffer_view, _spec_aware_nonspec, _spec_forward,
+ *        cpu_gdn_attention_core)
+ *   [P]  "Qwen4ExpPLELayer" (__init__, _short_conv_dilated_dispatch,
+ *        _short_conv)
+ *
+ * Arithmetic: inputs are widened to fp32, every sum is accumulated in fp32 in
+ * the order bias, tap 0, tap 1, ... (no fused multiply-add: the file is built
+ * with -ffp-contract=off), the activation is applied in fp32 and the result is
+ * rounded to nearest-even into the storage type. State columns are copied as
+ * raw bits. The pages give fp32 accumulation through their bf16 torch modules;
+ * this file does the same, one element at a time, with no blocking or reuse.
+ *
+ * Storage types: dtype 0 = fp32, dtype 1 = bf16 (raw uint16 bits).
+ * Conv-state pools are [slot, channel, column] views given by three element
+ * strides (the canonical layout of [P] _short_conv and [G] _conv_buffer_view).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORC_F32 0
+#define ORC_BF16 1
+
+/* ---- storage conversions ------------------------------------------------ */
+
+static float orc_bf16_to_f32(uint16_t h) {
+  uint32_t u = (uint32_t)h << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return f;
+}
+
+/* Round-to-nearest-even fp32 -> bf16 by integer rounding of the upper half. */
+uint16_t orc_f32_to_bf16(float f) {
+  uint32_t u;
+  memcpy(&u, &f, sizeof u);
+  if ((u & 0x7fffffffu) > 0x7f800000u) return (uint16_t)((u >> 16) | 0x0040u);
+  u += 0x7fffu + ((u >> 16) & 1u);
+  return (uint16_t)(u >> 16);
+}
+
+static size_t orc_esize(int dtype) { return dtype == ORC_F32 ? 4 : 2; }
+
+static float orc_get(const void* p, int64_t i, int dtype) {
+  if (dtype == ORC_F32) return ((const float*)p)[i];
+  return orc_bf16_to_f32(((const uint16_t*)p)[i]);
+}
+
+static void orc_put(void* p, int64_t i, int dtype, float v) {
+  if (dtype == ORC_F32)
+    ((float*)p)[i] = v;
+  else
+    ((uint16_t*)p)[i] = orc_f32_to_bf16(v);
+}
+
+/* A raw element (bits), so that state copies are exact whatever the value. */
+typedef uint32_t orc_raw;
+
+static orc_raw orc_get_raw(const void* p, int64_t i, int dtype) {
+  if (dtype == ORC_F32) {
+    uint32_t u;
+    memcpy(&u, (const char*)p + i * 4, 4);
+    return u;
+  }
+  return ((const uint16_t*)p)[i];
+}
+
+static void orc_put_raw(void* p, int64_t i, int dtype, orc_raw r) {
+  if (dtype == ORC_F32)
+    memcpy((char*)p + i * 4, &r, 4);
+  else
+    ((uint16_t*)p)[i] = (uint16_t)r;
+}
+
+static float orc_raw_to_f32(orc_raw r, int dtype) {
+  if (dtype == ORC_F32) {
+    float f;
+    memcpy(&f, &r, 4);
+    return f;
+  }
+  return orc_bf16_to_f32((uint16_t)r);
+}
+
+/* SiLU in fp32: v * sigmoid(v) = v / (1 + exp(-v)) ([G] activation "silu",
+ * [P] self.activation = "silu"). */
+static float orc_act(float v, int act) {
+  if (act == 1) return v / (1.0f + expf(-v));
+  return v;
+}
+
+/* ---- depthwise causal conv over one extended window --------------------- */
+
+/*
+ * y[j] = act(bias + sum_{k=0}^{W-1} w[k] * xt[S + j - (W-1-k)*D]),  j in [0, L)
+ *
+ * xt holds S history elements followed by the L inputs of one channel. The
+ * tap orientation is PyTorch's cross-correlation with left padding: w[W-1]
+ * multiplies the current token ([G] _spec_forward: F.conv1d over
+ * cat([prior, x_seq]); [P] nn.Conv1d(padding=conv_state_len, dilation=d)).
+ */
+static void orc_depthwise_channel(const orc_raw* xt, int S, int L, const void* w,
+                                  int64_t w_off, const void* bias, int64_t c, int W,
+                                  int D, int act, int dtype, void* out, int64_t out_off,
+                                  int64_t out_rs) {
+  for (int j = 0; j < L; ++j) {
+    float acc = bias ? orc_get(bias, c, dtype) : 0.0f;
+    for (int k = 0; k < W; ++k) {
+      float wk = orc_get(w, w_off + k, dtype);
+      float xv = orc_raw_to_f32(xt[S + j - (W - 1 - k) * D], dtype);
+      acc = acc + wk * xv;
+    }
+    orc_put(out, out_off + (int64_t)j * out_rs, dtype, orc_act(acc, act));
+  }
+}
+
+/*
+ * Varlen prefill/decode with state ([G] _spec_aware_nonspec, the prefill
+ * branch; [P] ple_conv mode="prefill"/"decode"; [Z] _mix_with_state for the
+ * history rule).
+ *
+ * For sequence s: tokens x[cu[s] .. cu[s+1]), slot = state_idx[s],
+ * h = has_init[s] and slot >= 0. The extended input is the slot's columns
+ * [0, S) when h holds, else S zeros, followed by the tokens; S = (W-1)*D.
+ * Outputs follow orc_depthwise_channel. When slot >= 0, columns [0, S) of the
+ * slot become the last S elements of the extended input (a bit copy); other
+ * columns are untouched. A slot < 0 is a padding row: zero history, no write.
+ */
+int oracle_cconv_fwd_varlen(const void* x, int64_t x_rs, const void* w, const void* bias,
+                            void* pool, int64_t s_slot, int64_t s_chan, int64_t s_col,
+                            int32_t num_slots, int32_t cap, const int32_t* state_idx,
+                            const int32_t* cu_seqlens, const uint8_t* has_init,
+                            int32_t num_seqs, int32_t C, int32_t W, int32_t D, int32_t act,
+                            int32_t dtype, void* out, int64_t out_rs) {
+  const int S = (W - 1) * D;
+  if (S > cap) return -1;
+  for (int s = 0; s < num_seqs; ++s) {
+    const int64_t start = cu_seqlens[s];
+    const int L = cu_seqlens[s + 1] - cu_seqlens[s];
+    const int slot = state_idx[s];
+    if (L < 0 || slot >= num_slots) return -1;
+    const int h = (has_init ? has_init[s] != 0 : 1) && slot >= 0;
+    orc_raw* xt = (orc_raw*)malloc(sizeof(orc_raw) * (size_t)(S + L + 1));
+    for (int64_t c = 0; c < C; ++c) {
+      for (int i = 0; i < S; ++i)
+        xt[i] = h ? orc_get_raw(pool, slot * s_slot + c * s_chan + i * s_col, dtype) : 0u;
+      for (int i = 0; i < L; ++i) xt[S + i] = orc_get_raw(x, (start + i) * x_rs + c, dtype);
+      orc_depthwise_channel(xt, S, L, w, c * W, bias, c, W, D, act, dtype, out,
+                            start * out_rs + c, out_rs);
+      if (slot >= 0)
+        for (int i = 0; i < S; ++i)
+          orc_put_raw(pool, slot * s_slot + c * s_chan + i * s_col, dtype, xt[L + i]);
+    }
+    free(xt);
+  }
+  return 0;
+}
+
+/*
+ * Decode (n_spec == 0) and speculative decode (n_spec > 0) with q = 1 + n_spec
+ * tokens per request, request s owning rows [s*q, s*q + q) of x and out.
+ *
+ * n_spec == 0 ([G] _spec_aware_nonspec decode branch: only the first S columns
+ * hold the state): identical to oracle_cconv_fwd_varlen with L = 1.
+ *
+ * n_spec > 0 ([G] _spec_forward, the per-request rolling-buffer loop; [P]
+ * ple_conv mode="spec"): B = the slot's cap columns (zeros when !h),
+ * off = num_accepted[s] - 1, prior = B[off, off + S), outputs over
+ * [prior, x_seq], then the slot becomes B[off+1, off+1+cap-q] ++ x_seq
+ * (all of B is read before any column is written).
+ */
+int oracle_cconv_update(const void* x, int64_t x_rs, void* pool, int64_t s_slot,
+                        int64_t s_chan, int64_t s_col, int32_t num_slots, int32_t cap,
+                        const void* w, const void* bias, const int32_t* state_idx,
+                        int32_t num_seqs, int32_t n_spec, const int32_t* num_accepted,
+                        const uint8_t* has_init, int32_t C, int32_t W, int32_t D, int32_t act,
+                        int32_t dtype, void* out, int64_t out_rs) {
+  const int S = (W - 1) * D;
+  const int q = 1 + n_spec;
+  if (S + n_spec > cap) return -1;
+  orc_raw* Bc = (orc_raw*)malloc(sizeof(orc_raw) * (size_t)(cap + 1));
+  orc_raw* xt = (orc_raw*)malloc(sizeof(orc_raw) * (size_t)(S + q + 1));
+  for (int s = 0; s < num_seqs; ++s) {
+    const int slot = state_idx[s];
+    if (slot >= num_slots) {
+      free(Bc);
+      free(xt);
+      return -1;
+    }
+    const int h = (has_init ? has_init[s] != 0 : 1) && slot >= 0;
+    const int off = n_spec > 0 ? num_accepted[s] - 1 : 0;
+    if (n_spec > 0 && (off < 0 || off >= q)) {
+      free(Bc);
+      free(xt);
+      return -1;
+    }
+    const int64_t row0 = (int64_t)s * q;
+    for (int64_t c = 0; c < C; ++c) {
+      const int ncols = n_spec > 0 ? cap : S;
+      for (int i = 0; i < ncols; ++i)
+        Bc[i] = h ? orc_get_raw(pool, slot * s_slot + c * s_chan + i * s_col, dtype) : 0u;
+      for (int i = 0; i < S; ++i) xt[i] = Bc[off + i];
+      for (int i = 0; i < q; ++i) xt[S + i] = orc_get_raw(x, (row0 + i) * x_rs + c, dtype);
+      orc_depthwise_channel(xt, S, q, w, c * W, bias, c, W, D, act, dtype, out,
+                            row0 * out_rs + c, out_rs);
+      if (slot < 0) continue;
+      if (n_spec == 0) {
+        for (int i = 0; i < S; ++i)
+          orc_put_raw(pool, slot * s_slot + c * s_chan + i * s_col, dtype, xt[1 + i]);
+      } else {
+        for (int i = 0; i < cap; ++i) {
+          orc_raw v = (i < cap - q) ? Bc[off + 1 + i] : xt[S + (i - (cap - q))];
+          orc_put_raw(pool, slot * s_slot + c * s_chan + i * s_col, dtype, v);
+        }
+      }
+    }
+  }
+  free(Bc);
+  free(xt);
+  return 0;
+}
+
+/*
+ * Zaya CCA q/k conv with state and the delayed half of v ([Z] ZayaCCA.__init__,
+ * _conv, project, _mix_with_state, _cca_state_shapes).
+ *
+ * Per request s (tokens x[start, start+L), slot, h as above), with history
+ * n = T0 + T1 - 2 and group size gs = Cqk / G:
+ *   xt[c]   = (h ? conv_state[slot][c][0..n) : zeros) ++ qk[start .. start+L)[c]
+ *   u[c][p] = round(b_dw[c] + sum_k w_dw[c][k] * xt[c][n + p - (T0-1-k)]),
+ *             p in [-(T1-1), L)   (the depthwise nn.Conv1d, bias on; its output
+ *             is stored in the module dtype before the grouped conv reads it)
+ *   v[o][j] = round(b_gr[o] + sum_{i<gs} sum_{k<T1}
+ *                   w_gr[o][i][k] * u[g*gs + i][j - (T1-1-k)]),  g = o / gs
+ *   out_delayed_prev[start]     = h ? delayed_state[slot] : delayed_init
+ *   out_delayed_prev[start + j] = delayed[start + j - 1]       (j >= 1)
+ *   conv_state[slot][c][i]      = xt[c][L + i]                 (i < n)
+ *   delayed_state[slot]         = L > 0 ? delayed[start + L - 1]
+ *                                       : (h ? delayed_state[slot] : delayed_init)
+ * A slot < 0 is a padding row: zero history, initial delayed value, no write.
+ */
+int oracle_cca_qk_conv(const void* qk, int64_t qk_rs, const void* w_dw, const void* b_dw,
+                       const void* w_gr, const void* b_gr, int32_t G, int32_t T0, int32_t T1,
+                       const void* delayed, int64_t delayed_rs, const void* delayed_init,
+                       int32_t Dv, void* pool, int64_t s_slot, int64_t s_chan, int64_t s_col,
+                       int32_t num_slots, int32_t cap, void* delayed_state,
+                       int64_t dstate_rs, const int32_t* state_idx,
+                       const int32_t* cu_seqlens, const uint8_t* has_init, int32_t num_seqs,
+                       int32_t Cqk, int32_t dtype, void* out_qk, int64_t out_rs,
+                       void* out_dprev, int64_t dprev_rs) {
+  const int n = T0 + T1 - 2;
+  if (G <= 0 || Cqk % G != 0 || n > cap) return -1;
+  const int gs = Cqk / G;
+  for (int s = 0; s < num_seqs; ++s) {
+    const int64_t start = cu_seqlens[s];
+    const int L = cu_seqlens[s + 1] - cu_seqlens[s];
+    const int slot = state_idx[s];
+    if (L < 0 || slot >= num_slots) return -1;
+    const int h = (has_init ? has_init[s] != 0 : 1) && slot >= 0;
+    const int nu = (T1 - 1) + L; /* u positions -(T1-1) .. L-1 */
+    orc_raw* xt = (orc_raw*)malloc(sizeof(orc_raw) * (size_t)Cqk * (size_t)(n + L + 1));
+    float* u = (float*)malloc(sizeof(float) * (size_t)Cqk * (size_t)(nu + 1));
+    for (int64_t c = 0; c < Cqk; ++c) {
+      orc_raw* xc = xt + c * (n + L);
+      for (int i = 0; i < n; ++i)
+        xc[i] = h ? orc_get_raw(pool, slot * s_slot + c * s_chan + i * s_col, dtype) : 0u;
+      for (int i = 0; i < L; ++i) xc[n + i] = orc_get_raw(qk, (start + i) * qk_rs + c, dtype);
+      for (int m = 0; m < nu; ++m) {
+        const int p = m - (T1 - 1);
+        float acc = b_dw ? orc_get(b_dw, c, dtype) : 0.0f;
+        for (int k = 0; k < T0; ++k)
+          acc = acc + orc_get(w_dw, c * T0 + k, dtype) *
+                          orc_raw_to_f32(xc[n + p - (T0 - 1 - k)], dtype);
+        /* round to the storage type, as the chained modules store it */
+        float r;
+        if (dtype == ORC_F32)
+          r = acc;
+        else
+          r = orc_bf16_to_f32(orc_f32_to_bf16(acc));
+        u[c * nu + m] = r;
+      }
+    }
+    for (int64_t o = 0; o < Cqk; ++o) {
+      const int64_t g = o / gs;
+      for (int j = 0; j < L; ++j) {
+        float acc = b_gr ? orc_get(b_gr, o, dtype) : 0.0f;
+        for (int i = 0; i < gs; ++i)
+          for (int k = 0; k < T1; ++k) {
+            const int m = (T1 - 1) + j - (T1 - 1 - k);
+            acc = acc + orc_get(w_gr, (o * gs + i) * T1 + k, dtype) * u[(g * gs + i) * nu + m];
+          }
+        orc_put(out_qk, (start + j) * out_rs + o, dtype, acc);
+      }
+    }
+    for (int64_t c = 0; c < Dv; ++c) {
+      orc_raw first = h ? orc_get_raw(delayed_state, slot * dstate_rs + c, dtype)
+                        : orc_get_raw(delayed_init, c, dtype);
+      if (L > 0) orc_put_raw(out_dprev, start * dprev_rs + c, dtype, first);
+      for (int j = 1; j < L; ++j)
+        orc_put_raw(out_dprev, (start + j) * dprev_rs + c, dtype,
+                    orc_get_raw(delayed, (start + j - 1) * delayed_rs + c, dtype));
+      if (slot >= 0) {
+        orc_raw last = L > 0 ? orc_get_raw(delayed, (start + L - 1) * delayed_rs + c, dtype)
+                             : first;
+        orc_put_raw(delayed_state, slot * dstate_rs + c, dtype, last);
+      }
+    }
+    if (slot >= 0)
+      for (int64_t c = 0; c < Cqk; ++c)
+        for (int i = 0; i < n; ++i)
+          orc_put_raw(pool, slot * s_slot + c * s_chan + i * s_col, dtype,
+                      xt[c * (n + L) + L + i]);
+    free(xt);
+    free(u);
+  }
+  return 0;
+}
+
+/* Exposed for the tests of the conversion itself. */
+float oracle_bf16_to_f32(uint16_t h) { return orc_bf16_to_f32(h); }
+uint16_t oracle_f32_to_bf16(float f) { return orc_f32_to_bf16(f); }
+size_t oracle_esize(int dtype) { return orc_esize(dtype); }
