@@ -1,0 +1,222 @@
+/*
+ * cconv.h -- C ABI of libcconv.so: the state-cached causal short convolution
+ * on GB300 (sm_103a).
+ *
+ * The operation is the causal conv1d that hybrid LLM layers run over a
+ * continuously batched, packed varlen token stream, with each request's last
+ * (width-1)*dilation inputs kept in a slot of a conv-state pool:
+ *   - the depthwise conv before the gated-delta-rule core
+ *     (page "vllm.model_executor.layers.mamba.ops.cpu.gdn_attention",
+ *     _spec_aware_nonspec and _spec_forward);
+ *   - the dilated depthwise PLE conv with speculative decode
+ *     (page "Qwen4ExpPLELayer", __init__ conv1d / conv_state_len and
+ *     _short_conv_dilated_dispatch);
+ *   - Zaya CCA's two-stage q/k conv and the one-token-delayed half of v
+ *     (page "vllm.model_executor.models.zaya", ZayaCCA.__init__ and
+ *     _mix_with_state).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Memory.   Every pointer argument is DEVICE memory owned by the caller; the
+ *           library keeps no pointer after a call returns and allocates no
+ *           memory. Tensors are row-major; a "row stride" is in elements.
+ * Types.    dtype CCONV_DTYPE_F32 or CCONV_DTYPE_BF16 names the storage type
+ *           of activations, weights, biases, outputs and state pools of one
+ *           call (they share it). Arithmetic accumulates in fp32; outputs are
+ *           rounded to nearest-even into the storage type.
+ * Tap order. PyTorch cross-correlation with left history: weight column
+ *           width-1 multiplies the current token, column k the input
+ *           (width-1-k)*dilation tokens earlier.
+ * Pools.    A conv-state pool is passed as a [slot, channel, column] view
+ *           (cconv_pool_t: base pointer plus three element strides), so both
+ *           cache layouts of the pages work: channel-first [slots, C, cols]
+ *           and column-first [slots, cols, C] (the PLE page reduces both to
+ *           one [slot, channel, window] view before its conv). The
+ *           fast paths are the dense channel-first view (s_col == 1,
+ *           s_chan == cap) and the column-first view (s_chan == 1); any other
+ *           strides use per-element accesses.
+ * State.    Non-speculative calls keep the state in columns [0, S) of a slot,
+ *           S = (width-1)*dilation, as the GDN page's non-speculative path
+ *           does on a buffer widened for speculation; columns >= S are left
+ *           as they are.
+ *           state_idx[s] < 0 marks a padding row: it reads a zero history and
+ *           writes nothing. Non-negative entries must be distinct within one
+ *           call (two requests on one slot race).
+ * Streams.  Every call only enqueues work on `stream` and returns; it never
+ *           synchronises with the host (as the Zaya page's state path is
+ *           written to avoid). Each call writes only its outputs and the pool slots
+ *           named by state_idx.
+ * Status.   CCONV_OK (0); CCONV_ERR_INVALID (-1: a null required pointer, a
+ *           size or stride out of range, a misaligned pointer); CCONV_ERR_
+ *           UNSUPPORTED (-2: a legal combination this build has no kernel
+ *           for); CCONV_ERR_LAUNCH (-3: the CUDA launch failed; the CUDA error
+ *           is left to cudaGetLastError by the caller). Nothing is enqueued
+ *           when a call returns non-zero.
+ * Device-detected bad data. If dev_err is not NULL, the kernels OR bits into
+ *           *dev_err (CCONV_DERR_*) for bad index data that only the device
+ *           sees -- a state index >= num_slots, a cu_seqlens entry that is
+ *           negative, decreasing or beyond num_tokens, a num_accepted outside
+ *           [1, 1+n_spec] -- and skip the affected request. They never trap.
+ *           Outputs of skipped requests are left untouched.
+ */
+#ifndef CCONV_H
+#define CCONV_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st* cconv_stream_t;
+
+enum {
+  CCONV_OK = 0,
+  CCONV_ERR_INVALID = -1,
+  CCONV_ERR_UNSUPPORTED = -2,
+  CCONV_ERR_LAUNCH = -3
+};
+
+enum { CCONV_DTYPE_F32 = 0, CCONV_DTYPE_BF16 = 1 };
+enum { CCONV_ACT_NONE = 0, CCONV_ACT_SILU = 1 };
+
+/* Bits OR-ed into *dev_err. */
+enum {
+  CCONV_DERR_SLOT_RANGE = 1,   /* state_idx[s] >= num_slots            */
+  CCONV_DERR_CU_SEQLENS = 2,   /* cu_seqlens negative/decreasing/> T   */
+  CCONV_DERR_NUM_ACCEPTED = 4, /* num_accepted[s] outside [1, 1+n_spec] */
+  CCONV_DERR_TIMEOUT = 8       /* a bounded on-chip wait ran out; the call's
+                                  outputs are incomplete                 */
+};
+
+/* [slot, channel, column] view of a conv-state pool (element strides). */
+typedef struct cconv_pool {
+  void* p;           /* device address of element [0][0][0] of the view */
+  int64_t s_slot;    /* element stride between slots                    */
+  int64_t s_chan;    /* element stride between channels                 */
+  int64_t s_col;     /* element stride between columns                  */
+  int32_t num_slots; /* slots in the pool                               */
+  int32_t cap;       /* columns in the view                             */
+} cconv_pool_t;
+
+/*
+ * cconv_fwd_varlen -- causal depthwise conv over a packed varlen batch,
+ * reading and writing each sequence's state (prefill, and decodes passed as
+ * one-token sequences).
+ *
+ * Defined by: "gdn_attention" _spec_aware_nonspec (the prefill conv over
+ * x.transpose(0,1) with query_start_loc, cache_indices and
+ * has_initial_state; a decode is a one-token request whose history is
+ * always its slot), the
+ * "Qwen4ExpPLELayer" conv1d (groups = channels, dilation = ngram_size, no
+ * bias, state_len = (kernel-1)*dilation) and the Zaya page's history rule
+ * (the slot ends up holding the final n elements of history followed by the
+ * request's tokens).
+ *
+ * For sequence s: tokens x[cu_seqlens[s] .. cu_seqlens[s+1]), S = (width-1)*
+ * dilation, history = columns [0,S) of slot state_idx[s] if has_init[s]
+ * (NULL: all true) else zeros;
+ *   out[t, c] = act(bias[c] + sum_k w[c, k] * xe[t - (width-1-k)*dilation, c])
+ * over xe = history ++ tokens; then columns [0,S) of the slot become the last
+ * S elements of xe.
+ *
+ *   x            [num_tokens, C], row stride x_row_stride (>= C, multiple of
+ *                the 16-byte vector: 4 fp32 / 8 bf16 elements); 16-byte aligned
+ *   w            [C, width] contiguous; bias [C] or NULL
+ *   conv_states  pool view, cap >= S
+ *   state_idx    int32 [num_seqs]; cu_seqlens int32 [num_seqs+1] (cu[0] >= 0,
+ *                non-decreasing, cu[num_seqs] <= num_tokens)
+ *   has_init     uint8 [num_seqs] or NULL
+ *   C            multiple of 8 (bf16) or 4 (fp32)
+ *   width        2..4;  dilation 1..4;  act CCONV_ACT_*
+ *   out          [num_tokens, C], row stride out_row_stride; must not alias x.
+ *                Rows outside every sequence are not written.
+ */
+int cconv_fwd_varlen(const void* x, int64_t x_row_stride, const void* w, const void* bias,
+                     cconv_pool_t conv_states, const int32_t* state_idx,
+                     const int32_t* cu_seqlens, const uint8_t* has_init, int32_t num_seqs,
+                     int32_t num_tokens, int32_t C, int32_t width, int32_t dilation,
+                     int32_t act, int32_t dtype, void* out, int64_t out_row_stride,
+                     int32_t* dev_err, cconv_stream_t stream);
+
+/*
+ * cconv_update -- decode (n_spec == 0: one token per request) or speculative
+ * decode (n_spec > 0: q = 1 + n_spec tokens per request) against the pool.
+ *
+ * Defined by: "gdn_attention" _spec_aware_nonspec decode branch (update on
+ * the first width-1 columns) and _spec_forward's per-request rolling buffer
+ * (the window restarts after the last accepted draft token and the new draft
+ * tokens go to the end, the buffer width unchanged), with the PLE page's
+ * dilation and its capacity check (cap >= conv_state_len + num_spec).
+ *
+ * Request s owns rows [s*q, s*q+q) of x and out.
+ *   n_spec == 0: exactly cconv_fwd_varlen with one-token sequences.
+ *   n_spec  > 0: B = the slot's cap columns (zeros if !has_init[s]),
+ *                off = num_accepted[s] - 1, prior = B[off, off+S);
+ *                out over prior ++ tokens as above; then the slot becomes
+ *                B[off+1, off+1+cap-q) ++ tokens.
+ *
+ *   x, out       [num_seqs*q, C] with row strides as for cconv_fwd_varlen
+ *   num_accepted int32 [num_seqs], required when n_spec > 0, else ignored
+ *   has_init     uint8 [num_seqs] or NULL (all true)
+ *   n_spec       0..7;  cap >= S + n_spec;  width 2..4; dilation 1..4
+ */
+int cconv_update(const void* x, int64_t x_row_stride, cconv_pool_t conv_states,
+                 const void* w, const void* bias, const int32_t* state_idx,
+                 int32_t num_seqs, int32_t n_spec, const int32_t* num_accepted,
+                 const uint8_t* has_init, int32_t C, int32_t width, int32_t dilation,
+                 int32_t act, int32_t dtype, void* out, int64_t out_row_stride,
+                 int32_t* dev_err, cconv_stream_t stream);
+
+/*
+ * cca_qk_conv -- Zaya CCA: depthwise conv (width t0, bias) then grouped conv
+ * (width t1, `groups` groups, bias) of the raw q/k projections, with each
+ * request's raw history of n = t0 + t1 - 2 tokens in the pool, plus the
+ * one-token delay of the v_proj_delayed half of v.
+ *
+ * Defined by: "vllm.model_executor.models.zaya" ZayaCCA.__init__
+ * (conv_qk_depthwise, conv_qk_grouped, history_len), _conv, project and
+ * _mix_with_state, and _cca_state_shapes (state = (heads*head_dim, history)
+ * and (kv_heads*head_dim/2,)).
+ *
+ * Per request (tokens [cu[s], cu[s+1]), slot, has_init as above):
+ *   xe       = (has_init ? conv_state[slot][:, 0:n] : 0) ++ tokens
+ *   u[p]     = bf16(b_dw + sum_k w_dw[:, k] * xe[p-(t0-1-k)])  (depthwise output,
+ *              stored in the module dtype as the chained modules do)
+ *   out_qk[t, o] = bf16(b_gr[o] + sum_{i,k} w_gr[o, i, k] * u[t-(t1-1-k), g*gs+i])
+ *   out_delayed_prev[first] = has_init ? delayed_state[slot] : delayed_init,
+ *   out_delayed_prev[t]     = delayed[t-1] for the other tokens;
+ *   conv_state[slot][:, 0:n] = last n of xe; delayed_state[slot] = delayed[last]
+ *   (unchanged if the request is empty and has_init, delayed_init if empty
+ *   and !has_init).
+ *
+ *   qk, out_qk        [num_tokens, Cqk] with row strides; Cqk = groups * 128
+ *   w_dw [Cqk, t0], b_dw [Cqk] or NULL; w_gr [Cqk, 128, t1], b_gr [Cqk] or NULL
+ *   delayed, out_delayed_prev [num_tokens, Dv] with row strides; delayed_init [Dv]
+ *   conv_state        pool view with cap >= n; delayed_state [num_slots, Dv]
+ *                     with row stride delayed_state_row_stride
+ *   t0 1..4, t1 1..2, dtype CCONV_DTYPE_BF16 (fp32 returns -2), Dv % 8 == 0
+ */
+int cca_qk_conv(const void* qk, int64_t qk_row_stride, const void* w_dw, const void* b_dw,
+                const void* w_gr, const void* b_gr, int32_t groups, int32_t t0, int32_t t1,
+                const void* delayed, int64_t delayed_row_stride, const void* delayed_init,
+                int32_t Dv, cconv_pool_t conv_state, void* delayed_state,
+                int64_t delayed_state_row_stride, const int32_t* state_idx,
+                const int32_t* cu_seqlens, const uint8_t* has_init, int32_t num_seqs,
+                int32_t num_tokens, int32_t Cqk, int32_t dtype, void* out_qk,
+                int64_t out_qk_row_stride, void* out_delayed_prev,
+                int64_t out_delayed_prev_row_stride, int32_t* dev_err,
+                cconv_stream_t stream);
+
+/* Static English text for a status code. */
+const char* cconv_status_string(int status);
+
+/* ABI version of this header (increments on any signature change). */
+int cconv_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CCONV_H */

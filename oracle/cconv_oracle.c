@@ -171,8 +171,9 @@ int oracle_cconv_fwd_varlen(const void* x, int64_t x_rs, const void* w, const vo
  * Decode (n_spec == 0) and speculative decode (n_spec > 0) with q = 1 + n_spec
  * tokens per request, request s owning rows [s*q, s*q + q) of x and out.
  *
- * n_spec == 0 ([G] _spec_aware_nonspec decode branch: only the first S columns
- * hold the state): identical to oracle_cconv_fwd_varlen with L = 1.
+ * n_spec == 0 ([G] _spec_aware_nonspec decode branch, which updates columns
+ * [0, S) of a possibly wider buffer): identical to oracle_cconv_fwd_varlen
+ * with L = 1.
  *
  * n_spec > 0 ([G] _spec_forward, the per-request rolling-buffer loop; [P]
  * ple_conv mode="spec"): B = the slot's cap columns (zeros when !h),

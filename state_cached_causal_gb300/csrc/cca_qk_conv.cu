@@ -1,0 +1,849 @@
+// Zaya CCA: depthwise conv -> grouped conv of the raw q/k projections with a
+// per-request history in the conv-state pool, plus the one-token delay of the
+// v_proj_delayed half of v.
+//
+// Page: "vllm.model_executor.models.zaya" -- ZayaCCA.__init__
+// (conv_qk_depthwise: groups = channels, width cca_time0, bias; conv_qk_grouped:
+// groups = heads, width cca_time1, bias; history_len = time0 + time1 - 2),
+// _mix_with_state (the history rule, the delayed shift and both state
+// writes) and _cca_state_shapes.
+//
+// GB300 design. The grouped stage is a dense per-group contraction
+// (K = t1 * 128 = 256, N = 128), so it runs on the 5th-generation tensor
+// cores: tcgen05.mma (M = 128 tokens, N = 128 output channels, bf16 in, fp32
+// accumulate in TMEM). One persistent CTA per SM walks a contiguous range of
+// work units (group g, token tile) with warp-specialised roles:
+//   warp 0      scheduler: tile metadata (row -> sequence, history flags,
+//               owned requests) into a 4-deep ring, and the TMA load of the
+//               tile's x rows (plus the history halo) into a 2-deep ring;
+//   warp 1      TMEM allocation and the single MMA-issuing thread;
+//   warps 2-5   epilogue: tcgen05.ld of the accumulator, bias, bf16 round,
+//               store; the delayed-v shift and delayed-state update;
+//   warps 6-13  producers: the depthwise stage for both taps (u at t-1 and t)
+//               straight into the two A operands in shared memory, the group's
+//               weights into the B operand, and the raw-history state writes.
+// Token tiles hold at most 128 rows and never split the first n tokens of a
+// request (the only tokens that read its history), so the tile that reads a
+// request's state is also the only one that writes it: one launch, no race,
+// no host sync. Every wait is bounded; a timeout sets an error bit and the
+// kernel drains and exits.
+#include <cuda.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "common.cuh"
+
+namespace cca {
+
+using cconv::Pool;
+
+constexpr int kGS = 128;          // channels per group (= head_dim)
+constexpr int kRows = 128;        // MMA M: rows (tokens) per tile
+constexpr int kMaxN = 4;          // history columns supported (t0 + t1 - 2)
+constexpr int kXStages = 2;
+constexpr int kMetaStages = 4;
+constexpr int kProdWarps = 8;
+constexpr int kEpiWarps = 4;
+constexpr int kWarpSched = 0, kWarpMma = 1, kWarpEpi0 = 2, kWarpProd0 = 2 + kEpiWarps;
+constexpr int kWarps = kWarpProd0 + kProdWarps;
+constexpr int kThreads = kWarps * 32;
+constexpr int kXRowBytes = kGS * 2;                    // one tile row of a group: 256 B
+constexpr int kXBoxRows = kRows + kMaxN;               // rows per x stage
+constexpr int kXStageBytes = kXBoxRows * kXRowBytes;   // 33792 B
+constexpr int kLboA = kRows * 16 + 16;                 // padded k-chunk stride of A
+constexpr int kTapA = (kGS / 8) * kLboA;               // one tap of A: 33024 B
+constexpr int kLboB = kGS * 16;                        // k-chunk stride of B: 2048 B
+constexpr int kTapB = (kGS / 8) * kLboB;               // one tap of B: 32768 B
+constexpr int kAccCols = 128;                          // fp32 accumulator columns
+constexpr int kTmemCols = 2 * kAccCols;
+constexpr long long kWaitCycles = 2000000000LL;        // ~1 s at GB300 clocks
+constexpr int kDerrTimeout = CCONV_DERR_TIMEOUT;
+
+struct Meta {
+  int lo, len, g, own_lo, own_hi, pad0, pad1, pad2;
+  int rowj[kRows];      // position of the row in its request, -1 outside every request
+  int rowslot[kRows];   // slot whose history the row reads, -1 for a zero history
+};
+
+struct Args {
+  const char* qk;
+  int64_t qk_rs;
+  const char* w_dw;
+  const char* b_dw;
+  const char* w_gr;
+  const char* b_gr;
+  const char* delayed;
+  int64_t delayed_rs;
+  const char* delayed_init;
+  int32_t Dv;
+  Pool pool;
+  char* dstate;
+  int64_t dstate_rs;
+  const int32_t* state_idx;
+  const int32_t* cu;
+  const uint8_t* has_init;
+  int32_t B, T, Cqk, G, n;
+  int32_t num_tiles, tile_pitch, units, units_per_cta;
+  char* out;
+  int64_t out_rs;
+  char* dprev;
+  int64_t dprev_rs;
+  int32_t* dev_err;
+};
+
+// ---- PTX wrappers -----------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint64_t* b, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(b)), "r"(count)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* b) {
+  asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(
+                   smem_u32(b))
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_tx(uint64_t* b, uint32_t bytes) {
+  asm volatile(
+      "{\n\t.reg .b64 st;\n\tmbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(
+          smem_u32(b)),
+      "r"(bytes)
+      : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint64_t* b, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(b)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                         uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
+      "%28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+        "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+        "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor, K-major, no swizzle: core matrices of
+// 8 rows x 16 bytes; `lbo` = byte distance between core matrices adjacent in
+// K, `sbo` = between core matrices adjacent in M/N; bit 46 is the fixed
+// descriptor version; swizzle mode 0.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  return static_cast<uint64_t>((addr >> 4) & 0x3FFFu) |
+         (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
+         (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46);
+}
+
+// Instruction descriptor of kind::f16: fp32 D (bits 4-5 = 1), bf16 A and B
+// (bits 7-9 = 1, 10-12 = 1), both K-major, N >> 3 at bit 17, M >> 4 at bit 24.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// ---- shared state ----------------------------------------------------------
+
+struct Ctl {
+  uint64_t meta_full[kMetaStages], meta_empty[kMetaStages];
+  uint64_t x_full[kXStages], x_empty[kXStages];
+  uint64_t a_full, a_empty, prod_done;
+  uint64_t acc_full[2], acc_empty[2];
+  uint32_t tmem_base;
+  volatile int abort;
+};
+
+struct Waiter {
+  Ctl* ctl;
+  int32_t* dev_err;
+  // Bounded wait: false when the kernel is aborting (this or another wait
+  // timed out); never spins forever.
+  __device__ bool wait(uint64_t* bar, uint32_t parity) const {
+    const long long t0 = clock64();
+    for (uint32_t it = 0;; ++it) {
+      if (mbar_try(bar, parity)) return true;
+      if ((it & 63u) == 63u) {
+        if (ctl->abort) return false;
+        if (clock64() - t0 > kWaitCycles) {
+          ctl->abort = 1;
+          cconv::flag_error(dev_err, kDerrTimeout);
+          return false;
+        }
+      }
+    }
+  }
+  // Drain wait before exit: bounded by time only, so that an async copy or
+  // MMA still in flight is waited for even while aborting.
+  __device__ void drain(uint64_t* bar, uint32_t parity) const {
+    const long long t0 = clock64();
+    while (!mbar_try(bar, parity))
+      if (clock64() - t0 > kWaitCycles) {
+        cconv::flag_error(dev_err, kDerrTimeout);
+        return;
+      }
+  }
+};
+
+// ---- small helpers ---------------------------------------------------------
+
+__device__ __forceinline__ uint4 hist_load(const Pool& P, int slot, int c0, int col) {
+  const char* base = P.p + (int64_t)slot * P.s_slot * 2;
+  if (P.mode == cconv::kPoolSD)
+    return *reinterpret_cast<const uint4*>(base + ((int64_t)col * P.s_col + c0) * 2);
+  uint32_t h[8];
+#pragma unroll
+  for (int v = 0; v < 8; ++v)
+    h[v] = *reinterpret_cast<const uint16_t*>(
+        base + ((int64_t)(c0 + v) * P.s_chan + (int64_t)col * P.s_col) * 2);
+  return make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16),
+                    h[6] | (h[7] << 16));
+}
+
+__device__ __forceinline__ void hist_store(const Pool& P, int slot, int c0, int col, uint4 u) {
+  char* base = P.p + (int64_t)slot * P.s_slot * 2;
+  if (P.mode == cconv::kPoolSD) {
+    *reinterpret_cast<uint4*>(base + ((int64_t)col * P.s_col + c0) * 2) = u;
+    return;
+  }
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int v = 0; v < 8; ++v)
+    *reinterpret_cast<uint16_t*>(base + ((int64_t)(c0 + v) * P.s_chan + (int64_t)col * P.s_col) *
+                                            2) = static_cast<uint16_t>(w[v >> 1] >> ((v & 1) * 16));
+}
+
+// Number of requests s in [0, B) with cu[s] <= p (strict: cu[s] < p), found by
+// a warp-wide walk from `from` (a count known not to exceed the answer).
+// cu is non-decreasing for valid input; the walk stays in bounds either way.
+__device__ int count_le(const int32_t* __restrict__ cu, int B, int p, bool strict, int from) {
+  const int lane = threadIdx.x & 31;
+  int c = from;
+  for (;;) {
+    const int idx = c + lane;
+    bool ok = false;
+    if (idx < B) {
+      const int v = __ldg(cu + idx);
+      ok = strict ? (v < p) : (v <= p);
+    }
+    const unsigned m = __ballot_sync(0xffffffffu, ok);
+    const int k = __popc(m);
+    c += k;
+    if (k < 32) return c;
+  }
+}
+
+// Tile boundary: tau * pitch moved back to its request's start when it would
+// split that request's first n tokens.
+// `from` is a lower bound of count_le(p).
+__device__ int tile_edge(const Args& a, int tau, int from) {
+  if (tau <= 0) return 0;
+  if (tau >= a.num_tiles) return a.T;
+  const int p = tau * a.tile_pitch;
+  const int c = count_le(a.cu, a.B, p, false, from);
+  const int s = c - 1;
+  if (s >= 0 && s < a.B) {
+    const int st = __ldg(a.cu + s), en = __ldg(a.cu + s + 1);
+    if (p < en && p - st > 0 && p - st < a.n) return st;
+  }
+  return p;
+}
+
+// ---- the kernel ----------------------------------------------------------------
+
+template <int T0, int T1>
+__global__ void __launch_bounds__(kThreads, 1)
+    cca_kernel(const __grid_constant__ CUtensorMap xmap, const Args a) {
+  extern __shared__ __align__(1024) unsigned char dsm[];
+  unsigned char* base = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(dsm) + 1023) & ~static_cast<uintptr_t>(1023));
+  unsigned char* sB = base;                          // T1 taps of B
+  unsigned char* sA = sB + T1 * kTapB;               // T1 taps of A
+  unsigned char* sX = sA + T1 * kTapA;               // x stages
+  Meta* meta = reinterpret_cast<Meta*>(sX + kXStages * kXStageBytes);
+  Ctl* ctl = reinterpret_cast<Ctl*>(meta + kMetaStages);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int u0 = blockIdx.x * a.units_per_cta;
+  const int u1 = min(a.units, u0 + a.units_per_cta);
+  const int ntiles = max(u1 - u0, 0);
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kMetaStages; ++i) {
+      mbar_init(&ctl->meta_full[i], 1);
+      mbar_init(&ctl->meta_empty[i], kProdWarps + kEpiWarps);
+    }
+    for (int i = 0; i < kXStages; ++i) {
+      mbar_init(&ctl->x_full[i], 1);
+      mbar_init(&ctl->x_empty[i], kProdWarps);
+    }
+    mbar_init(&ctl->a_full, kProdWarps);
+    mbar_init(&ctl->a_empty, 1);
+    mbar_init(&ctl->prod_done, kProdWarps);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&ctl->acc_full[i], 1);
+      mbar_init(&ctl->acc_empty[i], kEpiWarps);
+    }
+    ctl->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == kWarpMma) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(&ctl->tmem_base)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl->tmem_base;
+  const Waiter W{ctl, a.dev_err};
+
+  if (warp == kWarpSched) {
+    // ------------------------------------------------------------ scheduler
+    // Consecutive tiles of one group carry their edge and the request counts
+    // forward, so each count_le below walks from a cursor (usually one round).
+    int prev_tau = -2, prev_g = -1, hi_prev = 0, own_hi_prev = 0;
+    int issued = 0;
+    if (blockIdx.x == 0) {   // index data is checked once per call
+      for (int s = lane; s < a.B; s += 32) {
+        const int c0v = __ldg(a.cu + s), c1v = __ldg(a.cu + s + 1);
+        if (c0v < 0 || c1v < c0v || c1v > a.T) cconv::flag_error(a.dev_err, CCONV_DERR_CU_SEQLENS);
+        if (__ldg(a.state_idx + s) >= a.pool.num_slots)
+          cconv::flag_error(a.dev_err, CCONV_DERR_SLOT_RANGE);
+      }
+    }
+    for (int i = 0; i < ntiles; ++i) {
+      const int u = u0 + i;
+      const int g = u / a.num_tiles, tau = u - g * a.num_tiles;
+      const int ms = i % kMetaStages, xs = i % kXStages;
+      if (!W.wait(&ctl->meta_empty[ms], ((i / kMetaStages) & 1) ^ 1)) break;
+      const bool cont = (g == prev_g && tau == prev_tau + 1);
+      const int lo = cont ? hi_prev : tile_edge(a, tau, 0);
+      const int own_lo = cont ? own_hi_prev : count_le(a.cu, a.B, lo, true, 0);
+      const int nle_lo = count_le(a.cu, a.B, lo, false, own_lo);   // requests with cu <= lo
+      const int hi = tile_edge(a, tau + 1, nle_lo);
+      const int len = max(hi - lo, 0);
+      // owned requests: lo <= cu[s] < hi (the last tile also owns cu[s] >= T)
+      const int own_hi =
+          (tau == a.num_tiles - 1) ? a.B : count_le(a.cu, a.B, hi, true, own_lo);
+      Meta& M = meta[ms];
+      // row -> request, 32 rows per batch; sc = request holding the batch's first row
+      int sc = max(nle_lo - 1, 0);
+      for (int r0 = 0; r0 < kRows; r0 += 32) {
+        const int r = r0 + lane;
+        const int t = lo + r;
+        int j = -1, slot = -1;
+        if (r < len) {
+          int sr = sc;
+          while (sr + 1 < a.B && __ldg(a.cu + sr + 1) <= t) ++sr;
+          const int st = __ldg(a.cu + sr), en = __ldg(a.cu + sr + 1);
+          if (st >= 0 && st <= t && t < en && en <= a.T) {
+            const int sl = __ldg(a.state_idx + sr);
+            const bool h = (a.has_init == nullptr || __ldg(a.has_init + sr) != 0);
+            if (sl < a.pool.num_slots) {   // out-of-range slots are skipped and reported
+              j = t - st;
+              slot = (h && sl >= 0) ? sl : -1;
+            }
+          }
+        }
+        M.rowj[r] = j;
+        M.rowslot[r] = slot;
+        const int last = min(lo + r0 + 31, hi - 1);   // same walk on every lane
+        while (sc + 1 < a.B && __ldg(a.cu + sc + 1) <= last) ++sc;
+      }
+      if (lane == 0) {
+        M.lo = lo;
+        M.len = len;
+        M.g = g;
+        M.own_lo = own_lo;
+        M.own_hi = own_hi;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl->meta_full[ms]);
+      // x rows [lo - n, lo - n + kXBoxRows) of the group's channels
+      if (!W.wait(&ctl->x_empty[xs], ((i / kXStages) & 1) ^ 1)) break;
+      if (lane == 0) {
+        if (a.T > 0) {
+          mbar_arrive_tx(&ctl->x_full[xs], kXStageBytes);
+          tma_load_2d(sX + xs * kXStageBytes, &xmap, g * kGS, lo - a.n, &ctl->x_full[xs]);
+        } else {
+          mbar_arrive(&ctl->x_full[xs]);
+        }
+      }
+      __syncwarp();
+      ++issued;
+      prev_g = g;
+      prev_tau = tau;
+      hi_prev = hi;
+      own_hi_prev = own_hi;
+    }
+    // drain: no TMA may land after the CTA exits
+    for (int i = max(issued - kXStages, 0); i < issued; ++i)
+      W.drain(&ctl->x_full[i % kXStages], (i / kXStages) & 1);
+  } else if (warp == kWarpMma) {
+    // ------------------------------------------------------------------ MMA
+    constexpr uint32_t idesc = idesc_bf16(kRows, kGS);
+    const uint32_t a_addr = smem_u32(sA), b_addr = smem_u32(sB);
+    int done = 0;
+    for (int i = 0; i < ntiles; ++i) {
+      const int ab = i & 1;
+      if (!W.wait(&ctl->a_full, i & 1)) break;
+      if (!W.wait(&ctl->acc_empty[ab], ((i >> 1) & 1) ^ 1)) break;
+      tc_fence_after();
+      if (lane == 0) {
+        const uint32_t d = tmem + ab * kAccCols;
+#pragma unroll
+        for (int kt = 0; kt < T1; ++kt) {
+#pragma unroll
+          for (int ks = 0; ks < kGS / 16; ++ks) {
+            const uint64_t ad =
+                smem_desc(a_addr + kt * kTapA + 2 * ks * kLboA, kLboA, 128);
+            const uint64_t bd =
+                smem_desc(b_addr + kt * kTapB + 2 * ks * kLboB, kLboB, 128);
+            mma_bf16(d, ad, bd, idesc, (kt | ks) != 0 ? 1u : 0u);
+          }
+        }
+        mma_commit(&ctl->a_empty);
+        mma_commit(&ctl->acc_full[ab]);
+      }
+      __syncwarp();
+      done = i + 1;
+    }
+    // drain: every issued MMA completes before TMEM is released
+    if (done > 0) W.drain(&ctl->a_empty, (done - 1) & 1);
+  } else if (warp < kWarpProd0) {
+    // ------------------------------------------------------------- epilogue
+    const int q = warp & 3;                      // TMEM lane quadrant of this warp
+    const int ew = warp - kWarpEpi0;
+    const int row = q * 32 + lane;
+    const int dunits = a.Dv / 8;                 // 16-byte units per delayed row
+    for (int i = 0; i < ntiles; ++i) {
+      const int ms = i % kMetaStages, ab = i & 1;
+      if (!W.wait(&ctl->meta_full[ms], (i / kMetaStages) & 1)) break;
+      const Meta& M = meta[ms];
+      const int g = M.g, lo = M.lo, len = M.len;
+      if (!W.wait(&ctl->acc_full[ab], (i >> 1) & 1)) break;
+      tc_fence_after();
+      const bool valid = row < len && M.rowj[row] >= 0;
+      char* orow = a.out + ((int64_t)(lo + row) * a.out_rs + (int64_t)g * kGS) * 2;
+      const char* brow = a.b_gr ? a.b_gr + (int64_t)g * kGS * 2 : nullptr;
+#pragma unroll 1
+      for (int c = 0; c < kGS / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + ab * kAccCols + c * 32, r);
+        tmem_wait_ld();
+        if (valid) {
+          float f[32];
+#pragma unroll
+          for (int k = 0; k < 32; ++k) f[k] = __uint_as_float(r[k]);
+          if (brow) {
+#pragma unroll
+            for (int k = 0; k < 32; k += 8) {
+              float bb[8];
+              cconv::unpack16<__nv_bfloat16>(cconv::ldg16(brow + (c * 32 + k) * 2), bb);
+#pragma unroll
+              for (int e = 0; e < 8; ++e) f[k + e] += bb[e];
+            }
+          }
+#pragma unroll
+          for (int k = 0; k < 32; k += 8) {
+            float h[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) h[e] = f[k + e];
+            cconv::stg16(orow + (c * 32 + k) * 2, cconv::pack16<__nv_bfloat16>(h));
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl->acc_empty[ab]);
+      // delayed half of v: rows r = g, g+G, ... of the tile with j >= 1 copy the
+      // previous token's value
+      for (int r = g + ew * a.G; r < len; r += kEpiWarps * a.G) {
+        if (M.rowj[r] >= 1) {
+          const int64_t t = lo + r;
+          for (int k = lane; k < dunits; k += 32)
+            cconv::stg16(a.dprev + (t * a.dprev_rs + k * 8) * 2,
+                         cconv::ldg16(a.delayed + ((t - 1) * a.delayed_rs + k * 8) * 2));
+        }
+      }
+      // owned requests s with s % G == g: first delayed value and delayed state
+      for (int s = M.own_lo + ((g - M.own_lo % a.G) % a.G + a.G) % a.G + ew * a.G;
+           s < M.own_hi; s += kEpiWarps * a.G) {
+        const int st = __ldg(a.cu + s), en = __ldg(a.cu + s + 1);
+        const int slot = __ldg(a.state_idx + s);
+        if (st < 0 || en < st || en > a.T) {
+          if (lane == 0) cconv::flag_error(a.dev_err, CCONV_DERR_CU_SEQLENS);
+          continue;
+        }
+        if (slot >= a.pool.num_slots) continue;
+        const bool h = slot >= 0 && (a.has_init == nullptr || __ldg(a.has_init + s) != 0);
+        for (int k = lane; k < dunits; k += 32) {
+          const uint4 first =
+              h ? *reinterpret_cast<const uint4*>(a.dstate + ((int64_t)slot * a.dstate_rs + k * 8) * 2)
+                : cconv::ldg16(a.delayed_init + k * 16);
+          if (en > st) cconv::stg16(a.dprev + ((int64_t)st * a.dprev_rs + k * 8) * 2, first);
+          if (slot >= 0) {
+            const uint4 last =
+                en > st ? cconv::ldg16(a.delayed + ((int64_t)(en - 1) * a.delayed_rs + k * 8) * 2)
+                        : first;
+            *reinterpret_cast<uint4*>(a.dstate + ((int64_t)slot * a.dstate_rs + k * 8) * 2) =
+                last;
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl->meta_empty[ms]);
+    }
+  } else {
+    // ------------------------------------------------------------- producers
+    const int p = threadIdx.x - kWarpProd0 * 32;   // 0 .. 255
+    const int kc = p & 15;                         // 8-channel chunk within the group
+    const int strip = p >> 4;                      // rows strip*8 .. strip*8+7
+    int cur_g = -1;
+    float w0[T0][8], b0[8];
+    for (int i = 0; i < ntiles; ++i) {
+      const int ms = i % kMetaStages, xs = i % kXStages;
+      if (!W.wait(&ctl->meta_full[ms], (i / kMetaStages) & 1)) break;
+      const Meta& M = meta[ms];
+      const int g = M.g, len = M.len;
+      if (!W.wait(&ctl->x_full[xs], (i / kXStages) & 1)) break;
+      if (!W.wait(&ctl->a_empty, (i & 1) ^ 1)) break;   // MMA of the previous tile done
+      const int c0 = g * kGS + kc * 8;
+      if (g != cur_g) {
+        // B operand of group g: B[tap][k-chunk][n] = w_gr[g*128 + n][k-chunk*8 + e][tap]
+        for (int pr = p; pr < kGS * (kGS / 8); pr += kProdWarps * 32) {
+          const int o = pr & (kGS - 1), bkc = pr >> 7;
+          const char* src = a.w_gr + ((int64_t)(g * kGS + o) * kGS + bkc * 8) * T1 * 2;
+          uint32_t e[8 * T1];
+#pragma unroll
+          for (int v = 0; v < T1; ++v) {
+            const uint4 r = cconv::ldg16(src + v * 16);
+            e[v * 8 + 0] = r.x & 0xffffu;
+            e[v * 8 + 1] = r.x >> 16;
+            e[v * 8 + 2] = r.y & 0xffffu;
+            e[v * 8 + 3] = r.y >> 16;
+            e[v * 8 + 4] = r.z & 0xffffu;
+            e[v * 8 + 5] = r.z >> 16;
+            e[v * 8 + 6] = r.w & 0xffffu;
+            e[v * 8 + 7] = r.w >> 16;
+          }
+#pragma unroll
+          for (int kt = 0; kt < T1; ++kt) {
+            uint32_t h[8];
+#pragma unroll
+            for (int ee = 0; ee < 8; ++ee) h[ee] = e[ee * T1 + kt];
+            *reinterpret_cast<uint4*>(sB + kt * kTapB + bkc * kLboB + o * 16) =
+                make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16),
+                           h[6] | (h[7] << 16));
+          }
+        }
+#pragma unroll
+        for (int v = 0; v < 8; ++v) {
+#pragma unroll
+          for (int k = 0; k < T0; ++k)
+            w0[k][v] = cconv::load_f32<__nv_bfloat16>(a.w_dw, (int64_t)(c0 + v) * T0 + k);
+          b0[v] = a.b_dw ? cconv::load_f32<__nv_bfloat16>(a.b_dw, c0 + v) : 0.0f;
+        }
+        cur_g = g;
+      }
+      // A operands: A[tap kt][k-chunk][row] = u(j - (T1-1-kt)) of the row's request
+      const unsigned char* xst = sX + xs * kXStageBytes;
+#pragma unroll 1
+      for (int rr = 0; rr < 8; ++rr) {
+        const int r = strip * 8 + rr;
+        uint4 outv[T1];
+        const int j = (r < len) ? M.rowj[r] : -1;
+        if (j < 0) {
+#pragma unroll
+          for (int kt = 0; kt < T1; ++kt) outv[kt] = make_uint4(0u, 0u, 0u, 0u);
+        } else {
+          const int hslot = M.rowslot[r];
+          constexpr int NW = T0 + T1 - 1;        // x~[j - m], m = 0 .. n
+          float xw[NW][8];
+#pragma unroll
+          for (int m = 0; m < NW; ++m) {
+            uint4 raw;
+            if (j - m >= 0) {
+              raw = *reinterpret_cast<const uint4*>(xst + (r + a.n - m) * kXRowBytes + kc * 16);
+            } else if (hslot >= 0) {
+              raw = hist_load(a.pool, hslot, c0, a.n + j - m);
+            } else {
+              raw = make_uint4(0u, 0u, 0u, 0u);
+            }
+            cconv::unpack16<__nv_bfloat16>(raw, xw[m]);
+          }
+#pragma unroll
+          for (int kt = 0; kt < T1; ++kt) {
+            const int mp = T1 - 1 - kt;          // u at j - mp
+            float uu[8];
+#pragma unroll
+            for (int v = 0; v < 8; ++v) {
+              float acc = b0[v];
+#pragma unroll
+              for (int k = 0; k < T0; ++k) acc = fmaf(w0[k][v], xw[mp + T0 - 1 - k][v], acc);
+              uu[v] = acc;
+            }
+            outv[kt] = cconv::pack16<__nv_bfloat16>(uu);
+          }
+        }
+#pragma unroll
+        for (int kt = 0; kt < T1; ++kt)
+          *reinterpret_cast<uint4*>(sA + kt * kTapA + kc * kLboA + r * 16) = outv[kt];
+      }
+      fence_proxy_async();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&ctl->a_full);
+        mbar_arrive(&ctl->x_empty[xs]);
+        mbar_arrive(&ctl->prod_done);
+      }
+      // raw-history state of owned requests (all history reads of this tile
+      // are done once every producer warp has arrived)
+      if (!W.wait(&ctl->prod_done, i & 1)) break;
+      const int nown = M.own_hi - M.own_lo;
+      for (int task = p; task < nown * (kGS / 8); task += kProdWarps * 32) {
+        const int s = M.own_lo + (task >> 4);
+        const int tc0 = g * kGS + (task & 15) * 8;
+        const int st = __ldg(a.cu + s), en = __ldg(a.cu + s + 1);
+        const int slot = __ldg(a.state_idx + s);
+        if (st < 0 || en < st || en > a.T) continue;
+        if (slot >= a.pool.num_slots) {
+          if ((task & 15) == 0) cconv::flag_error(a.dev_err, CCONV_DERR_SLOT_RANGE);
+          continue;
+        }
+        if (slot < 0) continue;
+        const bool h = a.has_init == nullptr || __ldg(a.has_init + s) != 0;
+        const int L = en - st;
+        for (int col = 0; col < a.n; ++col) {
+          const int src = L - a.n + col;
+          uint4 v;
+          if (src >= 0)
+            v = cconv::ldg16(a.qk + ((int64_t)(st + src) * a.qk_rs + tc0) * 2);
+          else if (h)
+            v = hist_load(a.pool, slot, tc0, L + col);
+          else
+            v = make_uint4(0u, 0u, 0u, 0u);
+          hist_store(a.pool, slot, tc0, col, v);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl->meta_empty[ms]);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kWarpMma) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(kTmemCols)
+                 : "memory");
+  }
+}
+
+// ---- host side --------------------------------------------------------------
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+static size_t smem_bytes(int T1) {
+  return 1024 + (size_t)T1 * (kTapB + kTapA) + (size_t)kXStages * kXStageBytes +
+         kMetaStages * sizeof(Meta) + sizeof(Ctl);
+}
+
+template <int T0, int T1>
+static cudaError_t launch(const CUtensorMap& map, const Args& a, int grid, cudaStream_t st) {
+  const size_t smem = smem_bytes(T1);
+  cudaError_t e = cudaFuncSetAttribute(cca_kernel<T0, T1>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  cca_kernel<T0, T1><<<grid, kThreads, smem, st>>>(map, a);
+  return cudaGetLastError();
+}
+
+static bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace cca
+
+using namespace cca;
+
+extern "C" int cca_qk_conv(const void* qk, int64_t qk_row_stride, const void* w_dw,
+                           const void* b_dw, const void* w_gr, const void* b_gr, int32_t groups,
+                           int32_t t0, int32_t t1, const void* delayed,
+                           int64_t delayed_row_stride, const void* delayed_init, int32_t Dv,
+                           cconv_pool_t conv_state, void* delayed_state,
+                           int64_t delayed_state_row_stride, const int32_t* state_idx,
+                           const int32_t* cu_seqlens, const uint8_t* has_init,
+                           int32_t num_seqs, int32_t num_tokens, int32_t Cqk, int32_t dtype,
+                           void* out_qk, int64_t out_qk_row_stride, void* out_delayed_prev,
+                           int64_t out_delayed_prev_row_stride, int32_t* dev_err,
+                           cconv_stream_t stream) {
+  if (dtype != CCONV_DTYPE_BF16 && dtype != CCONV_DTYPE_F32) return CCONV_ERR_INVALID;
+  if (!w_dw || !w_gr || !delayed_init || !conv_state.p || !delayed_state || !state_idx ||
+      !cu_seqlens)
+    return CCONV_ERR_INVALID;
+  if (num_tokens > 0 && (!qk || !delayed || !out_qk || !out_delayed_prev))
+    return CCONV_ERR_INVALID;
+  if (num_seqs < 0 || num_tokens < 0 || groups <= 0 || Cqk <= 0 || Dv <= 0 || t0 < 1 || t1 < 1)
+    return CCONV_ERR_INVALID;
+  if (Cqk % groups != 0) return CCONV_ERR_INVALID;
+  if (dtype == CCONV_DTYPE_F32) return CCONV_ERR_UNSUPPORTED;
+  if (Cqk / groups != kGS || t0 > 4 || t1 > 2) return CCONV_ERR_UNSUPPORTED;
+  const int n = t0 + t1 - 2;
+  if (conv_state.cap < n || conv_state.num_slots <= 0 || conv_state.s_slot <= 0 ||
+      conv_state.s_chan <= 0 || conv_state.s_col <= 0)
+    return CCONV_ERR_INVALID;
+  if (!al16(w_gr) || (b_gr && !al16(b_gr))) return CCONV_ERR_INVALID;
+  if (Dv % 8 != 0 || !al16(delayed_init) || !al16(delayed_state) ||
+      delayed_state_row_stride < Dv || delayed_state_row_stride % 8 != 0)
+    return CCONV_ERR_INVALID;
+  if (num_tokens > 0) {
+    if (!al16(qk) || !al16(out_qk) || !al16(delayed) || !al16(out_delayed_prev))
+      return CCONV_ERR_INVALID;
+    if (qk_row_stride < Cqk || qk_row_stride % 8 != 0 || out_qk_row_stride < Cqk ||
+        out_qk_row_stride % 8 != 0 || delayed_row_stride < Dv || delayed_row_stride % 8 != 0 ||
+        out_delayed_prev_row_stride < Dv || out_delayed_prev_row_stride % 8 != 0)
+      return CCONV_ERR_INVALID;
+  }
+  if (num_seqs == 0) return CCONV_OK;
+
+  Args a;
+  a.qk = static_cast<const char*>(qk);
+  a.qk_rs = qk_row_stride;
+  a.w_dw = static_cast<const char*>(w_dw);
+  a.b_dw = static_cast<const char*>(b_dw);
+  a.w_gr = static_cast<const char*>(w_gr);
+  a.b_gr = static_cast<const char*>(b_gr);
+  a.delayed = static_cast<const char*>(delayed);
+  a.delayed_rs = delayed_row_stride;
+  a.delayed_init = static_cast<const char*>(delayed_init);
+  a.Dv = Dv;
+  a.pool.p = static_cast<char*>(conv_state.p);
+  a.pool.s_slot = conv_state.s_slot;
+  a.pool.s_chan = conv_state.s_chan;
+  a.pool.s_col = conv_state.s_col;
+  a.pool.num_slots = conv_state.num_slots;
+  a.pool.cap = conv_state.cap;
+  a.pool.mode = (conv_state.s_chan == 1 && al16(conv_state.p) && conv_state.s_col % 8 == 0 &&
+                 conv_state.s_slot % 8 == 0)
+                    ? cconv::kPoolSD
+                    : cconv::kPoolGeneric;
+  a.dstate = static_cast<char*>(delayed_state);
+  a.dstate_rs = delayed_state_row_stride;
+  a.state_idx = state_idx;
+  a.cu = cu_seqlens;
+  a.has_init = has_init;
+  a.B = num_seqs;
+  a.T = num_tokens;
+  a.Cqk = Cqk;
+  a.G = groups;
+  a.n = n;
+  a.tile_pitch = kRows - std::max(n - 1, 0);
+  a.num_tiles = std::max(1, (num_tokens + a.tile_pitch - 1) / a.tile_pitch);
+  a.units = a.num_tiles * groups;
+  a.out = static_cast<char*>(out_qk);
+  a.out_rs = out_qk_row_stride;
+  a.dprev = static_cast<char*>(out_delayed_prev);
+  a.dprev_rs = out_delayed_prev_row_stride;
+  a.dev_err = dev_err;
+
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return CCONV_ERR_LAUNCH;
+  const int ctas0 = std::min(sms, a.units);
+  a.units_per_cta = (a.units + ctas0 - 1) / ctas0;
+  const int grid = (a.units + a.units_per_cta - 1) / a.units_per_cta;
+
+  CUtensorMap map;
+  memset(&map, 0, sizeof(map));
+  if (num_tokens > 0) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return CCONV_ERR_LAUNCH;
+    const cuuint64_t dims[2] = {(cuuint64_t)Cqk, (cuuint64_t)num_tokens};
+    const cuuint64_t strides[1] = {(cuuint64_t)qk_row_stride * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)kGS, (cuuint32_t)kXBoxRows};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(qk), dims,
+                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return CCONV_ERR_INVALID;
+  }
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaErrorInvalidValue;
+#define CCA_CASE(a0, a1) \
+  if (t0 == a0 && t1 == a1) e = launch<a0, a1>(map, a, grid, st);
+  CCA_CASE(1, 1) CCA_CASE(2, 1) CCA_CASE(3, 1) CCA_CASE(4, 1)
+  CCA_CASE(1, 2) CCA_CASE(2, 2) CCA_CASE(3, 2) CCA_CASE(4, 2)
+#undef CCA_CASE
+  return e == cudaSuccess ? CCONV_OK : CCONV_ERR_LAUNCH;
+}

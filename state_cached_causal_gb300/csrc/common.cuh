@@ -1,0 +1,228 @@
+// Device helpers shared by the conv kernels of libcconv.so (sm_103a).
+//
+// Storage types are fp32 and bf16; every kernel moves data in 16-byte
+// vectors ("units") of 4 fp32 or 8 bf16 channels and accumulates in fp32.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "cconv.h"
+
+namespace cconv {
+
+constexpr int kMaxSpec = 7;   // n_spec limit of cconv_update (q <= 8)
+
+template <typename T>
+struct Elem;
+template <>
+struct Elem<float> {
+  static constexpr int V = 4;      // channels per 16-byte unit
+  static constexpr int bytes = 4;
+};
+template <>
+struct Elem<__nv_bfloat16> {
+  static constexpr int V = 8;
+  static constexpr int bytes = 2;
+};
+
+// ---- 16-byte unit <-> fp32 lanes ---------------------------------------
+
+template <typename T>
+__device__ __forceinline__ void unpack16(const uint4& r, float (&f)[Elem<T>::V]);
+
+template <>
+__device__ __forceinline__ void unpack16<float>(const uint4& r, float (&f)[4]) {
+  f[0] = __uint_as_float(r.x);
+  f[1] = __uint_as_float(r.y);
+  f[2] = __uint_as_float(r.z);
+  f[3] = __uint_as_float(r.w);
+}
+
+// bf16 -> fp32 is exact: the bf16 bits are the upper half of the fp32 bits.
+template <>
+__device__ __forceinline__ void unpack16<__nv_bfloat16>(const uint4& r, float (&f)[8]) {
+  f[0] = __uint_as_float(r.x << 16);
+  f[1] = __uint_as_float(r.x & 0xffff0000u);
+  f[2] = __uint_as_float(r.y << 16);
+  f[3] = __uint_as_float(r.y & 0xffff0000u);
+  f[4] = __uint_as_float(r.z << 16);
+  f[5] = __uint_as_float(r.z & 0xffff0000u);
+  f[6] = __uint_as_float(r.w << 16);
+  f[7] = __uint_as_float(r.w & 0xffff0000u);
+}
+
+template <typename T>
+__device__ __forceinline__ uint4 pack16(const float (&f)[Elem<T>::V]);
+
+template <>
+__device__ __forceinline__ uint4 pack16<float>(const float (&f)[4]) {
+  return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]),
+                    __float_as_uint(f[3]));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);   // round to nearest even
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+template <>
+__device__ __forceinline__ uint4 pack16<__nv_bfloat16>(const float (&f)[8]) {
+  return make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]),
+                    pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
+}
+
+template <typename T>
+__device__ __forceinline__ float load_f32(const char* base, int64_t i) {
+  if constexpr (sizeof(T) == 4) {
+    return reinterpret_cast<const float*>(base)[i];
+  } else {
+    const uint16_t b = reinterpret_cast<const uint16_t*>(base)[i];
+    return __uint_as_float(static_cast<uint32_t>(b) << 16);
+  }
+}
+
+// Read-only 16-byte load of activations (never written during the call).
+__device__ __forceinline__ uint4 ldg16(const char* p) {
+  return __ldg(reinterpret_cast<const uint4*>(p));
+}
+
+__device__ __forceinline__ void stg16(char* p, const uint4& v) {
+  *reinterpret_cast<uint4*>(p) = v;
+}
+
+// SiLU v * sigmoid(v). fp32 storage keeps the accurate exp and division;
+// bf16 storage (8 mantissa bits) takes the fast exp and reciprocal.
+template <typename T>
+__device__ __forceinline__ float silu(float v) {
+  if constexpr (sizeof(T) == 4) {
+    return v / (1.0f + expf(-v));
+  } else {
+    return __fdividef(v, 1.0f + __expf(-v));
+  }
+}
+
+// ---- conv-state pool access ----------------------------------------------
+
+enum PoolMode : int32_t {
+  kPoolDS = 0,    // s_col == 1 && s_chan == cap: a unit-aligned channel-first slab
+  kPoolSD = 1,    // s_chan == 1: one 16-byte unit per column
+  kPoolGeneric = 2
+};
+
+struct Pool {
+  char* p;
+  int64_t s_slot, s_chan, s_col;   // element strides
+  int32_t num_slots, cap;
+  int32_t mode;
+};
+
+// A thread's pool block lives in shared memory as `cap` 16-byte columns,
+// column `col` at blk[col * nt] (threads interleaved so that a column access
+// by a warp is conflict-free). Element v of a column is channel c0 + v.
+template <typename T>
+__device__ __forceinline__ void set_elem(uint4* unit, int v, uint32_t bits) {
+  if constexpr (sizeof(T) == 4)
+    reinterpret_cast<uint32_t*>(unit)[v] = bits;
+  else
+    reinterpret_cast<uint16_t*>(unit)[v] = static_cast<uint16_t>(bits);
+}
+
+template <typename T>
+__device__ __forceinline__ uint32_t get_elem(const uint4* unit, int v) {
+  if constexpr (sizeof(T) == 4)
+    return reinterpret_cast<const uint32_t*>(unit)[v];
+  else
+    return reinterpret_cast<const uint16_t*>(unit)[v];
+}
+
+// Load columns [0, ncols) of the thread's channels of `slot` (the DS mode
+// loads the whole slab of cap columns so that a later store can rewrite it).
+template <typename T>
+__device__ void pool_load(const Pool& P, int slot, int c0, int ncols, uint4* blk, int nt) {
+  constexpr int V = Elem<T>::V, E = Elem<T>::bytes;
+  const char* base = P.p + (int64_t)slot * P.s_slot * E;
+  if (P.mode == kPoolSD) {
+    for (int col = 0; col < ncols; ++col)
+      blk[col * nt] = *reinterpret_cast<const uint4*>(base + ((int64_t)col * P.s_col + c0) * E);
+  } else if (P.mode == kPoolDS) {
+    const uint4* src = reinterpret_cast<const uint4*>(base + (int64_t)c0 * P.cap * E);
+    int v = 0, col = 0;
+    for (int k = 0; k < P.cap; ++k) {
+      const uint4 r = src[k];
+      const uint32_t wd[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+      for (int t = 0; t < V; ++t) {
+        const uint32_t bits = (E == 4) ? wd[t] : ((wd[t >> 1] >> ((t & 1) * 16)) & 0xffffu);
+        set_elem<T>(blk + col * nt, v, bits);
+        if (++col == P.cap) {
+          col = 0;
+          ++v;
+        }
+      }
+    }
+  } else {
+    for (int col = 0; col < ncols; ++col) {
+#pragma unroll
+      for (int v = 0; v < V; ++v) {
+        const int64_t off = ((int64_t)(c0 + v) * P.s_chan + (int64_t)col * P.s_col) * E;
+        uint32_t bits;
+        if (E == 4)
+          bits = *reinterpret_cast<const uint32_t*>(base + off);
+        else
+          bits = *reinterpret_cast<const uint16_t*>(base + off);
+        set_elem<T>(blk + col * nt, v, bits);
+      }
+    }
+  }
+}
+
+// Store columns [0, ncols) back (the DS mode rewrites the whole slab).
+template <typename T>
+__device__ void pool_store(const Pool& P, int slot, int c0, int ncols, const uint4* blk,
+                           int nt) {
+  constexpr int V = Elem<T>::V, E = Elem<T>::bytes;
+  char* base = P.p + (int64_t)slot * P.s_slot * E;
+  if (P.mode == kPoolSD) {
+    for (int col = 0; col < ncols; ++col)
+      *reinterpret_cast<uint4*>(base + ((int64_t)col * P.s_col + c0) * E) = blk[col * nt];
+  } else if (P.mode == kPoolDS) {
+    uint4* dst = reinterpret_cast<uint4*>(base + (int64_t)c0 * P.cap * E);
+    int v = 0, col = 0;
+    for (int k = 0; k < P.cap; ++k) {
+      uint32_t wd[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+      for (int t = 0; t < V; ++t) {
+        const uint32_t bits = get_elem<T>(blk + col * nt, v);
+        if (E == 4)
+          wd[t] = bits;
+        else
+          wd[t >> 1] |= bits << ((t & 1) * 16);
+        if (++col == P.cap) {
+          col = 0;
+          ++v;
+        }
+      }
+      dst[k] = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+    }
+  } else {
+    for (int col = 0; col < ncols; ++col) {
+#pragma unroll
+      for (int v = 0; v < V; ++v) {
+        const int64_t off = ((int64_t)(c0 + v) * P.s_chan + (int64_t)col * P.s_col) * E;
+        const uint32_t bits = get_elem<T>(blk + col * nt, v);
+        if (E == 4)
+          *reinterpret_cast<uint32_t*>(base + off) = bits;
+        else
+          *reinterpret_cast<uint16_t*>(base + off) = static_cast<uint16_t>(bits);
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void flag_error(int32_t* dev_err, int bits) {
+  if (dev_err) atomicOr(dev_err, bits);
+}
+
+}  // namespace cconv

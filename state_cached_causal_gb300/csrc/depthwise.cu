@@ -1,0 +1,457 @@
+// Depthwise causal conv with a conv-state pool: varlen prefill/decode
+// (cconv_fwd_varlen) and decode / speculative decode (cconv_update).
+//
+// Pages: "vllm.model_executor.layers.mamba.ops.cpu.gdn_attention"
+// (_spec_aware_nonspec prefill and decode conv, _spec_forward rolling buffer)
+// and "Qwen4ExpPLELayer" (dilated depthwise conv1d, state_len =
+// (kernel-1)*dilation, spec/decode/prefill dispatch).
+//
+// Design (GB300): the op is HBM-bound (4 FMAs per 4 bytes moved), so each
+// thread owns one 16-byte unit of channels (8 bf16 / 4 fp32) and walks down
+// the time axis; a warp moves 512 contiguous bytes per row. A dilated conv
+// with dilation d is walked as d interleaved undilated chains (rows
+// r, r+d, r+2d, ...), so the register window holds only width-1 rows
+// whatever the dilation. Eight rows are loaded before any is used to keep
+// enough bytes in flight per SM.
+#include <algorithm>
+
+#include "common.cuh"
+
+namespace cconv {
+
+constexpr int kChunk = 64;      // tokens per varlen block (>= (width-1)*dilation)
+constexpr int kUnroll = 8;      // rows in flight per thread
+
+struct FwdArgs {
+  const char* x;
+  int64_t x_rs;
+  const char* w;
+  const char* bias;
+  Pool pool;
+  const int32_t* state_idx;
+  const int32_t* cu;
+  const uint8_t* has_init;
+  int32_t B, T, C;
+  int32_t act;
+  char* out;
+  int64_t out_rs;
+  int32_t* dev_err;
+};
+
+// Block -> (sequence, chunk) map without a host sync. Chunk j of sequence s
+// gets id K(s) + j with K(s) = floor(cu[s]/kChunk) + s; K is strictly
+// increasing and K(s) + nchunks(s) <= K(s+1), so a grid of
+// floor(T/kChunk) + B + 1 blocks covers every chunk (spare ids exit).
+// One warp finds max{s : K(s) <= b} with a 32-way search.
+__device__ int find_chunk_seq(const int32_t* __restrict__ cu, int B, int b) {
+  const int lane = threadIdx.x & 31;
+  if (B <= 0) return -1;
+  int lo = 0, hi = B;
+  while (hi - lo > 1) {
+    const int step = (hi - lo + 31) / 32;
+    const int idx = lo + lane * step;
+    bool ok = false;
+    if (idx < hi) ok = (__ldg(cu + idx) / kChunk + idx) <= b;
+    const unsigned m = __ballot_sync(0xffffffffu, ok);
+    if (m == 0u) return -1;   // only when K(lo) > b, i.e. b before the first chunk
+    lo = lo + (31 - __clz(m)) * step;
+    hi = min(lo + step, hi);
+  }
+  return (__ldg(cu + lo) / kChunk + lo) <= b ? lo : -1;
+}
+
+template <typename T, int W, int D>
+__global__ void __launch_bounds__(128) fwd_varlen_kernel(const FwdArgs a) {
+  constexpr int S = (W - 1) * D;
+  constexpr int V = Elem<T>::V, E = Elem<T>::bytes, U = kUnroll;
+  extern __shared__ uint4 dyn_smem[];
+  __shared__ int sh_seq;
+  const int nt = blockDim.x, tid = threadIdx.x;
+  const int b = blockIdx.x;
+
+  if (tid < 32) {
+    const int s = find_chunk_seq(a.cu, a.B, b);
+    if (tid == 0) {
+      sh_seq = s;
+      // Each sequence's index data is checked once, by block (s, 0).
+      if (blockIdx.y == 0 && b < a.B) {
+        const int c0v = a.cu[b], c1v = a.cu[b + 1];
+        if (c0v < 0 || c1v < c0v || c1v > a.T) flag_error(a.dev_err, CCONV_DERR_CU_SEQLENS);
+        if (a.state_idx[b] >= a.pool.num_slots) flag_error(a.dev_err, CCONV_DERR_SLOT_RANGE);
+      }
+    }
+  }
+  __syncthreads();
+  const int s = sh_seq;
+  if (s < 0) return;
+  const int start = a.cu[s], end = a.cu[s + 1];
+  if (start < 0 || end < start || end > a.T) return;
+  const int L = end - start;
+  const int nch = L > 0 ? (L + kChunk - 1) / kChunk : 1;
+  const int j = b - (start / kChunk + s);
+  if (j < 0 || j >= nch) return;
+  const int c0 = (blockIdx.y * nt + tid) * V;
+  if (c0 >= a.C) return;
+  const int slot = a.state_idx[s];
+  if (slot >= a.pool.num_slots) return;
+  const bool hs = slot >= 0 && (a.has_init == nullptr || a.has_init[s] != 0);
+
+  float wk[W][V], bv[V];
+#pragma unroll
+  for (int v = 0; v < V; ++v) {
+#pragma unroll
+    for (int k = 0; k < W; ++k) wk[k][v] = load_f32<T>(a.w, (int64_t)(c0 + v) * W + k);
+    bv[v] = a.bias ? load_f32<T>(a.bias, c0 + v) : 0.0f;
+  }
+
+  uint4* blk = dyn_smem + tid;
+  const int r0 = j * kChunk, r1 = min(L, r0 + kChunk);
+  if (j == 0) {
+    if (slot >= 0) pool_load<T>(a.pool, slot, c0, S, blk, nt);
+    if (!hs)
+      for (int col = 0; col < S; ++col) blk[col * nt] = make_uint4(0u, 0u, 0u, 0u);
+  }
+  const char* xs = a.x + ((int64_t)start * a.x_rs + c0) * E;
+  char* os = a.out + ((int64_t)start * a.out_rs + c0) * E;
+  const int64_t xstep = a.x_rs * E, ostep = a.out_rs * E;
+  const bool silu_on = a.act == CCONV_ACT_SILU;
+
+#pragma unroll
+  for (int rho = 0; rho < D; ++rho) {
+    float win[W - 1][V];
+#pragma unroll
+    for (int k = 0; k < W - 1; ++k) {
+      const int p = r0 + rho - (W - 1 - k) * D;   // p >= -S; p < 0 only in chunk 0
+      const uint4 r = (p >= 0) ? ldg16(xs + (int64_t)p * xstep) : blk[(S + p) * nt];
+      unpack16<T>(r, win[k]);
+    }
+    for (int r = r0 + rho; r < r1; r += U * D) {
+      uint4 raw[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int p = r + u * D;
+        raw[u] = (p < r1) ? ldg16(xs + (int64_t)p * xstep) : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        float cur[V], y[V];
+        unpack16<T>(raw[u], cur);
+#pragma unroll
+        for (int v = 0; v < V; ++v) {
+          float acc = bv[v];
+#pragma unroll
+          for (int k = 0; k < W - 1; ++k) acc = fmaf(wk[k][v], win[k][v], acc);
+          acc = fmaf(wk[W - 1][v], cur[v], acc);
+          y[v] = silu_on ? silu<T>(acc) : acc;
+        }
+        const int p = r + u * D;
+        if (p < r1) stg16(os + (int64_t)p * ostep, pack16<T>(y));
+#pragma unroll
+        for (int k = 0; k < W - 2; ++k) {
+#pragma unroll
+          for (int v = 0; v < V; ++v) win[k][v] = win[k + 1][v];
+        }
+#pragma unroll
+        for (int v = 0; v < V; ++v) win[W - 2][v] = cur[v];
+      }
+    }
+  }
+
+  // Chunk 0 owns the slot: it alone read the old columns, so it alone writes
+  // the new ones -- the last S elements of history ++ tokens. Moving column
+  // L+i down to column i reads ahead of every write (L >= 0).
+  if (j == 0 && slot >= 0) {
+    for (int i = 0; i < S; ++i) {
+      const int src = L - S + i;
+      blk[i * nt] = (src >= 0) ? ldg16(xs + (int64_t)src * xstep) : blk[(S + src) * nt];
+    }
+    pool_store<T>(a.pool, slot, c0, S, blk, nt);
+  }
+}
+
+struct UpdArgs {
+  const char* x;
+  int64_t x_rs;
+  Pool pool;
+  const char* w;
+  const char* bias;
+  const int32_t* state_idx;
+  int32_t B, n_spec;
+  const int32_t* num_accepted;
+  const uint8_t* has_init;
+  int32_t C, act, ctiles;
+  char* out;
+  int64_t out_rs;
+  int32_t* dev_err;
+};
+
+// One thread = one 16-byte channel unit of one request. The request's pool
+// columns are staged in shared memory, where the spec window offset
+// (num_accepted - 1) and the roll are plain indexed moves.
+template <typename T, int W, int D>
+__global__ void __launch_bounds__(128) update_kernel(const UpdArgs a) {
+  constexpr int S = (W - 1) * D;
+  constexpr int V = Elem<T>::V, E = Elem<T>::bytes, QM = kMaxSpec + 1;
+  extern __shared__ uint4 dyn_smem[];
+  const int nt = blockDim.x, tid = threadIdx.x;
+  const int s = blockIdx.x / a.ctiles;
+  const int ct = blockIdx.x - s * a.ctiles;
+  const int c0 = (ct * nt + tid) * V;
+  if (c0 >= a.C) return;
+  const int q = 1 + a.n_spec;
+  const int slot = a.state_idx[s];
+  if (slot >= a.pool.num_slots) {
+    if (c0 == 0) flag_error(a.dev_err, CCONV_DERR_SLOT_RANGE);
+    return;
+  }
+  int off = 0;
+  if (a.n_spec > 0) {
+    off = a.num_accepted[s] - 1;
+    if (off < 0 || off >= q) {
+      if (c0 == 0) flag_error(a.dev_err, CCONV_DERR_NUM_ACCEPTED);
+      return;
+    }
+  }
+  const bool hs = slot >= 0 && (a.has_init == nullptr || a.has_init[s] != 0);
+  const int ncols = a.n_spec > 0 ? a.pool.cap : S;
+  uint4* blk = dyn_smem + tid;
+  if (slot >= 0) pool_load<T>(a.pool, slot, c0, ncols, blk, nt);
+  if (!hs)
+    for (int col = 0; col < ncols; ++col) blk[col * nt] = make_uint4(0u, 0u, 0u, 0u);
+
+  float wk[W][V], bv[V];
+#pragma unroll
+  for (int v = 0; v < V; ++v) {
+#pragma unroll
+    for (int k = 0; k < W; ++k) wk[k][v] = load_f32<T>(a.w, (int64_t)(c0 + v) * W + k);
+    bv[v] = a.bias ? load_f32<T>(a.bias, c0 + v) : 0.0f;
+  }
+  const int64_t row0 = (int64_t)s * q;
+  const char* xs = a.x + (row0 * a.x_rs + c0) * E;
+  char* os = a.out + (row0 * a.out_rs + c0) * E;
+  uint4 xr[QM];
+#pragma unroll
+  for (int u = 0; u < QM; ++u)
+    xr[u] = (u < q) ? ldg16(xs + (int64_t)u * a.x_rs * E) : make_uint4(0u, 0u, 0u, 0u);
+
+  const bool silu_on = a.act == CCONV_ACT_SILU;
+#pragma unroll
+  for (int i = 0; i < QM; ++i) {
+    if (i < q) {
+      float y[V];
+#pragma unroll
+      for (int v = 0; v < V; ++v) y[v] = bv[v];
+#pragma unroll
+      for (int k = 0; k < W; ++k) {
+        const int idx = S + i - (W - 1 - k) * D;   // position in prior ++ tokens
+        float xv[V];
+        if (idx >= S)
+          unpack16<T>(xr[idx - S], xv);
+        else
+          unpack16<T>(blk[(off + idx) * nt], xv);
+#pragma unroll
+        for (int v = 0; v < V; ++v) y[v] = fmaf(wk[k][v], xv[v], y[v]);
+      }
+      if (silu_on) {
+#pragma unroll
+        for (int v = 0; v < V; ++v) y[v] = silu<T>(y[v]);
+      }
+      stg16(os + (int64_t)i * a.out_rs * E, pack16<T>(y));
+    }
+  }
+
+  if (slot >= 0) {
+    if (a.n_spec == 0) {
+      for (int i = 0; i + 1 < S; ++i) blk[i * nt] = blk[(i + 1) * nt];
+      blk[(S - 1) * nt] = xr[0];
+    } else {
+      const int keep = a.pool.cap - q;   // columns kept: B[off+1, off+1+keep)
+      for (int i = 0; i < keep; ++i) blk[i * nt] = blk[(off + 1 + i) * nt];
+#pragma unroll
+      for (int u = 0; u < QM; ++u)
+        if (u < q) blk[(keep + u) * nt] = xr[u];
+    }
+    pool_store<T>(a.pool, slot, c0, ncols, blk, nt);
+  }
+}
+
+// ---- host side -----------------------------------------------------------
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+static int pool_mode(const cconv_pool_t& pv, int esize, int V) {
+  const bool base_ok = aligned16(pv.p);
+  if (pv.s_col == 1 && pv.s_chan == pv.cap && base_ok && (pv.s_slot * esize) % 16 == 0)
+    return kPoolDS;
+  if (pv.s_chan == 1 && base_ok && pv.s_col % V == 0 && pv.s_slot % V == 0) return kPoolSD;
+  return kPoolGeneric;
+}
+
+static Pool make_pool(const cconv_pool_t& pv, int esize, int V) {
+  Pool P;
+  P.p = static_cast<char*>(pv.p);
+  P.s_slot = pv.s_slot;
+  P.s_chan = pv.s_chan;
+  P.s_col = pv.s_col;
+  P.num_slots = pv.num_slots;
+  P.cap = pv.cap;
+  P.mode = pool_mode(pv, esize, V);
+  return P;
+}
+
+// Threads per block: up to 128 channel units, fewer when the per-thread pool
+// block (cap * 16 bytes) would pass 48 KB of shared memory.
+static int pick_threads(int units, int cap) {
+  int nt = std::min(128, ((units + 31) / 32) * 32);
+  const int by_smem = (48 * 1024) / std::max(1, cap * 16);
+  nt = std::min(nt, (by_smem / 32) * 32);
+  return std::max(nt, 32);
+}
+
+// `rows` is the number of activation rows the call covers; x and out may be
+// NULL only when it is zero (an empty tensor has no storage).
+static int check_common(const void* x, int64_t x_rs, const void* w, const cconv_pool_t& pv,
+                        const int32_t* state_idx, int32_t C, int32_t width, int32_t dilation,
+                        int32_t act, int32_t dtype, const void* out, int64_t out_rs,
+                        int64_t rows, int* esize, int* V) {
+  if (dtype != CCONV_DTYPE_F32 && dtype != CCONV_DTYPE_BF16) return CCONV_ERR_INVALID;
+  *esize = dtype == CCONV_DTYPE_F32 ? 4 : 2;
+  *V = 16 / *esize;
+  if (!w || !pv.p || !state_idx) return CCONV_ERR_INVALID;
+  if (rows > 0 && (!x || !out)) return CCONV_ERR_INVALID;
+  if (C <= 0 || C % *V != 0) return CCONV_ERR_INVALID;
+  if (width < 1 || dilation < 1) return CCONV_ERR_INVALID;
+  if (width < 2 || width > 4 || dilation > 4) return CCONV_ERR_UNSUPPORTED;
+  if (act != CCONV_ACT_NONE && act != CCONV_ACT_SILU) return CCONV_ERR_INVALID;
+  if (!aligned16(x) || !aligned16(out)) return CCONV_ERR_INVALID;
+  if (x_rs < C || out_rs < C || x_rs % *V != 0 || out_rs % *V != 0) return CCONV_ERR_INVALID;
+  if (pv.num_slots <= 0 || pv.cap <= 0 || pv.cap > 96) return CCONV_ERR_INVALID;
+  if (pv.s_slot <= 0 || pv.s_chan <= 0 || pv.s_col <= 0) return CCONV_ERR_INVALID;
+  return CCONV_OK;
+}
+
+template <typename T>
+static cudaError_t launch_fwd(int W, int D, dim3 grid, int nt, size_t smem,
+                              cudaStream_t st, const FwdArgs& a) {
+#define CCONV_FWD_CASE(w_, d_)                                              \
+  if (W == w_ && D == d_) {                                                 \
+    fwd_varlen_kernel<T, w_, d_><<<grid, nt, smem, st>>>(a);                \
+    return cudaGetLastError();                                              \
+  }
+  CCONV_FWD_CASE(2, 1) CCONV_FWD_CASE(2, 2) CCONV_FWD_CASE(2, 3) CCONV_FWD_CASE(2, 4)
+  CCONV_FWD_CASE(3, 1) CCONV_FWD_CASE(3, 2) CCONV_FWD_CASE(3, 3) CCONV_FWD_CASE(3, 4)
+  CCONV_FWD_CASE(4, 1) CCONV_FWD_CASE(4, 2) CCONV_FWD_CASE(4, 3) CCONV_FWD_CASE(4, 4)
+#undef CCONV_FWD_CASE
+  return cudaErrorInvalidValue;
+}
+
+template <typename T>
+static cudaError_t launch_upd(int W, int D, dim3 grid, int nt, size_t smem,
+                              cudaStream_t st, const UpdArgs& a) {
+#define CCONV_UPD_CASE(w_, d_)                                              \
+  if (W == w_ && D == d_) {                                                 \
+    update_kernel<T, w_, d_><<<grid, nt, smem, st>>>(a);                    \
+    return cudaGetLastError();                                              \
+  }
+  CCONV_UPD_CASE(2, 1) CCONV_UPD_CASE(2, 2) CCONV_UPD_CASE(2, 3) CCONV_UPD_CASE(2, 4)
+  CCONV_UPD_CASE(3, 1) CCONV_UPD_CASE(3, 2) CCONV_UPD_CASE(3, 3) CCONV_UPD_CASE(3, 4)
+  CCONV_UPD_CASE(4, 1) CCONV_UPD_CASE(4, 2) CCONV_UPD_CASE(4, 3) CCONV_UPD_CASE(4, 4)
+#undef CCONV_UPD_CASE
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace cconv
+
+using namespace cconv;
+
+extern "C" int cconv_fwd_varlen(const void* x, int64_t x_row_stride, const void* w,
+                                const void* bias, cconv_pool_t conv_states,
+                                const int32_t* state_idx, const int32_t* cu_seqlens,
+                                const uint8_t* has_init, int32_t num_seqs, int32_t num_tokens,
+                                int32_t C, int32_t width, int32_t dilation, int32_t act,
+                                int32_t dtype, void* out, int64_t out_row_stride,
+                                int32_t* dev_err, cconv_stream_t stream) {
+  int esize = 0, V = 0;
+  int rc = check_common(x, x_row_stride, w, conv_states, state_idx, C, width, dilation, act,
+                        dtype, out, out_row_stride, num_tokens, &esize, &V);
+  if (rc != CCONV_OK) return rc;
+  if (!cu_seqlens || num_seqs < 0 || num_tokens < 0) return CCONV_ERR_INVALID;
+  const int S = (width - 1) * dilation;
+  if (conv_states.cap < S) return CCONV_ERR_INVALID;
+  if (num_seqs == 0) return CCONV_OK;
+  FwdArgs a;
+  a.x = static_cast<const char*>(x);
+  a.x_rs = x_row_stride;
+  a.w = static_cast<const char*>(w);
+  a.bias = static_cast<const char*>(bias);
+  a.pool = make_pool(conv_states, esize, V);
+  a.state_idx = state_idx;
+  a.cu = cu_seqlens;
+  a.has_init = has_init;
+  a.B = num_seqs;
+  a.T = num_tokens;
+  a.C = C;
+  a.act = act;
+  a.out = static_cast<char*>(out);
+  a.out_rs = out_row_stride;
+  a.dev_err = dev_err;
+  const int units = C / V;
+  const int nt = pick_threads(units, conv_states.cap);
+  const int ctiles = (units + nt - 1) / nt;
+  const int64_t nblk = (int64_t)num_tokens / kChunk + num_seqs + 1;
+  if (nblk > 0x7fffffff || ctiles > 65535) return CCONV_ERR_INVALID;
+  const dim3 grid((unsigned)nblk, (unsigned)ctiles);
+  const size_t smem = (size_t)nt * conv_states.cap * 16;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = dtype == CCONV_DTYPE_F32
+                      ? launch_fwd<float>(width, dilation, grid, nt, smem, st, a)
+                      : launch_fwd<__nv_bfloat16>(width, dilation, grid, nt, smem, st, a);
+  return e == cudaSuccess ? CCONV_OK : CCONV_ERR_LAUNCH;
+}
+
+extern "C" int cconv_update(const void* x, int64_t x_row_stride, cconv_pool_t conv_states,
+                            const void* w, const void* bias, const int32_t* state_idx,
+                            int32_t num_seqs, int32_t n_spec, const int32_t* num_accepted,
+                            const uint8_t* has_init, int32_t C, int32_t width,
+                            int32_t dilation, int32_t act, int32_t dtype, void* out,
+                            int64_t out_row_stride, int32_t* dev_err, cconv_stream_t stream) {
+  int esize = 0, V = 0;
+  int rc = check_common(x, x_row_stride, w, conv_states, state_idx, C, width, dilation, act,
+                        dtype, out, out_row_stride, (int64_t)num_seqs * (1 + n_spec), &esize,
+                        &V);
+  if (rc != CCONV_OK) return rc;
+  if (num_seqs < 0 || n_spec < 0) return CCONV_ERR_INVALID;
+  if (n_spec > kMaxSpec) return CCONV_ERR_UNSUPPORTED;
+  if (n_spec > 0 && !num_accepted) return CCONV_ERR_INVALID;
+  const int S = (width - 1) * dilation;
+  if (conv_states.cap < S + n_spec) return CCONV_ERR_INVALID;
+  if (num_seqs == 0) return CCONV_OK;
+  UpdArgs a;
+  a.x = static_cast<const char*>(x);
+  a.x_rs = x_row_stride;
+  a.pool = make_pool(conv_states, esize, V);
+  a.w = static_cast<const char*>(w);
+  a.bias = static_cast<const char*>(bias);
+  a.state_idx = state_idx;
+  a.B = num_seqs;
+  a.n_spec = n_spec;
+  a.num_accepted = num_accepted;
+  a.has_init = has_init;
+  a.C = C;
+  a.act = act;
+  a.out = static_cast<char*>(out);
+  a.out_rs = out_row_stride;
+  a.dev_err = dev_err;
+  const int units = C / V;
+  const int nt = pick_threads(units, conv_states.cap);
+  a.ctiles = (units + nt - 1) / nt;
+  const int64_t nblk = (int64_t)num_seqs * a.ctiles;
+  if (nblk > 0x7fffffff) return CCONV_ERR_INVALID;
+  const size_t smem = (size_t)nt * conv_states.cap * 16;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const dim3 grid((unsigned)nblk);
+  cudaError_t e = dtype == CCONV_DTYPE_F32
+                      ? launch_upd<float>(width, dilation, grid, nt, smem, st, a)
+                      : launch_upd<__nv_bfloat16>(width, dilation, grid, nt, smem, st, a);
+  return e == cudaSuccess ? CCONV_OK : CCONV_ERR_LAUNCH;
+}

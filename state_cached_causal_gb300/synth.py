@@ -137,7 +137,7 @@ def depthwise_case(seed, device, *, lens, C, width, dilation, act, dtype, w_std,
     """Generic varlen (+ optional spec) case.
 
     ``lens``: lengths of the varlen sequences (the first ``decode_prefix`` of
-    them are decodes that always continue from their state). ``has_init``:
+    them are one-token decodes whose history is always their slot). ``has_init``:
     "bernoulli" (p = 0.5 for non-decodes), "all", "none". ``spec_requests``
     speculative requests with q = 1 + n_spec tokens each use slots disjoint
     from the varlen sequences. ``padding_every`` > 0 marks every k-th varlen

@@ -1,0 +1,118 @@
+"""The C ABI library: it loads, exports every symbol include/cconv.h declares,
+and validates arguments on the host. No compute call reaches a GPU here: the
+checked calls are rejected before any launch, and the one valid call is made
+only where no CUDA device exists, to show that it fails loudly instead of
+falling back to anything."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+from state_cached_causal_gb300 import build as cbuild
+from state_cached_causal_gb300 import ops
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "cconv.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    cbuild.build()
+    return ops.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    names = re.findall(r"^\s*(?:const\s+)?\w+\s*\**\s*(\w+)\s*\(", text, flags=re.M)
+    return sorted(set(n for n in names if n not in ("if", "while", "for")))
+
+
+def test_header_declares_the_three_operations():
+    names = declared_functions()
+    for n in ("cconv_fwd_varlen", "cconv_update", "cca_qk_conv", "cconv_status_string",
+              "cconv_abi_version"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for n in declared_functions():
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    assert ops.status_string(0) == "ok"
+    for s in (-1, -2, -3):
+        assert ops.status_string(s) not in ("ok", "unknown status")
+    assert ops.status_string(17) == "unknown status"
+    assert ops.abi_version() == 1
+
+
+FAKE = 0x10000  # 16-byte aligned, never dereferenced: every call below fails validation
+
+# Calls with fake pointers run only where no CUDA device exists, so that a
+# validation bug can never launch a kernel on a fake address.
+no_gpu = pytest.mark.skipif(torch.cuda.is_available(), reason="fake pointers: CPU-only")
+
+
+def _pool(num_slots=4, C=16, cap=3, layout="DS"):
+    if layout == "DS":
+        return ops.Pool(ctypes.c_void_p(FAKE), C * cap, cap, 1, num_slots, cap)
+    return ops.Pool(ctypes.c_void_p(FAKE), C * cap, 1, C, num_slots, cap)
+
+
+def fwd(lib, **kw):
+    a = dict(x=FAKE, xrs=16, w=FAKE, bias=None, pool=_pool(), sidx=FAKE, cu=FAKE, hi=None,
+             B=2, T=8, C=16, W=4, D=1, act=1, dt=1, out=FAKE, ors=16)
+    a.update(kw)
+    P = lambda v: None if v is None else ctypes.c_void_p(v)
+    return lib.cconv_fwd_varlen(P(a["x"]), a["xrs"], P(a["w"]), P(a["bias"]), a["pool"],
+                                P(a["sidx"]), P(a["cu"]), P(a["hi"]), a["B"], a["T"], a["C"],
+                                a["W"], a["D"], a["act"], a["dt"], P(a["out"]), a["ors"], None,
+                                None)
+
+
+def upd(lib, **kw):
+    a = dict(x=FAKE, xrs=16, pool=_pool(cap=6), w=FAKE, bias=None, sidx=FAKE, B=2, ns=3,
+             na=FAKE, hi=None, C=16, W=4, D=1, act=1, dt=1, out=FAKE, ors=16)
+    a.update(kw)
+    P = lambda v: None if v is None else ctypes.c_void_p(v)
+    return lib.cconv_update(P(a["x"]), a["xrs"], a["pool"], P(a["w"]), P(a["bias"]),
+                            P(a["sidx"]), a["B"], a["ns"], P(a["na"]), P(a["hi"]), a["C"],
+                            a["W"], a["D"], a["act"], a["dt"], P(a["out"]), a["ors"], None, None)
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(x=None), -1), (dict(x=None, out=None, T=0), -3), (dict(w=None), -1), (dict(out=None), -1), (dict(sidx=None), -1),
+    (dict(cu=None), -1), (dict(C=12), -1), (dict(C=0), -1), (dict(x=FAKE + 2), -1),
+    (dict(out=FAKE + 8), -1), (dict(xrs=8), -1), (dict(ors=20), -1), (dict(dt=5), -1),
+    (dict(act=7), -1), (dict(W=0), -1), (dict(W=5), -2), (dict(D=5), -2), (dict(D=0), -1),
+    (dict(pool=_pool(cap=2)), -1), (dict(B=-1), -1), (dict(T=-1), -1),
+    (dict(pool=_pool(num_slots=0)), -1)])
+@no_gpu
+def test_fwd_varlen_rejects_bad_arguments(lib, kw, want):
+    assert fwd(lib, **kw) == want
+
+
+@no_gpu
+def test_fwd_varlen_empty_batch_is_a_noop(lib):
+    assert fwd(lib, B=0) == 0
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(na=None), -1), (dict(ns=8), -2), (dict(ns=-1), -1),
+    (dict(pool=_pool(cap=5)), -1), (dict(C=4, dt=1), -1), (dict(x=None), -1),
+    (dict(W=5), -2)])
+@no_gpu
+def test_update_rejects_bad_arguments(lib, kw, want):
+    assert upd(lib, **kw) == want
+
+
+@no_gpu
+def test_valid_call_without_gpu_fails_loudly(lib):
+    # A valid request on a machine with no CUDA device must report a launch
+    # failure, never compute anything on the host.
+    assert fwd(lib, C=16) == -3
