@@ -747,8 +747,8 @@ extern "C" int cca_qk_conv(const void* qk, int64_t qk_row_stride, const void* w_
                            int64_t out_delayed_prev_row_stride, int32_t* dev_err,
                            cconv_stream_t stream) {
   if (dtype != CCONV_DTYPE_BF16 && dtype != CCONV_DTYPE_F32) return CCONV_ERR_INVALID;
-  if (!w_dw || !w_gr || !delayed_init || !conv_state.p || !delayed_state || !state_idx ||
-      !cu_seqlens)
+  if (!w_dw || !w_gr || !delayed_init || !conv_state.p || !delayed_state ||
+      (num_seqs > 0 && (!state_idx || !cu_seqlens)))
     return CCONV_ERR_INVALID;
   if (num_tokens > 0 && (!qk || !delayed || !out_qk || !out_delayed_prev))
     return CCONV_ERR_INVALID;

@@ -311,13 +311,13 @@ static int pick_threads(int units, int cap) {
 // `rows` is the number of activation rows the call covers; x and out may be
 // NULL only when it is zero (an empty tensor has no storage).
 static int check_common(const void* x, int64_t x_rs, const void* w, const cconv_pool_t& pv,
-                        const int32_t* state_idx, int32_t C, int32_t width, int32_t dilation,
-                        int32_t act, int32_t dtype, const void* out, int64_t out_rs,
-                        int64_t rows, int* esize, int* V) {
+                        const int32_t* state_idx, int32_t num_seqs, int32_t C, int32_t width,
+                        int32_t dilation, int32_t act, int32_t dtype, const void* out,
+                        int64_t out_rs, int64_t rows, int* esize, int* V) {
   if (dtype != CCONV_DTYPE_F32 && dtype != CCONV_DTYPE_BF16) return CCONV_ERR_INVALID;
   *esize = dtype == CCONV_DTYPE_F32 ? 4 : 2;
   *V = 16 / *esize;
-  if (!w || !pv.p || !state_idx) return CCONV_ERR_INVALID;
+  if (!w || !pv.p || (num_seqs > 0 && !state_idx)) return CCONV_ERR_INVALID;
   if (rows > 0 && (!x || !out)) return CCONV_ERR_INVALID;
   if (C <= 0 || C % *V != 0) return CCONV_ERR_INVALID;
   if (width < 1 || dilation < 1) return CCONV_ERR_INVALID;
@@ -372,10 +372,10 @@ extern "C" int cconv_fwd_varlen(const void* x, int64_t x_row_stride, const void*
                                 int32_t dtype, void* out, int64_t out_row_stride,
                                 int32_t* dev_err, cconv_stream_t stream) {
   int esize = 0, V = 0;
-  int rc = check_common(x, x_row_stride, w, conv_states, state_idx, C, width, dilation, act,
-                        dtype, out, out_row_stride, num_tokens, &esize, &V);
+  int rc = check_common(x, x_row_stride, w, conv_states, state_idx, num_seqs, C, width,
+                        dilation, act, dtype, out, out_row_stride, num_tokens, &esize, &V);
   if (rc != CCONV_OK) return rc;
-  if (!cu_seqlens || num_seqs < 0 || num_tokens < 0) return CCONV_ERR_INVALID;
+  if ((num_seqs > 0 && !cu_seqlens) || num_seqs < 0 || num_tokens < 0) return CCONV_ERR_INVALID;
   const int S = (width - 1) * dilation;
   if (conv_states.cap < S) return CCONV_ERR_INVALID;
   if (num_seqs == 0) return CCONV_OK;
@@ -416,13 +416,13 @@ extern "C" int cconv_update(const void* x, int64_t x_row_stride, cconv_pool_t co
                             int32_t dilation, int32_t act, int32_t dtype, void* out,
                             int64_t out_row_stride, int32_t* dev_err, cconv_stream_t stream) {
   int esize = 0, V = 0;
-  int rc = check_common(x, x_row_stride, w, conv_states, state_idx, C, width, dilation, act,
-                        dtype, out, out_row_stride, (int64_t)num_seqs * (1 + n_spec), &esize,
-                        &V);
+  int rc = check_common(x, x_row_stride, w, conv_states, state_idx, num_seqs, C, width,
+                        dilation, act, dtype, out, out_row_stride,
+                        (int64_t)num_seqs * (1 + n_spec), &esize, &V);
   if (rc != CCONV_OK) return rc;
   if (num_seqs < 0 || n_spec < 0) return CCONV_ERR_INVALID;
   if (n_spec > kMaxSpec) return CCONV_ERR_UNSUPPORTED;
-  if (n_spec > 0 && !num_accepted) return CCONV_ERR_INVALID;
+  if (n_spec > 0 && num_seqs > 0 && !num_accepted) return CCONV_ERR_INVALID;
   const int S = (width - 1) * dilation;
   if (conv_states.cap < S + n_spec) return CCONV_ERR_INVALID;
   if (num_seqs == 0) return CCONV_OK;
