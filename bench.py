@@ -1,0 +1,527 @@
+#!/usr/bin/env python
+"""Benchmark of the state-cached causal short convolution on GB300.
+
+One step = one pass of the whole hot path over one batch of each serving
+shape, all through the C ABI of libcconv.so:
+  gdn_decode  64 requests x 1 token x 8192 channels        (cconv_update)
+  gdn_mixed   128 decodes + 16 prefills (seeded), 8192 ch   (cconv_fwd_varlen)
+  zaya_cca    256 decodes + 8 x 4096 prefill, 2560 q/k ch   (cca_qk_conv)
+  ple_spec    32 x 2048 prefill + 512 x 4 spec, 16384 ch    (cconv_fwd_varlen
+              and cconv_update with 3 speculative tokens)
+Every input is seeded and synthetic and resident in HBM before timing; the
+step moves about 5.7 GB, far more than the 129 MB L2, so no flush is needed.
+`value` is tokens*channels processed per second (whole job), `e2e` the same
+metric with the inputs copied from pinned host memory and the outputs copied
+back inside the timed region. `roofline` reports the dominant kernel's
+achieved HBM bandwidth (algorithmic bytes / CUDA-event duration) against the
+measured copy bandwidth. `cpu_baseline` times the plain-C oracle on a bounded
+channel/request sample of the same step on the host cores.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload hybrid_step|ple_prefill_small|cca_small|...]
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = ("causal-conv G(tokens·channels)/s and achieved HBM GB/s vs GB300 peak, 1 GPU")
+UNIT = "G(tokens*channels)/s"
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ---- workloads ---------------------------------------------------------------
+
+class Call:
+    """One launch of the hot path with its algorithmic byte/flop counts."""
+
+    def __init__(self, name, kernel, fn, units, nbytes, flops=0.0, h2d=None, d2h=None):
+        self.name, self.kernel, self.fn = name, kernel, fn
+        self.units, self.bytes, self.flops = units, nbytes, flops
+        self.h2d = h2d or []     # (device tensor, pinned host tensor): inputs
+        self.d2h = d2h or []     # (device tensor, pinned host tensor): outputs
+
+
+def _e(t):
+    return t.element_size()
+
+
+def depthwise_calls(name, case, dev_err):
+    from state_cached_causal_gb300 import ops
+    calls = []
+    e, C, W, S = _e(case.w), case.C, case.width, case.meta["S"]
+    wbytes = C * W * e + (C * e if case.bias is not None else 0)
+    if case.x is not None:
+        out = torch.empty_like(case.x)
+        hi = case.has_init.to(torch.int64).cpu()
+        valid = (case.state_idx.cpu() >= 0).to(torch.int64)
+        nread = int((hi * valid).sum())
+        nwrite = int(valid.sum())
+        T = case.num_tokens
+        nbytes = 2 * T * C * e + wbytes + C * e * S * (nread + nwrite)
+
+        def f(case=case, out=out):
+            ops.cconv_fwd_varlen(case.x, case.w, case.bias, case.pool, case.state_idx,
+                                 case.cu_seqlens, case.has_init, case.width, case.dilation,
+                                 case.act, out, dev_err=dev_err)
+        calls.append(Call(f"{name}.fwd_varlen", "cconv_fwd_varlen", f, T * C, nbytes,
+                          h2d=[case.x], d2h=[out]))
+    if case.x_spec is not None:
+        out = torch.empty_like(case.x_spec)
+        R = int(case.spec_state_idx.numel())
+        q = 1 + case.n_spec
+        cols_w = case.meta["cap"] if case.n_spec else S
+        nbytes = 2 * R * q * C * e + wbytes + R * C * e * (S + cols_w)
+        na = case.num_accepted if case.n_spec else None
+
+        def g(case=case, out=out, na=na):
+            ops.cconv_update(case.x_spec, case.pool, case.w, case.bias, case.spec_state_idx,
+                             case.n_spec, na, case.spec_has_init, case.width, case.dilation,
+                             case.act, out, dev_err=dev_err)
+        calls.append(Call(f"{name}.update", "cconv_update", g, R * q * C, nbytes,
+                          h2d=[case.x_spec], d2h=[out]))
+    return calls
+
+
+def cca_calls(name, cc, dev_err):
+    from state_cached_causal_gb300 import ops
+    out = torch.empty_like(cc.qk)
+    dprev = torch.empty_like(cc.delayed)
+    e, T, Cqk, Dv, n = _e(cc.qk), int(cc.qk.shape[0]), cc.Cqk, cc.Dv, cc.meta["n"]
+    hi = cc.has_init.to(torch.int64).cpu()
+    valid = (cc.state_idx.cpu() >= 0).to(torch.int64)
+    nread, nwrite = int((hi * valid).sum()), int(valid.sum())
+    wbytes = sum(_e(t) * t.numel() for t in (cc.w_dw, cc.b_dw, cc.w_gr, cc.b_gr)
+                 if t is not None)
+    nbytes = (2 * T * Cqk * e + 2 * T * Dv * e + wbytes + Dv * e
+              + (nread + nwrite) * (n * Cqk * e + Dv * e))
+    flops = 2.0 * T * Cqk * (Cqk // cc.groups) * cc.t1 + 2.0 * (T + 1) * Cqk * cc.t0
+
+    def f(cc=cc, out=out, dprev=dprev):
+        ops.cca_qk_conv(cc.qk, cc.w_dw, cc.b_dw, cc.w_gr, cc.b_gr, cc.groups, cc.t0, cc.t1,
+                        cc.delayed, cc.delayed_init, cc.pool, cc.delayed_state, cc.state_idx,
+                        cc.cu_seqlens, cc.has_init, out, dprev, dev_err=dev_err)
+    return [Call(f"{name}.cca_qk_conv", "cca_qk_conv", f, T * Cqk, nbytes, flops,
+                 h2d=[cc.qk, cc.delayed], d2h=[out, dprev])]
+
+
+def build_workload(name, dev, dev_err):
+    from state_cached_causal_gb300 import synth
+    if name == "hybrid_step":
+        calls = []
+        calls += depthwise_calls("gdn_decode", synth.gdn_decode(dev), dev_err)
+        calls += depthwise_calls("gdn_mixed", synth.gdn_mixed(dev), dev_err)
+        calls += cca_calls("zaya_cca", synth.zaya_cca(dev), dev_err)
+        calls += depthwise_calls("ple_spec", synth.ple_spec(dev), dev_err)
+        desc = ("hybrid_step: gdn_decode 64x1 tok x 8192 ch (cconv_update) + gdn_mixed "
+                "128 decodes + 16 prefills U[1,2048] x 8192 ch (cconv_fwd_varlen) + "
+                "zaya_cca 256 decodes + 8x4096 prefill, 20 groups x 128 ch, t0=t1=2 "
+                "(cca_qk_conv) + ple_spec 32x2048 prefill + 512x(1+3) spec x 16384 ch, "
+                "width 4 dilation 3 (cconv_fwd_varlen + cconv_update)")
+        return calls, desc
+    # small single-kernel cases for profiling (a few GB at most, > L2)
+    if name == "ple_prefill_small":
+        case = synth.depthwise_case(2001, dev, lens=[2048] * 8, C=16384, width=4, dilation=3,
+                                    act=1, dtype=torch.bfloat16, w_std=0.1, num_slots=64)
+        return depthwise_calls("ple_prefill_small", case, dev_err), \
+            "ple prefill 8x2048 tok x 16384 ch, width 4 dilation 3"
+    if name == "ple_spec_small":
+        case = synth.depthwise_case(2002, dev, lens=[], C=16384, width=4, dilation=3, act=1,
+                                    dtype=torch.bfloat16, w_std=0.1, num_slots=1024,
+                                    spec_requests=512, n_spec=3)
+        return depthwise_calls("ple_spec_small", case, dev_err), \
+            "ple spec 512x(1+3) tok x 16384 ch"
+    if name == "gdn_mixed":
+        return depthwise_calls("gdn_mixed", synth.gdn_mixed(dev), dev_err), "gdn_mixed"
+    if name == "gdn_decode":
+        return depthwise_calls("gdn_decode", synth.gdn_decode(dev), dev_err), "gdn_decode"
+    if name == "cca_small":
+        cc = synth.cca_case(2003, dev, lens=[1] * 256 + [4096] * 2, decode_prefix=256,
+                            num_slots=512)
+        return cca_calls("cca_small", cc, dev_err), "zaya cca 256 decodes + 2x4096"
+    if name == "zaya_cca":
+        return cca_calls("zaya_cca", synth.zaya_cca(dev), dev_err), "zaya_cca"
+    raise SystemExit(f"unknown workload {name}")
+
+
+# ---- measurement helpers -----------------------------------------------------
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d.get("bf16_tflops", 1900.0)), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, 1900.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples while the timed region runs."""
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index, self.proc, self.lines = index, None, []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx.append(float(f[1]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[4:8]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "state_cached_causal_gb300", "csrc")
+    for f in sorted(os.listdir(d)):
+        with open(os.path.join(d, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel):
+    """DRAM bytes per launch from a committed ncu summary, if it still matches the code."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        rec = d[kernel]
+        if rec.get("source_hash") != kernel_source_hash():
+            return None
+        return float(rec["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+# ---- CPU oracle sample ---------------------------------------------------------
+
+def cpu_sample(dev, light=False):
+    """Bounded sample of the hybrid step for the oracle: channel / request subsets."""
+    import numpy as np
+    from state_cached_causal_gb300 import synth
+    from oracle.torch_io import pool_np, to_np
+    import oracle
+    jobs = []
+
+    def dw(name, case, chans):
+        sl = slice(0, chans)
+        w = np.ascontiguousarray(to_np(case.w)[sl])
+        b = None if case.bias is None else np.ascontiguousarray(to_np(case.bias)[sl])
+        pool = pool_np(case.pool[:, sl, :].contiguous())
+        if case.x is not None:
+            x = np.ascontiguousarray(to_np(case.x[:, sl].contiguous()))
+            args = (to_np(case.state_idx), to_np(case.cu_seqlens), to_np(case.has_init))
+
+            def run(x=x, w=w, b=b, pool=pool, args=args, case=case):
+                oracle.cconv_fwd_varlen(x, w, b, pool.copy(), *args, case.width, case.dilation,
+                                        case.act, np.zeros_like(x))
+            jobs.append((f"{name}.fwd_varlen", run, x.shape[0] * chans))
+        if case.x_spec is not None:
+            xs = np.ascontiguousarray(to_np(case.x_spec[:, sl].contiguous()))
+            na = to_np(case.num_accepted) if case.n_spec else None
+
+            def run2(xs=xs, w=w, b=b, pool=pool, case=case, na=na):
+                oracle.cconv_update(xs, pool.copy(), w, b, to_np(case.spec_state_idx),
+                                    case.n_spec, na, None, case.width, case.dilation, case.act,
+                                    np.zeros_like(xs))
+            jobs.append((f"{name}.update", run2, xs.shape[0] * chans))
+
+    dw("gdn_decode", synth.gdn_decode(dev), 256 if not light else 64)
+    dw("gdn_mixed", synth.gdn_mixed(dev), 32 if not light else 8)
+    cc = synth.zaya_cca(dev)
+    nreq = 257   # the 256 decodes and the first 4096-token prefill
+    T = int(cc.cu_seqlens[nreq].item())
+    sl = slice(0, 128)
+    qk = np.ascontiguousarray(to_np(cc.qk[:T, sl].contiguous()))
+    dl = np.ascontiguousarray(to_np(cc.delayed[:T].contiguous()))
+    args = dict(w_dw=np.ascontiguousarray(to_np(cc.w_dw)[sl]),
+                b_dw=np.ascontiguousarray(to_np(cc.b_dw)[sl]),
+                w_gr=np.ascontiguousarray(to_np(cc.w_gr)[sl]),
+                b_gr=np.ascontiguousarray(to_np(cc.b_gr)[sl]))
+    pool = pool_np(cc.pool[:, sl, :].contiguous())
+    ds = to_np(cc.delayed_state).copy()
+    meta = (to_np(cc.state_idx[:nreq]), to_np(cc.cu_seqlens[:nreq + 1]),
+            to_np(cc.has_init[:nreq]))
+
+    def run3():
+        oracle.cca_qk_conv(qk, args["w_dw"], args["b_dw"], args["w_gr"], args["b_gr"], 1, 2, 2,
+                           dl, to_np(cc.delayed_init), pool.copy(), ds.copy(), *meta,
+                           np.zeros_like(qk), np.zeros_like(dl))
+    jobs.append(("zaya_cca.cca_qk_conv", run3, T * 128))
+    dw("ple_spec", synth.ple_spec(dev), 32 if not light else 8)
+    units = sum(j[2] for j in jobs)
+    desc = ("oracle (1 thread) on: gdn_decode 256 ch, gdn_mixed 32 ch, zaya_cca 1 group x "
+            f"{nreq} requests ({T} tokens), ple_spec 32 ch; all tokens of the sampled "
+            f"requests; {units} tokens*channels")
+    if light:
+        desc = desc.replace("256 ch", "64 ch").replace("32 ch", "8 ch")
+    return jobs, units, desc
+
+
+def run_cpu_sample(jobs):
+    t0 = time.perf_counter()
+    for _, fn, _ in jobs:
+        fn()
+    return time.perf_counter() - t0
+
+
+# ---- arms ----------------------------------------------------------------------
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def reduce_max(value, ws):
+    if ws <= 1:
+        return value
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64,
+                     device="cuda" if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def arm_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    dev = torch.device("cuda" if torch.cuda.is_available() else "cpu")
+    jobs, units, desc = cpu_sample(dev, light=True)
+    for _ in range(args.warmup):
+        run_cpu_sample(jobs)
+    times = [run_cpu_sample(jobs) for _ in range(args.steps)]
+    total = sum(times)
+    value = units * args.steps / total / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32-accumulate bf16",
+        "data": "synthetic",
+        "config": {"workload": "hybrid_step (oracle sample)", "sample": desc,
+                   "parallelism": "host, 1 thread"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def arm_ours(args):
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if ws > 1 else 0)
+    torch.cuda.set_device(dev)
+    from state_cached_causal_gb300 import ops
+    ops.load()
+    dev_err = torch.zeros(1, dtype=torch.int32, device=dev)
+    calls, desc = build_workload(args.workload, dev, dev_err)
+    stream = torch.cuda.current_stream(dev)
+    units_per_step = sum(c.units for c in calls)
+    bytes_per_step = sum(c.bytes for c in calls)
+
+    def step():
+        for c in calls:
+            c.fn()
+
+    for _ in range(max(args.warmup, 0)):
+        step()
+    torch.cuda.synchronize()
+    if int(dev_err.item()) != 0:
+        raise SystemExit(f"device error flag {int(dev_err.item())} during warm-up")
+
+    # timed region: K steps, events per launch on the launching stream
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in calls] for _ in range(args.steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index) as clk:
+        start.record(stream)
+        for k in range(args.steps):
+            for c, (a, b) in zip(calls, ev[k]):
+                a.record(stream)
+                c.fn()
+                b.record(stream)
+        stop.record(stream)
+        torch.cuda.synchronize()
+    if ws > 1:
+        dist.barrier()
+    elapsed = start.elapsed_time(stop) / 1e3
+    elapsed = reduce_max(elapsed, ws)
+    per_call = {c.name: sum(ev[k][i][0].elapsed_time(ev[k][i][1]) for k in range(args.steps))
+                / args.steps / 1e3 for i, c in enumerate(calls)}
+    if int(dev_err.item()) != 0:
+        raise SystemExit(f"device error flag {int(dev_err.item())} in the timed region")
+
+    value = ws * units_per_step * args.steps / elapsed / 1e9
+    hbm_peak, bf16_peak, peak_src = measured_peaks()
+    dom = max(calls, key=lambda c: per_call[c.name])
+    t_dom = per_call[dom.name]
+    achieved = dom.bytes / t_dom / 1e9
+    traffic = recorded_traffic(dom.kernel)
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                "frac": achieved / hbm_peak, "traffic": traffic, "kernel": dom.name,
+                "algorithmic_bytes": dom.bytes, "ms_per_launch": t_dom * 1e3,
+                "peak_source": f"{peak_src} hbm_gbs"}
+    breakdown = {}
+    for c in calls:
+        t = per_call[c.name]
+        d = {"ms": t * 1e3, "Gtokch_per_s": c.units / t / 1e9, "GB_per_s": c.bytes / t / 1e9,
+             "hbm_frac": c.bytes / t / 1e9 / hbm_peak, "bytes": c.bytes}
+        if c.flops:
+            d["TFLOP_per_s"] = c.flops / t / 1e12
+            d["tensor_frac_of_bf16_peak"] = c.flops / t / 1e12 / bf16_peak
+        breakdown[c.name] = d
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * elapsed / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": desc, "l2": "inputs larger than L2 each step "
+                   f"({bytes_per_step / 1e9:.2f} GB algorithmic), no flush",
+                   "parallelism": "replicas" if ws > 1 else "1 GPU"},
+        "hbm_GBps": bytes_per_step * args.steps / elapsed / 1e9,
+        "gpu_launches": len(calls) * args.steps,
+        "roofline": roofline,
+        "clocks": clk.summary(),
+        "per_call": breakdown,
+    }
+
+    if not args.no_e2e:
+        line["e2e"] = e2e_run(args, calls, stream, dev, ws)
+    if rank == 0 and not args.no_cpu_baseline and ws == 1:
+        jobs, units, sdesc = cpu_sample(dev)
+        run_cpu_sample(jobs)
+        ts = [run_cpu_sample(jobs) for _ in range(2)]
+        t = min(ts)
+        line["cpu_baseline"] = {"value": units / t / 1e9, "unit": UNIT, "cores": 1,
+                                "kind": "oracle", "sample": sdesc,
+                                "seconds_per_sample": t}
+    if rank == 0:
+        print(json.dumps(line))
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def e2e_run(args, calls, stream, dev, ws):
+    """Same step through the C ABI with the inputs copied in from pinned host
+    memory and the outputs copied out, all inside the timed region."""
+    pairs_in, pairs_out = [], []
+    for c in calls:
+        for t in c.h2d:
+            pairs_in.append((t, torch.empty(t.shape, dtype=t.dtype, pin_memory=True)))
+        for t in c.d2h:
+            pairs_out.append((t, torch.empty(t.shape, dtype=t.dtype, pin_memory=True)))
+    for d, h in pairs_in:
+        h.copy_(d)
+    h2d = sum(d.numel() * d.element_size() for d, _ in pairs_in)
+    d2h = sum(d.numel() * d.element_size() for d, _ in pairs_out)
+    steps = max(3, min(args.steps, 20))
+
+    def step():
+        for d, h in pairs_in:
+            d.copy_(h, non_blocking=True)
+        for c in calls:
+            c.fn()
+        for d, h in pairs_out:
+            h.copy_(d, non_blocking=True)
+
+    step()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    el = reduce_max(a.elapsed_time(b) / 1e3, ws)
+    units = sum(c.units for c in calls)
+    return {"value": ws * units * steps / el / 1e9, "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": steps}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="hybrid_step")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 0 or args.steps < 1:
+        raise SystemExit("--steps >= 1 and --warmup >= 0")
+    if args.impl == "reference":
+        return arm_reference(args)
+    return arm_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

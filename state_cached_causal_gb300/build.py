@@ -56,6 +56,12 @@ def _compile(nvcc, src, extra_flags, verbose):
     obj = os.path.join(BUILD, f"{name}.{_digest(src, extra_flags)}.o")
     if os.path.exists(obj):
         return obj
+    for f in os.listdir(BUILD):   # objects of older versions of this source
+        if f.startswith(name + ".") and f.endswith(".o"):
+            try:
+                os.remove(os.path.join(BUILD, f))
+            except OSError:
+                pass
     tmp = obj + f".{os.getpid()}.tmp"
     cmd = [nvcc] + CFLAGS + extra_flags + ["-c", src, "-o", tmp]
     r = subprocess.run(cmd, capture_output=True, text=True)

@@ -59,6 +59,7 @@ constexpr int kAccCols = 128;                          // fp32 accumulator colum
 constexpr int kTmemCols = 2 * kAccCols;
 constexpr long long kWaitCycles = 2000000000LL;        // ~1 s at GB300 clocks
 constexpr int kDerrTimeout = CCONV_DERR_TIMEOUT;
+constexpr int kStageReqs = 1536;                       // index data staged in smem up to this
 
 struct Meta {
   int lo, len, g, own_lo, own_hi, pad0, pad1, pad2;
@@ -85,6 +86,7 @@ struct Args {
   const uint8_t* has_init;
   int32_t B, T, Cqk, G, n;
   int32_t num_tiles, tile_pitch, units, units_per_cta;
+  int32_t staged;                                      // index data copied to smem
   char* out;
   int64_t out_rs;
   char* dprev;
@@ -265,14 +267,14 @@ __device__ __forceinline__ void hist_store(const Pool& P, int slot, int c0, int 
 // Number of requests s in [0, B) with cu[s] <= p (strict: cu[s] < p), found by
 // a warp-wide walk from `from` (a count known not to exceed the answer).
 // cu is non-decreasing for valid input; the walk stays in bounds either way.
-__device__ int count_le(const int32_t* __restrict__ cu, int B, int p, bool strict, int from) {
+__device__ int count_le(const int32_t* cu, int B, int p, bool strict, int from) {
   const int lane = threadIdx.x & 31;
   int c = from;
   for (;;) {
     const int idx = c + lane;
     bool ok = false;
     if (idx < B) {
-      const int v = __ldg(cu + idx);
+      const int v = cu[idx];
       ok = strict ? (v < p) : (v <= p);
     }
     const unsigned m = __ballot_sync(0xffffffffu, ok);
@@ -285,14 +287,14 @@ __device__ int count_le(const int32_t* __restrict__ cu, int B, int p, bool stric
 // Tile boundary: tau * pitch moved back to its request's start when it would
 // split that request's first n tokens.
 // `from` is a lower bound of count_le(p).
-__device__ int tile_edge(const Args& a, int tau, int from) {
+__device__ int tile_edge(const Args& a, const int32_t* cu, int tau, int from) {
   if (tau <= 0) return 0;
   if (tau >= a.num_tiles) return a.T;
   const int p = tau * a.tile_pitch;
-  const int c = count_le(a.cu, a.B, p, false, from);
+  const int c = count_le(cu, a.B, p, false, from);
   const int s = c - 1;
   if (s >= 0 && s < a.B) {
-    const int st = __ldg(a.cu + s), en = __ldg(a.cu + s + 1);
+    const int st = cu[s], en = cu[s + 1];
     if (p < en && p - st > 0 && p - st < a.n) return st;
   }
   return p;
@@ -311,6 +313,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   unsigned char* sX = sA + T1 * kTapA;               // x stages
   Meta* meta = reinterpret_cast<Meta*>(sX + kXStages * kXStageBytes);
   Ctl* ctl = reinterpret_cast<Ctl*>(meta + kMetaStages);
+  // Request index data: the scheduler reads it many times per tile, so it is
+  // copied to shared memory once when it fits (cu, state_idx, has_init).
+  int32_t* s_cu = reinterpret_cast<int32_t*>(reinterpret_cast<unsigned char*>(ctl) +
+                                             ((sizeof(Ctl) + 15) / 16) * 16);
+  int32_t* s_idx = s_cu + ((a.B + 1 + 3) / 4) * 4;
+  uint8_t* s_hi = reinterpret_cast<uint8_t*>(s_idx + ((a.B + 3) / 4) * 4);
+  if (a.staged) {
+    for (int i = threadIdx.x; i <= a.B; i += blockDim.x) s_cu[i] = a.cu[i];
+    for (int i = threadIdx.x; i < a.B; i += blockDim.x) {
+      s_idx[i] = a.state_idx[i];
+      s_hi[i] = a.has_init ? a.has_init[i] : 1;
+    }
+  }
+  const int32_t* cu = a.staged ? s_cu : a.cu;
+  const int32_t* sidx = a.staged ? s_idx : a.state_idx;
+  const uint8_t* hini = a.staged ? s_hi : a.has_init;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int u0 = blockIdx.x * a.units_per_cta;
@@ -357,10 +375,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     int issued = 0;
     if (blockIdx.x == 0) {   // index data is checked once per call
       for (int s = lane; s < a.B; s += 32) {
-        const int c0v = __ldg(a.cu + s), c1v = __ldg(a.cu + s + 1);
+        const int c0v = cu[s], c1v = cu[s + 1];
         if (c0v < 0 || c1v < c0v || c1v > a.T) cconv::flag_error(a.dev_err, CCONV_DERR_CU_SEQLENS);
-        if (__ldg(a.state_idx + s) >= a.pool.num_slots)
-          cconv::flag_error(a.dev_err, CCONV_DERR_SLOT_RANGE);
+        if (sidx[s] >= a.pool.num_slots) cconv::flag_error(a.dev_err, CCONV_DERR_SLOT_RANGE);
       }
     }
     for (int i = 0; i < ntiles; ++i) {
@@ -369,38 +386,50 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int ms = i % kMetaStages, xs = i % kXStages;
       if (!W.wait(&ctl->meta_empty[ms], ((i / kMetaStages) & 1) ^ 1)) break;
       const bool cont = (g == prev_g && tau == prev_tau + 1);
-      const int lo = cont ? hi_prev : tile_edge(a, tau, 0);
-      const int own_lo = cont ? own_hi_prev : count_le(a.cu, a.B, lo, true, 0);
-      const int nle_lo = count_le(a.cu, a.B, lo, false, own_lo);   // requests with cu <= lo
-      const int hi = tile_edge(a, tau + 1, nle_lo);
+      const int lo = cont ? hi_prev : tile_edge(a, cu, tau, 0);
+      const int own_lo = cont ? own_hi_prev : count_le(cu, a.B, lo, true, 0);
+      const int nle_lo = count_le(cu, a.B, lo, false, own_lo);   // requests with cu <= lo
+      const int hi = tile_edge(a, cu, tau + 1, nle_lo);
       const int len = max(hi - lo, 0);
       // owned requests: lo <= cu[s] < hi (the last tile also owns cu[s] >= T)
-      const int own_hi =
-          (tau == a.num_tiles - 1) ? a.B : count_le(a.cu, a.B, hi, true, own_lo);
+      const int own_hi = (tau == a.num_tiles - 1) ? a.B : count_le(cu, a.B, hi, true, own_lo);
       Meta& M = meta[ms];
-      // row -> request, 32 rows per batch; sc = request holding the batch's first row
+      // row -> request; sc = request holding row lo
       int sc = max(nle_lo - 1, 0);
-      for (int r0 = 0; r0 < kRows; r0 += 32) {
-        const int r = r0 + lane;
-        const int t = lo + r;
-        int j = -1, slot = -1;
-        if (r < len) {
-          int sr = sc;
-          while (sr + 1 < a.B && __ldg(a.cu + sr + 1) <= t) ++sr;
-          const int st = __ldg(a.cu + sr), en = __ldg(a.cu + sr + 1);
-          if (st >= 0 && st <= t && t < en && en <= a.T) {
-            const int sl = __ldg(a.state_idx + sr);
-            const bool h = (a.has_init == nullptr || __ldg(a.has_init + sr) != 0);
-            if (sl < a.pool.num_slots) {   // out-of-range slots are skipped and reported
-              j = t - st;
-              slot = (h && sl >= 0) ? sl : -1;
+      const int st0 = cu[sc], en0 = cu[sc + 1];
+      if (st0 >= 0 && st0 <= lo && en0 >= hi && en0 <= a.T) {
+        // the whole tile lies inside one request
+        const int sl = sidx[sc];
+        const bool h = hini == nullptr || hini[sc] != 0;
+        const bool ok = sl < a.pool.num_slots;
+        const int slot = (h && sl >= 0) ? sl : -1;
+        for (int r = lane; r < kRows; r += 32) {
+          M.rowj[r] = (ok && r < len) ? lo + r - st0 : -1;
+          M.rowslot[r] = slot;
+        }
+      } else {
+        for (int r0 = 0; r0 < kRows; r0 += 32) {
+          const int r = r0 + lane;
+          const int t = lo + r;
+          int j = -1, slot = -1;
+          if (r < len) {
+            int sr = sc;
+            while (sr + 1 < a.B && cu[sr + 1] <= t) ++sr;
+            const int st = cu[sr], en = cu[sr + 1];
+            if (st >= 0 && st <= t && t < en && en <= a.T) {
+              const int sl = sidx[sr];
+              const bool h = (hini == nullptr || hini[sr] != 0);
+              if (sl < a.pool.num_slots) {   // out-of-range slots are skipped and reported
+                j = t - st;
+                slot = (h && sl >= 0) ? sl : -1;
+              }
             }
           }
+          M.rowj[r] = j;
+          M.rowslot[r] = slot;
+          const int last = min(lo + r0 + 31, hi - 1);   // same walk on every lane
+          while (sc + 1 < a.B && cu[sc + 1] <= last) ++sc;
         }
-        M.rowj[r] = j;
-        M.rowslot[r] = slot;
-        const int last = min(lo + r0 + 31, hi - 1);   // same walk on every lane
-        while (sc + 1 < a.B && __ldg(a.cu + sc + 1) <= last) ++sc;
       }
       if (lane == 0) {
         M.lo = lo;
@@ -521,14 +550,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       // owned requests s with s % G == g: first delayed value and delayed state
       for (int s = M.own_lo + ((g - M.own_lo % a.G) % a.G + a.G) % a.G + ew * a.G;
            s < M.own_hi; s += kEpiWarps * a.G) {
-        const int st = __ldg(a.cu + s), en = __ldg(a.cu + s + 1);
-        const int slot = __ldg(a.state_idx + s);
+        const int st = cu[s], en = cu[s + 1];
+        const int slot = sidx[s];
         if (st < 0 || en < st || en > a.T) {
           if (lane == 0) cconv::flag_error(a.dev_err, CCONV_DERR_CU_SEQLENS);
           continue;
         }
         if (slot >= a.pool.num_slots) continue;
-        const bool h = slot >= 0 && (a.has_init == nullptr || __ldg(a.has_init + s) != 0);
+        const bool h = slot >= 0 && (hini == nullptr || hini[s] != 0);
         for (int k = lane; k < dunits; k += 32) {
           const uint4 first =
               h ? *reinterpret_cast<const uint4*>(a.dstate + ((int64_t)slot * a.dstate_rs + k * 8) * 2)
@@ -656,15 +685,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int task = p; task < nown * (kGS / 8); task += kProdWarps * 32) {
         const int s = M.own_lo + (task >> 4);
         const int tc0 = g * kGS + (task & 15) * 8;
-        const int st = __ldg(a.cu + s), en = __ldg(a.cu + s + 1);
-        const int slot = __ldg(a.state_idx + s);
+        const int st = cu[s], en = cu[s + 1];
+        const int slot = sidx[s];
         if (st < 0 || en < st || en > a.T) continue;
         if (slot >= a.pool.num_slots) {
           if ((task & 15) == 0) cconv::flag_error(a.dev_err, CCONV_DERR_SLOT_RANGE);
           continue;
         }
         if (slot < 0) continue;
-        const bool h = a.has_init == nullptr || __ldg(a.has_init + s) != 0;
+        const bool h = hini == nullptr || hini[s] != 0;
         const int L = en - st;
         for (int col = 0; col < a.n; ++col) {
           const int src = L - a.n + col;
@@ -714,14 +743,17 @@ static EncodeTiledFn encode_fn() {
   return fn;
 }
 
-static size_t smem_bytes(int T1) {
+static size_t smem_bytes(int T1, int staged_reqs) {
+  size_t stage = 0;
+  if (staged_reqs > 0)
+    stage = 16 + ((staged_reqs + 1 + 3) / 4) * 16 + ((staged_reqs + 3) / 4) * 16 + staged_reqs;
   return 1024 + (size_t)T1 * (kTapB + kTapA) + (size_t)kXStages * kXStageBytes +
-         kMetaStages * sizeof(Meta) + sizeof(Ctl);
+         kMetaStages * sizeof(Meta) + ((sizeof(Ctl) + 15) / 16) * 16 + stage;
 }
 
 template <int T0, int T1>
 static cudaError_t launch(const CUtensorMap& map, const Args& a, int grid, cudaStream_t st) {
-  const size_t smem = smem_bytes(T1);
+  const size_t smem = smem_bytes(T1, a.staged ? a.B : 0);
   cudaError_t e = cudaFuncSetAttribute(cca_kernel<T0, T1>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
@@ -809,6 +841,7 @@ extern "C" int cca_qk_conv(const void* qk, int64_t qk_row_stride, const void* w_
   a.tile_pitch = kRows - std::max(n - 1, 0);
   a.num_tiles = std::max(1, (num_tokens + a.tile_pitch - 1) / a.tile_pitch);
   a.units = a.num_tiles * groups;
+  a.staged = num_seqs <= kStageReqs ? 1 : 0;
   a.out = static_cast<char*>(out_qk);
   a.out_rs = out_qk_row_stride;
   a.dprev = static_cast<char*>(out_delayed_prev);

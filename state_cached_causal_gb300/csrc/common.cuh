@@ -92,15 +92,44 @@ __device__ __forceinline__ void stg16(char* p, const uint4& v) {
   *reinterpret_cast<uint4*>(p) = v;
 }
 
-// SiLU v * sigmoid(v). fp32 storage keeps the accurate exp and division;
-// bf16 storage (8 mantissa bits) takes the fast exp and reciprocal.
+__device__ __forceinline__ float tanh_approx(float v) {
+  float t;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(v));
+  return t;
+}
+
+// SiLU v * sigmoid(v). fp32 storage keeps the accurate exp and division.
+// bf16 storage (8 mantissa bits) uses sigmoid(v) = (1 + tanh(v/2)) / 2 with
+// the hardware tanh (relative error about 2^-11, well under a bf16 ulp):
+// one MUFU operation per output instead of two.
 template <typename T>
 __device__ __forceinline__ float silu(float v) {
   if constexpr (sizeof(T) == 4) {
     return v / (1.0f + expf(-v));
   } else {
-    return __fdividef(v, 1.0f + __expf(-v));
+    const float h = 0.5f * v;
+    return fmaf(h, tanh_approx(h), h);
   }
+}
+
+// ---- asynchronous global -> shared copies (per thread, 16 bytes) ---------
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// Copies 16 bytes, or writes 16 zero bytes without reading when !pred.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool pred) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+               "r"(pred ? 16 : 0)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 // ---- conv-state pool access ----------------------------------------------

@@ -20,7 +20,8 @@
 namespace cconv {
 
 constexpr int kChunk = 64;      // tokens per varlen block (>= (width-1)*dilation)
-constexpr int kUnroll = 8;      // rows in flight per thread
+constexpr int kPrefetch = 12;   // token rows in flight per thread (cp.async ring)
+constexpr int kRing = 16;       // ring slots per thread (> kPrefetch + 1, power of 2)
 
 struct FwdArgs {
   const char* x;
@@ -61,9 +62,10 @@ __device__ int find_chunk_seq(const int32_t* __restrict__ cu, int B, int b) {
 }
 
 template <typename T, int W, int D>
-__global__ void __launch_bounds__(128) fwd_varlen_kernel(const FwdArgs a) {
+__global__ void __launch_bounds__(128, 4) fwd_varlen_kernel(const FwdArgs a) {
   constexpr int S = (W - 1) * D;
-  constexpr int V = Elem<T>::V, E = Elem<T>::bytes, U = kUnroll;
+  constexpr int V = Elem<T>::V, E = Elem<T>::bytes;
+  constexpr int PF = kPrefetch, RING = kRing;
   extern __shared__ uint4 dyn_smem[];
   __shared__ int sh_seq;
   const int nt = blockDim.x, tid = threadIdx.x;
@@ -96,6 +98,39 @@ __global__ void __launch_bounds__(128) fwd_varlen_kernel(const FwdArgs a) {
   if (slot >= a.pool.num_slots) return;
   const bool hs = slot >= 0 && (a.has_init == nullptr || a.has_init[s] != 0);
 
+  const int r0 = j * kChunk, r1 = min(L, r0 + kChunk);
+  const char* xs = a.x + ((int64_t)start * a.x_rs + c0) * E;
+  char* os = a.out + ((int64_t)start * a.out_rs + c0) * E;
+  const int64_t xstep = a.x_rs * E, ostep = a.out_rs * E;
+
+  // Token rows stream through a per-thread ring of 16-byte units in shared
+  // memory, PF rows ahead of use (cp.async, no registers held while in
+  // flight). Stream order = the order of use: dilation class rho = 0..D-1,
+  // and within a class rows r0+rho, r0+rho+D, ...
+  uint4* blk = dyn_smem + tid;                       // pool columns (chunk 0 only)
+  uint4* ring = dyn_smem + a.pool.cap * nt + tid;    // RING stream slots
+  const uint32_t ring0 = smem_addr(ring);
+  const uint32_t slot_bytes = nt * 16;
+  int pr = 0, pm = 0, issued = 0;
+  auto issue = [&]() {
+    const int r = r0 + pr + pm * D;
+    const bool ok = pr < D && r < r1;
+    if (ok) {
+      ++pm;
+      if (r0 + pr + pm * D >= r1) {
+        ++pr;
+        pm = 0;
+        if (r0 + pr >= r1) pr = D;   // later classes are empty too
+      }
+    }
+    cp_async16(ring0 + (issued & (RING - 1)) * slot_bytes, ok ? xs + (int64_t)r * xstep : xs,
+               ok);
+    cp_async_commit();
+    ++issued;
+  };
+#pragma unroll
+  for (int i = 0; i < PF; ++i) issue();
+
   float wk[W][V], bv[V];
 #pragma unroll
   for (int v = 0; v < V; ++v) {
@@ -103,21 +138,16 @@ __global__ void __launch_bounds__(128) fwd_varlen_kernel(const FwdArgs a) {
     for (int k = 0; k < W; ++k) wk[k][v] = load_f32<T>(a.w, (int64_t)(c0 + v) * W + k);
     bv[v] = a.bias ? load_f32<T>(a.bias, c0 + v) : 0.0f;
   }
-
-  uint4* blk = dyn_smem + tid;
-  const int r0 = j * kChunk, r1 = min(L, r0 + kChunk);
   if (j == 0) {
     if (slot >= 0) pool_load<T>(a.pool, slot, c0, S, blk, nt);
     if (!hs)
       for (int col = 0; col < S; ++col) blk[col * nt] = make_uint4(0u, 0u, 0u, 0u);
   }
-  const char* xs = a.x + ((int64_t)start * a.x_rs + c0) * E;
-  char* os = a.out + ((int64_t)start * a.out_rs + c0) * E;
-  const int64_t xstep = a.x_rs * E, ostep = a.out_rs * E;
   const bool silu_on = a.act == CCONV_ACT_SILU;
 
-#pragma unroll
-  for (int rho = 0; rho < D; ++rho) {
+  int used = 0;
+#pragma unroll 1
+  for (int rho = 0; rho < D && r0 + rho < r1; ++rho) {
     float win[W - 1][V];
 #pragma unroll
     for (int k = 0; k < W - 1; ++k) {
@@ -125,37 +155,32 @@ __global__ void __launch_bounds__(128) fwd_varlen_kernel(const FwdArgs a) {
       const uint4 r = (p >= 0) ? ldg16(xs + (int64_t)p * xstep) : blk[(S + p) * nt];
       unpack16<T>(r, win[k]);
     }
-    for (int r = r0 + rho; r < r1; r += U * D) {
-      uint4 raw[U];
+#pragma unroll 2
+    for (int r = r0 + rho; r < r1; r += D) {
+      cp_async_wait<PF - 1>();
+      float cur[V], y[V];
+      unpack16<T>(ring[(used & (RING - 1)) * nt], cur);
+      ++used;
+      issue();
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int p = r + u * D;
-        raw[u] = (p < r1) ? ldg16(xs + (int64_t)p * xstep) : make_uint4(0u, 0u, 0u, 0u);
+      for (int v = 0; v < V; ++v) {
+        float acc = bv[v];
+#pragma unroll
+        for (int k = 0; k < W - 1; ++k) acc = fmaf(wk[k][v], win[k][v], acc);
+        acc = fmaf(wk[W - 1][v], cur[v], acc);
+        y[v] = silu_on ? silu<T>(acc) : acc;
+      }
+      stg16(os + (int64_t)r * ostep, pack16<T>(y));
+#pragma unroll
+      for (int k = 0; k < W - 2; ++k) {
+#pragma unroll
+        for (int v = 0; v < V; ++v) win[k][v] = win[k + 1][v];
       }
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        float cur[V], y[V];
-        unpack16<T>(raw[u], cur);
-#pragma unroll
-        for (int v = 0; v < V; ++v) {
-          float acc = bv[v];
-#pragma unroll
-          for (int k = 0; k < W - 1; ++k) acc = fmaf(wk[k][v], win[k][v], acc);
-          acc = fmaf(wk[W - 1][v], cur[v], acc);
-          y[v] = silu_on ? silu<T>(acc) : acc;
-        }
-        const int p = r + u * D;
-        if (p < r1) stg16(os + (int64_t)p * ostep, pack16<T>(y));
-#pragma unroll
-        for (int k = 0; k < W - 2; ++k) {
-#pragma unroll
-          for (int v = 0; v < V; ++v) win[k][v] = win[k + 1][v];
-        }
-#pragma unroll
-        for (int v = 0; v < V; ++v) win[W - 2][v] = cur[v];
-      }
+      for (int v = 0; v < V; ++v) win[W - 2][v] = cur[v];
     }
   }
+  cp_async_wait<0>();   // no copy may land after the thread exits
 
   // Chunk 0 owns the slot: it alone read the old columns, so it alone writes
   // the new ones -- the last S elements of history ++ tokens. Moving column
@@ -299,11 +324,12 @@ static Pool make_pool(const cconv_pool_t& pv, int esize, int V) {
   return P;
 }
 
-// Threads per block: up to 128 channel units, fewer when the per-thread pool
-// block (cap * 16 bytes) would pass 48 KB of shared memory.
-static int pick_threads(int units, int cap) {
+// Threads per block: up to 128 channel units, fewer when the per-thread
+// shared-memory columns (cols * 16 bytes) would pass the 48 KB a block gets
+// without opting in (less 1 KB for the kernels' static shared memory).
+static int pick_threads(int units, int cols) {
   int nt = std::min(128, ((units + 31) / 32) * 32);
-  const int by_smem = (48 * 1024) / std::max(1, cap * 16);
+  const int by_smem = (47 * 1024) / std::max(1, cols * 16);
   nt = std::min(nt, (by_smem / 32) * 32);
   return std::max(nt, 32);
 }
@@ -396,12 +422,12 @@ extern "C" int cconv_fwd_varlen(const void* x, int64_t x_row_stride, const void*
   a.out_rs = out_row_stride;
   a.dev_err = dev_err;
   const int units = C / V;
-  const int nt = pick_threads(units, conv_states.cap);
+  const int nt = pick_threads(units, conv_states.cap + kRing);
   const int ctiles = (units + nt - 1) / nt;
   const int64_t nblk = (int64_t)num_tokens / kChunk + num_seqs + 1;
   if (nblk > 0x7fffffff || ctiles > 65535) return CCONV_ERR_INVALID;
   const dim3 grid((unsigned)nblk, (unsigned)ctiles);
-  const size_t smem = (size_t)nt * conv_states.cap * 16;
+  const size_t smem = (size_t)nt * (conv_states.cap + kRing) * 16;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = dtype == CCONV_DTYPE_F32
                       ? launch_fwd<float>(width, dilation, grid, nt, smem, st, a)
