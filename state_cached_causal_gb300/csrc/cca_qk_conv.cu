@@ -306,8 +306,10 @@ template <int T0, int T1>
 __global__ void __launch_bounds__(kThreads, 1)
     cca_kernel(const __grid_constant__ CUtensorMap xmap, const Args a) {
   extern __shared__ __align__(1024) unsigned char dsm[];
-  unsigned char* base = reinterpret_cast<unsigned char*>(
-      (reinterpret_cast<uintptr_t>(dsm) + 1023) & ~static_cast<uintptr_t>(1023));
+  // 1024-byte alignment as an offset on the shared pointer itself, so that every
+  // pointer derived from it stays in the shared address space (a round trip
+  // through an integer would turn all of them into generic accesses).
+  unsigned char* base = dsm + ((1024u - (smem_u32(dsm) & 1023u)) & 1023u);
   unsigned char* sB = base;                          // T1 taps of B
   unsigned char* sA = sB + T1 * kTapB;               // T1 taps of A
   unsigned char* sX = sA + T1 * kTapA;               // x stages
