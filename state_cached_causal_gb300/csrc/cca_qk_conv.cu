@@ -59,7 +59,9 @@ constexpr int kAccCols = 128;                          // fp32 accumulator colum
 constexpr int kTmemCols = 2 * kAccCols;
 constexpr long long kWaitCycles = 2000000000LL;        // ~1 s at GB300 clocks
 constexpr int kDerrTimeout = CCONV_DERR_TIMEOUT;
-constexpr int kStageReqs = 1536;                       // index data staged in smem up to this
+constexpr int kStageReqs = 1024;                       // index data staged in smem up to this
+constexpr int kOutRowPitch = 80;                       // 64 bytes of a row + 16 (no bank conflicts)
+constexpr int kOutStageBytes = 32 * kOutRowPitch + kGS * 4;   // per epilogue warp, + bias
 
 struct Meta {
   int lo, len, g, own_lo, own_hi, pad0, pad1, pad2;
@@ -305,6 +307,7 @@ __device__ int tile_edge(const Args& a, const int32_t* cu, int tau, int from) {
 template <int T0, int T1>
 __global__ void __launch_bounds__(kThreads, 1)
     cca_kernel(const __grid_constant__ CUtensorMap xmap, const Args a) {
+  constexpr int NH = T0 + T1 - 2;               // history columns
   extern __shared__ __align__(1024) unsigned char dsm[];
   // 1024-byte alignment as an offset on the shared pointer itself, so that every
   // pointer derived from it stays in the shared address space (a round trip
@@ -313,7 +316,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   unsigned char* sB = base;                          // T1 taps of B
   unsigned char* sA = sB + T1 * kTapB;               // T1 taps of A
   unsigned char* sX = sA + T1 * kTapA;               // x stages
-  Meta* meta = reinterpret_cast<Meta*>(sX + kXStages * kXStageBytes);
+  unsigned char* sOut = sX + kXStages * kXStageBytes;  // epilogue transpose buffers
+  Meta* meta = reinterpret_cast<Meta*>(sOut + kEpiWarps * kOutStageBytes);
   Ctl* ctl = reinterpret_cast<Ctl*>(meta + kMetaStages);
   // Request index data: the scheduler reads it many times per tile, so it is
   // copied to shared memory once when it fits (cu, state_idx, has_init).
@@ -497,90 +501,67 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------- epilogue
     const int q = warp & 3;                      // TMEM lane quadrant of this warp
     const int ew = warp - kWarpEpi0;
-    const int row = q * 32 + lane;
-    const int dunits = a.Dv / 8;                 // 16-byte units per delayed row
+    unsigned char* stage = sOut + ew * kOutStageBytes;   // 32 rows x 64 bytes, padded
+    float* sbias = reinterpret_cast<float*>(stage + 32 * kOutRowPitch);
     for (int i = 0; i < ntiles; ++i) {
       const int ms = i % kMetaStages, ab = i & 1;
       if (!W.wait(&ctl->meta_full[ms], (i / kMetaStages) & 1)) break;
       const Meta& M = meta[ms];
       const int g = M.g, lo = M.lo, len = M.len;
+      for (int k = lane; k < kGS; k += 32)
+        sbias[k] = a.b_gr ? cconv::load_f32<__nv_bfloat16>(a.b_gr, (int64_t)g * kGS + k) : 0.0f;
+
+      // q/k outputs: TMEM -> +bias -> bf16 -> shared-memory transpose -> global,
+      // 32 columns at a time (the next 32 columns' TMEM load in flight), so that
+      // a store instruction covers 8 rows x 64 contiguous bytes.
       if (!W.wait(&ctl->acc_full[ab], (i >> 1) & 1)) break;
       tc_fence_after();
-      const bool valid = row < len && M.rowj[row] >= 0;
-      char* orow = a.out + ((int64_t)(lo + row) * a.out_rs + (int64_t)g * kGS) * 2;
-      const char* brow = a.b_gr ? a.b_gr + (int64_t)g * kGS * 2 : nullptr;
-#pragma unroll 1
+      const int seg = lane & 3;
+      const uint32_t tbase = tmem + (static_cast<uint32_t>(q * 32) << 16) + ab * kAccCols;
+      uint32_t ra[32], rb[32];
+      tmem_ld32(tbase, ra);
+#pragma unroll
       for (int c = 0; c < kGS / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld32(tmem + (static_cast<uint32_t>(q * 32) << 16) + ab * kAccCols + c * 32, r);
+        uint32_t (&cur)[32] = (c & 1) ? rb : ra;
+        uint32_t (&nxt)[32] = (c & 1) ? ra : rb;
         tmem_wait_ld();
-        if (valid) {
-          float f[32];
+        if (c + 1 < kGS / 32) tmem_ld32(tbase + (c + 1) * 32, nxt);
 #pragma unroll
-          for (int k = 0; k < 32; ++k) f[k] = __uint_as_float(r[k]);
-          if (brow) {
+        for (int k = 0; k < 32; k += 8) {
+          const float4 b0v = *reinterpret_cast<const float4*>(sbias + c * 32 + k);
+          const float4 b1v = *reinterpret_cast<const float4*>(sbias + c * 32 + k + 4);
+          const float bb[8] = {b0v.x, b0v.y, b0v.z, b0v.w, b1v.x, b1v.y, b1v.z, b1v.w};
+          float hh[8];
 #pragma unroll
-            for (int k = 0; k < 32; k += 8) {
-              float bb[8];
-              cconv::unpack16<__nv_bfloat16>(cconv::ldg16(brow + (c * 32 + k) * 2), bb);
-#pragma unroll
-              for (int e = 0; e < 8; ++e) f[k + e] += bb[e];
-            }
-          }
-#pragma unroll
-          for (int k = 0; k < 32; k += 8) {
-            float h[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) h[e] = f[k + e];
-            cconv::stg16(orow + (c * 32 + k) * 2, cconv::pack16<__nv_bfloat16>(h));
-          }
+          for (int e = 0; e < 8; ++e) hh[e] = __uint_as_float(cur[k + e]) + bb[e];
+          *reinterpret_cast<uint4*>(stage + lane * kOutRowPitch + k * 2) =
+              cconv::pack16<__nv_bfloat16>(hh);
         }
+        __syncwarp();
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int rr = k * 8 + (lane >> 2);    // row within this warp's 32
+          const int tr = q * 32 + rr;            // row within the tile
+          const uint4 v = *reinterpret_cast<const uint4*>(stage + rr * kOutRowPitch + seg * 16);
+          if (tr < len && M.rowj[tr] >= 0)
+            cconv::stg16(a.out + ((int64_t)(lo + tr) * a.out_rs + (int64_t)g * kGS + c * 32 +
+                                  seg * 8) * 2, v);
+        }
+        __syncwarp();
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&ctl->acc_empty[ab]);
-      // delayed half of v: rows r = g, g+G, ... of the tile with j >= 1 copy the
-      // previous token's value
-      for (int r = g + ew * a.G; r < len; r += kEpiWarps * a.G) {
-        if (M.rowj[r] >= 1) {
-          const int64_t t = lo + r;
-          for (int k = lane; k < dunits; k += 32)
-            cconv::stg16(a.dprev + (t * a.dprev_rs + k * 8) * 2,
-                         cconv::ldg16(a.delayed + ((t - 1) * a.delayed_rs + k * 8) * 2));
-        }
+      if (lane == 0) {
+        mbar_arrive(&ctl->acc_empty[ab]);
+        mbar_arrive(&ctl->meta_empty[ms]);
       }
-      // owned requests s with s % G == g: first delayed value and delayed state
-      for (int s = M.own_lo + ((g - M.own_lo % a.G) % a.G + a.G) % a.G + ew * a.G;
-           s < M.own_hi; s += kEpiWarps * a.G) {
-        const int st = cu[s], en = cu[s + 1];
-        const int slot = sidx[s];
-        if (st < 0 || en < st || en > a.T) {
-          if (lane == 0) cconv::flag_error(a.dev_err, CCONV_DERR_CU_SEQLENS);
-          continue;
-        }
-        if (slot >= a.pool.num_slots) continue;
-        const bool h = slot >= 0 && (hini == nullptr || hini[s] != 0);
-        for (int k = lane; k < dunits; k += 32) {
-          const uint4 first =
-              h ? *reinterpret_cast<const uint4*>(a.dstate + ((int64_t)slot * a.dstate_rs + k * 8) * 2)
-                : cconv::ldg16(a.delayed_init + k * 16);
-          if (en > st) cconv::stg16(a.dprev + ((int64_t)st * a.dprev_rs + k * 8) * 2, first);
-          if (slot >= 0) {
-            const uint4 last =
-                en > st ? cconv::ldg16(a.delayed + ((int64_t)(en - 1) * a.delayed_rs + k * 8) * 2)
-                        : first;
-            *reinterpret_cast<uint4*>(a.dstate + ((int64_t)slot * a.dstate_rs + k * 8) * 2) =
-                last;
-          }
-        }
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&ctl->meta_empty[ms]);
     }
   } else {
     // ------------------------------------------------------------- producers
     const int p = threadIdx.x - kWarpProd0 * 32;   // 0 .. 255
     const int kc = p & 15;                         // 8-channel chunk within the group
+    const int pw = warp - kWarpProd0;              // producer warp 0 .. 7
+    const int dunits = a.Dv / 8;                   // 16-byte units per delayed row
     const int strip = p >> 4;                      // rows strip*8 .. strip*8+7
     int cur_g = -1;
     float w0[T0][8], b0[8];
@@ -588,7 +569,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int ms = i % kMetaStages, xs = i % kXStages;
       if (!W.wait(&ctl->meta_full[ms], (i / kMetaStages) & 1)) break;
       const Meta& M = meta[ms];
-      const int g = M.g, len = M.len;
+      const int g = M.g, lo = M.lo, len = M.len;
       if (!W.wait(&ctl->x_full[xs], (i / kXStages) & 1)) break;
       if (!W.wait(&ctl->a_empty, (i & 1) ^ 1)) break;   // MMA of the previous tile done
       const int c0 = g * kGS + kc * 8;
@@ -631,8 +612,45 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // A operands: A[tap kt][k-chunk][row] = u(j - (T1-1-kt)) of the row's request
       const unsigned char* xst = sX + xs * kXStageBytes;
+      const int rs0 = strip * 8;
+      const int jf = rs0 + 7 < len ? M.rowj[rs0] : -1;
+      const bool fast = jf >= NH && M.rowj[rs0 + 7] == jf + 7;
+      if (fast) {
+        // The strip's 8 rows are consecutive tokens of one request past its
+        // history: all 8 + n x rows are loaded at once, then a register window
+        // slides over them (one load per row instead of n + 1).
+        uint4 raw[8 + NH];
+#pragma unroll
+        for (int k = 0; k < 8 + NH; ++k)
+          raw[k] = *reinterpret_cast<const uint4*>(xst + (rs0 + k) * kXRowBytes + kc * 16);
+        float xw[NH + 1][8];             // xw[m] = x~[j - m] of the current row
+#pragma unroll
+        for (int m = 1; m <= NH; ++m) cconv::unpack16<__nv_bfloat16>(raw[NH - m], xw[m]);
+#pragma unroll
+        for (int rr = 0; rr < 8; ++rr) {
+          cconv::unpack16<__nv_bfloat16>(raw[rr + NH], xw[0]);
+#pragma unroll
+          for (int kt = 0; kt < T1; ++kt) {
+            const int mp = T1 - 1 - kt;
+            float uu[8];
+#pragma unroll
+            for (int v = 0; v < 8; ++v) {
+              float acc = b0[v];
+#pragma unroll
+              for (int k = 0; k < T0; ++k) acc = fmaf(w0[k][v], xw[mp + T0 - 1 - k][v], acc);
+              uu[v] = acc;
+            }
+            *reinterpret_cast<uint4*>(sA + kt * kTapA + kc * kLboA + (rs0 + rr) * 16) =
+                cconv::pack16<__nv_bfloat16>(uu);
+          }
+#pragma unroll
+          for (int m = NH; m >= 1; --m)
+#pragma unroll
+            for (int v = 0; v < 8; ++v) xw[m][v] = xw[m - 1][v];
+        }
+      }
 #pragma unroll 1
-      for (int rr = 0; rr < 8; ++rr) {
+      for (int rr = 0; rr < (fast ? 0 : 8); ++rr) {
         const int r = strip * 8 + rr;
         uint4 outv[T1];
         const int j = (r < len) ? M.rowj[r] : -1;
@@ -647,7 +665,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int m = 0; m < NW; ++m) {
             uint4 raw;
             if (j - m >= 0) {
-              raw = *reinterpret_cast<const uint4*>(xst + (r + a.n - m) * kXRowBytes + kc * 16);
+              raw = *reinterpret_cast<const uint4*>(xst + (r + NH - m) * kXRowBytes + kc * 16);
             } else if (hslot >= 0) {
               raw = hist_load(a.pool, hslot, c0, a.n + j - m);
             } else {
@@ -709,6 +727,53 @@ __global__ void __launch_bounds__(kThreads, 1)
           hist_store(a.pool, slot, tc0, col, v);
         }
       }
+      // Delayed half of v (independent of the MMA; the producer warps are idle
+      // until the next tile). Rows r = g, g+G, ... of the tile with j >= 1 take
+      // the previous token's value; four rows' loads are issued before their
+      // stores.
+      for (int k = lane; k < dunits; k += 32) {
+        for (int rb = g + pw * a.G; rb < len; rb += 4 * kProdWarps * a.G) {
+          uint4 v[4];
+          bool ok[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int r = rb + u * kProdWarps * a.G;
+            ok[u] = r < len && M.rowj[r] >= 1;
+            if (ok[u])
+              v[u] = cconv::ldg16(a.delayed + ((int64_t)(lo + r - 1) * a.delayed_rs + k * 8) * 2);
+          }
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            if (ok[u])
+              cconv::stg16(a.dprev + ((int64_t)(lo + rb + u * kProdWarps * a.G) * a.dprev_rs +
+                                      k * 8) * 2, v[u]);
+        }
+      }
+      // owned requests s with s % G == g: first delayed value and delayed state
+      for (int s = M.own_lo + ((g - M.own_lo % a.G) % a.G + a.G) % a.G + pw * a.G;
+           s < M.own_hi; s += kProdWarps * a.G) {
+        const int st = cu[s], en = cu[s + 1];
+        const int slot = sidx[s];
+        if (st < 0 || en < st || en > a.T) {
+          if (lane == 0) cconv::flag_error(a.dev_err, CCONV_DERR_CU_SEQLENS);
+          continue;
+        }
+        if (slot >= a.pool.num_slots) continue;
+        const bool h = slot >= 0 && (hini == nullptr || hini[s] != 0);
+        for (int k = lane; k < dunits; k += 32) {
+          const uint4 first =
+              h ? *reinterpret_cast<const uint4*>(a.dstate + ((int64_t)slot * a.dstate_rs + k * 8) * 2)
+                : cconv::ldg16(a.delayed_init + k * 16);
+          const uint4 last =
+              en > st ? cconv::ldg16(a.delayed + ((int64_t)(en - 1) * a.delayed_rs + k * 8) * 2)
+                      : first;
+          if (en > st) cconv::stg16(a.dprev + ((int64_t)st * a.dprev_rs + k * 8) * 2, first);
+          if (slot >= 0)
+            *reinterpret_cast<uint4*>(a.dstate + ((int64_t)slot * a.dstate_rs + k * 8) * 2) = last;
+        }
+      }
+      __syncwarp();
+
       __syncwarp();
       if (lane == 0) mbar_arrive(&ctl->meta_empty[ms]);
     }
@@ -750,7 +815,8 @@ static size_t smem_bytes(int T1, int staged_reqs) {
   if (staged_reqs > 0)
     stage = 16 + ((staged_reqs + 1 + 3) / 4) * 16 + ((staged_reqs + 3) / 4) * 16 + staged_reqs;
   return 1024 + (size_t)T1 * (kTapB + kTapA) + (size_t)kXStages * kXStageBytes +
-         kMetaStages * sizeof(Meta) + ((sizeof(Ctl) + 15) / 16) * 16 + stage;
+         (size_t)kEpiWarps * kOutStageBytes + kMetaStages * sizeof(Meta) +
+         ((sizeof(Ctl) + 15) / 16) * 16 + stage;
 }
 
 template <int T0, int T1>
