@@ -8,6 +8,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <type_traits>
+
 #include "cconv.h"
 
 namespace cconv {
@@ -80,6 +82,25 @@ __device__ __forceinline__ float load_f32(const char* base, int64_t i) {
   } else {
     const uint16_t b = reinterpret_cast<const uint16_t*>(base)[i];
     return __uint_as_float(static_cast<uint32_t>(b) << 16);
+  }
+}
+
+// Single elements as raw storage bits.
+template <typename T>
+__device__ __forceinline__ float raw_to_f32(uint32_t bits) {
+  if constexpr (sizeof(T) == 4)
+    return __uint_as_float(bits);
+  else
+    return __uint_as_float(bits << 16);
+}
+template <typename T>
+__device__ __forceinline__ typename std::conditional<sizeof(T) == 4, uint32_t, uint16_t>::type
+f32_to_raw(float v) {
+  if constexpr (sizeof(T) == 4) {
+    return __float_as_uint(v);
+  } else {
+    __nv_bfloat16 h = __float2bfloat16_rn(v);   // round to nearest even
+    return *reinterpret_cast<uint16_t*>(&h);
   }
 }
 

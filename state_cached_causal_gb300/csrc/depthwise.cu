@@ -14,6 +14,7 @@
 // whatever the dilation. Eight rows are loaded before any is used to keep
 // enough bytes in flight per SM.
 #include <algorithm>
+#include <type_traits>
 
 #include "common.cuh"
 
@@ -210,93 +211,144 @@ struct UpdArgs {
   int32_t* dev_err;
 };
 
-// One thread = one 16-byte channel unit of one request. The request's pool
-// columns are staged in shared memory, where the spec window offset
-// (num_accepted - 1) and the roll are plain indexed moves.
+// One block = one request x (up to) 256 channels, one thread per channel.
+// Everything the block touches in HBM is moved cooperatively in 16-byte
+// coalesced units through shared memory: the request's state for those
+// channels (contiguous in a channel-first pool, `cap` contiguous rows in a
+// column-first one), its q token rows and its q output rows. Only the
+// per-channel arithmetic -- the prior window at num_accepted - 1, the taps and
+// the roll -- touches single elements, in shared memory.
 template <typename T, int W, int D>
-__global__ void __launch_bounds__(128) update_kernel(const UpdArgs a) {
+__global__ void __launch_bounds__(256) update_kernel(const UpdArgs a) {
   constexpr int S = (W - 1) * D;
-  constexpr int V = Elem<T>::V, E = Elem<T>::bytes, QM = kMaxSpec + 1;
+  constexpr int E = Elem<T>::bytes, QM = kMaxSpec + 1;
+  using R = typename std::conditional<E == 4, uint32_t, uint16_t>::type;   // raw element
   extern __shared__ uint4 dyn_smem[];
   const int nt = blockDim.x, tid = threadIdx.x;
   const int s = blockIdx.x / a.ctiles;
-  const int ct = blockIdx.x - s * a.ctiles;
-  const int c0 = (ct * nt + tid) * V;
-  if (c0 >= a.C) return;
+  const int cb = (blockIdx.x - s * a.ctiles) * nt;     // first channel of the block
+  const int nch = min(nt, a.C - cb);                   // channels of the block (multiple of 8/4)
   const int q = 1 + a.n_spec;
   const int slot = a.state_idx[s];
   if (slot >= a.pool.num_slots) {
-    if (c0 == 0) flag_error(a.dev_err, CCONV_DERR_SLOT_RANGE);
+    if (cb == 0 && tid == 0) flag_error(a.dev_err, CCONV_DERR_SLOT_RANGE);
     return;
   }
   int off = 0;
   if (a.n_spec > 0) {
     off = a.num_accepted[s] - 1;
     if (off < 0 || off >= q) {
-      if (c0 == 0) flag_error(a.dev_err, CCONV_DERR_NUM_ACCEPTED);
+      if (cb == 0 && tid == 0) flag_error(a.dev_err, CCONV_DERR_NUM_ACCEPTED);
       return;
     }
   }
   const bool hs = slot >= 0 && (a.has_init == nullptr || a.has_init[s] != 0);
-  const int ncols = a.n_spec > 0 ? a.pool.cap : S;
-  uint4* blk = dyn_smem + tid;
-  if (slot >= 0) pool_load<T>(a.pool, slot, c0, ncols, blk, nt);
-  if (!hs)
-    for (int col = 0; col < ncols; ++col) blk[col * nt] = make_uint4(0u, 0u, 0u, 0u);
-
-  float wk[W][V], bv[V];
-#pragma unroll
-  for (int v = 0; v < V; ++v) {
-#pragma unroll
-    for (int k = 0; k < W; ++k) wk[k][v] = load_f32<T>(a.w, (int64_t)(c0 + v) * W + k);
-    bv[v] = a.bias ? load_f32<T>(a.bias, c0 + v) : 0.0f;
-  }
+  const int cap = a.pool.cap;
+  const int ncols = a.n_spec > 0 ? cap : S;
+  const int region = nt * cap;                          // elements of one state copy
+  R* old_s = reinterpret_cast<R*>(dyn_smem);
+  R* new_s = old_s + region;
+  R* xs = new_s + region;                               // [QM][nt]
+  R* os = xs + QM * nt;                                 // [QM][nt]
+  const bool ds = a.pool.mode == kPoolDS;
+  // element (channel c, column col) of a state copy
+  auto at = [&](int c, int col) { return ds ? c * cap + col : col * nt + c; };
+  const int64_t elem0 = (int64_t)slot * a.pool.s_slot;  // pool element of slot, channel 0
   const int64_t row0 = (int64_t)s * q;
-  const char* xs = a.x + (row0 * a.x_rs + c0) * E;
-  char* os = a.out + (row0 * a.out_rs + c0) * E;
-  uint4 xr[QM];
-#pragma unroll
-  for (int u = 0; u < QM; ++u)
-    xr[u] = (u < q) ? ldg16(xs + (int64_t)u * a.x_rs * E) : make_uint4(0u, 0u, 0u, 0u);
 
-  const bool silu_on = a.act == CCONV_ACT_SILU;
-#pragma unroll
-  for (int i = 0; i < QM; ++i) {
-    if (i < q) {
-      float y[V];
-#pragma unroll
-      for (int v = 0; v < V; ++v) y[v] = bv[v];
-#pragma unroll
-      for (int k = 0; k < W; ++k) {
-        const int idx = S + i - (W - 1 - k) * D;   // position in prior ++ tokens
-        float xv[V];
-        if (idx >= S)
-          unpack16<T>(xr[idx - S], xv);
-        else
-          unpack16<T>(blk[(off + idx) * nt], xv);
-#pragma unroll
-        for (int v = 0; v < V; ++v) y[v] = fmaf(wk[k][v], xv[v], y[v]);
+  // 1. loads: state (cooperative 16-byte units where the layout allows), x rows
+  if (slot >= 0) {
+    if (ds) {
+      const uint4* src = reinterpret_cast<const uint4*>(a.pool.p + (elem0 + (int64_t)cb * cap) * E);
+      const int units = nch * cap * E / 16;
+      for (int u = tid; u < units; u += nt) reinterpret_cast<uint4*>(old_s)[u] = src[u];
+    } else if (a.pool.mode == kPoolSD) {
+      const int upr = nch * E / 16;                     // units per column row
+      for (int u = tid; u < upr * cap; u += nt) {
+        const int col = u / upr, k = u - col * upr;
+        reinterpret_cast<uint4*>(old_s + col * nt)[k] = *reinterpret_cast<const uint4*>(
+            a.pool.p + (elem0 + (int64_t)col * a.pool.s_col + cb) * E + k * 16);
       }
-      if (silu_on) {
-#pragma unroll
-        for (int v = 0; v < V; ++v) y[v] = silu<T>(y[v]);
-      }
-      stg16(os + (int64_t)i * a.out_rs * E, pack16<T>(y));
+    } else if (tid < nch) {
+      for (int col = 0; col < cap; ++col)
+        old_s[at(tid, col)] = *reinterpret_cast<const R*>(
+            a.pool.p + (elem0 + (int64_t)(cb + tid) * a.pool.s_chan + (int64_t)col * a.pool.s_col) * E);
     }
   }
-
-  if (slot >= 0) {
-    if (a.n_spec == 0) {
-      for (int i = 0; i + 1 < S; ++i) blk[i * nt] = blk[(i + 1) * nt];
-      blk[(S - 1) * nt] = xr[0];
-    } else {
-      const int keep = a.pool.cap - q;   // columns kept: B[off+1, off+1+keep)
-      for (int i = 0; i < keep; ++i) blk[i * nt] = blk[(off + 1 + i) * nt];
-#pragma unroll
-      for (int u = 0; u < QM; ++u)
-        if (u < q) blk[(keep + u) * nt] = xr[u];
+  {
+    const int upr = nch * E / 16;
+    for (int u = tid; u < upr * q; u += nt) {
+      const int r = u / upr, k = u - r * upr;
+      reinterpret_cast<uint4*>(xs + r * nt)[k] =
+          ldg16(a.x + ((row0 + r) * a.x_rs + cb) * E + k * 16);
     }
-    pool_store<T>(a.pool, slot, c0, ncols, blk, nt);
+  }
+  __syncthreads();
+
+  // 2. per-channel arithmetic in shared memory
+  if (tid < nch) {
+    const int c = tid;
+    if (!hs)
+      for (int col = 0; col < ncols; ++col) old_s[at(c, col)] = 0;
+    float wk[W];
+#pragma unroll
+    for (int k = 0; k < W; ++k) wk[k] = load_f32<T>(a.w, (int64_t)(cb + c) * W + k);
+    const float bv = a.bias ? load_f32<T>(a.bias, cb + c) : 0.0f;
+    const bool silu_on = a.act == CCONV_ACT_SILU;
+#pragma unroll
+    for (int i = 0; i < QM; ++i) {
+      if (i < q) {
+        float acc = bv;
+#pragma unroll
+        for (int k = 0; k < W; ++k) {
+          const int idx = S + i - (W - 1 - k) * D;   // position in prior ++ tokens
+          const R raw = idx >= S ? xs[(idx - S) * nt + c] : old_s[at(c, off + idx)];
+          acc = fmaf(wk[k], raw_to_f32<T>(raw), acc);
+        }
+        if (silu_on) acc = silu<T>(acc);
+        os[i * nt + c] = f32_to_raw<T>(acc);
+      }
+    }
+    if (slot >= 0) {
+      if (a.n_spec == 0) {
+        for (int col = 0; col + 1 < S; ++col) new_s[at(c, col)] = old_s[at(c, col + 1)];
+        new_s[at(c, S - 1)] = xs[c];
+        for (int col = S; col < cap; ++col) new_s[at(c, col)] = old_s[at(c, col)];
+      } else {
+        const int keep = cap - q;   // columns kept: B[off+1, off+1+keep)
+        for (int col = 0; col < keep; ++col) new_s[at(c, col)] = old_s[at(c, off + 1 + col)];
+        for (int u = 0; u < q; ++u) new_s[at(c, keep + u)] = xs[u * nt + c];
+      }
+    }
+  }
+  __syncthreads();
+
+  // 3. stores: outputs, new state
+  {
+    const int upr = nch * E / 16;
+    for (int u = tid; u < upr * q; u += nt) {
+      const int r = u / upr, k = u - r * upr;
+      stg16(a.out + ((row0 + r) * a.out_rs + cb) * E + k * 16,
+            reinterpret_cast<const uint4*>(os + r * nt)[k]);
+    }
+  }
+  if (slot >= 0) {
+    if (ds) {
+      uint4* dst = reinterpret_cast<uint4*>(a.pool.p + (elem0 + (int64_t)cb * cap) * E);
+      const int units = nch * cap * E / 16;
+      for (int u = tid; u < units; u += nt) dst[u] = reinterpret_cast<const uint4*>(new_s)[u];
+    } else if (a.pool.mode == kPoolSD) {
+      const int upr = nch * E / 16;
+      for (int u = tid; u < upr * ncols; u += nt) {
+        const int col = u / upr, k = u - col * upr;
+        *reinterpret_cast<uint4*>(a.pool.p + (elem0 + (int64_t)col * a.pool.s_col + cb) * E +
+                                  k * 16) = reinterpret_cast<const uint4*>(new_s + col * nt)[k];
+      }
+    } else if (tid < nch) {
+      for (int col = 0; col < ncols; ++col)
+        *reinterpret_cast<R*>(a.pool.p + (elem0 + (int64_t)(cb + tid) * a.pool.s_chan +
+                                          (int64_t)col * a.pool.s_col) * E) = new_s[at(tid, col)];
+    }
   }
 }
 
@@ -468,12 +520,23 @@ extern "C" int cconv_update(const void* x, int64_t x_row_stride, cconv_pool_t co
   a.out = static_cast<char*>(out);
   a.out_rs = out_row_stride;
   a.dev_err = dev_err;
-  const int units = C / V;
-  const int nt = pick_threads(units, conv_states.cap);
-  a.ctiles = (units + nt - 1) / nt;
+  // one block = one request x up to 256 channels; shared memory holds two
+  // copies of the state (old, new) and q token and output rows
+  int nt = 256;
+  auto smem_for = [&](int n) {
+    return (size_t)n * (2 * conv_states.cap + 2 * (kMaxSpec + 1)) * esize;
+  };
+  while (nt > 32 && smem_for(nt) > 47 * 1024) nt /= 2;
+  nt = std::min(nt, ((C + 31) / 32) * 32);
+  a.ctiles = (C + nt - 1) / nt;
   const int64_t nblk = (int64_t)num_seqs * a.ctiles;
   if (nblk > 0x7fffffff) return CCONV_ERR_INVALID;
-  const size_t smem = (size_t)nt * conv_states.cap * 16;
+  const size_t smem = smem_for(nt);
+  // the channel-first block region must start on 16 bytes for every slot
+  if (a.pool.mode == kPoolDS && ((uintptr_t)conv_states.p % 16 != 0 ||
+                                 (conv_states.s_slot * esize) % 16 != 0 ||
+                                 ((int64_t)nt * conv_states.cap * esize) % 16 != 0))
+    a.pool.mode = kPoolGeneric;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const dim3 grid((unsigned)nblk);
   cudaError_t e = dtype == CCONV_DTYPE_F32
