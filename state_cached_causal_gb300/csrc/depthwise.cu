@@ -23,6 +23,7 @@ namespace cconv {
 constexpr int kChunk = 64;      // tokens per varlen block (>= (width-1)*dilation)
 constexpr int kPrefetch = 12;   // token rows in flight per thread (cp.async ring)
 constexpr int kRing = 16;       // ring slots per thread (> kPrefetch + 1, power of 2)
+constexpr int kUpdChan = 2;     // channels per thread of the update kernel
 
 struct FwdArgs {
   const char* x;
@@ -211,7 +212,7 @@ struct UpdArgs {
   int32_t* dev_err;
 };
 
-// One block = one request x (up to) 256 channels, one thread per channel.
+// One block = one request x (up to) 512 channels, two channels per thread.
 // Everything the block touches in HBM is moved cooperatively in 16-byte
 // coalesced units through shared memory: the request's state for those
 // channels (contiguous in a channel-first pool, `cap` contiguous rows in a
@@ -221,13 +222,14 @@ struct UpdArgs {
 template <typename T, int W, int D>
 __global__ void __launch_bounds__(256) update_kernel(const UpdArgs a) {
   constexpr int S = (W - 1) * D;
-  constexpr int E = Elem<T>::bytes, QM = kMaxSpec + 1;
+  constexpr int E = Elem<T>::bytes, QM = kMaxSpec + 1, K = kUpdChan;
   using R = typename std::conditional<E == 4, uint32_t, uint16_t>::type;   // raw element
   extern __shared__ uint4 dyn_smem[];
   const int nt = blockDim.x, tid = threadIdx.x;
   const int s = blockIdx.x / a.ctiles;
-  const int cb = (blockIdx.x - s * a.ctiles) * nt;     // first channel of the block
-  const int nch = min(nt, a.C - cb);                   // channels of the block (multiple of 8/4)
+  const int nb = K * nt;                               // channels per block
+  const int cb = (blockIdx.x - s * a.ctiles) * nb;     // first channel of the block
+  const int nch = min(nb, a.C - cb);                   // channels of the block (multiple of 8/4)
   const int q = 1 + a.n_spec;
   const int slot = a.state_idx[s];
   if (slot >= a.pool.num_slots) {
@@ -245,14 +247,14 @@ __global__ void __launch_bounds__(256) update_kernel(const UpdArgs a) {
   const bool hs = slot >= 0 && (a.has_init == nullptr || a.has_init[s] != 0);
   const int cap = a.pool.cap;
   const int ncols = a.n_spec > 0 ? cap : S;
-  const int region = nt * cap;                          // elements of one state copy
-  R* old_s = reinterpret_cast<R*>(dyn_smem);
-  R* new_s = old_s + region;
-  R* xs = new_s + region;                               // [QM][nt]
-  R* os = xs + QM * nt;                                 // [QM][nt]
+  // The state is rolled in place (a channel's columns are private to its
+  // thread) and the outputs overwrite the token rows once the roll has read
+  // them: shared memory holds one state copy and q rows.
+  R* st_s = reinterpret_cast<R*>(dyn_smem);             // state of the block's channels
+  R* xs = st_s + nb * cap;                              // [QM][nb]: tokens, then outputs
   const bool ds = a.pool.mode == kPoolDS;
-  // element (channel c, column col) of a state copy
-  auto at = [&](int c, int col) { return ds ? c * cap + col : col * nt + c; };
+  // element (channel c, column col) of the state copy
+  auto at = [&](int c, int col) { return ds ? c * cap + col : col * nb + c; };
   const int64_t elem0 = (int64_t)slot * a.pool.s_slot;  // pool element of slot, channel 0
   const int64_t row0 = (int64_t)s * q;
 
@@ -261,65 +263,77 @@ __global__ void __launch_bounds__(256) update_kernel(const UpdArgs a) {
     if (ds) {
       const uint4* src = reinterpret_cast<const uint4*>(a.pool.p + (elem0 + (int64_t)cb * cap) * E);
       const int units = nch * cap * E / 16;
-      for (int u = tid; u < units; u += nt) reinterpret_cast<uint4*>(old_s)[u] = src[u];
+      for (int u = tid; u < units; u += nt) reinterpret_cast<uint4*>(st_s)[u] = src[u];
     } else if (a.pool.mode == kPoolSD) {
       const int upr = nch * E / 16;                     // units per column row
       for (int u = tid; u < upr * cap; u += nt) {
         const int col = u / upr, k = u - col * upr;
-        reinterpret_cast<uint4*>(old_s + col * nt)[k] = *reinterpret_cast<const uint4*>(
+        reinterpret_cast<uint4*>(st_s + col * nb)[k] = *reinterpret_cast<const uint4*>(
             a.pool.p + (elem0 + (int64_t)col * a.pool.s_col + cb) * E + k * 16);
       }
-    } else if (tid < nch) {
-      for (int col = 0; col < cap; ++col)
-        old_s[at(tid, col)] = *reinterpret_cast<const R*>(
-            a.pool.p + (elem0 + (int64_t)(cb + tid) * a.pool.s_chan + (int64_t)col * a.pool.s_col) * E);
+    } else {
+      for (int c = tid; c < nch; c += nt)
+        for (int col = 0; col < cap; ++col)
+          st_s[at(c, col)] = *reinterpret_cast<const R*>(
+              a.pool.p + (elem0 + (int64_t)(cb + c) * a.pool.s_chan + (int64_t)col * a.pool.s_col) * E);
     }
   }
   {
     const int upr = nch * E / 16;
     for (int u = tid; u < upr * q; u += nt) {
       const int r = u / upr, k = u - r * upr;
-      reinterpret_cast<uint4*>(xs + r * nt)[k] =
+      reinterpret_cast<uint4*>(xs + r * nb)[k] =
           ldg16(a.x + ((row0 + r) * a.x_rs + cb) * E + k * 16);
     }
+  }
+  // this thread's weights and biases, loaded alongside the state
+  float wk[K][W], bv[K];
+#pragma unroll
+  for (int kc = 0; kc < K; ++kc) {
+    const int c = min(tid + kc * nt, nch - 1);
+#pragma unroll
+    for (int k = 0; k < W; ++k) wk[kc][k] = load_f32<T>(a.w, (int64_t)(cb + c) * W + k);
+    bv[kc] = a.bias ? load_f32<T>(a.bias, cb + c) : 0.0f;
   }
   __syncthreads();
 
   // 2. per-channel arithmetic in shared memory
-  if (tid < nch) {
-    const int c = tid;
-    if (!hs)
-      for (int col = 0; col < ncols; ++col) old_s[at(c, col)] = 0;
-    float wk[W];
+  const bool silu_on = a.act == CCONV_ACT_SILU;
 #pragma unroll
-    for (int k = 0; k < W; ++k) wk[k] = load_f32<T>(a.w, (int64_t)(cb + c) * W + k);
-    const float bv = a.bias ? load_f32<T>(a.bias, cb + c) : 0.0f;
-    const bool silu_on = a.act == CCONV_ACT_SILU;
+  for (int kc = 0; kc < K; ++kc) {
+    const int c = tid + kc * nt;
+    if (c >= nch) break;
+    if (!hs)
+      for (int col = 0; col < ncols; ++col) st_s[at(c, col)] = 0;
+    float y[QM];
 #pragma unroll
     for (int i = 0; i < QM; ++i) {
+      y[i] = 0.0f;
       if (i < q) {
-        float acc = bv;
+        float acc = bv[kc];
 #pragma unroll
         for (int k = 0; k < W; ++k) {
           const int idx = S + i - (W - 1 - k) * D;   // position in prior ++ tokens
-          const R raw = idx >= S ? xs[(idx - S) * nt + c] : old_s[at(c, off + idx)];
-          acc = fmaf(wk[k], raw_to_f32<T>(raw), acc);
+          const R raw = idx >= S ? xs[(idx - S) * nb + c] : st_s[at(c, off + idx)];
+          acc = fmaf(wk[kc][k], raw_to_f32<T>(raw), acc);
         }
-        if (silu_on) acc = silu<T>(acc);
-        os[i * nt + c] = f32_to_raw<T>(acc);
+        y[i] = silu_on ? silu<T>(acc) : acc;
       }
     }
     if (slot >= 0) {
+      // moving column off+1+col down to col reads ahead of every write
       if (a.n_spec == 0) {
-        for (int col = 0; col + 1 < S; ++col) new_s[at(c, col)] = old_s[at(c, col + 1)];
-        new_s[at(c, S - 1)] = xs[c];
-        for (int col = S; col < cap; ++col) new_s[at(c, col)] = old_s[at(c, col)];
+        for (int col = 0; col + 1 < S; ++col) st_s[at(c, col)] = st_s[at(c, col + 1)];
+        st_s[at(c, S - 1)] = xs[c];
       } else {
         const int keep = cap - q;   // columns kept: B[off+1, off+1+keep)
-        for (int col = 0; col < keep; ++col) new_s[at(c, col)] = old_s[at(c, off + 1 + col)];
-        for (int u = 0; u < q; ++u) new_s[at(c, keep + u)] = xs[u * nt + c];
+        for (int col = 0; col < keep; ++col) st_s[at(c, col)] = st_s[at(c, off + 1 + col)];
+        for (int u = 0; u < q; ++u) st_s[at(c, keep + u)] = xs[u * nb + c];
       }
     }
+#pragma unroll
+    for (int i = 0; i < QM; ++i)
+      if (i < q) xs[i * nb + c] = f32_to_raw<T>(y[i]);
   }
   __syncthreads();
 
@@ -329,25 +343,26 @@ __global__ void __launch_bounds__(256) update_kernel(const UpdArgs a) {
     for (int u = tid; u < upr * q; u += nt) {
       const int r = u / upr, k = u - r * upr;
       stg16(a.out + ((row0 + r) * a.out_rs + cb) * E + k * 16,
-            reinterpret_cast<const uint4*>(os + r * nt)[k]);
+            reinterpret_cast<const uint4*>(xs + r * nb)[k]);
     }
   }
   if (slot >= 0) {
     if (ds) {
       uint4* dst = reinterpret_cast<uint4*>(a.pool.p + (elem0 + (int64_t)cb * cap) * E);
       const int units = nch * cap * E / 16;
-      for (int u = tid; u < units; u += nt) dst[u] = reinterpret_cast<const uint4*>(new_s)[u];
+      for (int u = tid; u < units; u += nt) dst[u] = reinterpret_cast<const uint4*>(st_s)[u];
     } else if (a.pool.mode == kPoolSD) {
       const int upr = nch * E / 16;
       for (int u = tid; u < upr * ncols; u += nt) {
         const int col = u / upr, k = u - col * upr;
         *reinterpret_cast<uint4*>(a.pool.p + (elem0 + (int64_t)col * a.pool.s_col + cb) * E +
-                                  k * 16) = reinterpret_cast<const uint4*>(new_s + col * nt)[k];
+                                  k * 16) = reinterpret_cast<const uint4*>(st_s + col * nb)[k];
       }
-    } else if (tid < nch) {
-      for (int col = 0; col < ncols; ++col)
-        *reinterpret_cast<R*>(a.pool.p + (elem0 + (int64_t)(cb + tid) * a.pool.s_chan +
-                                          (int64_t)col * a.pool.s_col) * E) = new_s[at(tid, col)];
+    } else {
+      for (int c = tid; c < nch; c += nt)
+        for (int col = 0; col < ncols; ++col)
+          *reinterpret_cast<R*>(a.pool.p + (elem0 + (int64_t)(cb + c) * a.pool.s_chan +
+                                            (int64_t)col * a.pool.s_col) * E) = st_s[at(c, col)];
     }
   }
 }
@@ -524,18 +539,18 @@ extern "C" int cconv_update(const void* x, int64_t x_row_stride, cconv_pool_t co
   // copies of the state (old, new) and q token and output rows
   int nt = 256;
   auto smem_for = [&](int n) {
-    return (size_t)n * (2 * conv_states.cap + 2 * (kMaxSpec + 1)) * esize;
+    return (size_t)kUpdChan * n * (conv_states.cap + kMaxSpec + 1) * esize;
   };
   while (nt > 32 && smem_for(nt) > 47 * 1024) nt /= 2;
-  nt = std::min(nt, ((C + 31) / 32) * 32);
-  a.ctiles = (C + nt - 1) / nt;
+  nt = std::min(nt, ((C + kUpdChan * 32 - 1) / (kUpdChan * 32)) * 32);
+  a.ctiles = (C + kUpdChan * nt - 1) / (kUpdChan * nt);
   const int64_t nblk = (int64_t)num_seqs * a.ctiles;
   if (nblk > 0x7fffffff) return CCONV_ERR_INVALID;
   const size_t smem = smem_for(nt);
   // the channel-first block region must start on 16 bytes for every slot
   if (a.pool.mode == kPoolDS && ((uintptr_t)conv_states.p % 16 != 0 ||
                                  (conv_states.s_slot * esize) % 16 != 0 ||
-                                 ((int64_t)nt * conv_states.cap * esize) % 16 != 0))
+                                 ((int64_t)kUpdChan * nt * conv_states.cap * esize) % 16 != 0))
     a.pool.mode = kPoolGeneric;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const dim3 grid((unsigned)nblk);
