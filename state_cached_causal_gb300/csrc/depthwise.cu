@@ -17,6 +17,7 @@
 #include <type_traits>
 
 #include "common.cuh"
+#include "update.cuh"
 
 namespace cconv {
 
@@ -196,29 +197,17 @@ __global__ void __launch_bounds__(128, 4) fwd_varlen_kernel(const FwdArgs a) {
   }
 }
 
-struct UpdArgs {
-  const char* x;
-  int64_t x_rs;
-  Pool pool;
-  const char* w;
-  const char* bias;
-  const int32_t* state_idx;
-  int32_t B, n_spec;
-  const int32_t* num_accepted;
-  const uint8_t* has_init;
-  int32_t C, act, ctiles;
-  char* out;
-  int64_t out_rs;
-  int32_t* dev_err;
-};
-
-// One block = one request x (up to) 512 channels, two channels per thread.
-// Everything the block touches in HBM is moved cooperatively in 16-byte
-// coalesced units through shared memory: the request's state for those
-// channels (contiguous in a channel-first pool, `cap` contiguous rows in a
-// column-first one), its q token rows and its q output rows. Only the
-// per-channel arithmetic -- the prior window at num_accepted - 1, the taps and
-// the roll -- touches single elements, in shared memory.
+// Pools that are not channel-first (column-first or arbitrary strides): one
+// block = one request x (up to) 512 channels, two channels per thread.
+// (Channel-first pools take the bulk-copy pipeline of update_bulk.cu.)
+// Everything the block touches in HBM goes through shared memory: the
+// request's state for those channels (`cap` contiguous 16-byte rows in a
+// column-first pool, single elements otherwise), its q token rows and its q
+// output rows, the rows in coalesced 16-byte units. The per-channel
+// arithmetic reads the prior window (S columns from num_accepted - 1) into
+// registers once, computes the q outputs from registers, and writes the new
+// buffer -- prior[1..S) ++ (older kept columns) ++ tokens -- back in place.
+// The shared copy of the state is column-major: [cap][channels of the block].
 template <typename T, int W, int D>
 __global__ void __launch_bounds__(256) update_kernel(const UpdArgs a) {
   constexpr int S = (W - 1) * D;
@@ -248,23 +237,17 @@ __global__ void __launch_bounds__(256) update_kernel(const UpdArgs a) {
   const int cap = a.pool.cap;
   const int ncols = a.n_spec > 0 ? cap : S;
   // The state is rolled in place (a channel's columns are private to its
-  // thread) and the outputs overwrite the token rows once the roll has read
-  // them: shared memory holds one state copy and q rows.
+  // thread) and the outputs overwrite the token rows once they are in
+  // registers: shared memory holds one state copy and q rows.
   R* st_s = reinterpret_cast<R*>(dyn_smem);             // state of the block's channels
   R* xs = st_s + nb * cap;                              // [QM][nb]: tokens, then outputs
-  const bool ds = a.pool.mode == kPoolDS;
-  // element (channel c, column col) of the state copy
-  auto at = [&](int c, int col) { return ds ? c * cap + col : col * nb + c; };
+  const int cs = nb;                                    // column step of the state copy
   const int64_t elem0 = (int64_t)slot * a.pool.s_slot;  // pool element of slot, channel 0
   const int64_t row0 = (int64_t)s * q;
 
   // 1. loads: state (cooperative 16-byte units where the layout allows), x rows
   if (slot >= 0) {
-    if (ds) {
-      const uint4* src = reinterpret_cast<const uint4*>(a.pool.p + (elem0 + (int64_t)cb * cap) * E);
-      const int units = nch * cap * E / 16;
-      for (int u = tid; u < units; u += nt) reinterpret_cast<uint4*>(st_s)[u] = src[u];
-    } else if (a.pool.mode == kPoolSD) {
+    if (a.pool.mode == kPoolSD) {
       const int upr = nch * E / 16;                     // units per column row
       for (int u = tid; u < upr * cap; u += nt) {
         const int col = u / upr, k = u - col * upr;
@@ -274,7 +257,7 @@ __global__ void __launch_bounds__(256) update_kernel(const UpdArgs a) {
     } else {
       for (int c = tid; c < nch; c += nt)
         for (int col = 0; col < cap; ++col)
-          st_s[at(c, col)] = *reinterpret_cast<const R*>(
+          st_s[col * nb + c] = *reinterpret_cast<const R*>(
               a.pool.p + (elem0 + (int64_t)(cb + c) * a.pool.s_chan + (int64_t)col * a.pool.s_col) * E);
     }
   }
@@ -297,43 +280,57 @@ __global__ void __launch_bounds__(256) update_kernel(const UpdArgs a) {
   }
   __syncthreads();
 
-  // 2. per-channel arithmetic in shared memory
+  // 2. per-channel arithmetic: prior window and tokens in registers
   const bool silu_on = a.act == CCONV_ACT_SILU;
+  const int keep = ncols - q;   // spec: kept columns B[off+1, off+1+keep), keep >= S-1
 #pragma unroll
   for (int kc = 0; kc < K; ++kc) {
     const int c = tid + kc * nt;
     if (c >= nch) break;
-    if (!hs)
-      for (int col = 0; col < ncols; ++col) st_s[at(c, col)] = 0;
-    float y[QM];
+    R* row = st_s + c;                                 // column col at row[col * cs]
+    float pr[S];                                        // B[off + i], zero without history
+    R pb[S];
+#pragma unroll
+    for (int i = 0; i < S; ++i) {
+      pb[i] = hs ? row[(off + i) * cs] : R(0);
+      pr[i] = raw_to_f32<T>(pb[i]);
+    }
+    R xb[QM];
+    float xf[QM];
+#pragma unroll
+    for (int u = 0; u < QM; ++u) {
+      xb[u] = u < q ? xs[u * nb + c] : R(0);
+      xf[u] = raw_to_f32<T>(xb[u]);
+    }
 #pragma unroll
     for (int i = 0; i < QM; ++i) {
-      y[i] = 0.0f;
       if (i < q) {
         float acc = bv[kc];
 #pragma unroll
         for (int k = 0; k < W; ++k) {
           const int idx = S + i - (W - 1 - k) * D;   // position in prior ++ tokens
-          const R raw = idx >= S ? xs[(idx - S) * nb + c] : st_s[at(c, off + idx)];
-          acc = fmaf(wk[kc][k], raw_to_f32<T>(raw), acc);
+          acc = fmaf(wk[kc][k], idx >= S ? xf[idx - S] : pr[idx], acc);
         }
-        y[i] = silu_on ? silu<T>(acc) : acc;
+        xs[i * nb + c] = f32_to_raw<T>(silu_on ? silu<T>(acc) : acc);
       }
     }
     if (slot >= 0) {
-      // moving column off+1+col down to col reads ahead of every write
       if (a.n_spec == 0) {
-        for (int col = 0; col + 1 < S; ++col) st_s[at(c, col)] = st_s[at(c, col + 1)];
-        st_s[at(c, S - 1)] = xs[c];
+#pragma unroll
+        for (int col = 0; col + 1 < S; ++col) row[col * cs] = pb[col + 1];
+        row[(S - 1) * cs] = xb[0];
       } else {
-        const int keep = cap - q;   // columns kept: B[off+1, off+1+keep)
-        for (int col = 0; col < keep; ++col) st_s[at(c, col)] = st_s[at(c, off + 1 + col)];
-        for (int u = 0; u < q; ++u) st_s[at(c, keep + u)] = xs[u * nb + c];
+        // B[off+1+col] for col < S-1 is pb[col+1]; wider buffers keep more
+        // columns, read ahead of every write
+#pragma unroll
+        for (int col = 0; col + 1 < S; ++col) row[col * cs] = pb[col + 1];
+        for (int col = S - 1; col < keep; ++col)
+          row[col * cs] = hs ? row[(off + 1 + col) * cs] : R(0);
+#pragma unroll
+        for (int u = 0; u < QM; ++u)
+          if (u < q) row[(keep + u) * cs] = xb[u];
       }
     }
-#pragma unroll
-    for (int i = 0; i < QM; ++i)
-      if (i < q) xs[i * nb + c] = f32_to_raw<T>(y[i]);
   }
   __syncthreads();
 
@@ -347,11 +344,7 @@ __global__ void __launch_bounds__(256) update_kernel(const UpdArgs a) {
     }
   }
   if (slot >= 0) {
-    if (ds) {
-      uint4* dst = reinterpret_cast<uint4*>(a.pool.p + (elem0 + (int64_t)cb * cap) * E);
-      const int units = nch * cap * E / 16;
-      for (int u = tid; u < units; u += nt) dst[u] = reinterpret_cast<const uint4*>(st_s)[u];
-    } else if (a.pool.mode == kPoolSD) {
+    if (a.pool.mode == kPoolSD) {
       const int upr = nch * E / 16;
       for (int u = tid; u < upr * ncols; u += nt) {
         const int col = u / upr, k = u - col * upr;
@@ -362,7 +355,7 @@ __global__ void __launch_bounds__(256) update_kernel(const UpdArgs a) {
       for (int c = tid; c < nch; c += nt)
         for (int col = 0; col < ncols; ++col)
           *reinterpret_cast<R*>(a.pool.p + (elem0 + (int64_t)(cb + c) * a.pool.s_chan +
-                                            (int64_t)col * a.pool.s_col) * E) = st_s[at(c, col)];
+                                            (int64_t)col * a.pool.s_col) * E) = st_s[col * nb + c];
     }
   }
 }
@@ -535,8 +528,8 @@ extern "C" int cconv_update(const void* x, int64_t x_row_stride, cconv_pool_t co
   a.out = static_cast<char*>(out);
   a.out_rs = out_row_stride;
   a.dev_err = dev_err;
-  // one block = one request x up to 256 channels; shared memory holds two
-  // copies of the state (old, new) and q token and output rows
+  // one block = one request x up to 512 channels; shared memory holds the
+  // block's state (rolled in place) and q token rows (then output rows)
   int nt = 256;
   auto smem_for = [&](int n) {
     return (size_t)kUpdChan * n * (conv_states.cap + kMaxSpec + 1) * esize;
@@ -547,12 +540,14 @@ extern "C" int cconv_update(const void* x, int64_t x_row_stride, cconv_pool_t co
   const int64_t nblk = (int64_t)num_seqs * a.ctiles;
   if (nblk > 0x7fffffff) return CCONV_ERR_INVALID;
   const size_t smem = smem_for(nt);
-  // the channel-first block region must start on 16 bytes for every slot
-  if (a.pool.mode == kPoolDS && ((uintptr_t)conv_states.p % 16 != 0 ||
-                                 (conv_states.s_slot * esize) % 16 != 0 ||
-                                 ((int64_t)kUpdChan * nt * conv_states.cap * esize) % 16 != 0))
-    a.pool.mode = kPoolGeneric;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  // A channel-first pool whose slot slabs start on 16 bytes streams through
+  // the bulk-copy pipeline; anything else takes the block-per-request kernel.
+  if (a.pool.mode == kPoolDS) {
+    const cudaError_t eb = launch_update_bulk(a, width, dilation, dtype, esize, st);
+    if (eb != cudaErrorNotSupported) return eb == cudaSuccess ? CCONV_OK : CCONV_ERR_LAUNCH;
+    a.pool.mode = kPoolGeneric;
+  }
   const dim3 grid((unsigned)nblk);
   cudaError_t e = dtype == CCONV_DTYPE_F32
                       ? launch_upd<float>(width, dilation, grid, nt, smem, st, a)

@@ -1,0 +1,35 @@
+// Arguments of the decode / speculative-decode kernels (cconv_update) and the
+// launcher of the bulk-copy pipeline used for channel-first pools.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace cconv {
+
+struct UpdArgs {
+  const char* x;
+  int64_t x_rs;
+  Pool pool;
+  const char* w;
+  const char* bias;
+  const int32_t* state_idx;
+  int32_t B, n_spec;
+  const int32_t* num_accepted;
+  const uint8_t* has_init;
+  int32_t C, act, ctiles;
+  char* out;
+  int64_t out_rs;
+  int32_t* dev_err;
+};
+
+// Launches the persistent bulk-copy pipeline for a channel-first pool whose
+// per-slot slabs start on 16 bytes (Pool::mode == kPoolDS). Returns
+// cudaErrorNotSupported when the shapes do not fit it (the caller then uses
+// the block-per-request kernel).
+cudaError_t launch_update_bulk(UpdArgs a, int width, int dilation, int dtype, int esize,
+                               cudaStream_t st);
+
+}  // namespace cconv

@@ -151,6 +151,22 @@ def test_layouts_and_epilogues(layout, act, bias):
     check_upd(case)
 
 
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_update_decode_of_wide_buffer_keeps_extra_columns(dtype):
+    """n_spec == 0 on a channel-first buffer wider than S: columns >= S are
+    neither read nor changed, with or without history."""
+    case = synth.depthwise_case(309, DEV, lens=[], C=1032 if dtype == torch.bfloat16 else 516,
+                                width=4, dilation=2, act=1, dtype=dtype, w_std=0.5,
+                                bias_std=0.1, spec_requests=23, n_spec=0, cap=11)
+    g = torch.Generator(device=DEV).manual_seed(6)
+    case.spec_has_init = (torch.rand(23, generator=g, device=DEV) < 0.5).to(torch.uint8)
+    case.spec_state_idx[::5] = -1
+    check_upd(case)
+    _, pool = gpu_upd(case)
+    torch.cuda.synchronize()
+    assert torch.equal(pool[:, :, 6:], case.pool[:, :, 6:])
+
+
 def test_row_strides_and_untouched_rows():
     C = 1024
     case = synth.depthwise_case(302, DEV, lens=[5, 70, 3], C=C, width=4, dilation=1, act=1,
