@@ -68,6 +68,7 @@ struct Meta {
   int lo, len, g, own_lo, own_hi, pad0, pad1, pad2;
   int rowj[kRows];      // position of the row in its request, -1 outside every request
   int rowslot[kRows];   // slot whose history the row reads, -1 for a zero history
+  int rowwr[kRows];     // slot the row's producer writes at once (one-token request), else -1
 };
 
 struct Args {
@@ -216,30 +217,97 @@ struct Waiter {
 
 // ---- small helpers ---------------------------------------------------------
 
-__device__ __forceinline__ uint4 hist_load(const Pool& P, int slot, int c0, int col) {
-  const char* base = P.p + (int64_t)slot * P.s_slot * 2;
-  if (P.mode == cconv::kPoolSD)
-    return *reinterpret_cast<const uint4*>(base + ((int64_t)col * P.s_col + c0) * 2);
-  uint32_t h[8];
+// h[idx] for a runtime idx, by masks (zero when idx is outside [0, N)): a
+// select chain over a register array could be folded into an indexed, hence
+// local-memory, access.
+template <int N>
+__device__ __forceinline__ uint4 pick(const uint4 (&h)[N], int idx) {
+  uint4 r = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
-  for (int v = 0; v < 8; ++v)
-    h[v] = *reinterpret_cast<const uint16_t*>(
-        base + ((int64_t)(c0 + v) * P.s_chan + (int64_t)col * P.s_col) * 2);
-  return make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16),
-                    h[6] | (h[7] << 16));
+  for (int c = 0; c < N; ++c) {
+    const uint32_t m = 0u - static_cast<uint32_t>(c == idx);
+    r.x |= h[c].x & m;
+    r.y |= h[c].y & m;
+    r.z |= h[c].z & m;
+    r.w |= h[c].w & m;
+  }
+  return r;
 }
 
-__device__ __forceinline__ void hist_store(const Pool& P, int slot, int c0, int col, uint4 u) {
-  char* base = P.p + (int64_t)slot * P.s_slot * 2;
-  if (P.mode == cconv::kPoolSD) {
-    *reinterpret_cast<uint4*>(base + ((int64_t)col * P.s_col + c0) * 2) = u;
+// All NH history columns of channels c0 .. c0+7 of `slot`, one 16-byte unit
+// per column. Channel-first pools (cap == NH) hold the 8 x NH values in NH
+// contiguous units, interleaved by channel; column-first pools hold one unit
+// per column; any other stride goes element by element.
+template <int NH>
+__device__ __forceinline__ void hist_load_all(const Pool& P, int slot, int c0, uint4 (&h)[NH]) {
+  const char* base = P.p + (int64_t)slot * P.s_slot * 2;
+  if (P.mode == cconv::kPoolDS) {
+    uint32_t w[4 * NH];
+#pragma unroll
+    for (int k = 0; k < NH; ++k) {
+      const uint4 r = *reinterpret_cast<const uint4*>(base + (int64_t)c0 * NH * 2 + k * 16);
+      w[4 * k] = r.x;
+      w[4 * k + 1] = r.y;
+      w[4 * k + 2] = r.z;
+      w[4 * k + 3] = r.w;
+    }
+    auto el = [&](int i) { return (w[i >> 1] >> ((i & 1) * 16)) & 0xffffu; };
+#pragma unroll
+    for (int col = 0; col < NH; ++col)
+      h[col] = make_uint4(el(0 * NH + col) | (el(1 * NH + col) << 16),
+                          el(2 * NH + col) | (el(3 * NH + col) << 16),
+                          el(4 * NH + col) | (el(5 * NH + col) << 16),
+                          el(6 * NH + col) | (el(7 * NH + col) << 16));
     return;
   }
-  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-  for (int v = 0; v < 8; ++v)
-    *reinterpret_cast<uint16_t*>(base + ((int64_t)(c0 + v) * P.s_chan + (int64_t)col * P.s_col) *
-                                            2) = static_cast<uint16_t>(w[v >> 1] >> ((v & 1) * 16));
+  for (int col = 0; col < NH; ++col) {
+    if (P.mode == cconv::kPoolSD) {
+      h[col] = *reinterpret_cast<const uint4*>(base + ((int64_t)col * P.s_col + c0) * 2);
+    } else {
+      uint32_t e[8];
+#pragma unroll
+      for (int v = 0; v < 8; ++v)
+        e[v] = *reinterpret_cast<const uint16_t*>(
+            base + ((int64_t)(c0 + v) * P.s_chan + (int64_t)col * P.s_col) * 2);
+      h[col] = make_uint4(e[0] | (e[1] << 16), e[2] | (e[3] << 16), e[4] | (e[5] << 16),
+                          e[6] | (e[7] << 16));
+    }
+  }
+}
+
+template <int NH>
+__device__ __forceinline__ void hist_store_all(const Pool& P, int slot, int c0,
+                                               const uint4 (&h)[NH]) {
+  char* base = P.p + (int64_t)slot * P.s_slot * 2;
+  if (P.mode == cconv::kPoolDS) {
+    uint32_t e[8 * NH];   // e[v * NH + col]: channel v, column col
+#pragma unroll
+    for (int col = 0; col < NH; ++col) {
+      const uint32_t wd[4] = {h[col].x, h[col].y, h[col].z, h[col].w};
+#pragma unroll
+      for (int v = 0; v < 8; ++v) e[v * NH + col] = (wd[v >> 1] >> ((v & 1) * 16)) & 0xffffu;
+    }
+#pragma unroll
+    for (int k = 0; k < NH; ++k)
+      *reinterpret_cast<uint4*>(base + (int64_t)c0 * NH * 2 + k * 16) =
+          make_uint4(e[8 * k] | (e[8 * k + 1] << 16), e[8 * k + 2] | (e[8 * k + 3] << 16),
+                     e[8 * k + 4] | (e[8 * k + 5] << 16), e[8 * k + 6] | (e[8 * k + 7] << 16));
+    return;
+  }
+#pragma unroll
+  for (int col = 0; col < NH; ++col) {
+    if (P.mode == cconv::kPoolSD) {
+      *reinterpret_cast<uint4*>(base + ((int64_t)col * P.s_col + c0) * 2) = h[col];
+    } else {
+      const uint32_t wd[4] = {h[col].x, h[col].y, h[col].z, h[col].w};
+#pragma unroll
+      for (int v = 0; v < 8; ++v)
+        *reinterpret_cast<uint16_t*>(base + ((int64_t)(c0 + v) * P.s_chan +
+                                             (int64_t)col * P.s_col) * 2) =
+            static_cast<uint16_t>(wd[v >> 1] >> ((v & 1) * 16));
+    }
+  }
 }
 
 // Number of requests s in [0, B) with cu[s] <= p (strict: cu[s] < p), found by
@@ -385,15 +453,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool h = hini == nullptr || hini[sc] != 0;
         const bool ok = sl < a.pool.num_slots;
         const int slot = (h && sl >= 0) ? sl : -1;
+        const int wr = (ok && sl >= 0 && en0 - st0 == 1) ? sl : -1;
         for (int r = lane; r < kRows; r += 32) {
           M.rowj[r] = (ok && r < len) ? lo + r - st0 : -1;
           M.rowslot[r] = slot;
+          M.rowwr[r] = r == 0 ? wr : -1;
         }
       } else {
         for (int r0 = 0; r0 < kRows; r0 += 32) {
           const int r = r0 + lane;
           const int t = lo + r;
-          int j = -1, slot = -1;
+          int j = -1, slot = -1, wr = -1;
           if (r < len) {
             int sr = sc;
             while (sr + 1 < a.B && cu[sr + 1] <= t) ++sr;
@@ -404,11 +474,13 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (sl < a.pool.num_slots) {   // out-of-range slots are skipped and reported
                 j = t - st;
                 slot = (h && sl >= 0) ? sl : -1;
+                wr = (en - st == 1 && sl >= 0) ? sl : -1;
               }
             }
           }
           M.rowj[r] = j;
           M.rowslot[r] = slot;
+          M.rowwr[r] = wr;
           const int last = min(lo + r0 + 31, hi - 1);   // same walk on every lane
           while (sc + 1 < a.B && cu[sc + 1] <= last) ++sc;
         }
@@ -625,47 +697,75 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int v = 0; v < 8; ++v) xw[m][v] = xw[m - 1][v];
         }
       }
+      // Rows near a request start (or of one-token requests): each row's
+      // inputs are gathered individually, with the history of RB rows loaded
+      // before any of them is used.
+      constexpr int NHH = NH > 0 ? NH : 1;
+      constexpr int RB = NH <= 1 ? 4 : 2;
 #pragma unroll 1
-      for (int rr = 0; rr < (fast ? 0 : 8); ++rr) {
-        const int r = strip * 8 + rr;
-        uint4 outv[T1];
-        const int j = (r < len) ? M.rowj[r] : -1;
-        if (j < 0) {
+      for (int rb = 0; rb < (fast ? 0 : 8); rb += RB) {
+        uint4 hh[RB][NHH];
 #pragma unroll
-          for (int kt = 0; kt < T1; ++kt) outv[kt] = make_uint4(0u, 0u, 0u, 0u);
-        } else {
+        for (int qq = 0; qq < RB; ++qq) {
+          const int r = strip * 8 + rb + qq;
+          const int j = (r < len) ? M.rowj[r] : -1;
           const int hslot = M.rowslot[r];
-          constexpr int NW = T0 + T1 - 1;        // x~[j - m], m = 0 .. n
-          float xw[NW][8];
+          if (NH > 0 && j >= 0 && j < NH && hslot >= 0) {
+            hist_load_all<NHH>(a.pool, hslot, c0, hh[qq]);
+          } else {
 #pragma unroll
-          for (int m = 0; m < NW; ++m) {
-            uint4 raw;
-            if (j - m >= 0) {
-              raw = *reinterpret_cast<const uint4*>(xst + (r + NH - m) * kXRowBytes + kc * 16);
-            } else if (hslot >= 0) {
-              raw = hist_load(a.pool, hslot, c0, a.n + j - m);
-            } else {
-              raw = make_uint4(0u, 0u, 0u, 0u);
-            }
-            cconv::unpack16<__nv_bfloat16>(raw, xw[m]);
-          }
-#pragma unroll
-          for (int kt = 0; kt < T1; ++kt) {
-            const int mp = T1 - 1 - kt;          // u at j - mp
-            float uu[8];
-#pragma unroll
-            for (int v = 0; v < 8; ++v) {
-              float acc = b0[v];
-#pragma unroll
-              for (int k = 0; k < T0; ++k) acc = fmaf(w0[k][v], xw[mp + T0 - 1 - k][v], acc);
-              uu[v] = acc;
-            }
-            outv[kt] = cconv::pack16<__nv_bfloat16>(uu);
+            for (int c = 0; c < NHH; ++c) hh[qq][c] = make_uint4(0u, 0u, 0u, 0u);
           }
         }
 #pragma unroll
-        for (int kt = 0; kt < T1; ++kt)
-          *reinterpret_cast<uint4*>(sA + kt * kTapA + kc * kLboA + r * 16) = outv[kt];
+        for (int qq = 0; qq < RB; ++qq) {
+          const int r = strip * 8 + rb + qq;
+          uint4 outv[T1];
+          const int j = (r < len) ? M.rowj[r] : -1;
+          if (j < 0) {
+#pragma unroll
+            for (int kt = 0; kt < T1; ++kt) outv[kt] = make_uint4(0u, 0u, 0u, 0u);
+          } else {
+            constexpr int NW = T0 + T1 - 1;        // x~[j - m], m = 0 .. n
+            float xw[NW][8];
+#pragma unroll
+            for (int m = 0; m < NW; ++m) {
+              const uint4 raw =
+                  j - m >= 0
+                      ? *reinterpret_cast<const uint4*>(xst + (r + NH - m) * kXRowBytes + kc * 16)
+                      : pick<NHH>(hh[qq], NH + j - m);
+              cconv::unpack16<__nv_bfloat16>(raw, xw[m]);
+            }
+#pragma unroll
+            for (int kt = 0; kt < T1; ++kt) {
+              const int mp = T1 - 1 - kt;          // u at j - mp
+              float uu[8];
+#pragma unroll
+              for (int v = 0; v < 8; ++v) {
+                float acc = b0[v];
+#pragma unroll
+                for (int k = 0; k < T0; ++k) acc = fmaf(w0[k][v], xw[mp + T0 - 1 - k][v], acc);
+                uu[v] = acc;
+              }
+              outv[kt] = cconv::pack16<__nv_bfloat16>(uu);
+            }
+            // A one-token request's history is read by this row alone: its new
+            // state (history columns 1 .. n-1, then the token) is written here.
+            const int wr = M.rowwr[r];
+            if (NH > 0 && wr >= 0) {
+              uint4 ns[NHH];
+#pragma unroll
+              for (int c = 0; c < NHH; ++c)
+                ns[c] = c + 1 < NH ? hh[qq][(c + 1) % NHH]
+                                   : *reinterpret_cast<const uint4*>(xst + (r + NH) * kXRowBytes +
+                                                                     kc * 16);
+              hist_store_all<NHH>(a.pool, wr, c0, ns);
+            }
+          }
+#pragma unroll
+          for (int kt = 0; kt < T1; ++kt)
+            *reinterpret_cast<uint4*>(sA + kt * kTapA + kc * kLboA + r * 16) = outv[kt];
+        }
       }
       fence_proxy_async();
       __syncwarp();
@@ -691,16 +791,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (slot < 0) continue;
         const bool h = hini == nullptr || hini[s] != 0;
         const int L = en - st;
-        for (int col = 0; col < a.n; ++col) {
-          const int src = L - a.n + col;
-          uint4 v;
-          if (src >= 0)
-            v = cconv::ldg16(a.qk + ((int64_t)(st + src) * a.qk_rs + tc0) * 2);
-          else if (h)
-            v = hist_load(a.pool, slot, tc0, L + col);
-          else
-            v = make_uint4(0u, 0u, 0u, 0u);
-          hist_store(a.pool, slot, tc0, col, v);
+        if (L == 1) continue;   // written by the producer of its row
+        if (NH > 0) {
+          uint4 old[NHH], ns[NHH];
+          if (h && L < NH) {
+            hist_load_all<NHH>(a.pool, slot, tc0, old);
+          } else {
+#pragma unroll
+            for (int c = 0; c < NHH; ++c) old[c] = make_uint4(0u, 0u, 0u, 0u);
+          }
+#pragma unroll
+          for (int col = 0; col < NHH; ++col) {
+            const int src = L - NH + col;
+            ns[col] = src >= 0 ? cconv::ldg16(a.qk + ((int64_t)(st + src) * a.qk_rs + tc0) * 2)
+                               : pick<NHH>(old, L + col);
+          }
+          hist_store_all<NHH>(a.pool, slot, tc0, ns);
         }
       }
       // Delayed half of v (independent of the MMA; the producer warps are idle
@@ -868,10 +974,16 @@ extern "C" int cca_qk_conv(const void* qk, int64_t qk_row_stride, const void* w_
   a.pool.s_col = conv_state.s_col;
   a.pool.num_slots = conv_state.num_slots;
   a.pool.cap = conv_state.cap;
-  a.pool.mode = (conv_state.s_chan == 1 && al16(conv_state.p) && conv_state.s_col % 8 == 0 &&
-                 conv_state.s_slot % 8 == 0)
-                    ? cconv::kPoolSD
-                    : cconv::kPoolGeneric;
+  // channel-first with exactly n columns: a channel chunk's history is n
+  // contiguous 16-byte units; column-first: one unit per column
+  if (n > 0 && conv_state.s_col == 1 && conv_state.s_chan == n && conv_state.cap == n &&
+      al16(conv_state.p) && conv_state.s_slot % 8 == 0)
+    a.pool.mode = cconv::kPoolDS;
+  else if (conv_state.s_chan == 1 && al16(conv_state.p) && conv_state.s_col % 8 == 0 &&
+           conv_state.s_slot % 8 == 0)
+    a.pool.mode = cconv::kPoolSD;
+  else
+    a.pool.mode = cconv::kPoolGeneric;
   a.dstate = static_cast<char*>(delayed_state);
   a.dstate_rs = delayed_state_row_stride;
   a.state_idx = state_idx;
