@@ -17,11 +17,19 @@
 //               owned requests) into a 4-deep ring, and the TMA load of the
 //               tile's x rows (plus the history halo) into a 2-deep ring;
 //   warp 1      TMEM allocation and the single MMA-issuing thread;
-//   warps 2-5   epilogue: tcgen05.ld of the accumulator, bias, bf16 round,
-//               store; the delayed-v shift and delayed-state update;
-//   warps 6-13  producers: the depthwise stage for both taps (u at t-1 and t)
-//               straight into the two A operands in shared memory, the group's
-//               weights into the B operand, and the raw-history state writes.
+//   warps 2-9   epilogue: tcgen05.ld of the accumulator (two warps per TMEM
+//               lane quadrant, one half of the columns each), bias, bf16
+//               round, store;
+//   warps 10-13 producers: the depthwise stage straight into an A operand in
+//               shared memory, the group's weights into the B operand, and
+//               the new state of one-token requests;
+//   warps 14-15 aux: the delayed-v shift, the delayed state and the raw-history
+//               state of longer requests.
+// A tile whose rows are consecutive tokens of one request stores u once, for
+// rows -1 .. 127, and the MMA of tap t-1 reads it one row earlier (a 16-byte
+// shift of the descriptor's start address): half the depthwise work, and one
+// of two A buffers, so the depthwise stage of the next tile overlaps the MMA.
+// Other tiles store u(t) and u(t-1) per row, in both buffers.
 // Token tiles hold at most 128 rows and never split the first n tokens of a
 // request (the only tokens that read its history), so the tile that reads a
 // request's state is also the only one that writes it: one launch, no race,
@@ -30,6 +38,7 @@
 #include <cuda.h>
 
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 
 #include "async.cuh"
@@ -44,28 +53,33 @@ constexpr int kRows = 128;        // MMA M: rows (tokens) per tile
 constexpr int kMaxN = 4;          // history columns supported (t0 + t1 - 2)
 constexpr int kXStages = 2;
 constexpr int kMetaStages = 4;
-constexpr int kProdWarps = 8;
-constexpr int kEpiWarps = 4;
-constexpr int kWarpSched = 0, kWarpMma = 1, kWarpEpi0 = 2, kWarpProd0 = 2 + kEpiWarps;
-constexpr int kWarps = kWarpProd0 + kProdWarps;
+constexpr int kProdWarps = 4;
+constexpr int kEpiWarps = 8;
+constexpr int kAuxWarps = 2;
+constexpr int kWarpSched = 0, kWarpMma = 1, kWarpEpi0 = 2, kWarpProd0 = kWarpEpi0 + kEpiWarps;
+constexpr int kWarpAux0 = kWarpProd0 + kProdWarps;
+constexpr int kWarps = kWarpAux0 + kAuxWarps;
 constexpr int kThreads = kWarps * 32;
 constexpr int kXRowBytes = kGS * 2;                    // one tile row of a group: 256 B
 constexpr int kXBoxRows = kRows + kMaxN;               // rows per x stage
 constexpr int kXStageBytes = kXBoxRows * kXRowBytes;   // 33792 B
-constexpr int kLboA = kRows * 16 + 16;                 // padded k-chunk stride of A
-constexpr int kTapA = (kGS / 8) * kLboA;               // one tap of A: 33024 B
+constexpr int kLboA = (kRows + 1) * 16;                // k-chunk stride of A: rows -1 .. 127
+constexpr int kABuf = (kGS / 8) * kLboA;               // one A buffer: 33024 B
 constexpr int kLboB = kGS * 16;                        // k-chunk stride of B: 2048 B
 constexpr int kTapB = (kGS / 8) * kLboB;               // one tap of B: 32768 B
 constexpr int kAccCols = 128;                          // fp32 accumulator columns
 constexpr int kTmemCols = 2 * kAccCols;
 constexpr long long kWaitCycles = 2000000000LL;        // ~1 s at GB300 clocks
 constexpr int kDerrTimeout = CCONV_DERR_TIMEOUT;
-constexpr int kStageReqs = 1024;                       // index data staged in smem up to this
 constexpr int kOutRowPitch = 80;                       // 64 bytes of a row + 16 (no bank conflicts)
-constexpr int kOutStageBytes = 32 * kOutRowPitch + kGS * 4;   // per epilogue warp, + bias
+constexpr int kEpiCols = kGS / (kEpiWarps / 4);       // accumulator columns per epilogue warp
+constexpr int kProdRows = kRows / (kProdWarps * 2);    // rows per producer thread (16 per chunk)
+constexpr int kOutStageBytes = 32 * kOutRowPitch + kEpiCols * 4;   // per epilogue warp, + bias
 
 struct Meta {
-  int lo, len, g, own_lo, own_hi, pad0, pad1, pad2;
+  int lo, len, g, own_lo, own_hi;
+  int single;           // rows are consecutive tokens of one request (one A buffer)
+  int pad1, pad2;
   int rowj[kRows];      // position of the row in its request, -1 outside every request
   int rowslot[kRows];   // slot whose history the row reads, -1 for a zero history
   int rowwr[kRows];     // slot the row's producer writes at once (one-token request), else -1
@@ -89,8 +103,9 @@ struct Args {
   const int32_t* cu;
   const uint8_t* has_init;
   int32_t B, T, Cqk, G, n;
-  int32_t num_tiles, tile_pitch, units, units_per_cta;
-  int32_t staged;                                      // index data copied to smem
+  int32_t num_tiles, tile_pitch, units;
+  int32_t static_units;   // units per CTA in the static part of the split
+  int32_t epoch;          // this launch's slot of the work counters
   char* out;
   int64_t out_rs;
   char* dprev;
@@ -177,8 +192,9 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
 
 struct Ctl {
   uint64_t meta_full[kMetaStages], meta_empty[kMetaStages];
+  uint64_t prod_done[kMetaStages];   // producers have read the tile's history
   uint64_t x_full[kXStages], x_empty[kXStages];
-  uint64_t a_full, a_empty, prod_done;
+  uint64_t a_full[2], a_empty[2];
   uint64_t acc_full[2], acc_empty[2];
   uint32_t tmem_base;
   volatile int abort;
@@ -234,6 +250,19 @@ __device__ __forceinline__ uint4 pick(const uint4 (&h)[N], int idx) {
   return r;
 }
 
+// The NH columns of 8 channels from their channel-first words (channel v,
+// column col at 16-bit element v * NH + col).
+template <int NH>
+__device__ __forceinline__ void hist_from_words(const uint32_t (&w)[4 * NH], uint4 (&h)[NH]) {
+  auto el = [&](int i) { return (w[i >> 1] >> ((i & 1) * 16)) & 0xffffu; };
+#pragma unroll
+  for (int col = 0; col < NH; ++col)
+    h[col] = make_uint4(el(0 * NH + col) | (el(1 * NH + col) << 16),
+                        el(2 * NH + col) | (el(3 * NH + col) << 16),
+                        el(4 * NH + col) | (el(5 * NH + col) << 16),
+                        el(6 * NH + col) | (el(7 * NH + col) << 16));
+}
+
 // All NH history columns of channels c0 .. c0+7 of `slot`, one 16-byte unit
 // per column. Channel-first pools (cap == NH) hold the 8 x NH values in NH
 // contiguous units, interleaved by channel; column-first pools hold one unit
@@ -251,13 +280,7 @@ __device__ __forceinline__ void hist_load_all(const Pool& P, int slot, int c0, u
       w[4 * k + 2] = r.z;
       w[4 * k + 3] = r.w;
     }
-    auto el = [&](int i) { return (w[i >> 1] >> ((i & 1) * 16)) & 0xffffu; };
-#pragma unroll
-    for (int col = 0; col < NH; ++col)
-      h[col] = make_uint4(el(0 * NH + col) | (el(1 * NH + col) << 16),
-                          el(2 * NH + col) | (el(3 * NH + col) << 16),
-                          el(4 * NH + col) | (el(5 * NH + col) << 16),
-                          el(6 * NH + col) | (el(7 * NH + col) << 16));
+    hist_from_words<NH>(w, h);
     return;
   }
 #pragma unroll
@@ -348,56 +371,50 @@ __device__ int tile_edge(const Args& a, const int32_t* cu, int tau, int from) {
 
 // ---- the kernel ----------------------------------------------------------------
 
+// Work counters of the dynamic part of the split, one slot per launch in
+// flight (a launch takes slot epoch % kEpochs; its last CTA clears it).
+constexpr int kEpochs = 64;
+constexpr int kDynChunk = 2;                 // units per dynamic grab
+constexpr int kStaticPercent = 90;           // share of the units split statically
+__device__ unsigned int g_work_next[kEpochs];
+__device__ unsigned int g_work_done[kEpochs];
+
 template <int T0, int T1>
 __global__ void __launch_bounds__(kThreads, 1)
     cca_kernel(const __grid_constant__ CUtensorMap xmap, const Args a) {
   constexpr int NH = T0 + T1 - 2;               // history columns
+  constexpr int NHH = NH > 0 ? NH : 1;          // array extent for NH columns
+  constexpr int NW = T0 + T1 - 1;               // x~[j - m], m = 0 .. NH, per row
   extern __shared__ __align__(1024) unsigned char dsm[];
   // 1024-byte alignment as an offset on the shared pointer itself, so that every
   // pointer derived from it stays in the shared address space (a round trip
   // through an integer would turn all of them into generic accesses).
   unsigned char* base = dsm + ((1024u - (smem_u32(dsm) & 1023u)) & 1023u);
   unsigned char* sB = base;                          // T1 taps of B
-  unsigned char* sA = sB + T1 * kTapB;               // T1 taps of A
-  unsigned char* sX = sA + T1 * kTapA;               // x stages
+  unsigned char* sA = sB + T1 * kTapB;               // two A buffers
+  unsigned char* sX = sA + 2 * kABuf;                // x stages
   unsigned char* sOut = sX + kXStages * kXStageBytes;  // epilogue transpose buffers
   Meta* meta = reinterpret_cast<Meta*>(sOut + kEpiWarps * kOutStageBytes);
   Ctl* ctl = reinterpret_cast<Ctl*>(meta + kMetaStages);
-  // Request index data: the scheduler reads it many times per tile, so it is
-  // copied to shared memory once when it fits (cu, state_idx, has_init).
-  int32_t* s_cu = reinterpret_cast<int32_t*>(reinterpret_cast<unsigned char*>(ctl) +
-                                             ((sizeof(Ctl) + 15) / 16) * 16);
-  int32_t* s_idx = s_cu + ((a.B + 1 + 3) / 4) * 4;
-  uint8_t* s_hi = reinterpret_cast<uint8_t*>(s_idx + ((a.B + 3) / 4) * 4);
-  if (a.staged) {
-    for (int i = threadIdx.x; i <= a.B; i += blockDim.x) s_cu[i] = a.cu[i];
-    for (int i = threadIdx.x; i < a.B; i += blockDim.x) {
-      s_idx[i] = a.state_idx[i];
-      s_hi[i] = a.has_init ? a.has_init[i] : 1;
-    }
-  }
-  const int32_t* cu = a.staged ? s_cu : a.cu;
-  const int32_t* sidx = a.staged ? s_idx : a.state_idx;
-  const uint8_t* hini = a.staged ? s_hi : a.has_init;
+  const int32_t* cu = a.cu;
+  const int32_t* sidx = a.state_idx;
+  const uint8_t* hini = a.has_init;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int u0 = blockIdx.x * a.units_per_cta;
-  const int u1 = min(a.units, u0 + a.units_per_cta);
-  const int ntiles = max(u1 - u0, 0);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kMetaStages; ++i) {
       mbar_init(&ctl->meta_full[i], 1);
-      mbar_init(&ctl->meta_empty[i], kProdWarps + kEpiWarps);
+      mbar_init(&ctl->meta_empty[i], kProdWarps + kEpiWarps + kAuxWarps + 1);
+      mbar_init(&ctl->prod_done[i], kProdWarps);
     }
     for (int i = 0; i < kXStages; ++i) {
       mbar_init(&ctl->x_full[i], 1);
       mbar_init(&ctl->x_empty[i], kProdWarps);
     }
-    mbar_init(&ctl->a_full, kProdWarps);
-    mbar_init(&ctl->a_empty, 1);
-    mbar_init(&ctl->prod_done, kProdWarps);
     for (int i = 0; i < 2; ++i) {
+      mbar_init(&ctl->a_full[i], kProdWarps);
+      mbar_init(&ctl->a_empty[i], 1);
       mbar_init(&ctl->acc_full[i], 1);
       mbar_init(&ctl->acc_empty[i], kEpiWarps);
     }
@@ -430,11 +447,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (sidx[s] >= a.pool.num_slots) cconv::flag_error(a.dev_err, CCONV_DERR_SLOT_RANGE);
       }
     }
-    for (int i = 0; i < ntiles; ++i) {
-      const int u = u0 + i;
-      const int g = u / a.num_tiles, tau = u - g * a.num_tiles;
+    // Work split: units [c * S, (c + 1) * S) of CTA c first (one group's B
+    // for many consecutive tiles), then chunks of the remaining units from a
+    // counter shared by all CTAs, so that CTAs holding slow tiles (many
+    // requests, history reads) take fewer of them. A unit g < 0 in the meta
+    // ring tells every role to stop.
+    int cur = blockIdx.x * a.static_units, end = cur + a.static_units;
+    const int dyn0 = gridDim.x * a.static_units;
+    int i = 0;
+    for (;; ++i) {
       const int ms = i % kMetaStages, xs = i % kXStages;
       if (!W.wait(&ctl->meta_empty[ms], ((i / kMetaStages) & 1) ^ 1)) break;
+      if (cur >= end) {
+        int got = 0;
+        if (lane == 0) got = (int)atomicAdd(&g_work_next[a.epoch], (unsigned)kDynChunk);
+        got = __shfl_sync(0xffffffffu, got, 0);
+        cur = dyn0 + got;
+        end = min(cur + kDynChunk, a.units);
+      }
+      if (cur >= a.units) {
+        if (lane == 0) {
+          meta[ms].g = -1;
+          mbar_arrive(&ctl->meta_full[ms]);
+        }
+        __syncwarp();
+        break;
+      }
+      const int u = cur++;
+      const int g = u / a.num_tiles, tau = u - g * a.num_tiles;
       const bool cont = (g == prev_g && tau == prev_tau + 1);
       const int lo = cont ? hi_prev : tile_edge(a, cu, tau, 0);
       const int own_lo = cont ? own_hi_prev : count_le(cu, a.B, lo, true, 0);
@@ -447,8 +487,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       // row -> request; sc = request holding row lo
       int sc = max(nle_lo - 1, 0);
       const int st0 = cu[sc], en0 = cu[sc + 1];
+      int single = 0;
       if (st0 >= 0 && st0 <= lo && en0 >= hi && en0 <= a.T) {
-        // the whole tile lies inside one request
+        // the whole tile lies inside one request: row r's previous token is
+        // row r - 1 (row -1 for r = 0)
         const int sl = sidx[sc];
         const bool h = hini == nullptr || hini[sc] != 0;
         const bool ok = sl < a.pool.num_slots;
@@ -459,6 +501,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           M.rowslot[r] = slot;
           M.rowwr[r] = r == 0 ? wr : -1;
         }
+        single = ok ? 1 : 0;
       } else {
         for (int r0 = 0; r0 < kRows; r0 += 32) {
           const int r = r0 + lane;
@@ -491,6 +534,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         M.g = g;
         M.own_lo = own_lo;
         M.own_hi = own_hi;
+        M.single = single;
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&ctl->meta_full[ms]);
@@ -516,48 +560,66 @@ __global__ void __launch_bounds__(kThreads, 1)
       W.drain(&ctl->x_full[i % kXStages], (i / kXStages) & 1);
   } else if (warp == kWarpMma) {
     // ------------------------------------------------------------------ MMA
+    // A tile uses one A buffer (single: u rows -1 .. 127, tap kt reads rows
+    // shifted by kt - (T1 - 1)) or two (u(j) and u(j-1) per row); `abuf`
+    // counts buffer uses, buffer = use & 1, phase parity = (use >> 1) & 1.
     constexpr uint32_t idesc = idesc_bf16(kRows, kGS);
     const uint32_t a_addr = smem_u32(sA), b_addr = smem_u32(sB);
-    int done = 0;
-    for (int i = 0; i < ntiles; ++i) {
-      const int ab = i & 1;
-      if (!W.wait(&ctl->a_full, i & 1)) break;
-      if (!W.wait(&ctl->acc_empty[ab], ((i >> 1) & 1) ^ 1)) break;
+    int abuf = 0;
+    for (int i = 0;; ++i) {
+      const int ms = i % kMetaStages, ab = i & 1;
+      if (!W.wait(&ctl->meta_full[ms], (i / kMetaStages) & 1)) break;
+      if (meta[ms].g < 0) break;
+      const bool single = (T1 == 1) || meta[ms].single;
+      const int uses = single ? 1 : 2;
+      bool ok = true;
+      for (int u = 0; u < uses && ok; ++u)
+        ok = W.wait(&ctl->a_full[(abuf + u) & 1], ((abuf + u) >> 1) & 1);
+      if (!ok || !W.wait(&ctl->acc_empty[ab], ((i >> 1) & 1) ^ 1)) break;
       tc_fence_after();
       if (lane == 0) {
         const uint32_t d = tmem + ab * kAccCols;
+        const uint32_t au = a_addr + (abuf & 1) * kABuf + 16;          // u(j) of row 0
+        const uint32_t ap = a_addr + ((abuf + 1) & 1) * kABuf + 16;    // u(j-1) of row 0
 #pragma unroll
         for (int kt = 0; kt < T1; ++kt) {
+          // tap kt multiplies u(j - (T1 - 1 - kt))
+          const uint32_t at = (kt == T1 - 1) ? au : (single ? au - 16 : ap);
 #pragma unroll
           for (int ks = 0; ks < kGS / 16; ++ks) {
-            const uint64_t ad =
-                smem_desc(a_addr + kt * kTapA + 2 * ks * kLboA, kLboA, 128);
-            const uint64_t bd =
-                smem_desc(b_addr + kt * kTapB + 2 * ks * kLboB, kLboB, 128);
+            const uint64_t ad = smem_desc(at + 2 * ks * kLboA, kLboA, 128);
+            const uint64_t bd = smem_desc(b_addr + kt * kTapB + 2 * ks * kLboB, kLboB, 128);
             mma_bf16(d, ad, bd, idesc, (kt | ks) != 0 ? 1u : 0u);
           }
         }
-        mma_commit(&ctl->a_empty);
+        for (int u = 0; u < uses; ++u) mma_commit(&ctl->a_empty[(abuf + u) & 1]);
         mma_commit(&ctl->acc_full[ab]);
       }
       __syncwarp();
-      done = i + 1;
+      if (lane == 0) mbar_arrive(&ctl->meta_empty[ms]);
+      abuf += uses;
     }
     // drain: every issued MMA completes before TMEM is released
-    if (done > 0) W.drain(&ctl->a_empty, (done - 1) & 1);
+    if (abuf > 0) W.drain(&ctl->a_empty[(abuf - 1) & 1], ((abuf - 1) >> 1) & 1);
   } else if (warp < kWarpProd0) {
     // ------------------------------------------------------------- epilogue
-    const int q = warp & 3;                      // TMEM lane quadrant of this warp
+    // Warp w reads TMEM lanes 32 * (w % 4) .. + 31 (its rows) and one half of
+    // the 128 accumulator columns.
+    const int q = warp & 3;
     const int ew = warp - kWarpEpi0;
+    const int half = ew >> 2;                    // which kEpiCols columns
     unsigned char* stage = sOut + ew * kOutStageBytes;   // 32 rows x 64 bytes, padded
-    float* sbias = reinterpret_cast<float*>(stage + 32 * kOutRowPitch);
-    for (int i = 0; i < ntiles; ++i) {
+    float* sbias = reinterpret_cast<float*>(stage + 32 * kOutRowPitch);   // this half's bias
+    for (int i = 0;; ++i) {
       const int ms = i % kMetaStages, ab = i & 1;
       if (!W.wait(&ctl->meta_full[ms], (i / kMetaStages) & 1)) break;
+      if (meta[ms].g < 0) break;
       const Meta& M = meta[ms];
       const int g = M.g, lo = M.lo, len = M.len;
-      for (int k = lane; k < kGS; k += 32)
-        sbias[k] = a.b_gr ? cconv::load_f32<__nv_bfloat16>(a.b_gr, (int64_t)g * kGS + k) : 0.0f;
+      for (int k = lane; k < kEpiCols; k += 32)
+        sbias[k] = a.b_gr ? cconv::load_f32<__nv_bfloat16>(a.b_gr, (int64_t)g * kGS +
+                                                                     half * kEpiCols + k)
+                          : 0.0f;
 
       // q/k outputs: TMEM -> +bias -> bf16 -> shared-memory transpose -> global,
       // 32 columns at a time (the next 32 columns' TMEM load in flight), so that
@@ -565,15 +627,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!W.wait(&ctl->acc_full[ab], (i >> 1) & 1)) break;
       tc_fence_after();
       const int seg = lane & 3;
-      const uint32_t tbase = tmem + (static_cast<uint32_t>(q * 32) << 16) + ab * kAccCols;
+      const uint32_t tbase =
+          tmem + (static_cast<uint32_t>(q * 32) << 16) + ab * kAccCols + half * kEpiCols;
       uint32_t ra[32], rb[32];
       tmem_ld32(tbase, ra);
 #pragma unroll
-      for (int c = 0; c < kGS / 32; ++c) {
+      for (int c = 0; c < kEpiCols / 32; ++c) {
         uint32_t (&cur)[32] = (c & 1) ? rb : ra;
         uint32_t (&nxt)[32] = (c & 1) ? ra : rb;
         tmem_wait_ld();
-        if (c + 1 < kGS / 32) tmem_ld32(tbase + (c + 1) * 32, nxt);
+        if (c + 1 < kEpiCols / 32) tmem_ld32(tbase + (c + 1) * 32, nxt);
 #pragma unroll
         for (int k = 0; k < 32; k += 8) {
           const float4 b0v = *reinterpret_cast<const float4*>(sbias + c * 32 + k);
@@ -592,8 +655,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int tr = q * 32 + rr;            // row within the tile
           const uint4 v = *reinterpret_cast<const uint4*>(stage + rr * kOutRowPitch + seg * 16);
           if (tr < len && M.rowj[tr] >= 0)
-            cconv::stg16(a.out + ((int64_t)(lo + tr) * a.out_rs + (int64_t)g * kGS + c * 32 +
-                                  seg * 8) * 2, v);
+            cconv::stg16(a.out + ((int64_t)(lo + tr) * a.out_rs + (int64_t)g * kGS +
+                                  half * kEpiCols + c * 32 + seg * 8) * 2, v);
         }
         __syncwarp();
       }
@@ -604,26 +667,37 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(&ctl->meta_empty[ms]);
       }
     }
-  } else {
+  } else if (warp < kWarpAux0) {
     // ------------------------------------------------------------- producers
-    const int p = threadIdx.x - kWarpProd0 * 32;   // 0 .. 255
-    const int kc = p & 15;                         // 8-channel chunk within the group
-    const int pw = warp - kWarpProd0;              // producer warp 0 .. 7
-    const int dunits = a.Dv / 8;                   // 16-byte units per delayed row
-    const int strip = p >> 4;                      // rows strip*8 .. strip*8+7
-    int cur_g = -1;
+    // Thread p: channel chunk kc (8 channels) of rows kProdRows * strip .. + kProdRows-1.
+    const int p = threadIdx.x - kWarpProd0 * 32;   // 0 .. 32 * kProdWarps - 1
+    const int kc = p & 15;
+    const int strip = p >> 4;                      // 0 .. 2 * kProdWarps - 1
+    int cur_g = -1, abuf = 0;
     float w0[T0][8], b0[8];
-    for (int i = 0; i < ntiles; ++i) {
+    for (int i = 0;; ++i) {
       const int ms = i % kMetaStages, xs = i % kXStages;
       if (!W.wait(&ctl->meta_full[ms], (i / kMetaStages) & 1)) break;
+      if (meta[ms].g < 0) break;
       const Meta& M = meta[ms];
-      const int g = M.g, lo = M.lo, len = M.len;
+      const int g = M.g, len = M.len;
+      const bool single = (T1 == 1) || M.single;
+      const int uses = single ? 1 : 2;
+      // A new group rewrites B: every MMA issued so far must be done with it.
+      const int need = (g != cur_g) ? 2 : uses;
       if (!W.wait(&ctl->x_full[xs], (i / kXStages) & 1)) break;
-      if (!W.wait(&ctl->a_empty, (i & 1) ^ 1)) break;   // MMA of the previous tile done
+      bool ok = true;
+      for (int u = 0; u < need && ok; ++u)
+        ok = W.wait(&ctl->a_empty[(abuf + u) & 1], (((abuf + u) >> 1) & 1) ^ 1);
+      if (!ok) break;
       const int c0 = g * kGS + kc * 8;
       if (g != cur_g) {
         // B operand of group g: B[tap][k-chunk][n] = w_gr[g*128 + n][k-chunk*8 + e][tap]
-        for (int pr = p; pr < kGS * (kGS / 8); pr += kProdWarps * 32) {
+        // (unrolled so that several rows' loads are in flight at once)
+        constexpr int kBIter = kGS * (kGS / 8) / (kProdWarps * 32);
+#pragma unroll 8
+        for (int it = 0; it < kBIter; ++it) {
+          const int pr = p + it * (kProdWarps * 32);
           const int o = pr & (kGS - 1), bkc = pr >> 7;
           const char* src = a.w_gr + ((int64_t)(g * kGS + o) * kGS + bkc * 8) * T1 * 2;
           uint32_t e[8 * T1];
@@ -658,38 +732,193 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         cur_g = g;
       }
-      // A operands: A[tap kt][k-chunk][row] = u(j - (T1-1-kt)) of the row's request
+      // u(j) of row r goes to Au + r*16; two-tap tiles put u(j-1) at Ap + r*16.
+      unsigned char* Au = sA + (abuf & 1) * kABuf + kc * kLboA + 16;
+      unsigned char* Ap = sA + ((abuf + 1) & 1) * kABuf + kc * kLboA + 16;
       const unsigned char* xst = sX + xs * kXStageBytes;
-      const int rs0 = strip * 8;
-      const int jf = rs0 + 7 < len ? M.rowj[rs0] : -1;
-      const bool fast = jf >= NH && M.rowj[rs0 + 7] == jf + 7;
-      if (fast) {
-        // The strip's 8 rows are consecutive tokens of one request past its
-        // history: all 8 + n x rows are loaded at once, then a register window
-        // slides over them (one load per row instead of n + 1).
-        uint4 raw[8 + NH];
+      // xw[m] = x~[j - m] of the row -> its u(j) (and u(j-1))
+      auto put = [&](int r, const float (&xw)[NW][8]) {
+        float uu[8];
 #pragma unroll
-        for (int k = 0; k < 8 + NH; ++k)
-          raw[k] = *reinterpret_cast<const uint4*>(xst + (rs0 + k) * kXRowBytes + kc * 16);
-        float xw[NH + 1][8];             // xw[m] = x~[j - m] of the current row
+        for (int v = 0; v < 8; ++v) {
+          float acc = b0[v];
 #pragma unroll
-        for (int m = 1; m <= NH; ++m) cconv::unpack16<__nv_bfloat16>(raw[NH - m], xw[m]);
+          for (int k = 0; k < T0; ++k) acc = fmaf(w0[k][v], xw[T0 - 1 - k][v], acc);
+          uu[v] = acc;
+        }
+        *reinterpret_cast<uint4*>(Au + r * 16) = cconv::pack16<__nv_bfloat16>(uu);
+        if (T1 == 2 && !single) {
+#pragma unroll
+          for (int v = 0; v < 8; ++v) {
+            float acc = b0[v];
+#pragma unroll
+            for (int k = 0; k < T0; ++k) acc = fmaf(w0[k][v], xw[(T0 - k) % NW][v], acc);
+            uu[v] = acc;
+          }
+          *reinterpret_cast<uint4*>(Ap + r * 16) = cconv::pack16<__nv_bfloat16>(uu);
+        }
+      };
+      // Row -1 of a single-buffer tile: u at the token before row 0. (Before
+      // the rows: a one-token request's row rewrites the history it reads.)
+      if (T1 == 2 && single && strip == 0 && len > 0 && M.rowj[0] >= 0) {
+        const int j = M.rowj[0] - 1;
+        uint4 h1[NHH];
+        const int hslot = M.rowslot[0];
+        if (NH > 0 && j < T0 - 1 && hslot >= 0) {
+          hist_load_all<NHH>(a.pool, hslot, c0, h1);
+        } else {
+#pragma unroll
+          for (int c = 0; c < NHH; ++c) h1[c] = make_uint4(0u, 0u, 0u, 0u);
+        }
+        float uu[8];
+#pragma unroll
+        for (int v = 0; v < 8; ++v) uu[v] = b0[v];
+#pragma unroll
+        for (int k = 0; k < T0; ++k) {
+          const int m = T0 - 1 - k;   // x~[j - m]; stage row of token j - m is NH - 1 - m
+          const uint4 raw =
+              j - m >= 0
+                  ? *reinterpret_cast<const uint4*>(xst + (NH - 1 - m) * kXRowBytes + kc * 16)
+                  : pick<NHH>(h1, NH + j - m);
+          float xv[8];
+          cconv::unpack16<__nv_bfloat16>(raw, xv);
+#pragma unroll
+          for (int v = 0; v < 8; ++v) uu[v] = fmaf(w0[k][v], xv[v], uu[v]);
+        }
+        *reinterpret_cast<uint4*>(Au - 16) = cconv::pack16<__nv_bfloat16>(uu);
+      }
+      // History of the rows that read it (j < n, with a slot): in two-tap
+      // tiles with n <= 2 it is prefetched with cp.async into the row's own
+      // 16-byte slots of both A buffers (free until the row's A values
+      // overwrite them), so a tile of one-token requests waits for one round
+      // of loads; otherwise it is loaded when the row is computed.
+      constexpr bool kScratch = (T1 == 2) && (NH >= 1) && (NH <= 2);
+      const bool scratch = kScratch && !single && a.pool.mode != cconv::kPoolGeneric;
+      if (scratch) {
+#pragma unroll 1
+        for (int rr = 0; rr < kProdRows; ++rr) {
+          const int r = strip * kProdRows + rr;
+          const int j = r < len ? M.rowj[r] : -1;
+          const int hslot = M.rowslot[r];
+          if (j >= 0 && j < NH && hslot >= 0) {
+            const char* hb = a.pool.p + (int64_t)hslot * a.pool.s_slot * 2;
+            const char* s0 = a.pool.mode == cconv::kPoolDS ? hb + (int64_t)c0 * NH * 2
+                                                           : hb + (int64_t)c0 * 2;
+            const char* s1 = a.pool.mode == cconv::kPoolDS ? s0 + 16
+                                                           : hb + (a.pool.s_col + c0) * 2;
+            cconv::cp_async16(smem_u32(Au + r * 16), s0, true);
+            if (NH == 2) cconv::cp_async16(smem_u32(Ap + r * 16), s1, true);
+          }
+        }
+        cconv::cp_async_commit();
+        cconv::cp_async_wait<0>();
+      }
+      // the history columns of row r
+      auto hist_of = [&](int r, int hslot, uint4 (&h)[NHH]) {
+        if (kScratch && scratch) {
+          const uint4 s0 = *reinterpret_cast<const uint4*>(Au + r * 16);
+          const uint4 s1 = NH == 2 ? *reinterpret_cast<const uint4*>(Ap + r * 16) : s0;
+          if (a.pool.mode == cconv::kPoolDS) {
+            uint32_t w[4 * NHH];
+            w[0] = s0.x;
+            w[1] = s0.y;
+            w[2] = s0.z;
+            w[3] = s0.w;
+            if (NH == 2) {
+              w[(4 % (4 * NHH))] = s1.x;
+              w[(5 % (4 * NHH))] = s1.y;
+              w[(6 % (4 * NHH))] = s1.z;
+              w[(7 % (4 * NHH))] = s1.w;
+            }
+            hist_from_words<NHH>(w, h);
+          } else {
+            h[0] = s0;
+            if (NH == 2) h[1 % NHH] = s1;
+          }
+        } else {
+          hist_load_all<NHH>(a.pool, hslot, c0, h);
+        }
+      };
+#pragma unroll 1
+      for (int sub = 0; sub < kProdRows / 8; ++sub) {
+        const int rs0 = strip * kProdRows + sub * 8;
+        const int jf = rs0 < len ? M.rowj[rs0] : -1;
+        // consecutive tokens of one request past its history (rows past the
+        // tile of a one-request tile are computed and never stored)
+        const bool fast =
+            jf >= NH && (M.single || (rs0 + 7 < len && M.rowj[rs0 + 7] == jf + 7));
+        if (fast) {
+          // all 8 + n x rows are loaded at once, then a register window
+          // slides over them
+          uint4 raw[8 + NH];
+#pragma unroll
+          for (int k = 0; k < 8 + NH; ++k)
+            raw[k] = *reinterpret_cast<const uint4*>(xst + (rs0 + k) * kXRowBytes + kc * 16);
+          float xw[NW][8];
+#pragma unroll
+          for (int m = 1; m <= NH; ++m) cconv::unpack16<__nv_bfloat16>(raw[NH - m], xw[m]);
+#pragma unroll
+          for (int rr = 0; rr < 8; ++rr) {
+            cconv::unpack16<__nv_bfloat16>(raw[rr + NH], xw[0]);
+            put(rs0 + rr, xw);
+#pragma unroll
+            for (int m = NH; m >= 1; --m)
+#pragma unroll
+              for (int v = 0; v < 8; ++v) xw[m][v] = xw[m - 1][v];
+          }
+          continue;
+        }
+        // Mixed rows: the same window, with the inputs before a request's
+        // start taken from its history and zeros for rows outside every
+        // request.
+        float xw[NW][8];
+#pragma unroll
+        for (int m = 1; m <= NH; ++m)
+          cconv::unpack16<__nv_bfloat16>(
+              *reinterpret_cast<const uint4*>(xst + (rs0 + NH - m) * kXRowBytes + kc * 16), xw[m]);
 #pragma unroll
         for (int rr = 0; rr < 8; ++rr) {
-          cconv::unpack16<__nv_bfloat16>(raw[rr + NH], xw[0]);
+          const int r = rs0 + rr;
+          const uint4 cur = *reinterpret_cast<const uint4*>(xst + (r + NH) * kXRowBytes + kc * 16);
+          cconv::unpack16<__nv_bfloat16>(cur, xw[0]);
+          const int j = r < len ? M.rowj[r] : -1;
+          if (j < 0) {
+            const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+            *reinterpret_cast<uint4*>(Au + r * 16) = z;
+            if (T1 == 2 && !single) *reinterpret_cast<uint4*>(Ap + r * 16) = z;
+          } else if (j >= NH) {
+            put(r, xw);
+          } else {
+            uint4 hh[NHH];
+            const int hslot = M.rowslot[r];
+            if (hslot >= 0) {
+              hist_of(r, hslot, hh);
+            } else {
 #pragma unroll
-          for (int kt = 0; kt < T1; ++kt) {
-            const int mp = T1 - 1 - kt;
-            float uu[8];
-#pragma unroll
-            for (int v = 0; v < 8; ++v) {
-              float acc = b0[v];
-#pragma unroll
-              for (int k = 0; k < T0; ++k) acc = fmaf(w0[k][v], xw[mp + T0 - 1 - k][v], acc);
-              uu[v] = acc;
+              for (int c = 0; c < NHH; ++c) hh[c] = make_uint4(0u, 0u, 0u, 0u);
             }
-            *reinterpret_cast<uint4*>(sA + kt * kTapA + kc * kLboA + (rs0 + rr) * 16) =
-                cconv::pack16<__nv_bfloat16>(uu);
+            float xv[NW][8];
+#pragma unroll
+            for (int v = 0; v < 8; ++v) xv[0][v] = xw[0][v];
+#pragma unroll
+            for (int m = 1; m < NW; ++m) {
+              if (m <= j) {
+#pragma unroll
+                for (int v = 0; v < 8; ++v) xv[m][v] = xw[m][v];
+              } else {
+                cconv::unpack16<__nv_bfloat16>(pick<NHH>(hh, NH + j - m), xv[m]);
+              }
+            }
+            put(r, xv);
+            // A one-token request's history is read by this row alone: its new
+            // state (history columns 1 .. n-1, then the token) is written here.
+            const int wr = M.rowwr[r];
+            if (NH > 0 && wr >= 0) {
+              uint4 ns[NHH];
+#pragma unroll
+              for (int c = 0; c < NHH; ++c) ns[c] = c + 1 < NH ? hh[(c + 1) % NHH] : cur;
+              hist_store_all<NHH>(a.pool, wr, c0, ns);
+            }
           }
 #pragma unroll
           for (int m = NH; m >= 1; --m)
@@ -697,129 +926,38 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int v = 0; v < 8; ++v) xw[m][v] = xw[m - 1][v];
         }
       }
-      // Rows near a request start (or of one-token requests): each row's
-      // inputs are gathered individually, with the history of RB rows loaded
-      // before any of them is used.
-      constexpr int NHH = NH > 0 ? NH : 1;
-      constexpr int RB = NH <= 1 ? 4 : 2;
-#pragma unroll 1
-      for (int rb = 0; rb < (fast ? 0 : 8); rb += RB) {
-        uint4 hh[RB][NHH];
-#pragma unroll
-        for (int qq = 0; qq < RB; ++qq) {
-          const int r = strip * 8 + rb + qq;
-          const int j = (r < len) ? M.rowj[r] : -1;
-          const int hslot = M.rowslot[r];
-          if (NH > 0 && j >= 0 && j < NH && hslot >= 0) {
-            hist_load_all<NHH>(a.pool, hslot, c0, hh[qq]);
-          } else {
-#pragma unroll
-            for (int c = 0; c < NHH; ++c) hh[qq][c] = make_uint4(0u, 0u, 0u, 0u);
-          }
-        }
-#pragma unroll
-        for (int qq = 0; qq < RB; ++qq) {
-          const int r = strip * 8 + rb + qq;
-          uint4 outv[T1];
-          const int j = (r < len) ? M.rowj[r] : -1;
-          if (j < 0) {
-#pragma unroll
-            for (int kt = 0; kt < T1; ++kt) outv[kt] = make_uint4(0u, 0u, 0u, 0u);
-          } else {
-            constexpr int NW = T0 + T1 - 1;        // x~[j - m], m = 0 .. n
-            float xw[NW][8];
-#pragma unroll
-            for (int m = 0; m < NW; ++m) {
-              const uint4 raw =
-                  j - m >= 0
-                      ? *reinterpret_cast<const uint4*>(xst + (r + NH - m) * kXRowBytes + kc * 16)
-                      : pick<NHH>(hh[qq], NH + j - m);
-              cconv::unpack16<__nv_bfloat16>(raw, xw[m]);
-            }
-#pragma unroll
-            for (int kt = 0; kt < T1; ++kt) {
-              const int mp = T1 - 1 - kt;          // u at j - mp
-              float uu[8];
-#pragma unroll
-              for (int v = 0; v < 8; ++v) {
-                float acc = b0[v];
-#pragma unroll
-                for (int k = 0; k < T0; ++k) acc = fmaf(w0[k][v], xw[mp + T0 - 1 - k][v], acc);
-                uu[v] = acc;
-              }
-              outv[kt] = cconv::pack16<__nv_bfloat16>(uu);
-            }
-            // A one-token request's history is read by this row alone: its new
-            // state (history columns 1 .. n-1, then the token) is written here.
-            const int wr = M.rowwr[r];
-            if (NH > 0 && wr >= 0) {
-              uint4 ns[NHH];
-#pragma unroll
-              for (int c = 0; c < NHH; ++c)
-                ns[c] = c + 1 < NH ? hh[qq][(c + 1) % NHH]
-                                   : *reinterpret_cast<const uint4*>(xst + (r + NH) * kXRowBytes +
-                                                                     kc * 16);
-              hist_store_all<NHH>(a.pool, wr, c0, ns);
-            }
-          }
-#pragma unroll
-          for (int kt = 0; kt < T1; ++kt)
-            *reinterpret_cast<uint4*>(sA + kt * kTapA + kc * kLboA + r * 16) = outv[kt];
-        }
-      }
       fence_proxy_async();
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive(&ctl->a_full);
+        for (int u = 0; u < uses; ++u) mbar_arrive(&ctl->a_full[(abuf + u) & 1]);
         mbar_arrive(&ctl->x_empty[xs]);
-        mbar_arrive(&ctl->prod_done);
+        mbar_arrive(&ctl->prod_done[ms]);
+        mbar_arrive(&ctl->meta_empty[ms]);
       }
-      // raw-history state of owned requests (all history reads of this tile
-      // are done once every producer warp has arrived)
-      if (!W.wait(&ctl->prod_done, i & 1)) break;
-      const int nown = M.own_hi - M.own_lo;
-      for (int task = p; task < nown * (kGS / 8); task += kProdWarps * 32) {
-        const int s = M.own_lo + (task >> 4);
-        const int tc0 = g * kGS + (task & 15) * 8;
-        const int st = cu[s], en = cu[s + 1];
-        const int slot = sidx[s];
-        if (st < 0 || en < st || en > a.T) continue;
-        if (slot >= a.pool.num_slots) {
-          if ((task & 15) == 0) cconv::flag_error(a.dev_err, CCONV_DERR_SLOT_RANGE);
-          continue;
-        }
-        if (slot < 0) continue;
-        const bool h = hini == nullptr || hini[s] != 0;
-        const int L = en - st;
-        if (L == 1) continue;   // written by the producer of its row
-        if (NH > 0) {
-          uint4 old[NHH], ns[NHH];
-          if (h && L < NH) {
-            hist_load_all<NHH>(a.pool, slot, tc0, old);
-          } else {
-#pragma unroll
-            for (int c = 0; c < NHH; ++c) old[c] = make_uint4(0u, 0u, 0u, 0u);
-          }
-#pragma unroll
-          for (int col = 0; col < NHH; ++col) {
-            const int src = L - NH + col;
-            ns[col] = src >= 0 ? cconv::ldg16(a.qk + ((int64_t)(st + src) * a.qk_rs + tc0) * 2)
-                               : pick<NHH>(old, L + col);
-          }
-          hist_store_all<NHH>(a.pool, slot, tc0, ns);
-        }
-      }
-      // Delayed half of v (independent of the MMA; the producer warps are idle
-      // until the next tile). Rows r = g, g+G, ... of the tile with j >= 1 take
-      // the previous token's value; four rows' loads are issued before their
-      // stores.
+      abuf += uses;
+    }
+  } else {
+    // ------------------------------------------------------------------ aux
+    // The delayed half of v, the delayed state and the raw-history state of
+    // owned multi-token requests: none of it feeds the MMA.
+    const int aw = warp - kWarpAux0;               // 0 .. kAuxWarps-1
+    const int pa = threadIdx.x - kWarpAux0 * 32;   // 0 .. 32*kAuxWarps-1
+    const int dunits = a.Dv / 8;                   // 16-byte units per delayed row
+    for (int i = 0;; ++i) {
+      const int ms = i % kMetaStages;
+      if (!W.wait(&ctl->meta_full[ms], (i / kMetaStages) & 1)) break;
+      if (meta[ms].g < 0) break;
+      const Meta& M = meta[ms];
+      const int g = M.g, lo = M.lo, len = M.len;
+      // Rows r = g, g+G, ... of the tile with j >= 1 take the previous token's
+      // value; four rows' loads are issued before their stores.
       for (int k = lane; k < dunits; k += 32) {
-        for (int rb = g + pw * a.G; rb < len; rb += 4 * kProdWarps * a.G) {
+        for (int rb = g + aw * a.G; rb < len; rb += 4 * kAuxWarps * a.G) {
           uint4 v[4];
           bool ok[4];
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
-            const int r = rb + u * kProdWarps * a.G;
+            const int r = rb + u * kAuxWarps * a.G;
             ok[u] = r < len && M.rowj[r] >= 1;
             if (ok[u])
               v[u] = cconv::ldg16(a.delayed + ((int64_t)(lo + r - 1) * a.delayed_rs + k * 8) * 2);
@@ -827,13 +965,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int u = 0; u < 4; ++u)
             if (ok[u])
-              cconv::stg16(a.dprev + ((int64_t)(lo + rb + u * kProdWarps * a.G) * a.dprev_rs +
+              cconv::stg16(a.dprev + ((int64_t)(lo + rb + u * kAuxWarps * a.G) * a.dprev_rs +
                                       k * 8) * 2, v[u]);
         }
       }
       // owned requests s with s % G == g: first delayed value and delayed state
-      for (int s = M.own_lo + ((g - M.own_lo % a.G) % a.G + a.G) % a.G + pw * a.G;
-           s < M.own_hi; s += kProdWarps * a.G) {
+      for (int s = M.own_lo + ((g - M.own_lo % a.G) % a.G + a.G) % a.G + aw * a.G;
+           s < M.own_hi; s += kAuxWarps * a.G) {
         const int st = cu[s], en = cu[s + 1];
         const int slot = sidx[s];
         if (st < 0 || en < st || en > a.T) {
@@ -854,8 +992,42 @@ __global__ void __launch_bounds__(kThreads, 1)
             *reinterpret_cast<uint4*>(a.dstate + ((int64_t)slot * a.dstate_rs + k * 8) * 2) = last;
         }
       }
-      __syncwarp();
-
+      // Raw-history state of owned requests of two or more tokens, once every
+      // producer has read this tile's history (one-token requests are written
+      // by the producer of their row).
+      if (!W.wait(&ctl->prod_done[ms], (i / kMetaStages) & 1)) break;
+      const int nown = M.own_hi - M.own_lo;
+      for (int task = pa; task < nown * (kGS / 8); task += kAuxWarps * 32) {
+        const int s = M.own_lo + (task >> 4);
+        const int tc0 = g * kGS + (task & 15) * 8;
+        const int st = cu[s], en = cu[s + 1];
+        const int slot = sidx[s];
+        if (st < 0 || en < st || en > a.T) continue;
+        if (slot >= a.pool.num_slots) {
+          if ((task & 15) == 0) cconv::flag_error(a.dev_err, CCONV_DERR_SLOT_RANGE);
+          continue;
+        }
+        if (slot < 0) continue;
+        const bool h = hini == nullptr || hini[s] != 0;
+        const int L = en - st;
+        if (L == 1) continue;
+        if (NH > 0) {
+          uint4 old[NHH], ns[NHH];
+          if (h && L < NH) {
+            hist_load_all<NHH>(a.pool, slot, tc0, old);
+          } else {
+#pragma unroll
+            for (int c = 0; c < NHH; ++c) old[c] = make_uint4(0u, 0u, 0u, 0u);
+          }
+#pragma unroll
+          for (int col = 0; col < NHH; ++col) {
+            const int src = L - NH + col;
+            ns[col] = src >= 0 ? cconv::ldg16(a.qk + ((int64_t)(st + src) * a.qk_rs + tc0) * 2)
+                               : pick<NHH>(old, L + col);
+          }
+          hist_store_all<NHH>(a.pool, slot, tc0, ns);
+        }
+      }
       __syncwarp();
       if (lane == 0) mbar_arrive(&ctl->meta_empty[ms]);
     }
@@ -868,6 +1040,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                  "r"(kTmemCols)
                  : "memory");
+  }
+  // The last CTA out (all others have stopped taking units) clears this
+  // launch's counters for the next launch that gets the same slot.
+  if (threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(&g_work_done[a.epoch], 1u) == gridDim.x - 1) {
+      atomicExch(&g_work_next[a.epoch], 0u);
+      atomicExch(&g_work_done[a.epoch], 0u);
+    }
   }
 }
 
@@ -892,18 +1073,14 @@ static EncodeTiledFn encode_fn() {
   return fn;
 }
 
-static size_t smem_bytes(int T1, int staged_reqs) {
-  size_t stage = 0;
-  if (staged_reqs > 0)
-    stage = 16 + ((staged_reqs + 1 + 3) / 4) * 16 + ((staged_reqs + 3) / 4) * 16 + staged_reqs;
-  return 1024 + (size_t)T1 * (kTapB + kTapA) + (size_t)kXStages * kXStageBytes +
-         (size_t)kEpiWarps * kOutStageBytes + kMetaStages * sizeof(Meta) +
-         ((sizeof(Ctl) + 15) / 16) * 16 + stage;
+static size_t smem_bytes(int T1) {
+  return 1024 + (size_t)T1 * kTapB + 2 * (size_t)kABuf + (size_t)kXStages * kXStageBytes +
+         (size_t)kEpiWarps * kOutStageBytes + kMetaStages * sizeof(Meta) + sizeof(Ctl);
 }
 
 template <int T0, int T1>
 static cudaError_t launch(const CUtensorMap& map, const Args& a, int grid, cudaStream_t st) {
-  const size_t smem = smem_bytes(T1, a.staged ? a.B : 0);
+  const size_t smem = smem_bytes(T1);
   cudaError_t e = cudaFuncSetAttribute(cca_kernel<T0, T1>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
@@ -997,7 +1174,6 @@ extern "C" int cca_qk_conv(const void* qk, int64_t qk_row_stride, const void* w_
   a.tile_pitch = kRows - std::max(n - 1, 0);
   a.num_tiles = std::max(1, (num_tokens + a.tile_pitch - 1) / a.tile_pitch);
   a.units = a.num_tiles * groups;
-  a.staged = num_seqs <= kStageReqs ? 1 : 0;
   a.out = static_cast<char*>(out_qk);
   a.out_rs = out_qk_row_stride;
   a.dprev = static_cast<char*>(out_delayed_prev);
@@ -1008,9 +1184,10 @@ extern "C" int cca_qk_conv(const void* qk, int64_t qk_row_stride, const void* w_
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return CCONV_ERR_LAUNCH;
-  const int ctas0 = std::min(sms, a.units);
-  a.units_per_cta = (a.units + ctas0 - 1) / ctas0;
-  const int grid = (a.units + a.units_per_cta - 1) / a.units_per_cta;
+  const int grid = std::min(sms, a.units);
+  a.static_units = (int)((int64_t)a.units * kStaticPercent / 100 / grid);
+  static std::atomic<unsigned> launches{0};
+  a.epoch = (int)(launches.fetch_add(1u) % kEpochs);
 
   CUtensorMap map;
   memset(&map, 0, sizeof(map));

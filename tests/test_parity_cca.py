@@ -120,6 +120,17 @@ def test_cca_untouched_rows_and_bad_slot():
         assert_bits_equal(to_np(dprev)[a:b], w_dprev[a:b])
 
 
+@pytest.mark.parametrize("t0,t1", [(2, 2), (4, 2), (1, 2), (3, 1)])
+@pytest.mark.parametrize("L", [1, 2, 5, 130])
+def test_cca_one_request_per_call(t0, t1, L):
+    """A call holding one request: its tiles are single-request tiles, where the
+    token before row 0 comes from the history (and a one-token request also
+    rewrites that history in the same pass)."""
+    case = synth.cca_case(437 + L, DEV, lens=[L], decode_prefix=0, Hq=2, Hkv=1, t0=t0, t1=t1,
+                          has_init="all")
+    check(case)
+
+
 def test_cca_split_invariance_on_gpu_is_bitexact():
     L = 700
     case = synth.cca_case(435, DEV, lens=[L], decode_prefix=0, Hq=2, Hkv=1, has_init="all")
