@@ -21,7 +21,8 @@
 
 namespace cconv {
 
-constexpr int kChunk = 64;      // tokens per varlen block (>= (width-1)*dilation)
+constexpr int kChunkShiftMin = 6;   // tokens per varlen block: 64 (>= (width-1)*dilation) ...
+constexpr int kChunkShiftMax = 7;   // ... or 128 when the call has blocks for many waves
 constexpr int kPrefetch = 12;   // token rows in flight per thread (cp.async ring)
 constexpr int kRing = 16;       // ring slots per thread (> kPrefetch + 1, power of 2)
 constexpr int kUpdChan = 2;     // channels per thread of the update kernel
@@ -37,17 +38,19 @@ struct FwdArgs {
   const uint8_t* has_init;
   int32_t B, T, C;
   int32_t act;
+  int32_t chunk_shift;   // tokens per block = 1 << chunk_shift
   char* out;
   int64_t out_rs;
   int32_t* dev_err;
 };
 
 // Block -> (sequence, chunk) map without a host sync. Chunk j of sequence s
-// gets id K(s) + j with K(s) = floor(cu[s]/kChunk) + s; K is strictly
+// gets id K(s) + j with K(s) = floor(cu[s]/chunk) + s; K is strictly
 // increasing and K(s) + nchunks(s) <= K(s+1), so a grid of
-// floor(T/kChunk) + B + 1 blocks covers every chunk (spare ids exit).
+// floor(T/chunk) + B + 1 blocks covers every chunk (spare ids exit).
+// chunk = 1 << sh.
 // One warp finds max{s : K(s) <= b} with a 32-way search.
-__device__ int find_chunk_seq(const int32_t* __restrict__ cu, int B, int b) {
+__device__ int find_chunk_seq(const int32_t* __restrict__ cu, int B, int b, int sh) {
   const int lane = threadIdx.x & 31;
   if (B <= 0) return -1;
   int lo = 0, hi = B;
@@ -55,13 +58,13 @@ __device__ int find_chunk_seq(const int32_t* __restrict__ cu, int B, int b) {
     const int step = (hi - lo + 31) / 32;
     const int idx = lo + lane * step;
     bool ok = false;
-    if (idx < hi) ok = (__ldg(cu + idx) / kChunk + idx) <= b;
+    if (idx < hi) ok = (max(__ldg(cu + idx), 0) >> sh) + idx <= b;
     const unsigned m = __ballot_sync(0xffffffffu, ok);
     if (m == 0u) return -1;   // only when K(lo) > b, i.e. b before the first chunk
     lo = lo + (31 - __clz(m)) * step;
     hi = min(lo + step, hi);
   }
-  return (__ldg(cu + lo) / kChunk + lo) <= b ? lo : -1;
+  return (max(__ldg(cu + lo), 0) >> sh) + lo <= b ? lo : -1;
 }
 
 template <typename T, int W, int D>
@@ -75,7 +78,7 @@ __global__ void __launch_bounds__(128, 4) fwd_varlen_kernel(const FwdArgs a) {
   const int b = blockIdx.x;
 
   if (tid < 32) {
-    const int s = find_chunk_seq(a.cu, a.B, b);
+    const int s = find_chunk_seq(a.cu, a.B, b, a.chunk_shift);
     if (tid == 0) {
       sh_seq = s;
       // Each sequence's index data is checked once, by block (s, 0).
@@ -92,8 +95,9 @@ __global__ void __launch_bounds__(128, 4) fwd_varlen_kernel(const FwdArgs a) {
   const int start = a.cu[s], end = a.cu[s + 1];
   if (start < 0 || end < start || end > a.T) return;
   const int L = end - start;
-  const int nch = L > 0 ? (L + kChunk - 1) / kChunk : 1;
-  const int j = b - (start / kChunk + s);
+  const int sh = a.chunk_shift;
+  const int nch = L > 0 ? ((L - 1) >> sh) + 1 : 1;
+  const int j = b - ((start >> sh) + s);
   if (j < 0 || j >= nch) return;
   const int c0 = (blockIdx.y * nt + tid) * V;
   if (c0 >= a.C) return;
@@ -101,7 +105,7 @@ __global__ void __launch_bounds__(128, 4) fwd_varlen_kernel(const FwdArgs a) {
   if (slot >= a.pool.num_slots) return;
   const bool hs = slot >= 0 && (a.has_init == nullptr || a.has_init[s] != 0);
 
-  const int r0 = j * kChunk, r1 = min(L, r0 + kChunk);
+  const int r0 = j << sh, r1 = min(L, r0 + (1 << sh));
   const char* xs = a.x + ((int64_t)start * a.x_rs + c0) * E;
   char* os = a.out + ((int64_t)start * a.out_rs + c0) * E;
   const int64_t xstep = a.x_rs * E, ostep = a.out_rs * E;
@@ -109,20 +113,22 @@ __global__ void __launch_bounds__(128, 4) fwd_varlen_kernel(const FwdArgs a) {
   // Token rows stream through a per-thread ring of 16-byte units in shared
   // memory, PF rows ahead of use (cp.async, no registers held while in
   // flight). Stream order = the order of use: dilation class rho = 0..D-1,
-  // and within a class rows r0+rho, r0+rho+D, ...
+  // and within a class its W-1 window rows before the chunk (rows before the
+  // sequence come from the state instead: their entries load nothing), then
+  // rows r0+rho, r0+rho+D, ...
   uint4* blk = dyn_smem + tid;                       // pool columns (chunk 0 only)
   uint4* ring = dyn_smem + a.pool.cap * nt + tid;    // RING stream slots
   const uint32_t ring0 = smem_addr(ring);
   const uint32_t slot_bytes = nt * 16;
-  int pr = 0, pm = 0, issued = 0;
+  int pr = r0 < r1 ? 0 : D, pm = -(W - 1), issued = 0;
   auto issue = [&]() {
     const int r = r0 + pr + pm * D;
-    const bool ok = pr < D && r < r1;
-    if (ok) {
+    const bool ok = pr < D && r >= 0;
+    if (pr < D) {
       ++pm;
       if (r0 + pr + pm * D >= r1) {
         ++pr;
-        pm = 0;
+        pm = -(W - 1);
         if (r0 + pr >= r1) pr = D;   // later classes are empty too
       }
     }
@@ -155,7 +161,10 @@ __global__ void __launch_bounds__(128, 4) fwd_varlen_kernel(const FwdArgs a) {
 #pragma unroll
     for (int k = 0; k < W - 1; ++k) {
       const int p = r0 + rho - (W - 1 - k) * D;   // p >= -S; p < 0 only in chunk 0
-      const uint4 r = (p >= 0) ? ldg16(xs + (int64_t)p * xstep) : blk[(S + p) * nt];
+      cp_async_wait<PF - 1>();
+      const uint4 r = (p >= 0) ? ring[(used & (RING - 1)) * nt] : blk[(S + p) * nt];
+      ++used;
+      issue();
       unpack16<T>(r, win[k]);
     }
 #pragma unroll 2
@@ -484,7 +493,15 @@ extern "C" int cconv_fwd_varlen(const void* x, int64_t x_row_stride, const void*
   const int units = C / V;
   const int nt = pick_threads(units, conv_states.cap + kRing);
   const int ctiles = (units + nt - 1) / nt;
-  const int64_t nblk = (int64_t)num_tokens / kChunk + num_seqs + 1;
+  // 128-token chunks halve the per-block window and setup work; 64 keeps
+  // enough blocks in flight for smaller calls.
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return CCONV_ERR_LAUNCH;
+  const int64_t blocks_big = ((int64_t)num_tokens >> kChunkShiftMax) * ctiles;
+  a.chunk_shift = blocks_big >= (int64_t)32 * sms ? kChunkShiftMax : kChunkShiftMin;
+  const int64_t nblk = ((int64_t)num_tokens >> a.chunk_shift) + num_seqs + 1;
   if (nblk > 0x7fffffff || ctiles > 65535) return CCONV_ERR_INVALID;
   const dim3 grid((unsigned)nblk, (unsigned)ctiles);
   const size_t smem = (size_t)nt * (conv_states.cap + kRing) * 16;
