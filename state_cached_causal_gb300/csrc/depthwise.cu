@@ -23,6 +23,7 @@ namespace cconv {
 
 constexpr int kChunkShiftMin = 6;   // tokens per varlen block: 64 (>= (width-1)*dilation) ...
 constexpr int kChunkShiftMax = 7;   // ... or 128 when the call has blocks for many waves
+constexpr int kWaveBlocks = 32;     // (this many 128-token blocks per SM)
 constexpr int kPrefetch = 12;   // token rows in flight per thread (cp.async ring)
 constexpr int kRing = 16;       // ring slots per thread (> kPrefetch + 1, power of 2)
 constexpr int kUpdChan = 2;     // channels per thread of the update kernel
@@ -39,6 +40,8 @@ struct FwdArgs {
   int32_t B, T, C;
   int32_t act;
   int32_t chunk_shift;   // tokens per block = 1 << chunk_shift
+  int32_t nblk;          // chunk ids of the grid
+  int32_t order_lpt;     // grid = (ctiles, nblk), chunk ids in reverse
   char* out;
   int64_t out_rs;
   int32_t* dev_err;
@@ -75,14 +78,19 @@ __global__ void __launch_bounds__(128, 4) fwd_varlen_kernel(const FwdArgs a) {
   extern __shared__ uint4 dyn_smem[];
   __shared__ int sh_seq;
   const int nt = blockDim.x, tid = threadIdx.x;
-  const int b = blockIdx.x;
+  // Chunk id b and channel tile ct. With a.order_lpt the channel tiles are
+  // the fast grid dimension and chunk ids run backwards, so the blocks of the
+  // long prefills start first and the one-token decodes at the front of the
+  // batch fill the tail of the launch.
+  const int b = a.order_lpt ? a.nblk - 1 - (int)blockIdx.y : (int)blockIdx.x;
+  const int ct = a.order_lpt ? (int)blockIdx.x : (int)blockIdx.y;
 
   if (tid < 32) {
     const int s = find_chunk_seq(a.cu, a.B, b, a.chunk_shift);
     if (tid == 0) {
       sh_seq = s;
       // Each sequence's index data is checked once, by block (s, 0).
-      if (blockIdx.y == 0 && b < a.B) {
+      if (ct == 0 && b < a.B) {
         const int c0v = a.cu[b], c1v = a.cu[b + 1];
         if (c0v < 0 || c1v < c0v || c1v > a.T) flag_error(a.dev_err, CCONV_DERR_CU_SEQLENS);
         if (a.state_idx[b] >= a.pool.num_slots) flag_error(a.dev_err, CCONV_DERR_SLOT_RANGE);
@@ -99,7 +107,7 @@ __global__ void __launch_bounds__(128, 4) fwd_varlen_kernel(const FwdArgs a) {
   const int nch = L > 0 ? ((L - 1) >> sh) + 1 : 1;
   const int j = b - ((start >> sh) + s);
   if (j < 0 || j >= nch) return;
-  const int c0 = (blockIdx.y * nt + tid) * V;
+  const int c0 = (ct * nt + tid) * V;
   if (c0 >= a.C) return;
   const int slot = a.state_idx[s];
   if (slot >= a.pool.num_slots) return;
@@ -500,10 +508,14 @@ extern "C" int cconv_fwd_varlen(const void* x, int64_t x_row_stride, const void*
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return CCONV_ERR_LAUNCH;
   const int64_t blocks_big = ((int64_t)num_tokens >> kChunkShiftMax) * ctiles;
-  a.chunk_shift = blocks_big >= (int64_t)32 * sms ? kChunkShiftMax : kChunkShiftMin;
+  a.chunk_shift = blocks_big >= (int64_t)kWaveBlocks * sms ? kChunkShiftMax : kChunkShiftMin;
   const int64_t nblk = ((int64_t)num_tokens >> a.chunk_shift) + num_seqs + 1;
-  if (nblk > 0x7fffffff || ctiles > 65535) return CCONV_ERR_INVALID;
-  const dim3 grid((unsigned)nblk, (unsigned)ctiles);
+  if (nblk > 0x7fffffff) return CCONV_ERR_INVALID;
+  a.nblk = (int32_t)nblk;
+  a.order_lpt = nblk <= 65535 ? 1 : 0;
+  if (!a.order_lpt && ctiles > 65535) return CCONV_ERR_INVALID;
+  const dim3 grid = a.order_lpt ? dim3((unsigned)ctiles, (unsigned)nblk)
+                                : dim3((unsigned)nblk, (unsigned)ctiles);
   const size_t smem = (size_t)nt * (conv_states.cap + kRing) * 16;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = dtype == CCONV_DTYPE_F32
