@@ -65,6 +65,14 @@ def _load():
                 P, I64, P, P, P, P, I32, I32, I32, P, I64, P, I32, P, I64, I64, I64,
                 I32, I32, P, I64, P, P, P, I32, I32, I32, P, I64, P, I64]
             lib.oracle_cca_qk_conv.restype = ctypes.c_int
+            lib.oracle_cconv_fwd_varlen_fused.argtypes = [
+                P, I64, P, P, P, I64, I64, I64, I32, I32, P, P, P, I32, I32, I32, I32,
+                I32, I32, P, I32, P, I64, P, I64]
+            lib.oracle_cconv_fwd_varlen_fused.restype = ctypes.c_int
+            lib.oracle_cconv_update_fused.argtypes = [
+                P, I64, P, I64, I64, I64, I32, I32, P, P, P, I32, I32, P, P, I32, I32,
+                I32, I32, I32, P, I32, P, I64, P, I64]
+            lib.oracle_cconv_update_fused.restype = ctypes.c_int
             lib.oracle_f32_to_bf16.argtypes = [ctypes.c_float]
             lib.oracle_f32_to_bf16.restype = ctypes.c_uint16
             lib.oracle_bf16_to_f32.argtypes = [ctypes.c_uint16]
@@ -177,6 +185,57 @@ def cconv_update(x, pool, w, bias, state_idx, n_spec, num_accepted, has_init, wi
         _ptr(has_init), x.shape[1], width, dilation, act, dt, _ptr(out), _rows(out))
     if rc != 0:
         raise ValueError(f"oracle_cconv_update rejected its arguments ({rc})")
+
+
+def cconv_fwd_varlen_fused(x, w, bias, pool, state_idx, cu_seqlens, has_init, width,
+                           dilation, act, residual, outer=None, token_indices=None):
+    """cconv_fwd_varlen with the fused residual epilogue of "Qwen4ExpPLELayer"
+    _short_conv, in place on ``pool`` and ``residual``.
+
+    Logical row i (cu_seqlens index logical rows) is physical row
+    p = token_indices[i] (identity when None) of x, residual and outer;
+    residual[p] = round(residual[p] + act(conv)[i] + outer[p]) in fp32.
+    """
+    lib = _load()
+    dt = _dtype_code(x)
+    w, bias = _c(w), _c(bias)
+    state_idx = _c(state_idx, np.int32)
+    cu_seqlens = _c(cu_seqlens, np.int32)
+    has_init = _c(has_init, np.uint8)
+    token_indices = _c(token_indices, np.int32)
+    ss, sc, scol = _pool_strides(pool)
+    B = int(state_idx.shape[0])
+    rc = lib.oracle_cconv_fwd_varlen_fused(
+        _ptr(x), _rows(x), _ptr(w), _ptr(bias), _pool_base(pool), ss, sc, scol,
+        pool.shape[0], pool.shape[2], _ptr(state_idx), _ptr(cu_seqlens), _ptr(has_init),
+        B, x.shape[1], width, dilation, act, dt, _ptr(token_indices), x.shape[0],
+        _ptr(residual), _rows(residual), _ptr(outer), _rows(outer) if outer is not None else 0)
+    if rc != 0:
+        raise ValueError(f"oracle_cconv_fwd_varlen_fused rejected its arguments ({rc})")
+
+
+def cconv_update_fused(x, pool, w, bias, state_idx, n_spec, num_accepted, has_init, width,
+                       dilation, act, residual, outer=None, token_indices=None):
+    """cconv_update with the fused residual epilogue and logical row order of
+    "Qwen4ExpPLELayer" (_short_conv, _short_conv_dilated_dispatch); request s
+    owns logical rows [s*q, s*q + q)."""
+    lib = _load()
+    dt = _dtype_code(x)
+    w, bias = _c(w), _c(bias)
+    state_idx = _c(state_idx, np.int32)
+    num_accepted = _c(num_accepted, np.int32)
+    has_init = _c(has_init, np.uint8)
+    token_indices = _c(token_indices, np.int32)
+    ss, sc, scol = _pool_strides(pool)
+    B = int(state_idx.shape[0])
+    rc = lib.oracle_cconv_update_fused(
+        _ptr(x), _rows(x), _pool_base(pool), ss, sc, scol, pool.shape[0], pool.shape[2],
+        _ptr(w), _ptr(bias), _ptr(state_idx), B, n_spec, _ptr(num_accepted),
+        _ptr(has_init), x.shape[1], width, dilation, act, dt, _ptr(token_indices),
+        x.shape[0], _ptr(residual), _rows(residual), _ptr(outer),
+        _rows(outer) if outer is not None else 0)
+    if rc != 0:
+        raise ValueError(f"oracle_cconv_update_fused rejected its arguments ({rc})")
 
 
 def cca_qk_conv(qk, w_dw, b_dw, w_gr, b_gr, groups, t0, t1, delayed, delayed_init, pool,

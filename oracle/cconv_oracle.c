@@ -232,6 +232,145 @@ int oracle_cconv_update(const void* x, int64_t x_rs, void* pool, int64_t s_slot,
   return 0;
 }
 
+/* ---- fused residual epilogue and logical row order ----------------------- */
+
+/*
+ * [P] _short_conv ("optionally fusing both residual additions") and
+ * _short_conv_dilated_dispatch (token_indices: "the kernels map logical
+ * spec/non-spec rows instead of materializing both groups"). Logical row i of
+ * a call lives at physical row p(i) = tidx ? tidx[i] : i of x, residual and
+ * outer_residual. Instead of an output tensor, the conv result y (fp32, after
+ * the activation) is added to the residual row in place:
+ *   residual[p][c] = round(residual[p][c] + y[i][c] + outer_residual[p][c])
+ * summed in fp32 in that order (no outer term when outer_residual is NULL).
+ * Reading: the pages show the two additions (residual.add_ of the conv output
+ * and of the outer residual) but not the fused kernel's rounding, so the sum
+ * is rounded once, as a fused epilogue computes it.
+ */
+static void orc_depthwise_channel_res(const orc_raw* xt, int S, int L, const void* w,
+                                      int64_t w_off, const void* bias, int64_t c, int W,
+                                      int D, int act, int dtype, const int64_t* prow,
+                                      void* res, int64_t res_rs, const void* outer,
+                                      int64_t outer_rs) {
+  for (int j = 0; j < L; ++j) {
+    float acc = bias ? orc_get(bias, c, dtype) : 0.0f;
+    for (int k = 0; k < W; ++k) {
+      float wk = orc_get(w, w_off + k, dtype);
+      float xv = orc_raw_to_f32(xt[S + j - (W - 1 - k) * D], dtype);
+      acc = acc + wk * xv;
+    }
+    const float y = orc_act(acc, act);
+    const int64_t ri = prow[j] * res_rs + c;
+    float v = orc_get(res, ri, dtype) + y;
+    if (outer) v = v + orc_get(outer, prow[j] * outer_rs + c, dtype);
+    orc_put(res, ri, dtype, v);
+  }
+}
+
+/* oracle_cconv_fwd_varlen with the fused epilogue; -2 if a logical row maps
+ * outside [0, num_rows). */
+int oracle_cconv_fwd_varlen_fused(const void* x, int64_t x_rs, const void* w,
+                                  const void* bias, void* pool, int64_t s_slot, int64_t s_chan,
+                                  int64_t s_col, int32_t num_slots, int32_t cap,
+                                  const int32_t* state_idx, const int32_t* cu_seqlens,
+                                  const uint8_t* has_init, int32_t num_seqs, int32_t C,
+                                  int32_t W, int32_t D, int32_t act, int32_t dtype,
+                                  const int32_t* tidx, int32_t num_rows, void* res,
+                                  int64_t res_rs, const void* outer, int64_t outer_rs) {
+  const int S = (W - 1) * D;
+  if (S > cap) return -1;
+  for (int s = 0; s < num_seqs; ++s) {
+    const int64_t start = cu_seqlens[s];
+    const int L = cu_seqlens[s + 1] - cu_seqlens[s];
+    const int slot = state_idx[s];
+    if (L < 0 || slot >= num_slots) return -1;
+    const int h = (has_init ? has_init[s] != 0 : 1) && slot >= 0;
+    int64_t* prow = (int64_t*)malloc(sizeof(int64_t) * (size_t)(L + 1));
+    for (int i = 0; i < L; ++i) {
+      prow[i] = tidx ? tidx[start + i] : start + i;
+      if (prow[i] < 0 || prow[i] >= num_rows) {
+        free(prow);
+        return -2;
+      }
+    }
+    orc_raw* xt = (orc_raw*)malloc(sizeof(orc_raw) * (size_t)(S + L + 1));
+    for (int64_t c = 0; c < C; ++c) {
+      for (int i = 0; i < S; ++i)
+        xt[i] = h ? orc_get_raw(pool, slot * s_slot + c * s_chan + i * s_col, dtype) : 0u;
+      for (int i = 0; i < L; ++i) xt[S + i] = orc_get_raw(x, prow[i] * x_rs + c, dtype);
+      orc_depthwise_channel_res(xt, S, L, w, c * W, bias, c, W, D, act, dtype, prow, res,
+                                res_rs, outer, outer_rs);
+      if (slot >= 0)
+        for (int i = 0; i < S; ++i)
+          orc_put_raw(pool, slot * s_slot + c * s_chan + i * s_col, dtype, xt[L + i]);
+    }
+    free(xt);
+    free(prow);
+  }
+  return 0;
+}
+
+/* oracle_cconv_update with the fused epilogue; request s owns logical rows
+ * [s*q, s*q + q). -2 if a logical row maps outside [0, num_rows). */
+int oracle_cconv_update_fused(const void* x, int64_t x_rs, void* pool, int64_t s_slot,
+                              int64_t s_chan, int64_t s_col, int32_t num_slots, int32_t cap,
+                              const void* w, const void* bias, const int32_t* state_idx,
+                              int32_t num_seqs, int32_t n_spec, const int32_t* num_accepted,
+                              const uint8_t* has_init, int32_t C, int32_t W, int32_t D,
+                              int32_t act, int32_t dtype, const int32_t* tidx,
+                              int32_t num_rows, void* res, int64_t res_rs, const void* outer,
+                              int64_t outer_rs) {
+  const int S = (W - 1) * D;
+  const int q = 1 + n_spec;
+  if (S + n_spec > cap) return -1;
+  orc_raw* Bc = (orc_raw*)malloc(sizeof(orc_raw) * (size_t)(cap + 1));
+  orc_raw* xt = (orc_raw*)malloc(sizeof(orc_raw) * (size_t)(S + q + 1));
+  int64_t* prow = (int64_t*)malloc(sizeof(int64_t) * (size_t)(q + 1));
+  int rc = 0;
+  for (int s = 0; s < num_seqs && rc == 0; ++s) {
+    const int slot = state_idx[s];
+    if (slot >= num_slots) {
+      rc = -1;
+      break;
+    }
+    const int h = (has_init ? has_init[s] != 0 : 1) && slot >= 0;
+    const int off = n_spec > 0 ? num_accepted[s] - 1 : 0;
+    if (n_spec > 0 && (off < 0 || off >= q)) {
+      rc = -1;
+      break;
+    }
+    for (int i = 0; i < q; ++i) {
+      const int64_t li = (int64_t)s * q + i;
+      prow[i] = tidx ? tidx[li] : li;
+      if (prow[i] < 0 || prow[i] >= num_rows) rc = -2;
+    }
+    if (rc) break;
+    for (int64_t c = 0; c < C; ++c) {
+      const int ncols = n_spec > 0 ? cap : S;
+      for (int i = 0; i < ncols; ++i)
+        Bc[i] = h ? orc_get_raw(pool, slot * s_slot + c * s_chan + i * s_col, dtype) : 0u;
+      for (int i = 0; i < S; ++i) xt[i] = Bc[off + i];
+      for (int i = 0; i < q; ++i) xt[S + i] = orc_get_raw(x, prow[i] * x_rs + c, dtype);
+      orc_depthwise_channel_res(xt, S, q, w, c * W, bias, c, W, D, act, dtype, prow, res,
+                                res_rs, outer, outer_rs);
+      if (slot < 0) continue;
+      if (n_spec == 0) {
+        for (int i = 0; i < S; ++i)
+          orc_put_raw(pool, slot * s_slot + c * s_chan + i * s_col, dtype, xt[1 + i]);
+      } else {
+        for (int i = 0; i < cap; ++i) {
+          orc_raw v = (i < cap - q) ? Bc[off + 1 + i] : xt[S + (i - (cap - q))];
+          orc_put_raw(pool, slot * s_slot + c * s_chan + i * s_col, dtype, v);
+        }
+      }
+    }
+  }
+  free(Bc);
+  free(xt);
+  free(prow);
+  return rc;
+}
+
 /*
  * Zaya CCA q/k conv with state and the delayed half of v ([Z] ZayaCCA.__init__,
  * _conv, project, _mix_with_state, _cca_state_shapes).

@@ -1,0 +1,177 @@
+"""Pins for the oracle's fused epilogue (residual additions and logical row
+order of the "Qwen4ExpPLELayer" short conv), against things other than the
+oracle itself:
+
+* torch.nn.functional.conv1d in fp64 plus the two residual terms, on tiny
+  fp32 inputs with a random logical -> physical row permutation;
+* reduction to the plain operation: a zero residual, no outer residual and the
+  identity row order give the plain output bit for bit;
+* permutation invariance: moving the rows of x, residual and outer by a
+  permutation and passing it as token_indices moves the result with them;
+* rejection of a row index outside the physical rows.
+
+No CUDA is involved.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from state_cached_causal_gb300 import synth
+from tests._util import pool_np, to_np
+from tests.test_oracle_pins import conv_ref
+
+CPU = torch.device("cpu")
+
+
+def _case(seed, dtype, lens=(5, 1, 0, 9, 3), W=4, D=2, n_spec=0, spec=0):
+    return synth.depthwise_case(seed, CPU, lens=list(lens), C=16, width=W, dilation=D, act=1,
+                                dtype=dtype, w_std=0.5, bias_std=0.1, padding_every=4,
+                                spec_requests=spec, n_spec=n_spec)
+
+
+def _rand_rows(rows, C, seed, dtype):
+    g = torch.Generator().manual_seed(seed)
+    return to_np(torch.randn(rows, C, generator=g).to(dtype))
+
+
+def _f64(a):
+    return oracle.bf16_to_f32(a).astype(np.float64) if a.dtype == np.uint16 else a.astype(
+        np.float64)
+
+
+def test_fused_fwd_fp32_matches_conv1d_plus_residuals():
+    case = _case(901, torch.float32)
+    T, C = case.x.shape
+    perm = np.random.default_rng(3).permutation(T).astype(np.int32)
+    x_log = to_np(case.x)
+    x_phys = np.empty_like(x_log)
+    x_phys[perm] = x_log                                  # logical row i lives at perm[i]
+    res = _rand_rows(T, C, 11, torch.float32)
+    outer = _rand_rows(T, C, 12, torch.float32)
+    pool = pool_np(case.pool.clone())
+    got = res.copy()
+    oracle.cconv_fwd_varlen_fused(x_phys, to_np(case.w), to_np(case.bias), pool,
+                                  to_np(case.state_idx), to_np(case.cu_seqlens),
+                                  to_np(case.has_init), case.width, case.dilation, case.act,
+                                  got, outer, perm)
+    want = res.astype(np.float64).copy()
+    cu = to_np(case.cu_seqlens)
+    pool0 = pool_np(case.pool)
+    S = (case.width - 1) * case.dilation
+    for s in range(len(cu) - 1):
+        a, b = int(cu[s]), int(cu[s + 1])
+        if b == a:
+            continue
+        slot = int(case.state_idx[s])
+        h = slot >= 0 and int(case.has_init[s]) != 0
+        hist = pool0[slot, :, :S].astype(np.float64) if h else np.zeros((C, S))
+        y = conv_ref(hist, x_log[a:b].astype(np.float64), to_np(case.w).astype(np.float64),
+                     to_np(case.bias).astype(np.float64), case.dilation, case.act)
+        for i in range(a, b):
+            want[perm[i]] = res[perm[i]] + y[i - a] + outer[perm[i]]
+    assert np.abs(got - want).max() <= 1e-5
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_fused_fwd_reduces_to_plain(dtype):
+    case = _case(902, dtype)
+    x = to_np(case.x)
+    out = np.zeros_like(x)
+    pool_a = pool_np(case.pool.clone())
+    oracle.cconv_fwd_varlen(x, to_np(case.w), to_np(case.bias), pool_a, to_np(case.state_idx),
+                            to_np(case.cu_seqlens), to_np(case.has_init), case.width,
+                            case.dilation, case.act, out)
+    res = np.zeros_like(x)
+    pool_b = pool_np(case.pool.clone())
+    oracle.cconv_fwd_varlen_fused(x, to_np(case.w), to_np(case.bias), pool_b,
+                                  to_np(case.state_idx), to_np(case.cu_seqlens),
+                                  to_np(case.has_init), case.width, case.dilation, case.act,
+                                  res)
+    assert np.array_equal(res, out)
+    assert np.array_equal(pool_a, pool_b)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_fused_fwd_row_order_is_a_permutation(dtype):
+    case = _case(903, dtype)
+    T, C = case.x.shape
+    perm = np.random.default_rng(4).permutation(T).astype(np.int32)
+    x, res, outer = to_np(case.x), _rand_rows(T, C, 13, dtype), _rand_rows(T, C, 14, dtype)
+    args = (to_np(case.w), to_np(case.bias))
+    meta = (to_np(case.state_idx), to_np(case.cu_seqlens), to_np(case.has_init), case.width,
+            case.dilation, case.act)
+    r_id = res.copy()
+    p_id = pool_np(case.pool.clone())
+    oracle.cconv_fwd_varlen_fused(x, *args, p_id, *meta, r_id, outer)
+    xp, rp, op = (np.empty_like(a) for a in (x, res, outer))
+    xp[perm], rp[perm], op[perm] = x, res, outer
+    p_pm = pool_np(case.pool.clone())
+    oracle.cconv_fwd_varlen_fused(xp, *args, p_pm, *meta, rp, op, perm)
+    assert np.array_equal(rp[perm], r_id)
+    assert np.array_equal(p_pm, p_id)
+
+
+def test_fused_update_fp32_matches_conv1d_plus_residuals():
+    n_spec, W, D = 3, 4, 2
+    case = _case(904, torch.float32, lens=(), W=W, D=D, n_spec=n_spec, spec=6)
+    q = 1 + n_spec
+    R, C = case.x_spec.shape
+    perm = np.random.default_rng(5).permutation(R).astype(np.int32)
+    x_log = to_np(case.x_spec)
+    x_phys = np.empty_like(x_log)
+    x_phys[perm] = x_log
+    res = _rand_rows(R, C, 15, torch.float32)
+    outer = _rand_rows(R, C, 16, torch.float32)
+    pool = pool_np(case.pool.clone())
+    got = res.copy()
+    oracle.cconv_update_fused(x_phys, pool, to_np(case.w), to_np(case.bias),
+                              to_np(case.spec_state_idx), n_spec, to_np(case.num_accepted),
+                              to_np(case.spec_has_init), W, D, case.act, got, outer, perm)
+    S = (W - 1) * D
+    pool0 = pool_np(case.pool)
+    want = res.astype(np.float64).copy()
+    for s in range(R // q):
+        slot = int(case.spec_state_idx[s])
+        hi = case.spec_has_init
+        h = slot >= 0 and (hi is None or int(hi[s]) != 0)
+        off = int(case.num_accepted[s]) - 1
+        B = pool0[slot].astype(np.float64) if h else np.zeros((C, pool0.shape[2]))
+        y = conv_ref(B[:, off:off + S], x_log[s * q:(s + 1) * q].astype(np.float64),
+                     to_np(case.w).astype(np.float64), to_np(case.bias).astype(np.float64),
+                     D, case.act)
+        for i in range(q):
+            p = perm[s * q + i]
+            want[p] = res[p] + y[i] + outer[p]
+    assert np.abs(got - want).max() <= 1e-5
+
+
+@pytest.mark.parametrize("n_spec", [0, 3])
+def test_fused_update_reduces_to_plain(n_spec):
+    case = _case(905, torch.bfloat16, lens=(), W=4, D=3, n_spec=n_spec, spec=7)
+    x = to_np(case.x_spec)
+    na = to_np(case.num_accepted) if n_spec else None
+    out = np.zeros_like(x)
+    pool_a = pool_np(case.pool.clone())
+    oracle.cconv_update(x, pool_a, to_np(case.w), to_np(case.bias), to_np(case.spec_state_idx),
+                        n_spec, na, to_np(case.spec_has_init), 4, 3, case.act, out)
+    res = np.zeros_like(x)
+    pool_b = pool_np(case.pool.clone())
+    oracle.cconv_update_fused(x, pool_b, to_np(case.w), to_np(case.bias),
+                              to_np(case.spec_state_idx), n_spec, na,
+                              to_np(case.spec_has_init), 4, 3, case.act, res)
+    assert np.array_equal(res, out)
+    assert np.array_equal(pool_a, pool_b)
+
+
+def test_fused_rejects_row_index_outside_rows():
+    case = _case(906, torch.float32)
+    T, C = case.x.shape
+    idx = np.arange(T, dtype=np.int32)
+    idx[3] = T                                            # one past the last row
+    with pytest.raises(ValueError):
+        oracle.cconv_fwd_varlen_fused(to_np(case.x), to_np(case.w), to_np(case.bias),
+                                      pool_np(case.pool.clone()), to_np(case.state_idx),
+                                      to_np(case.cu_seqlens), to_np(case.has_init), case.width,
+                                      case.dilation, case.act, np.zeros((T, C), np.float32),
+                                      None, idx)
