@@ -86,8 +86,10 @@ enum {
   CCONV_DERR_SLOT_RANGE = 1,   /* state_idx[s] >= num_slots            */
   CCONV_DERR_CU_SEQLENS = 2,   /* cu_seqlens negative/decreasing/> T   */
   CCONV_DERR_NUM_ACCEPTED = 4, /* num_accepted[s] outside [1, 1+n_spec] */
-  CCONV_DERR_TIMEOUT = 8       /* a bounded on-chip wait ran out; the call's
+  CCONV_DERR_TIMEOUT = 8,      /* a bounded on-chip wait ran out; the call's
                                   outputs are incomplete                 */
+  CCONV_DERR_ROW_INDEX = 16    /* fused entry points: a logical row maps
+                                  outside [0, num_rows)                  */
 };
 
 /* [slot, channel, column] view of a conv-state pool (element strides). */
@@ -168,6 +170,65 @@ int cconv_update(const void* x, int64_t x_row_stride, cconv_pool_t conv_states,
                  const uint8_t* has_init, int32_t C, int32_t width, int32_t dilation,
                  int32_t act, int32_t dtype, void* out, int64_t out_row_stride,
                  int32_t* dev_err, cconv_stream_t stream);
+
+/*
+ * Epilogue of the fused entry points below.
+ *
+ * Defined by: "Qwen4ExpPLELayer" _short_conv (the conv "optionally fusing
+ * both residual additions": the conv result is added to `residual`, and the
+ * outer residual with it) and _short_conv_dilated_dispatch (a mixed batch
+ * keeps its row order: the kernels map logical spec/non-spec rows through
+ * token_indices instead of copying each group out).
+ *
+ * Logical row i of a call (cu_seqlens and the request rows of cconv_update
+ * count logical rows) lives at physical row p = token_indices[i] (p = i when
+ * token_indices is NULL) of x, residual and outer_residual. The call writes
+ *   residual[p][c] = round(residual[p][c] + act(conv)[i][c] + outer_residual[p][c])
+ * summed in fp32 in that order (no outer term when outer_residual is NULL);
+ * there is no separate output tensor.
+ *
+ *   residual        [num_rows, C], the call's dtype, row stride residual_row_stride
+ *                   (elements, >= C, 16-byte rows); read and written in place
+ *   outer_residual  [num_rows, C] with row stride outer_row_stride, or NULL
+ *   token_indices   int32 [logical rows] or NULL; entries distinct. An entry
+ *                   outside [0, num_rows) sets CCONV_DERR_ROW_INDEX and the
+ *                   affected chunk (varlen) or request (update) is skipped.
+ *   num_rows        physical rows of x, residual and outer_residual (>= the
+ *                   logical rows when token_indices is NULL)
+ * The caller owns all memory; residual must not alias x or outer_residual.
+ */
+typedef struct cconv_epilogue {
+  void* residual;
+  int64_t residual_row_stride;
+  const void* outer_residual;
+  int64_t outer_row_stride;
+  const int32_t* token_indices;
+  int32_t num_rows;
+} cconv_epilogue_t;
+
+/*
+ * cconv_fwd_varlen_fused -- cconv_fwd_varlen with the epilogue above in place
+ * of (out, out_row_stride). State handling, arguments and errors are those of
+ * cconv_fwd_varlen; num_tokens counts logical rows.
+ */
+int cconv_fwd_varlen_fused(const void* x, int64_t x_row_stride, const void* w,
+                           const void* bias, cconv_pool_t conv_states,
+                           const int32_t* state_idx, const int32_t* cu_seqlens,
+                           const uint8_t* has_init, int32_t num_seqs, int32_t num_tokens,
+                           int32_t C, int32_t width, int32_t dilation, int32_t act,
+                           int32_t dtype, cconv_epilogue_t epilogue, int32_t* dev_err,
+                           cconv_stream_t stream);
+
+/*
+ * cconv_update_fused -- cconv_update with the epilogue above in place of
+ * (out, out_row_stride): request s owns logical rows [s*q, s*q+q).
+ */
+int cconv_update_fused(const void* x, int64_t x_row_stride, cconv_pool_t conv_states,
+                       const void* w, const void* bias, const int32_t* state_idx,
+                       int32_t num_seqs, int32_t n_spec, const int32_t* num_accepted,
+                       const uint8_t* has_init, int32_t C, int32_t width, int32_t dilation,
+                       int32_t act, int32_t dtype, cconv_epilogue_t epilogue,
+                       int32_t* dev_err, cconv_stream_t stream);
 
 /*
  * cca_qk_conv -- Zaya CCA: depthwise conv (width t0, bias) then grouped conv

@@ -1,469 +1,6 @@
-// Depthwise causal conv with a conv-state pool: varlen prefill/decode
-// (cconv_fwd_varlen) and decode / speculative decode (cconv_update).
-//
-// Pages: "vllm.model_executor.layers.mamba.ops.cpu.gdn_attention"
-// (_spec_aware_nonspec prefill and decode conv, _spec_forward rolling buffer)
-// and "Qwen4ExpPLELayer" (dilated depthwise conv1d, state_len =
-// (kernel-1)*dilation, spec/decode/prefill dispatch).
-//
-// Design (GB300): the op is HBM-bound (4 FMAs per 4 bytes moved), so each
-// thread owns one 16-byte unit of channels (8 bf16 / 4 fp32) and walks down
-// the time axis; a warp moves 512 contiguous bytes per row. A dilated conv
-// with dilation d is walked as d interleaved undilated chains (rows
-// r, r+d, r+2d, ...), so the register window holds only width-1 rows
-// whatever the dilation. Eight rows are loaded before any is used to keep
-// enough bytes in flight per SM.
-#include <algorithm>
-#include <type_traits>
-
-#include "common.cuh"
-#include "update.cuh"
-
-namespace cconv {
-
-constexpr int kChunkShiftMin = 6;   // tokens per varlen block: 64 (>= (width-1)*dilation) ...
-constexpr int kChunkShiftMax = 7;   // ... or 128 when the call has blocks for many waves
-constexpr int kWaveBlocks = 32;     // (this many 128-token blocks per SM)
-constexpr int kPrefetch = 12;   // token rows in flight per thread (cp.async ring)
-constexpr int kRing = 16;       // ring slots per thread (> kPrefetch + 1, power of 2)
-constexpr int kUpdChan = 2;     // channels per thread of the update kernel
-
-struct FwdArgs {
-  const char* x;
-  int64_t x_rs;
-  const char* w;
-  const char* bias;
-  Pool pool;
-  const int32_t* state_idx;
-  const int32_t* cu;
-  const uint8_t* has_init;
-  int32_t B, T, C;
-  int32_t act;
-  int32_t chunk_shift;   // tokens per block = 1 << chunk_shift
-  int32_t nblk;          // chunk ids of the grid
-  int32_t order_lpt;     // grid = (ctiles, nblk), chunk ids in reverse
-  char* out;
-  int64_t out_rs;
-  int32_t* dev_err;
-};
-
-// Block -> (sequence, chunk) map without a host sync. Chunk j of sequence s
-// gets id K(s) + j with K(s) = floor(cu[s]/chunk) + s; K is strictly
-// increasing and K(s) + nchunks(s) <= K(s+1), so a grid of
-// floor(T/chunk) + B + 1 blocks covers every chunk (spare ids exit).
-// chunk = 1 << sh.
-// One warp finds max{s : K(s) <= b} with a 32-way search.
-__device__ int find_chunk_seq(const int32_t* __restrict__ cu, int B, int b, int sh) {
-  const int lane = threadIdx.x & 31;
-  if (B <= 0) return -1;
-  int lo = 0, hi = B;
-  while (hi - lo > 1) {
-    const int step = (hi - lo + 31) / 32;
-    const int idx = lo + lane * step;
-    bool ok = false;
-    if (idx < hi) ok = (max(__ldg(cu + idx), 0) >> sh) + idx <= b;
-    const unsigned m = __ballot_sync(0xffffffffu, ok);
-    if (m == 0u) return -1;   // only when K(lo) > b, i.e. b before the first chunk
-    lo = lo + (31 - __clz(m)) * step;
-    hi = min(lo + step, hi);
-  }
-  return (max(__ldg(cu + lo), 0) >> sh) + lo <= b ? lo : -1;
-}
-
-template <typename T, int W, int D>
-__global__ void __launch_bounds__(128, 4) fwd_varlen_kernel(const FwdArgs a) {
-  constexpr int S = (W - 1) * D;
-  constexpr int V = Elem<T>::V, E = Elem<T>::bytes;
-  constexpr int PF = kPrefetch, RING = kRing;
-  extern __shared__ uint4 dyn_smem[];
-  __shared__ int sh_seq;
-  const int nt = blockDim.x, tid = threadIdx.x;
-  // Chunk id b and channel tile ct. With a.order_lpt the channel tiles are
-  // the fast grid dimension and chunk ids run backwards, so the blocks of the
-  // long prefills start first and the one-token decodes at the front of the
-  // batch fill the tail of the launch.
-  const int b = a.order_lpt ? a.nblk - 1 - (int)blockIdx.y : (int)blockIdx.x;
-  const int ct = a.order_lpt ? (int)blockIdx.x : (int)blockIdx.y;
-
-  if (tid < 32) {
-    const int s = find_chunk_seq(a.cu, a.B, b, a.chunk_shift);
-    if (tid == 0) {
-      sh_seq = s;
-      // Each sequence's index data is checked once, by block (s, 0).
-      if (ct == 0 && b < a.B) {
-        const int c0v = a.cu[b], c1v = a.cu[b + 1];
-        if (c0v < 0 || c1v < c0v || c1v > a.T) flag_error(a.dev_err, CCONV_DERR_CU_SEQLENS);
-        if (a.state_idx[b] >= a.pool.num_slots) flag_error(a.dev_err, CCONV_DERR_SLOT_RANGE);
-      }
-    }
-  }
-  __syncthreads();
-  const int s = sh_seq;
-  if (s < 0) return;
-  const int start = a.cu[s], end = a.cu[s + 1];
-  if (start < 0 || end < start || end > a.T) return;
-  const int L = end - start;
-  const int sh = a.chunk_shift;
-  const int nch = L > 0 ? ((L - 1) >> sh) + 1 : 1;
-  const int j = b - ((start >> sh) + s);
-  if (j < 0 || j >= nch) return;
-  const int c0 = (ct * nt + tid) * V;
-  if (c0 >= a.C) return;
-  const int slot = a.state_idx[s];
-  if (slot >= a.pool.num_slots) return;
-  const bool hs = slot >= 0 && (a.has_init == nullptr || a.has_init[s] != 0);
-
-  const int r0 = j << sh, r1 = min(L, r0 + (1 << sh));
-  const char* xs = a.x + ((int64_t)start * a.x_rs + c0) * E;
-  char* os = a.out + ((int64_t)start * a.out_rs + c0) * E;
-  const int64_t xstep = a.x_rs * E, ostep = a.out_rs * E;
-
-  // Token rows stream through a per-thread ring of 16-byte units in shared
-  // memory, PF rows ahead of use (cp.async, no registers held while in
-  // flight). Stream order = the order of use: dilation class rho = 0..D-1,
-  // and within a class its W-1 window rows before the chunk (rows before the
-  // sequence come from the state instead: their entries load nothing), then
-  // rows r0+rho, r0+rho+D, ...
-  uint4* blk = dyn_smem + tid;                       // pool columns (chunk 0 only)
-  uint4* ring = dyn_smem + a.pool.cap * nt + tid;    // RING stream slots
-  const uint32_t ring0 = smem_addr(ring);
-  const uint32_t slot_bytes = nt * 16;
-  int pr = r0 < r1 ? 0 : D, pm = -(W - 1), issued = 0;
-  auto issue = [&]() {
-    const int r = r0 + pr + pm * D;
-    const bool ok = pr < D && r >= 0;
-    if (pr < D) {
-      ++pm;
-      if (r0 + pr + pm * D >= r1) {
-        ++pr;
-        pm = -(W - 1);
-        if (r0 + pr >= r1) pr = D;   // later classes are empty too
-      }
-    }
-    cp_async16(ring0 + (issued & (RING - 1)) * slot_bytes, ok ? xs + (int64_t)r * xstep : xs,
-               ok);
-    cp_async_commit();
-    ++issued;
-  };
-#pragma unroll
-  for (int i = 0; i < PF; ++i) issue();
-
-  float wk[W][V], bv[V];
-#pragma unroll
-  for (int v = 0; v < V; ++v) {
-#pragma unroll
-    for (int k = 0; k < W; ++k) wk[k][v] = load_f32<T>(a.w, (int64_t)(c0 + v) * W + k);
-    bv[v] = a.bias ? load_f32<T>(a.bias, c0 + v) : 0.0f;
-  }
-  if (j == 0) {
-    if (slot >= 0) pool_load<T>(a.pool, slot, c0, S, blk, nt);
-    if (!hs)
-      for (int col = 0; col < S; ++col) blk[col * nt] = make_uint4(0u, 0u, 0u, 0u);
-  }
-  const bool silu_on = a.act == CCONV_ACT_SILU;
-
-  int used = 0;
-#pragma unroll 1
-  for (int rho = 0; rho < D && r0 + rho < r1; ++rho) {
-    float win[W - 1][V];
-#pragma unroll
-    for (int k = 0; k < W - 1; ++k) {
-      const int p = r0 + rho - (W - 1 - k) * D;   // p >= -S; p < 0 only in chunk 0
-      cp_async_wait<PF - 1>();
-      const uint4 r = (p >= 0) ? ring[(used & (RING - 1)) * nt] : blk[(S + p) * nt];
-      ++used;
-      issue();
-      unpack16<T>(r, win[k]);
-    }
-#pragma unroll 2
-    for (int r = r0 + rho; r < r1; r += D) {
-      cp_async_wait<PF - 1>();
-      float cur[V], y[V];
-      unpack16<T>(ring[(used & (RING - 1)) * nt], cur);
-      ++used;
-      issue();
-#pragma unroll
-      for (int v = 0; v < V; ++v) {
-        float acc = bv[v];
-#pragma unroll
-        for (int k = 0; k < W - 1; ++k) acc = fmaf(wk[k][v], win[k][v], acc);
-        acc = fmaf(wk[W - 1][v], cur[v], acc);
-        y[v] = silu_on ? silu<T>(acc) : acc;
-      }
-      stg16(os + (int64_t)r * ostep, pack16<T>(y));
-#pragma unroll
-      for (int k = 0; k < W - 2; ++k) {
-#pragma unroll
-        for (int v = 0; v < V; ++v) win[k][v] = win[k + 1][v];
-      }
-#pragma unroll
-      for (int v = 0; v < V; ++v) win[W - 2][v] = cur[v];
-    }
-  }
-  cp_async_wait<0>();   // no copy may land after the thread exits
-
-  // Chunk 0 owns the slot: it alone read the old columns, so it alone writes
-  // the new ones -- the last S elements of history ++ tokens. Moving column
-  // L+i down to column i reads ahead of every write (L >= 0).
-  if (j == 0 && slot >= 0) {
-    for (int i = 0; i < S; ++i) {
-      const int src = L - S + i;
-      blk[i * nt] = (src >= 0) ? ldg16(xs + (int64_t)src * xstep) : blk[(S + src) * nt];
-    }
-    pool_store<T>(a.pool, slot, c0, S, blk, nt);
-  }
-}
-
-// Pools that are not channel-first (column-first or arbitrary strides): one
-// block = one request x (up to) 512 channels, two channels per thread.
-// (Channel-first pools take the bulk-copy pipeline of update_bulk.cu.)
-// Everything the block touches in HBM goes through shared memory: the
-// request's state for those channels (`cap` contiguous 16-byte rows in a
-// column-first pool, single elements otherwise), its q token rows and its q
-// output rows, the rows in coalesced 16-byte units. The per-channel
-// arithmetic reads the prior window (S columns from num_accepted - 1) into
-// registers once, computes the q outputs from registers, and writes the new
-// buffer -- prior[1..S) ++ (older kept columns) ++ tokens -- back in place.
-// The shared copy of the state is column-major: [cap][channels of the block].
-template <typename T, int W, int D>
-__global__ void __launch_bounds__(256) update_kernel(const UpdArgs a) {
-  constexpr int S = (W - 1) * D;
-  constexpr int E = Elem<T>::bytes, QM = kMaxSpec + 1, K = kUpdChan;
-  using R = typename std::conditional<E == 4, uint32_t, uint16_t>::type;   // raw element
-  extern __shared__ uint4 dyn_smem[];
-  const int nt = blockDim.x, tid = threadIdx.x;
-  const int s = blockIdx.x / a.ctiles;
-  const int nb = K * nt;                               // channels per block
-  const int cb = (blockIdx.x - s * a.ctiles) * nb;     // first channel of the block
-  const int nch = min(nb, a.C - cb);                   // channels of the block (multiple of 8/4)
-  const int q = 1 + a.n_spec;
-  const int slot = a.state_idx[s];
-  if (slot >= a.pool.num_slots) {
-    if (cb == 0 && tid == 0) flag_error(a.dev_err, CCONV_DERR_SLOT_RANGE);
-    return;
-  }
-  int off = 0;
-  if (a.n_spec > 0) {
-    off = a.num_accepted[s] - 1;
-    if (off < 0 || off >= q) {
-      if (cb == 0 && tid == 0) flag_error(a.dev_err, CCONV_DERR_NUM_ACCEPTED);
-      return;
-    }
-  }
-  const bool hs = slot >= 0 && (a.has_init == nullptr || a.has_init[s] != 0);
-  const int cap = a.pool.cap;
-  const int ncols = a.n_spec > 0 ? cap : S;
-  // The state is rolled in place (a channel's columns are private to its
-  // thread) and the outputs overwrite the token rows once they are in
-  // registers: shared memory holds one state copy and q rows.
-  R* st_s = reinterpret_cast<R*>(dyn_smem);             // state of the block's channels
-  R* xs = st_s + nb * cap;                              // [QM][nb]: tokens, then outputs
-  const int cs = nb;                                    // column step of the state copy
-  const int64_t elem0 = (int64_t)slot * a.pool.s_slot;  // pool element of slot, channel 0
-  const int64_t row0 = (int64_t)s * q;
-
-  // 1. loads: state (cooperative 16-byte units where the layout allows), x rows
-  if (slot >= 0) {
-    if (a.pool.mode == kPoolSD) {
-      const int upr = nch * E / 16;                     // units per column row
-      for (int u = tid; u < upr * cap; u += nt) {
-        const int col = u / upr, k = u - col * upr;
-        reinterpret_cast<uint4*>(st_s + col * nb)[k] = *reinterpret_cast<const uint4*>(
-            a.pool.p + (elem0 + (int64_t)col * a.pool.s_col + cb) * E + k * 16);
-      }
-    } else {
-      for (int c = tid; c < nch; c += nt)
-        for (int col = 0; col < cap; ++col)
-          st_s[col * nb + c] = *reinterpret_cast<const R*>(
-              a.pool.p + (elem0 + (int64_t)(cb + c) * a.pool.s_chan + (int64_t)col * a.pool.s_col) * E);
-    }
-  }
-  {
-    const int upr = nch * E / 16;
-    for (int u = tid; u < upr * q; u += nt) {
-      const int r = u / upr, k = u - r * upr;
-      reinterpret_cast<uint4*>(xs + r * nb)[k] =
-          ldg16(a.x + ((row0 + r) * a.x_rs + cb) * E + k * 16);
-    }
-  }
-  // this thread's weights and biases, loaded alongside the state
-  float wk[K][W], bv[K];
-#pragma unroll
-  for (int kc = 0; kc < K; ++kc) {
-    const int c = min(tid + kc * nt, nch - 1);
-#pragma unroll
-    for (int k = 0; k < W; ++k) wk[kc][k] = load_f32<T>(a.w, (int64_t)(cb + c) * W + k);
-    bv[kc] = a.bias ? load_f32<T>(a.bias, cb + c) : 0.0f;
-  }
-  __syncthreads();
-
-  // 2. per-channel arithmetic: prior window and tokens in registers
-  const bool silu_on = a.act == CCONV_ACT_SILU;
-  const int keep = ncols - q;   // spec: kept columns B[off+1, off+1+keep), keep >= S-1
-#pragma unroll
-  for (int kc = 0; kc < K; ++kc) {
-    const int c = tid + kc * nt;
-    if (c >= nch) break;
-    R* row = st_s + c;                                 // column col at row[col * cs]
-    float pr[S];                                        // B[off + i], zero without history
-    R pb[S];
-#pragma unroll
-    for (int i = 0; i < S; ++i) {
-      pb[i] = hs ? row[(off + i) * cs] : R(0);
-      pr[i] = raw_to_f32<T>(pb[i]);
-    }
-    R xb[QM];
-    float xf[QM];
-#pragma unroll
-    for (int u = 0; u < QM; ++u) {
-      xb[u] = u < q ? xs[u * nb + c] : R(0);
-      xf[u] = raw_to_f32<T>(xb[u]);
-    }
-#pragma unroll
-    for (int i = 0; i < QM; ++i) {
-      if (i < q) {
-        float acc = bv[kc];
-#pragma unroll
-        for (int k = 0; k < W; ++k) {
-          const int idx = S + i - (W - 1 - k) * D;   // position in prior ++ tokens
-          acc = fmaf(wk[kc][k], idx >= S ? xf[idx - S] : pr[idx], acc);
-        }
-        xs[i * nb + c] = f32_to_raw<T>(silu_on ? silu<T>(acc) : acc);
-      }
-    }
-    if (slot >= 0) {
-      if (a.n_spec == 0) {
-#pragma unroll
-        for (int col = 0; col + 1 < S; ++col) row[col * cs] = pb[col + 1];
-        row[(S - 1) * cs] = xb[0];
-      } else {
-        // B[off+1+col] for col < S-1 is pb[col+1]; wider buffers keep more
-        // columns, read ahead of every write
-#pragma unroll
-        for (int col = 0; col + 1 < S; ++col) row[col * cs] = pb[col + 1];
-        for (int col = S - 1; col < keep; ++col)
-          row[col * cs] = hs ? row[(off + 1 + col) * cs] : R(0);
-#pragma unroll
-        for (int u = 0; u < QM; ++u)
-          if (u < q) row[(keep + u) * cs] = xb[u];
-      }
-    }
-  }
-  __syncthreads();
-
-  // 3. stores: outputs, new state
-  {
-    const int upr = nch * E / 16;
-    for (int u = tid; u < upr * q; u += nt) {
-      const int r = u / upr, k = u - r * upr;
-      stg16(a.out + ((row0 + r) * a.out_rs + cb) * E + k * 16,
-            reinterpret_cast<const uint4*>(xs + r * nb)[k]);
-    }
-  }
-  if (slot >= 0) {
-    if (a.pool.mode == kPoolSD) {
-      const int upr = nch * E / 16;
-      for (int u = tid; u < upr * ncols; u += nt) {
-        const int col = u / upr, k = u - col * upr;
-        *reinterpret_cast<uint4*>(a.pool.p + (elem0 + (int64_t)col * a.pool.s_col + cb) * E +
-                                  k * 16) = reinterpret_cast<const uint4*>(st_s + col * nb)[k];
-      }
-    } else {
-      for (int c = tid; c < nch; c += nt)
-        for (int col = 0; col < ncols; ++col)
-          *reinterpret_cast<R*>(a.pool.p + (elem0 + (int64_t)(cb + c) * a.pool.s_chan +
-                                            (int64_t)col * a.pool.s_col) * E) = st_s[col * nb + c];
-    }
-  }
-}
-
-// ---- host side -----------------------------------------------------------
-
-static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
-static int pool_mode(const cconv_pool_t& pv, int esize, int V) {
-  const bool base_ok = aligned16(pv.p);
-  if (pv.s_col == 1 && pv.s_chan == pv.cap && base_ok && (pv.s_slot * esize) % 16 == 0)
-    return kPoolDS;
-  if (pv.s_chan == 1 && base_ok && pv.s_col % V == 0 && pv.s_slot % V == 0) return kPoolSD;
-  return kPoolGeneric;
-}
-
-static Pool make_pool(const cconv_pool_t& pv, int esize, int V) {
-  Pool P;
-  P.p = static_cast<char*>(pv.p);
-  P.s_slot = pv.s_slot;
-  P.s_chan = pv.s_chan;
-  P.s_col = pv.s_col;
-  P.num_slots = pv.num_slots;
-  P.cap = pv.cap;
-  P.mode = pool_mode(pv, esize, V);
-  return P;
-}
-
-// Threads per block: up to 128 channel units, fewer when the per-thread
-// shared-memory columns (cols * 16 bytes) would pass the 48 KB a block gets
-// without opting in (less 1 KB for the kernels' static shared memory).
-static int pick_threads(int units, int cols) {
-  int nt = std::min(128, ((units + 31) / 32) * 32);
-  const int by_smem = (47 * 1024) / std::max(1, cols * 16);
-  nt = std::min(nt, (by_smem / 32) * 32);
-  return std::max(nt, 32);
-}
-
-// `rows` is the number of activation rows the call covers; x and out may be
-// NULL only when it is zero (an empty tensor has no storage).
-static int check_common(const void* x, int64_t x_rs, const void* w, const cconv_pool_t& pv,
-                        const int32_t* state_idx, int32_t num_seqs, int32_t C, int32_t width,
-                        int32_t dilation, int32_t act, int32_t dtype, const void* out,
-                        int64_t out_rs, int64_t rows, int* esize, int* V) {
-  if (dtype != CCONV_DTYPE_F32 && dtype != CCONV_DTYPE_BF16) return CCONV_ERR_INVALID;
-  *esize = dtype == CCONV_DTYPE_F32 ? 4 : 2;
-  *V = 16 / *esize;
-  if (!w || !pv.p || (num_seqs > 0 && !state_idx)) return CCONV_ERR_INVALID;
-  if (rows > 0 && (!x || !out)) return CCONV_ERR_INVALID;
-  if (C <= 0 || C % *V != 0) return CCONV_ERR_INVALID;
-  if (width < 1 || dilation < 1) return CCONV_ERR_INVALID;
-  if (width < 2 || width > 4 || dilation > 4) return CCONV_ERR_UNSUPPORTED;
-  if (act != CCONV_ACT_NONE && act != CCONV_ACT_SILU) return CCONV_ERR_INVALID;
-  if (!aligned16(x) || !aligned16(out)) return CCONV_ERR_INVALID;
-  if (x_rs < C || out_rs < C || x_rs % *V != 0 || out_rs % *V != 0) return CCONV_ERR_INVALID;
-  if (pv.num_slots <= 0 || pv.cap <= 0 || pv.cap > 96) return CCONV_ERR_INVALID;
-  if (pv.s_slot <= 0 || pv.s_chan <= 0 || pv.s_col <= 0) return CCONV_ERR_INVALID;
-  return CCONV_OK;
-}
-
-template <typename T>
-static cudaError_t launch_fwd(int W, int D, dim3 grid, int nt, size_t smem,
-                              cudaStream_t st, const FwdArgs& a) {
-#define CCONV_FWD_CASE(w_, d_)                                              \
-  if (W == w_ && D == d_) {                                                 \
-    fwd_varlen_kernel<T, w_, d_><<<grid, nt, smem, st>>>(a);                \
-    return cudaGetLastError();                                              \
-  }
-  CCONV_FWD_CASE(2, 1) CCONV_FWD_CASE(2, 2) CCONV_FWD_CASE(2, 3) CCONV_FWD_CASE(2, 4)
-  CCONV_FWD_CASE(3, 1) CCONV_FWD_CASE(3, 2) CCONV_FWD_CASE(3, 3) CCONV_FWD_CASE(3, 4)
-  CCONV_FWD_CASE(4, 1) CCONV_FWD_CASE(4, 2) CCONV_FWD_CASE(4, 3) CCONV_FWD_CASE(4, 4)
-#undef CCONV_FWD_CASE
-  return cudaErrorInvalidValue;
-}
-
-template <typename T>
-static cudaError_t launch_upd(int W, int D, dim3 grid, int nt, size_t smem,
-                              cudaStream_t st, const UpdArgs& a) {
-#define CCONV_UPD_CASE(w_, d_)                                              \
-  if (W == w_ && D == d_) {                                                 \
-    update_kernel<T, w_, d_><<<grid, nt, smem, st>>>(a);                    \
-    return cudaGetLastError();                                              \
-  }
-  CCONV_UPD_CASE(2, 1) CCONV_UPD_CASE(2, 2) CCONV_UPD_CASE(2, 3) CCONV_UPD_CASE(2, 4)
-  CCONV_UPD_CASE(3, 1) CCONV_UPD_CASE(3, 2) CCONV_UPD_CASE(3, 3) CCONV_UPD_CASE(3, 4)
-  CCONV_UPD_CASE(4, 1) CCONV_UPD_CASE(4, 2) CCONV_UPD_CASE(4, 3) CCONV_UPD_CASE(4, 4)
-#undef CCONV_UPD_CASE
-  return cudaErrorInvalidValue;
-}
-
-}  // namespace cconv
+// Entry points cconv_fwd_varlen and cconv_update (kernels in depthwise.cuh
+// and update_bulk.cu).
+#include "depthwise.cuh"
 
 using namespace cconv;
 
@@ -474,55 +11,11 @@ extern "C" int cconv_fwd_varlen(const void* x, int64_t x_row_stride, const void*
                                 int32_t C, int32_t width, int32_t dilation, int32_t act,
                                 int32_t dtype, void* out, int64_t out_row_stride,
                                 int32_t* dev_err, cconv_stream_t stream) {
-  int esize = 0, V = 0;
-  int rc = check_common(x, x_row_stride, w, conv_states, state_idx, num_seqs, C, width,
-                        dilation, act, dtype, out, out_row_stride, num_tokens, &esize, &V);
-  if (rc != CCONV_OK) return rc;
-  if ((num_seqs > 0 && !cu_seqlens) || num_seqs < 0 || num_tokens < 0) return CCONV_ERR_INVALID;
-  const int S = (width - 1) * dilation;
-  if (conv_states.cap < S) return CCONV_ERR_INVALID;
-  if (num_seqs == 0) return CCONV_OK;
-  FwdArgs a;
-  a.x = static_cast<const char*>(x);
-  a.x_rs = x_row_stride;
-  a.w = static_cast<const char*>(w);
-  a.bias = static_cast<const char*>(bias);
-  a.pool = make_pool(conv_states, esize, V);
-  a.state_idx = state_idx;
-  a.cu = cu_seqlens;
-  a.has_init = has_init;
-  a.B = num_seqs;
-  a.T = num_tokens;
-  a.C = C;
-  a.act = act;
-  a.out = static_cast<char*>(out);
-  a.out_rs = out_row_stride;
-  a.dev_err = dev_err;
-  const int units = C / V;
-  const int nt = pick_threads(units, conv_states.cap + kRing);
-  const int ctiles = (units + nt - 1) / nt;
-  // 128-token chunks halve the per-block window and setup work; 64 keeps
-  // enough blocks in flight for smaller calls.
-  int dev = 0, sms = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-    return CCONV_ERR_LAUNCH;
-  const int64_t blocks_big = ((int64_t)num_tokens >> kChunkShiftMax) * ctiles;
-  a.chunk_shift = blocks_big >= (int64_t)kWaveBlocks * sms ? kChunkShiftMax : kChunkShiftMin;
-  const int64_t nblk = ((int64_t)num_tokens >> a.chunk_shift) + num_seqs + 1;
-  if (nblk > 0x7fffffff) return CCONV_ERR_INVALID;
-  a.nblk = (int32_t)nblk;
-  a.order_lpt = nblk <= 65535 ? 1 : 0;
-  if (!a.order_lpt && ctiles > 65535) return CCONV_ERR_INVALID;
-  const dim3 grid = a.order_lpt ? dim3((unsigned)ctiles, (unsigned)nblk)
-                                : dim3((unsigned)nblk, (unsigned)ctiles);
-  const size_t smem = (size_t)nt * (conv_states.cap + kRing) * 16;
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = dtype == CCONV_DTYPE_F32
-                      ? launch_fwd<float>(width, dilation, grid, nt, smem, st, a)
-                      : launch_fwd<__nv_bfloat16>(width, dilation, grid, nt, smem, st, a);
-  return e == cudaSuccess ? CCONV_OK : CCONV_ERR_LAUNCH;
+  return fwd_entry<false>(x, x_row_stride, w, bias, conv_states, state_idx, cu_seqlens,
+                          has_init, num_seqs, num_tokens, C, width, dilation, act, dtype, out,
+                          out_row_stride, nullptr, dev_err, stream);
 }
+
 
 extern "C" int cconv_update(const void* x, int64_t x_row_stride, cconv_pool_t conv_states,
                             const void* w, const void* bias, const int32_t* state_idx,
@@ -530,56 +23,7 @@ extern "C" int cconv_update(const void* x, int64_t x_row_stride, cconv_pool_t co
                             const uint8_t* has_init, int32_t C, int32_t width,
                             int32_t dilation, int32_t act, int32_t dtype, void* out,
                             int64_t out_row_stride, int32_t* dev_err, cconv_stream_t stream) {
-  int esize = 0, V = 0;
-  int rc = check_common(x, x_row_stride, w, conv_states, state_idx, num_seqs, C, width,
-                        dilation, act, dtype, out, out_row_stride,
-                        (int64_t)num_seqs * (1 + n_spec), &esize, &V);
-  if (rc != CCONV_OK) return rc;
-  if (num_seqs < 0 || n_spec < 0) return CCONV_ERR_INVALID;
-  if (n_spec > kMaxSpec) return CCONV_ERR_UNSUPPORTED;
-  if (n_spec > 0 && num_seqs > 0 && !num_accepted) return CCONV_ERR_INVALID;
-  const int S = (width - 1) * dilation;
-  if (conv_states.cap < S + n_spec) return CCONV_ERR_INVALID;
-  if (num_seqs == 0) return CCONV_OK;
-  UpdArgs a;
-  a.x = static_cast<const char*>(x);
-  a.x_rs = x_row_stride;
-  a.pool = make_pool(conv_states, esize, V);
-  a.w = static_cast<const char*>(w);
-  a.bias = static_cast<const char*>(bias);
-  a.state_idx = state_idx;
-  a.B = num_seqs;
-  a.n_spec = n_spec;
-  a.num_accepted = num_accepted;
-  a.has_init = has_init;
-  a.C = C;
-  a.act = act;
-  a.out = static_cast<char*>(out);
-  a.out_rs = out_row_stride;
-  a.dev_err = dev_err;
-  // one block = one request x up to 512 channels; shared memory holds the
-  // block's state (rolled in place) and q token rows (then output rows)
-  int nt = 256;
-  auto smem_for = [&](int n) {
-    return (size_t)kUpdChan * n * (conv_states.cap + kMaxSpec + 1) * esize;
-  };
-  while (nt > 32 && smem_for(nt) > 47 * 1024) nt /= 2;
-  nt = std::min(nt, ((C + kUpdChan * 32 - 1) / (kUpdChan * 32)) * 32);
-  a.ctiles = (C + kUpdChan * nt - 1) / (kUpdChan * nt);
-  const int64_t nblk = (int64_t)num_seqs * a.ctiles;
-  if (nblk > 0x7fffffff) return CCONV_ERR_INVALID;
-  const size_t smem = smem_for(nt);
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  // A channel-first pool whose slot slabs start on 16 bytes streams through
-  // the bulk-copy pipeline; anything else takes the block-per-request kernel.
-  if (a.pool.mode == kPoolDS) {
-    const cudaError_t eb = launch_update_bulk(a, width, dilation, dtype, esize, st);
-    if (eb != cudaErrorNotSupported) return eb == cudaSuccess ? CCONV_OK : CCONV_ERR_LAUNCH;
-    a.pool.mode = kPoolGeneric;
-  }
-  const dim3 grid((unsigned)nblk);
-  cudaError_t e = dtype == CCONV_DTYPE_F32
-                      ? launch_upd<float>(width, dilation, grid, nt, smem, st, a)
-                      : launch_upd<__nv_bfloat16>(width, dilation, grid, nt, smem, st, a);
-  return e == cudaSuccess ? CCONV_OK : CCONV_ERR_LAUNCH;
+  return upd_entry<false>(x, x_row_stride, conv_states, w, bias, state_idx, num_seqs, n_spec,
+                          num_accepted, has_init, C, width, dilation, act, dtype, out,
+                          out_row_stride, nullptr, dev_err, stream);
 }

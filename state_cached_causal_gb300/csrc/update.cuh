@@ -20,8 +20,12 @@ struct UpdArgs {
   const int32_t* num_accepted;
   const uint8_t* has_init;
   int32_t C, act, ctiles;
-  char* out;
+  char* out;            // output rows, or the residual rows of the fused entry point
   int64_t out_rs;
+  const char* outer;    // fused: outer residual rows or null
+  int64_t outer_rs;
+  const int32_t* tidx;  // fused: physical row of each logical row, or null
+  int32_t num_rows;     // fused: physical rows of x, residual and outer
   int32_t* dev_err;
 };
 
@@ -30,6 +34,6 @@ struct UpdArgs {
 // cudaErrorNotSupported when the shapes do not fit it (the caller then uses
 // the block-per-request kernel).
 cudaError_t launch_update_bulk(UpdArgs a, int width, int dilation, int dtype, int esize,
-                               cudaStream_t st);
+                               bool fused, cudaStream_t st);
 
 }  // namespace cconv

@@ -42,6 +42,7 @@ enum : int32_t { kSkip = 1, kHist = 2, kOwn = 4, kLoadState = 8 };
 
 struct Meta {
   int32_t s, ct, off, flags, slot;
+  int32_t prow[kMaxSpec + 1];   // physical row of the request's token r
 };
 
 struct Ctl {
@@ -56,6 +57,8 @@ struct BulkArgs {
   int32_t tile;          // channels per work item (multiple of 8)
   int32_t stage_bytes;   // bytes per stage (multiple of 128)
   int32_t xs_off;        // byte offset of the token rows within a stage
+  int32_t rs_off;        // fused: byte offset of the residual rows
+  int32_t os_off;        // fused: byte offset of the outer residual rows
   int64_t items;         // B * ctiles
 };
 
@@ -74,8 +77,10 @@ __device__ bool wait_bounded(Ctl* ctl, uint64_t* bar, uint32_t parity, int32_t* 
   }
 }
 
-// Request metadata of one item, validated: a slot beyond the pool or a
-// num_accepted outside [1, q] flags the error and skips the item.
+// Request metadata of one item, validated: a slot beyond the pool, a
+// num_accepted outside [1, q] or (fused) a token row outside the physical rows
+// flags the error and skips the item.
+template <bool FUSED>
 __device__ Meta item_meta(const UpdArgs& a, int64_t item, int S) {
   Meta m;
   m.s = (int32_t)(item % a.B);
@@ -97,6 +102,19 @@ __device__ Meta item_meta(const UpdArgs& a, int64_t item, int S) {
       return m;
     }
   }
+  if (FUSED) {
+    const int q = 1 + a.n_spec;
+    for (int r = 0; r < q; ++r) {
+      const int64_t li = (int64_t)m.s * q + r;
+      const int p = a.tidx ? a.tidx[li] : (int)li;
+      if (p < 0 || p >= a.num_rows) {
+        flag_error(a.dev_err, CCONV_DERR_ROW_INDEX);
+        m.flags = kSkip;
+        return m;
+      }
+      m.prow[r] = p;
+    }
+  }
   const bool hs = slot >= 0 && (a.has_init == nullptr || a.has_init[m.s] != 0);
   if (hs) m.flags |= kHist;
   if (slot >= 0) {
@@ -109,7 +127,7 @@ __device__ Meta item_meta(const UpdArgs& a, int64_t item, int S) {
   return m;
 }
 
-template <typename T, int W, int D>
+template <typename T, int W, int D, bool FUSED>
 __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
     update_bulk_kernel(const UpdArgs a, const BulkArgs b) {
   constexpr int S = (W - 1) * D;
@@ -148,19 +166,30 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
       const int cb = m.ct * tile, nch = min(tile, a.C - cb);
       const uint32_t row_bytes = (uint32_t)nch * E;
       const uint32_t slab_bytes = (uint32_t)nch * cap * E;
-      mbar_arrive_tx(&ctl->full[st],
-                     q * row_bytes + ((m.flags & kLoadState) ? slab_bytes : 0u));
-      for (int r = 0; r < q; ++r)
-        bulk_load(sb + b.xs_off + (size_t)r * tile * E,
-                  a.x + (((int64_t)m.s * q + r) * a.x_rs + cb) * E, row_bytes, &ctl->full[st]);
+      const int rows_per_token = FUSED ? (a.outer ? 3 : 2) : 1;
+      mbar_arrive_tx(&ctl->full[st], q * rows_per_token * row_bytes +
+                                         ((m.flags & kLoadState) ? slab_bytes : 0u));
+      for (int r = 0; r < q; ++r) {
+        const int64_t p = FUSED ? (int64_t)m.prow[r] : (int64_t)m.s * q + r;
+        bulk_load(sb + b.xs_off + (size_t)r * tile * E, a.x + (p * a.x_rs + cb) * E, row_bytes,
+                  &ctl->full[st]);
+        if (FUSED) {
+          bulk_load(sb + b.rs_off + (size_t)r * tile * E, a.out + (p * a.out_rs + cb) * E,
+                    row_bytes, &ctl->full[st]);
+          if (a.outer)
+            bulk_load(sb + b.os_off + (size_t)r * tile * E, a.outer + (p * a.outer_rs + cb) * E,
+                      row_bytes, &ctl->full[st]);
+        }
+      }
       if (m.flags & kLoadState)
         bulk_load(sb, a.pool.p + ((int64_t)m.slot * a.pool.s_slot + (int64_t)cb * cap) * E,
                   slab_bytes, &ctl->full[st]);
     };
     int issued = 0;
-    for (; issued < min(n, kStages); ++issued) issue_load(issued, item_meta(a, i0 + issued, S));
+    for (; issued < min(n, kStages); ++issued)
+      issue_load(issued, item_meta<FUSED>(a, i0 + issued, S));
     Meta next{};
-    if (issued < n) next = item_meta(a, i0 + issued, S);   // one item ahead
+    if (issued < n) next = item_meta<FUSED>(a, i0 + issued, S);   // one item ahead
     int j = 0;
     for (; j < n; ++j) {
       const int st = j % kStages;
@@ -171,7 +200,8 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
         const int cb = m.ct * tile, nch = min(tile, a.C - cb);
         const uint32_t row_bytes = (uint32_t)nch * E;
         for (int r = 0; r < q; ++r)
-          bulk_store(a.out + (((int64_t)m.s * q + r) * a.out_rs + cb) * E,
+          bulk_store(a.out + ((FUSED ? (int64_t)m.prow[r] : (int64_t)m.s * q + r) * a.out_rs +
+                              cb) * E,
                      sb + b.xs_off + (size_t)r * tile * E, row_bytes);
         if (m.flags & kOwn) {
           bulk_store(a.pool.p + ((int64_t)m.slot * a.pool.s_slot + (int64_t)cb * cap) * E, sb,
@@ -183,7 +213,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
         bulk_wait_read<0>();   // the stage's stores have read it
         issue_load(issued, next);
         ++issued;
-        if (issued < n) next = item_meta(a, i0 + issued, S);
+        if (issued < n) next = item_meta<FUSED>(a, i0 + issued, S);
       }
     }
     if (j < n) {
@@ -223,6 +253,9 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
       unsigned char* sb = stage0 + (size_t)st * b.stage_bytes;
       R* slab = reinterpret_cast<R*>(sb);
       R* xs = reinterpret_cast<R*>(sb + b.xs_off);
+      const R* rs = reinterpret_cast<const R*>(sb + b.rs_off);
+      const R* os = reinterpret_cast<const R*>(sb + b.os_off);
+      const bool has_outer = a.outer != nullptr;
       const bool hs = m.flags & kHist, own = m.flags & kOwn;
 #pragma unroll
       for (int kc = 0; kc < 2; ++kc) {
@@ -252,7 +285,12 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
               const int idx = S + i - (W - 1 - k) * D;   // position in prior ++ tokens
               acc = fmaf(wk[kc][k], idx >= S ? xf[idx - S] : pr[idx], acc);
             }
-            xs[i * tile + c] = f32_to_raw<T>(silu_on ? silu<T>(acc) : acc);
+            float y = silu_on ? silu<T>(acc) : acc;
+            if constexpr (FUSED) {
+              y = raw_to_f32<T>(rs[i * tile + c]) + y;
+              if (has_outer) y = y + raw_to_f32<T>(os[i * tile + c]);
+            }
+            xs[i * tile + c] = f32_to_raw<T>(y);
           }
         }
         if (own) {
@@ -286,10 +324,10 @@ struct LaunchCache {
   int per_sm = 0;
 };
 
-template <typename T, int W, int D>
+template <typename T, int W, int D, bool FUSED>
 cudaError_t launch_t(const UpdArgs& a, const BulkArgs& b, size_t smem, cudaStream_t st, int dev,
                      int num_sms) {
-  auto k = update_bulk_kernel<T, W, D>;
+  auto k = update_bulk_kernel<T, W, D, FUSED>;
   static LaunchCache cache;
   int per_sm = 0;
   {
@@ -314,11 +352,11 @@ cudaError_t launch_t(const UpdArgs& a, const BulkArgs& b, size_t smem, cudaStrea
   return cudaGetLastError();
 }
 
-template <typename T>
+template <typename T, bool FUSED>
 cudaError_t launch_wd(int W, int D, const UpdArgs& a, const BulkArgs& b, size_t smem,
                       cudaStream_t st, int dev, int num_sms) {
 #define CCONV_BULK_CASE(w_, d_) \
-  if (W == w_ && D == d_) return launch_t<T, w_, d_>(a, b, smem, st, dev, num_sms);
+  if (W == w_ && D == d_) return launch_t<T, w_, d_, FUSED>(a, b, smem, st, dev, num_sms);
   CCONV_BULK_CASE(2, 1) CCONV_BULK_CASE(2, 2) CCONV_BULK_CASE(2, 3) CCONV_BULK_CASE(2, 4)
   CCONV_BULK_CASE(3, 1) CCONV_BULK_CASE(3, 2) CCONV_BULK_CASE(3, 3) CCONV_BULK_CASE(3, 4)
   CCONV_BULK_CASE(4, 1) CCONV_BULK_CASE(4, 2) CCONV_BULK_CASE(4, 3) CCONV_BULK_CASE(4, 4)
@@ -329,15 +367,17 @@ cudaError_t launch_wd(int W, int D, const UpdArgs& a, const BulkArgs& b, size_t 
 }  // namespace
 
 cudaError_t launch_update_bulk(UpdArgs a, int width, int dilation, int dtype, int esize,
-                               cudaStream_t st) {
+                               bool fused, cudaStream_t st) {
   const int q = 1 + a.n_spec, cap = a.pool.cap;
   const int V = 16 / esize;
+  const int row_sets = fused ? 3 : 1;   // token rows (+ residual and outer rows)
   // Largest channel tile (a multiple of 8 channels, so every row and slab is
   // a multiple of 16 bytes) whose stages fit the budget.
   int tile = kTileMax;
+  auto rows_bytes = [&](int t) { return ((size_t)q * t * esize + 127) / 128 * 128; };
   auto stage_bytes = [&](int t) {
     const size_t slab = ((size_t)t * cap * esize + 127) / 128 * 128;
-    return ((slab + (size_t)q * t * esize) + 127) / 128 * 128;
+    return slab + row_sets * rows_bytes(t);
   };
   while (tile > 8 && stage_bytes(tile) * kStages > kStageBudget) tile /= 2;
   if (stage_bytes(tile) * kStages > kStageBudget || tile % V != 0) return cudaErrorNotSupported;
@@ -346,6 +386,8 @@ cudaError_t launch_update_bulk(UpdArgs a, int width, int dilation, int dtype, in
   b.tile = tile;
   b.stage_bytes = (int32_t)stage_bytes(tile);
   b.xs_off = (int32_t)(((size_t)tile * cap * esize + 127) / 128 * 128);
+  b.rs_off = b.xs_off + (int32_t)rows_bytes(tile);
+  b.os_off = b.rs_off + (int32_t)rows_bytes(tile);
   a.ctiles = (a.C + tile - 1) / tile;
   b.items = (int64_t)a.B * a.ctiles;
   if (b.items <= 0) return cudaSuccess;
@@ -355,9 +397,13 @@ cudaError_t launch_update_bulk(UpdArgs a, int width, int dilation, int dtype, in
   if (e != cudaSuccess) return e;
   if (dev >= 64) return cudaErrorNotSupported;
   const size_t smem = kCtlBytes + (size_t)kStages * b.stage_bytes;
+  if (fused)
+    return dtype == CCONV_DTYPE_F32
+               ? launch_wd<float, true>(width, dilation, a, b, smem, st, dev, num_sms)
+               : launch_wd<__nv_bfloat16, true>(width, dilation, a, b, smem, st, dev, num_sms);
   return dtype == CCONV_DTYPE_F32
-             ? launch_wd<float>(width, dilation, a, b, smem, st, dev, num_sms)
-             : launch_wd<__nv_bfloat16>(width, dilation, a, b, smem, st, dev, num_sms);
+             ? launch_wd<float, false>(width, dilation, a, b, smem, st, dev, num_sms)
+             : launch_wd<__nv_bfloat16, false>(width, dilation, a, b, smem, st, dev, num_sms);
 }
 
 }  // namespace cconv

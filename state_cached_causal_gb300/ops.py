@@ -21,9 +21,18 @@ OK, ERR_INVALID, ERR_UNSUPPORTED, ERR_LAUNCH = 0, -1, -2, -3
 DTYPE_F32, DTYPE_BF16 = 0, 1
 ACT_NONE, ACT_SILU = 0, 1
 DERR_SLOT_RANGE, DERR_CU_SEQLENS, DERR_NUM_ACCEPTED, DERR_TIMEOUT = 1, 2, 4, 8
+DERR_ROW_INDEX = 16
 
 _lock = threading.Lock()
 _lib = None
+
+
+class Epilogue(ctypes.Structure):
+    """cconv_epilogue_t: residual rows updated in place, optional outer residual,
+    optional logical -> physical row map."""
+    _fields_ = [("residual", ctypes.c_void_p), ("residual_row_stride", ctypes.c_int64),
+                ("outer_residual", ctypes.c_void_p), ("outer_row_stride", ctypes.c_int64),
+                ("token_indices", ctypes.c_void_p), ("num_rows", ctypes.c_int32)]
 
 
 class Pool(ctypes.Structure):
@@ -56,6 +65,12 @@ def load():
         lib.cconv_update.argtypes = [P, I64, Pool, P, P, P, I32, I32, P, P, I32, I32, I32, I32,
                                      I32, P, I64, P, P]
         lib.cconv_update.restype = ctypes.c_int
+        lib.cconv_fwd_varlen_fused.argtypes = [P, I64, P, P, Pool, P, P, P, I32, I32, I32, I32,
+                                               I32, I32, I32, Epilogue, P, P]
+        lib.cconv_fwd_varlen_fused.restype = ctypes.c_int
+        lib.cconv_update_fused.argtypes = [P, I64, Pool, P, P, P, I32, I32, P, P, I32, I32, I32,
+                                           I32, I32, Epilogue, P, P]
+        lib.cconv_update_fused.restype = ctypes.c_int
         lib.cca_qk_conv.argtypes = [P, I64, P, P, P, P, I32, I32, I32, P, I64, P, I32, Pool, P,
                                     I64, P, P, P, I32, I32, I32, I32, P, I64, P, I64, P, P]
         lib.cca_qk_conv.restype = ctypes.c_int
@@ -166,6 +181,51 @@ def cconv_update(x, conv_states, w, bias, state_idx, n_spec, num_accepted, has_i
         int(x.shape[1]), int(width), int(dilation), int(act), _dtype_code(x), _ptr(out),
         _rows(out), _ptr(dev_err), _stream(stream))
     _check("cconv_update", rc)
+
+
+def _epilogue(residual, outer, token_indices, x):
+    _i32(token_indices, "token_indices")
+    return Epilogue(_ptr(residual), _rows(residual), _ptr(outer),
+                    _rows(outer) if outer is not None else 0, _ptr(token_indices),
+                    int(x.shape[0]))
+
+
+def cconv_fwd_varlen_fused(x, w, bias, conv_states, state_idx, cu_seqlens, has_init, width,
+                           dilation, act, residual, outer=None, token_indices=None,
+                           dev_err=None, stream=None, num_tokens=None):
+    """cconv_fwd_varlen with the fused residual epilogue (see cconv_fwd_varlen_fused
+    in cconv.h): residual[p] += act(conv)[i] (+ outer[p]), p = token_indices[i].
+
+    x, residual, outer: [R, C] physical rows; num_tokens: logical rows (default
+    len(token_indices), else R).
+    """
+    _i32(state_idx, "state_idx")
+    _i32(cu_seqlens, "cu_seqlens")
+    _u8(has_init, "has_init")
+    if num_tokens is None:
+        num_tokens = int(token_indices.shape[0]) if token_indices is not None else int(x.shape[0])
+    rc = load().cconv_fwd_varlen_fused(
+        _ptr(x), _rows(x), _ptr(w), _ptr(bias), _pool(conv_states), _ptr(state_idx),
+        _ptr(cu_seqlens), _ptr(has_init), int(state_idx.shape[0]), int(num_tokens),
+        int(x.shape[1]), int(width), int(dilation), int(act), _dtype_code(x),
+        _epilogue(residual, outer, token_indices, x), _ptr(dev_err), _stream(stream))
+    _check("cconv_fwd_varlen_fused", rc)
+
+
+def cconv_update_fused(x, conv_states, w, bias, state_idx, n_spec, num_accepted, has_init,
+                       width, dilation, act, residual, outer=None, token_indices=None,
+                       dev_err=None, stream=None):
+    """cconv_update with the fused residual epilogue (see cconv_update_fused in
+    cconv.h); request s owns logical rows [s*q, s*q + q)."""
+    _i32(state_idx, "state_idx")
+    _i32(num_accepted, "num_accepted")
+    _u8(has_init, "has_init")
+    rc = load().cconv_update_fused(
+        _ptr(x), _rows(x), _pool(conv_states), _ptr(w), _ptr(bias), _ptr(state_idx),
+        int(state_idx.shape[0]), int(n_spec), _ptr(num_accepted), _ptr(has_init),
+        int(x.shape[1]), int(width), int(dilation), int(act), _dtype_code(x),
+        _epilogue(residual, outer, token_indices, x), _ptr(dev_err), _stream(stream))
+    _check("cconv_update_fused", rc)
 
 
 def cca_qk_conv(qk, w_dw, b_dw, w_gr, b_gr, groups, t0, t1, delayed, delayed_init,

@@ -33,8 +33,8 @@ def declared_functions():
 
 def test_header_declares_the_three_operations():
     names = declared_functions()
-    for n in ("cconv_fwd_varlen", "cconv_update", "cca_qk_conv", "cconv_status_string",
-              "cconv_abi_version"):
+    for n in ("cconv_fwd_varlen", "cconv_update", "cca_qk_conv", "cconv_fwd_varlen_fused",
+              "cconv_update_fused", "cconv_status_string", "cconv_abi_version"):
         assert n in names
 
 
@@ -48,7 +48,7 @@ def test_status_strings(lib):
     for s in (-1, -2, -3):
         assert ops.status_string(s) not in ("ok", "unknown status")
     assert ops.status_string(17) == "unknown status"
-    assert ops.abi_version() == 1
+    assert ops.abi_version() == 2
 
 
 FAKE = 0x10000  # 16-byte aligned, never dereferenced: every call below fails validation
@@ -116,3 +116,29 @@ def test_valid_call_without_gpu_fails_loudly(lib):
     # A valid request on a machine with no CUDA device must report a launch
     # failure, never compute anything on the host.
     assert fwd(lib, C=16) == -3
+
+
+def fwd_fused(lib, epi, **kw):
+    a = dict(x=FAKE, xrs=16, w=FAKE, bias=None, pool=_pool(), sidx=FAKE, cu=FAKE, hi=None,
+             B=2, T=8, C=16, W=4, D=1, act=1, dt=1)
+    a.update(kw)
+    P = lambda v: None if v is None else ctypes.c_void_p(v)
+    return lib.cconv_fwd_varlen_fused(P(a["x"]), a["xrs"], P(a["w"]), P(a["bias"]), a["pool"],
+                                      P(a["sidx"]), P(a["cu"]), P(a["hi"]), a["B"], a["T"],
+                                      a["C"], a["W"], a["D"], a["act"], a["dt"], epi, None,
+                                      None)
+
+
+def _epi(res=FAKE, rrs=16, outer=None, ors=0, idx=None, rows=8):
+    P = lambda v: None if v is None else v
+    return ops.Epilogue(P(res), rrs, P(outer), ors, P(idx), rows)
+
+
+@pytest.mark.parametrize("epi,want", [
+    (dict(res=None), -1), (dict(res=FAKE + 4), -1), (dict(rrs=8), -1),
+    (dict(rows=0), -1), (dict(rows=7), -1), (dict(outer=FAKE + 2, ors=16), -1),
+    (dict(outer=FAKE, ors=12), -1), (dict(rows=4, idx=FAKE), -3), (dict(), -3)])
+@no_gpu
+def test_fwd_fused_checks_its_epilogue(lib, epi, want):
+    # -3: the epilogue passed every check and the launch failed (no device)
+    assert fwd_fused(lib, _epi(**epi)) == want
