@@ -18,7 +18,7 @@ measured copy bandwidth. `cpu_baseline` times the plain-C oracle on a bounded
 channel/request sample of the same step on the host cores.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload hybrid_step|ple_prefill_small|cca_small|...]
+                  [--workload hybrid_step|ple_fused|ple_prefill_small|cca_small|...]
 """
 import argparse
 import hashlib
@@ -93,6 +93,59 @@ def depthwise_calls(name, case, dev_err):
     return calls
 
 
+def fused_calls(name, case, dev_err, seed=2100):
+    """The PLE layer's dispatch on one mixed batch kept in arrival order: the
+    spec requests (cconv_update_fused) and the prefills (cconv_fwd_varlen_fused)
+    read x and update residual (+ outer residual) at their own physical rows,
+    found through token_indices."""
+    from state_cached_causal_gb300 import ops
+    e, C, W, S = _e(case.w), case.C, case.width, case.meta["S"]
+    q = 1 + case.n_spec
+    lens_p = (case.cu_seqlens[1:] - case.cu_seqlens[:-1]).cpu().tolist()
+    Rs = int(case.spec_state_idx.numel())
+    blocks = [("p", i, L) for i, L in enumerate(lens_p)] + [("s", i, q) for i in range(Rs)]
+    g = torch.Generator().manual_seed(seed)
+    order = torch.randperm(len(blocks), generator=g).tolist()
+    T, Rtot = case.num_tokens, case.num_tokens + Rs * q
+    idx_p = torch.empty(T, dtype=torch.int32)
+    idx_s = torch.empty(Rs * q, dtype=torch.int32)
+    cu = case.cu_seqlens.cpu().tolist()
+    row = 0
+    for k in order:
+        kind, i, L = blocks[k]
+        if kind == "p":
+            idx_p[cu[i]:cu[i] + L] = torch.arange(row, row + L, dtype=torch.int32)
+        else:
+            idx_s[i * q:(i + 1) * q] = torch.arange(row, row + q, dtype=torch.int32)
+        row += L
+    idx_p, idx_s = idx_p.to(case.x.device), idx_s.to(case.x.device)
+    x = torch.empty(Rtot, C, dtype=case.x.dtype, device=case.x.device)
+    x[idx_p.long()] = case.x
+    x[idx_s.long()] = case.x_spec
+    case.x, case.x_spec = None, None                  # only the physical copy stays
+    res = torch.randn(Rtot, C, device=x.device).to(x.dtype)
+    outer = torch.randn(Rtot, C, device=x.device).to(x.dtype)
+    wbytes = C * W * e
+    hi = case.has_init.to(torch.int64).cpu()
+    valid = (case.state_idx.cpu() >= 0).to(torch.int64)
+    nread, nwrite = int((hi * valid).sum()), int(valid.sum())
+    nb_p = 4 * T * C * e + wbytes + C * e * S * (nread + nwrite) + 4 * T
+    nb_s = 4 * Rs * q * C * e + wbytes + Rs * C * e * (S + case.meta["cap"]) + 4 * Rs * q
+
+    def f(case=case):
+        ops.cconv_fwd_varlen_fused(x, case.w, case.bias, case.pool, case.state_idx,
+                                   case.cu_seqlens, case.has_init, W, case.dilation, case.act,
+                                   res, outer, idx_p, dev_err=dev_err, num_tokens=T)
+
+    def u(case=case):
+        ops.cconv_update_fused(x, case.pool, case.w, case.bias, case.spec_state_idx,
+                               case.n_spec, case.num_accepted, case.spec_has_init, W,
+                               case.dilation, case.act, res, outer, idx_s, dev_err=dev_err)
+    return [Call(f"{name}.update_fused", "cconv_update_fused", u, Rs * q * C, nb_s,
+                 h2d=[x, res, outer], d2h=[res]),
+            Call(f"{name}.fwd_varlen_fused", "cconv_fwd_varlen_fused", f, T * C, nb_p)]
+
+
 def cca_calls(name, cc, dev_err):
     from state_cached_causal_gb300 import ops
     out = torch.empty_like(cc.qk)
@@ -151,6 +204,18 @@ def build_workload(name, dev, dev_err):
         return cca_calls("cca_small", cc, dev_err), "zaya cca 256 decodes + 2x4096"
     if name == "zaya_cca":
         return cca_calls("zaya_cca", synth.zaya_cca(dev), dev_err), "zaya_cca"
+    if name == "ple_fused_small":
+        case = synth.depthwise_case(2004, dev, lens=[2048] * 8, C=16384, width=4, dilation=3,
+                                    act=1, dtype=torch.bfloat16, w_std=0.1, num_slots=256,
+                                    spec_requests=128, n_spec=3)
+        return fused_calls("ple_fused_small", case, dev_err), \
+            "ple fused 8x2048 prefill + 128x(1+3) spec x 16384 ch, random request order"
+    if name == "ple_fused":
+        return fused_calls("ple_fused", synth.ple_spec(dev), dev_err), (
+            "ple_fused: the ple_spec batch (32x2048 prefill + 512x(1+3) spec x 16384 ch, "
+            "width 4 dilation 3) in one physical tensor in a random request order, "
+            "residual += conv + outer residual through token_indices "
+            "(cconv_update_fused + cconv_fwd_varlen_fused)")
     raise SystemExit(f"unknown workload {name}")
 
 
@@ -222,10 +287,21 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def kernel_source_hash():
+# Sources that make up each entry point's kernels (a recorded DRAM traffic
+# figure stays valid while these files are unchanged).
+KERNEL_SOURCES = {
+    "cconv_fwd_varlen": ["depthwise.cuh", "depthwise.cu", "common.cuh", "update.cuh"],
+    "cconv_update": ["update_bulk.cu", "update.cuh", "async.cuh", "common.cuh"],
+    "cca_qk_conv": ["cca_qk_conv.cu", "async.cuh", "common.cuh"],
+    "cconv_fwd_varlen_fused": ["depthwise.cuh", "depthwise_fused.cu", "common.cuh"],
+    "cconv_update_fused": ["update_bulk.cu", "update.cuh", "async.cuh", "common.cuh"],
+}
+
+
+def kernel_source_hash(kernel):
     h = hashlib.sha256()
     d = os.path.join(ROOT, "state_cached_causal_gb300", "csrc")
-    for f in sorted(os.listdir(d)):
+    for f in sorted(KERNEL_SOURCES.get(kernel, os.listdir(d))):
         with open(os.path.join(d, f), "rb") as fh:
             h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
@@ -238,7 +314,7 @@ def recorded_traffic(kernel):
         with open(p) as f:
             d = json.load(f)
         rec = d[kernel]
-        if rec.get("source_hash") != kernel_source_hash():
+        if rec.get("source_hash") != kernel_source_hash(kernel):
             return None
         return float(rec["dram_bytes_per_launch"])
     except Exception:
