@@ -323,67 +323,100 @@ def recorded_traffic(kernel):
 
 # ---- CPU oracle sample ---------------------------------------------------------
 
-def cpu_sample(dev, light=False):
-    """Bounded sample of the hybrid step for the oracle: channel / request subsets."""
+# channels (groups for CCA) of each workload in the oracle sample: about 10 s of
+# single-core work on the GPU host; `light` is the reference arm's per-step sample
+SAMPLE_CHANNELS = {"gdn_decode": 8192, "gdn_mixed": 2048, "zaya_cca": 20, "ple_spec": 3072}
+LIGHT_CHANNELS = {"gdn_decode": 512, "gdn_mixed": 64, "zaya_cca": 1, "ple_spec": 64}
+
+
+def cpu_sample(dev, light=False, parts=1):
+    """Bounded sample of the hybrid step for the oracle: channel (group) subsets of
+    each workload, all tokens of the sampled requests. Each workload's channels are
+    split into `parts` disjoint blocks (independent jobs, for the all-cores run)."""
     import numpy as np
     from state_cached_causal_gb300 import synth
     from oracle.torch_io import pool_np, to_np
     import oracle
     jobs = []
+    nch = LIGHT_CHANNELS if light else SAMPLE_CHANNELS
+
+    def blocks(total, unit):
+        n = max(1, min(parts, total // unit))
+        edges = [(k * (total // unit) // n) * unit for k in range(n + 1)]
+        return [(edges[k], edges[k + 1]) for k in range(n)]
 
     def dw(name, case, chans):
-        sl = slice(0, chans)
-        w = np.ascontiguousarray(to_np(case.w)[sl])
-        b = None if case.bias is None else np.ascontiguousarray(to_np(case.bias)[sl])
-        pool = pool_np(case.pool[:, sl, :].contiguous())
-        if case.x is not None:
-            x = np.ascontiguousarray(to_np(case.x[:, sl].contiguous()))
-            args = (to_np(case.state_idx), to_np(case.cu_seqlens), to_np(case.has_init))
+        for lo, hi in blocks(chans, 8):
+            sl = slice(lo, hi)
+            w = np.ascontiguousarray(to_np(case.w)[sl])
+            b = None if case.bias is None else np.ascontiguousarray(to_np(case.bias)[sl])
+            pool = pool_np(case.pool[:, sl, :].contiguous())
+            if case.x is not None:
+                x = np.ascontiguousarray(to_np(case.x[:, sl].contiguous()))
+                args = (to_np(case.state_idx), to_np(case.cu_seqlens), to_np(case.has_init))
 
-            def run(x=x, w=w, b=b, pool=pool, args=args, case=case):
-                oracle.cconv_fwd_varlen(x, w, b, pool.copy(), *args, case.width, case.dilation,
-                                        case.act, np.zeros_like(x))
-            jobs.append((f"{name}.fwd_varlen", run, x.shape[0] * chans))
-        if case.x_spec is not None:
-            xs = np.ascontiguousarray(to_np(case.x_spec[:, sl].contiguous()))
-            na = to_np(case.num_accepted) if case.n_spec else None
+                def run(x=x, w=w, b=b, pool=pool, args=args, case=case):
+                    oracle.cconv_fwd_varlen(x, w, b, pool.copy(), *args, case.width,
+                                            case.dilation, case.act, np.zeros_like(x))
+                jobs.append((f"{name}.fwd_varlen", run, x.shape[0] * (hi - lo)))
+            if case.x_spec is not None:
+                xs = np.ascontiguousarray(to_np(case.x_spec[:, sl].contiguous()))
+                na = to_np(case.num_accepted) if case.n_spec else None
 
-            def run2(xs=xs, w=w, b=b, pool=pool, case=case, na=na):
-                oracle.cconv_update(xs, pool.copy(), w, b, to_np(case.spec_state_idx),
-                                    case.n_spec, na, None, case.width, case.dilation, case.act,
-                                    np.zeros_like(xs))
-            jobs.append((f"{name}.update", run2, xs.shape[0] * chans))
+                def run2(xs=xs, w=w, b=b, pool=pool, case=case, na=na):
+                    oracle.cconv_update(xs, pool.copy(), w, b, to_np(case.spec_state_idx),
+                                        case.n_spec, na, None, case.width, case.dilation,
+                                        case.act, np.zeros_like(xs))
+                jobs.append((f"{name}.update", run2, xs.shape[0] * (hi - lo)))
 
-    dw("gdn_decode", synth.gdn_decode(dev), 256 if not light else 64)
-    dw("gdn_mixed", synth.gdn_mixed(dev), 32 if not light else 8)
+    dw("gdn_decode", synth.gdn_decode(dev), nch["gdn_decode"])
+    dw("gdn_mixed", synth.gdn_mixed(dev), nch["gdn_mixed"])
     cc = synth.zaya_cca(dev)
     nreq = 257   # the 256 decodes and the first 4096-token prefill
     T = int(cc.cu_seqlens[nreq].item())
-    sl = slice(0, 128)
-    qk = np.ascontiguousarray(to_np(cc.qk[:T, sl].contiguous()))
     dl = np.ascontiguousarray(to_np(cc.delayed[:T].contiguous()))
-    args = dict(w_dw=np.ascontiguousarray(to_np(cc.w_dw)[sl]),
-                b_dw=np.ascontiguousarray(to_np(cc.b_dw)[sl]),
-                w_gr=np.ascontiguousarray(to_np(cc.w_gr)[sl]),
-                b_gr=np.ascontiguousarray(to_np(cc.b_gr)[sl]))
-    pool = pool_np(cc.pool[:, sl, :].contiguous())
     ds = to_np(cc.delayed_state).copy()
     meta = (to_np(cc.state_idx[:nreq]), to_np(cc.cu_seqlens[:nreq + 1]),
             to_np(cc.has_init[:nreq]))
+    for g0, g1 in blocks(nch["zaya_cca"], 1):
+        sl = slice(g0 * 128, g1 * 128)
+        qk = np.ascontiguousarray(to_np(cc.qk[:T, sl].contiguous()))
+        wts = [np.ascontiguousarray(to_np(t)[sl]) for t in (cc.w_dw, cc.b_dw, cc.w_gr, cc.b_gr)]
+        pool = pool_np(cc.pool[:, sl, :].contiguous())
 
-    def run3():
-        oracle.cca_qk_conv(qk, args["w_dw"], args["b_dw"], args["w_gr"], args["b_gr"], 1, 2, 2,
-                           dl, to_np(cc.delayed_init), pool.copy(), ds.copy(), *meta,
-                           np.zeros_like(qk), np.zeros_like(dl))
-    jobs.append(("zaya_cca.cca_qk_conv", run3, T * 128))
-    dw("ple_spec", synth.ple_spec(dev), 32 if not light else 8)
+        def run3(qk=qk, wts=wts, pool=pool, ng=g1 - g0):
+            oracle.cca_qk_conv(qk, *wts, ng, 2, 2, dl, to_np(cc.delayed_init), pool.copy(),
+                               ds.copy(), *meta, np.zeros_like(qk), np.zeros_like(dl))
+        jobs.append(("zaya_cca.cca_qk_conv", run3, T * (g1 - g0) * 128))
+    dw("ple_spec", synth.ple_spec(dev), nch["ple_spec"])
     units = sum(j[2] for j in jobs)
-    desc = ("oracle (1 thread) on: gdn_decode 256 ch, gdn_mixed 32 ch, zaya_cca 1 group x "
-            f"{nreq} requests ({T} tokens), ple_spec 32 ch; all tokens of the sampled "
-            f"requests; {units} tokens*channels")
-    if light:
-        desc = desc.replace("256 ch", "64 ch").replace("32 ch", "8 ch")
+    desc = (f"oracle on: gdn_decode {nch['gdn_decode']} ch, gdn_mixed {nch['gdn_mixed']} ch, "
+            f"zaya_cca {nch['zaya_cca']} group(s) x {nreq} requests ({T} tokens), ple_spec "
+            f"{nch['ple_spec']} ch; all tokens of the sampled requests; {units} "
+            "tokens*channels")
     return jobs, units, desc
+
+
+def run_cpu_parallel(jobs, threads):
+    """The jobs on `threads` host threads (the oracle's C calls release the GIL)."""
+    from concurrent.futures import ThreadPoolExecutor
+    order = sorted(jobs, key=lambda j: -j[2])
+    t0 = time.perf_counter()
+    with ThreadPoolExecutor(threads) as ex:
+        list(ex.map(lambda j: j[1](), order))
+    return time.perf_counter() - t0
+
+
+def cpu_model():
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu part")):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
 
 
 def run_cpu_sample(jobs):
@@ -530,13 +563,16 @@ def arm_ours(args):
     if not args.no_e2e:
         line["e2e"] = e2e_run(args, calls, stream, dev, ws)
     if rank == 0 and not args.no_cpu_baseline and ws == 1:
-        jobs, units, sdesc = cpu_sample(dev)
-        run_cpu_sample(jobs)
-        ts = [run_cpu_sample(jobs) for _ in range(2)]
-        t = min(ts)
+        ncores = os.cpu_count() or 1
+        jobs, units, sdesc = cpu_sample(dev, parts=ncores)
+        t = run_cpu_sample(jobs)
+        tp = min(run_cpu_parallel(jobs, ncores) for _ in range(2))
         line["cpu_baseline"] = {"value": units / t / 1e9, "unit": UNIT, "cores": 1,
-                                "kind": "oracle", "sample": sdesc,
-                                "seconds_per_sample": t}
+                                "kind": "oracle", "sample": sdesc + " (1 thread)",
+                                "seconds_per_sample": t,
+                                "all_cores": {"value": units / tp / 1e9, "cores": ncores,
+                                              "seconds_per_sample": tp,
+                                              "cpu": cpu_model()}}
     if rank == 0:
         print(json.dumps(line))
     if ws > 1:
