@@ -73,6 +73,10 @@ def _load():
                 P, I64, P, I64, I64, I64, I32, I32, P, P, P, I32, I32, P, P, I32, I32,
                 I32, I32, I32, P, I32, P, I64, P, I64]
             lib.oracle_cconv_update_fused.restype = ctypes.c_int
+            lib.oracle_cconv_checkpoint_export.argtypes = [
+                P, I64, P, I64, I64, I64, I32, I32, P, P, P, I32, P, I32, P, I32, I32, I32, I32,
+                I32]
+            lib.oracle_cconv_checkpoint_export.restype = ctypes.c_int
             lib.oracle_f32_to_bf16.argtypes = [ctypes.c_float]
             lib.oracle_f32_to_bf16.restype = ctypes.c_uint16
             lib.oracle_bf16_to_f32.argtypes = [ctypes.c_uint16]
@@ -236,6 +240,29 @@ def cconv_update_fused(x, pool, w, bias, state_idx, n_spec, num_accepted, has_in
         _rows(outer) if outer is not None else 0)
     if rc != 0:
         raise ValueError(f"oracle_cconv_update_fused rejected its arguments ({rc})")
+
+
+def cconv_checkpoint_export(x, pool, ck_seq, ck_off, ck_slot, cu_seqlens, width, dilation,
+                            token_indices=None):
+    """Prefill checkpoint export of "Qwen4ExpPLELayer" (the conv window ending at a
+    checkpoint is a copy of its last (width-1)*dilation inputs), in place on ``pool``.
+
+    Checkpoint k: request ck_seq[k], token offset ck_off[k] in [S, L], slot ck_slot[k].
+    """
+    lib = _load()
+    dt = _dtype_code(x)
+    ck_seq, ck_off, ck_slot = (np.ascontiguousarray(np.asarray(a, dtype=np.int32))
+                               for a in (ck_seq, ck_off, ck_slot))
+    cu_seqlens = _c(cu_seqlens, np.int32)
+    token_indices = _c(token_indices, np.int32)
+    ss, sc, scol = _pool_strides(pool)
+    rc = lib.oracle_cconv_checkpoint_export(
+        _ptr(x), _rows(x), _pool_base(pool), ss, sc, scol, pool.shape[0], pool.shape[2],
+        _ptr(ck_seq), _ptr(ck_off), _ptr(ck_slot), int(ck_seq.shape[0]), _ptr(cu_seqlens),
+        int(cu_seqlens.shape[0]) - 1, _ptr(token_indices), x.shape[0], x.shape[1], width,
+        dilation, dt)
+    if rc != 0:
+        raise ValueError(f"oracle_cconv_checkpoint_export rejected its arguments ({rc})")
 
 
 def cca_qk_conv(qk, w_dw, b_dw, w_gr, b_gr, groups, t0, t1, delayed, delayed_init, pool,

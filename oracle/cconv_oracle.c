@@ -371,6 +371,46 @@ int oracle_cconv_update_fused(const void* x, int64_t x_rs, void* pool, int64_t s
   return rc;
 }
 
+/* ---- prefill checkpoint export ------------------------------------------- */
+
+/*
+ * [P] __init__ ("the conv window ending at a checkpoint is a copy of its last
+ * inputs": MambaPrefillCheckpointExporter(state_len = (width-1)*dilation)),
+ * the export call of _short_conv_dilated_dispatch (raw inputs, conv_state,
+ * non-spec cu_seqlens, token_indices) and get_kv_cache_spec (checkpoint
+ * offsets are multiples of a grid >= state_len, "so the window holds only
+ * inputs"). Checkpoint k names request ck_seq[k], a token offset
+ * ck_off[k] in [S, L] of that request and a destination slot ck_slot[k]:
+ *   pool[ck_slot[k]][c][i] = x[p(cu[s] + ck_off[k] - S + i)][c],  i < S
+ * (a bit copy; p = token_indices or the identity). Columns >= S of the slot
+ * are untouched. Returns -2 on a checkpoint outside these ranges.
+ */
+int oracle_cconv_checkpoint_export(const void* x, int64_t x_rs, void* pool, int64_t s_slot,
+                                   int64_t s_chan, int64_t s_col, int32_t num_slots, int32_t cap,
+                                   const int32_t* ck_seq, const int32_t* ck_off,
+                                   const int32_t* ck_slot, int32_t num_ckpt,
+                                   const int32_t* cu_seqlens, int32_t num_seqs,
+                                   const int32_t* tidx, int32_t num_rows, int32_t C, int32_t W,
+                                   int32_t D, int32_t dtype) {
+  const int S = (W - 1) * D;
+  if (S > cap) return -1;
+  for (int k = 0; k < num_ckpt; ++k) {
+    const int s = ck_seq[k], off = ck_off[k], slot = ck_slot[k];
+    if (s < 0 || s >= num_seqs || slot < 0 || slot >= num_slots) return -2;
+    const int L = cu_seqlens[s + 1] - cu_seqlens[s];
+    if (off < S || off > L) return -2;
+    for (int i = 0; i < S; ++i) {
+      const int64_t li = (int64_t)cu_seqlens[s] + off - S + i;
+      const int64_t p = tidx ? tidx[li] : li;
+      if (p < 0 || p >= num_rows) return -2;
+      for (int64_t c = 0; c < C; ++c)
+        orc_put_raw(pool, slot * s_slot + c * s_chan + i * s_col, dtype,
+                    orc_get_raw(x, p * x_rs + c, dtype));
+    }
+  }
+  return 0;
+}
+
 /*
  * Zaya CCA q/k conv with state and the delayed half of v ([Z] ZayaCCA.__init__,
  * _conv, project, _mix_with_state, _cca_state_shapes).

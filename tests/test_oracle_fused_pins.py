@@ -175,3 +175,55 @@ def test_fused_rejects_row_index_outside_rows():
                                       to_np(case.cu_seqlens), to_np(case.has_init), case.width,
                                       case.dilation, case.act, np.zeros((T, C), np.float32),
                                       None, idx)
+
+
+# ---- prefill checkpoint export ----------------------------------------------
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("layout", ["DS", "SD"])
+def test_checkpoint_equals_state_after_prefilling_to_the_offset(dtype, layout):
+    """The window exported at offset k is the state a prefill of the request's
+    first k tokens leaves in the pool (whatever its history, since k >= S)."""
+    W, D = 4, 3
+    S = (W - 1) * D
+    lens = [40, 9, 25]
+    case = synth.depthwise_case(907, CPU, lens=lens, C=16, width=W, dilation=D, act=1,
+                                dtype=dtype, w_std=0.5, layout=layout, num_slots=12)
+    cu = to_np(case.cu_seqlens)
+    cks = [(0, 9), (0, 27), (0, 40), (1, 9), (2, 18)]
+    slots = [6, 7, 8, 9, 10]
+    pool = pool_np(case.pool.clone())
+    oracle.cconv_checkpoint_export(to_np(case.x), pool, [c[0] for c in cks],
+                                   [c[1] for c in cks], slots, cu, W, D)
+    for (s, k), d in zip(cks, slots):
+        x_pre = np.ascontiguousarray(to_np(case.x)[cu[s]:cu[s] + k])
+        p2 = pool_np(case.pool.clone())
+        oracle.cconv_fwd_varlen(x_pre, to_np(case.w), None, p2, np.array([d], np.int32),
+                                np.array([0, k], np.int32), np.array([1], np.uint8), W, D, 1,
+                                np.zeros_like(x_pre))
+        assert np.array_equal(pool[d, :, :S], p2[d, :, :S])
+    untouched = [i for i in range(pool.shape[0]) if i not in slots]
+    assert np.array_equal(pool[untouched], pool_np(case.pool)[untouched])
+
+
+def test_checkpoint_follows_token_indices_and_rejects_bad_offsets():
+    W, D = 3, 2
+    S = (W - 1) * D
+    case = synth.depthwise_case(908, CPU, lens=[12, 7], C=8, width=W, dilation=D, act=0,
+                                dtype=torch.float32, w_std=0.5, num_slots=4)
+    T = case.num_tokens
+    perm = np.random.default_rng(9).permutation(T).astype(np.int32)
+    xp = np.empty_like(to_np(case.x))
+    xp[perm] = to_np(case.x)
+    cu = to_np(case.cu_seqlens)
+    p1 = pool_np(case.pool.clone())
+    p2 = pool_np(case.pool.clone())
+    oracle.cconv_checkpoint_export(to_np(case.x), p1, [0, 1], [8, 7], [2, 3], cu, W, D)
+    oracle.cconv_checkpoint_export(xp, p2, [0, 1], [8, 7], [2, 3], cu, W, D, perm)
+    assert np.array_equal(p1, p2)
+    # slicing by hand
+    assert np.array_equal(p1[2, :, :S].T, to_np(case.x)[8 - S:8])
+    for bad in ([0], [S - 1], [2]), ([1], [8], [2]), ([2], [4], [2]):
+        with pytest.raises(ValueError):
+            oracle.cconv_checkpoint_export(to_np(case.x), pool_np(case.pool.clone()), bad[0],
+                                           bad[1], bad[2], cu, W, D)
