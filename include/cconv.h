@@ -34,7 +34,7 @@
  *           one [slot, channel, window] view before its conv). The
  *           fast paths are the dense channel-first view (s_col == 1,
  *           s_chan == cap) and the column-first view (s_chan == 1); any other
- *           strides use per-element accesses.
+ *           strides use per-element accesses. A view has at most 64 columns.
  * State.    Non-speculative calls keep the state in columns [0, S) of a slot,
  *           S = (width-1)*dilation, as the GDN page's non-speculative path
  *           does on a buffer widened for speculation; columns >= S are left
@@ -88,8 +88,10 @@ enum {
   CCONV_DERR_NUM_ACCEPTED = 4, /* num_accepted[s] outside [1, 1+n_spec] */
   CCONV_DERR_TIMEOUT = 8,      /* a bounded on-chip wait ran out; the call's
                                   outputs are incomplete                 */
-  CCONV_DERR_ROW_INDEX = 16    /* fused entry points: a logical row maps
-                                  outside [0, num_rows)                  */
+  CCONV_DERR_ROW_INDEX = 16,   /* fused entry points / checkpoint export: a
+                                  logical row maps outside [0, num_rows) */
+  CCONV_DERR_CHECKPOINT = 32   /* checkpoint export: request, offset or
+                                  slot out of range                      */
 };
 
 /* [slot, channel, column] view of a conv-state pool (element strides). */
@@ -229,6 +231,43 @@ int cconv_update_fused(const void* x, int64_t x_row_stride, cconv_pool_t conv_st
                        const uint8_t* has_init, int32_t C, int32_t width, int32_t dilation,
                        int32_t act, int32_t dtype, cconv_epilogue_t epilogue,
                        int32_t* dev_err, cconv_stream_t stream);
+
+/*
+ * cconv_checkpoint_export -- prefill checkpoints: the conv window ending at a
+ * checkpoint offset of a request, copied into a destination slot.
+ *
+ * Defined by: "Qwen4ExpPLELayer" __init__ (each layer exports a window of
+ * state_len = (width-1)*dilation: "the conv window ending at a checkpoint is a
+ * copy of its last inputs"), _short_conv_dilated_dispatch (the export after the
+ * prefill conv, with the raw inputs, the conv state, the non-spec cu_seqlens
+ * and token_indices) and get_kv_cache_spec (offsets lie on a grid >= state_len,
+ * "so the window holds only inputs").
+ *
+ * Checkpoint k (k < num_ckpt) names request ckpt_seq[k] (an index into
+ * cu_seqlens), a token offset ckpt_offset[k] in [S, L] of that request and a
+ * destination slot ckpt_slot[k]. The call writes, as a bit copy,
+ *   conv_states[ckpt_slot[k]][c][i] = x[p(cu_seqlens[s] + ckpt_offset[k] - S + i)][c],  i < S
+ * with p = token_indices (NULL: identity) over num_rows physical rows; columns
+ * >= S of the slot are untouched. It reads no history, so it may run after the
+ * prefill has updated the requests' own slots. Destination slots must be
+ * distinct from each other and from slots other calls on the stream are
+ * writing.
+ *
+ *   x            [num_rows, C] with row stride (as cconv_fwd_varlen)
+ *   ckpt_*       int32 [num_ckpt] (num_ckpt <= 65535)
+ *   cu_seqlens   int32 [num_seqs+1] over num_tokens logical rows
+ *   width 2..4, dilation 1..4, S in {1,2,3,4,6,8,9,12}
+ * A checkpoint whose request, offset or slot is out of range sets
+ * CCONV_DERR_CHECKPOINT (a row outside num_rows CCONV_DERR_ROW_INDEX) and is
+ * skipped.
+ */
+int cconv_checkpoint_export(const void* x, int64_t x_row_stride, cconv_pool_t conv_states,
+                            const int32_t* ckpt_seq, const int32_t* ckpt_offset,
+                            const int32_t* ckpt_slot, int32_t num_ckpt,
+                            const int32_t* cu_seqlens, int32_t num_seqs, int32_t num_tokens,
+                            const int32_t* token_indices, int32_t num_rows, int32_t C,
+                            int32_t width, int32_t dilation, int32_t dtype, int32_t* dev_err,
+                            cconv_stream_t stream);
 
 /*
  * cca_qk_conv -- Zaya CCA: depthwise conv (width t0, bias) then grouped conv

@@ -31,6 +31,10 @@ constexpr int kRing = 16;       // ring slots per thread (> kPrefetch + 1, power
 constexpr int kPrefetchFused = 6;   // the same for the fused entry point, whose
 constexpr int kRingFused = 8;       // output-row entries are three units
 constexpr int kUpdChan = 2;     // channels per thread of the update kernel
+// Columns a pool view may have: a thread keeps its 16-byte unit of every column
+// (plus its stream ring) in shared memory, within the 48 KB a block gets
+// without opting in, at 32 threads.
+constexpr int kMaxCap = 64;
 
 struct FwdArgs {
   const char* x;
@@ -535,7 +539,7 @@ static int check_common(const void* x, int64_t x_rs, const void* w, const cconv_
   if (act != CCONV_ACT_NONE && act != CCONV_ACT_SILU) return CCONV_ERR_INVALID;
   if (!aligned16(x) || !aligned16(out)) return CCONV_ERR_INVALID;
   if (x_rs < C || out_rs < C || x_rs % *V != 0 || out_rs % *V != 0) return CCONV_ERR_INVALID;
-  if (pv.num_slots <= 0 || pv.cap <= 0 || pv.cap > 96) return CCONV_ERR_INVALID;
+  if (pv.num_slots <= 0 || pv.cap <= 0 || pv.cap > kMaxCap) return CCONV_ERR_INVALID;
   if (pv.s_slot <= 0 || pv.s_chan <= 0 || pv.s_col <= 0) return CCONV_ERR_INVALID;
   return CCONV_OK;
 }

@@ -21,7 +21,7 @@ OK, ERR_INVALID, ERR_UNSUPPORTED, ERR_LAUNCH = 0, -1, -2, -3
 DTYPE_F32, DTYPE_BF16 = 0, 1
 ACT_NONE, ACT_SILU = 0, 1
 DERR_SLOT_RANGE, DERR_CU_SEQLENS, DERR_NUM_ACCEPTED, DERR_TIMEOUT = 1, 2, 4, 8
-DERR_ROW_INDEX = 16
+DERR_ROW_INDEX, DERR_CHECKPOINT = 16, 32
 
 _lock = threading.Lock()
 _lib = None
@@ -71,6 +71,9 @@ def load():
         lib.cconv_update_fused.argtypes = [P, I64, Pool, P, P, P, I32, I32, P, P, I32, I32, I32,
                                            I32, I32, Epilogue, P, P]
         lib.cconv_update_fused.restype = ctypes.c_int
+        lib.cconv_checkpoint_export.argtypes = [P, I64, Pool, P, P, P, I32, P, I32, I32, P, I32,
+                                                I32, I32, I32, I32, P, P]
+        lib.cconv_checkpoint_export.restype = ctypes.c_int
         lib.cca_qk_conv.argtypes = [P, I64, P, P, P, P, I32, I32, I32, P, I64, P, I32, Pool, P,
                                     I64, P, P, P, I32, I32, I32, I32, P, I64, P, I64, P, P]
         lib.cca_qk_conv.restype = ctypes.c_int
@@ -226,6 +229,28 @@ def cconv_update_fused(x, conv_states, w, bias, state_idx, n_spec, num_accepted,
         int(x.shape[1]), int(width), int(dilation), int(act), _dtype_code(x),
         _epilogue(residual, outer, token_indices, x), _ptr(dev_err), _stream(stream))
     _check("cconv_update_fused", rc)
+
+
+def cconv_checkpoint_export(x, conv_states, ckpt_seq, ckpt_offset, ckpt_slot, cu_seqlens,
+                            width, dilation, token_indices=None, num_tokens=None,
+                            dev_err=None, stream=None):
+    """Prefill checkpoint export (see cconv_checkpoint_export in cconv.h): the conv
+    window ending at ckpt_offset[k] of request ckpt_seq[k] into slot ckpt_slot[k].
+
+    x: [R, C] physical rows; ckpt_*: int32 [K]; cu_seqlens: int32 [B+1] over
+    num_tokens logical rows (default len(token_indices), else R).
+    """
+    for t, n in ((ckpt_seq, "ckpt_seq"), (ckpt_offset, "ckpt_offset"), (ckpt_slot, "ckpt_slot"),
+                 (cu_seqlens, "cu_seqlens"), (token_indices, "token_indices")):
+        _i32(t, n)
+    if num_tokens is None:
+        num_tokens = int(token_indices.shape[0]) if token_indices is not None else int(x.shape[0])
+    rc = load().cconv_checkpoint_export(
+        _ptr(x), _rows(x), _pool(conv_states), _ptr(ckpt_seq), _ptr(ckpt_offset),
+        _ptr(ckpt_slot), int(ckpt_seq.shape[0]), _ptr(cu_seqlens), int(cu_seqlens.shape[0]) - 1,
+        int(num_tokens), _ptr(token_indices), int(x.shape[0]), int(x.shape[1]), int(width),
+        int(dilation), _dtype_code(x), _ptr(dev_err), _stream(stream))
+    _check("cconv_checkpoint_export", rc)
 
 
 def cca_qk_conv(qk, w_dw, b_dw, w_gr, b_gr, groups, t0, t1, delayed, delayed_init,

@@ -48,7 +48,7 @@ def test_status_strings(lib):
     for s in (-1, -2, -3):
         assert ops.status_string(s) not in ("ok", "unknown status")
     assert ops.status_string(17) == "unknown status"
-    assert ops.abi_version() == 2
+    assert ops.abi_version() == 3
 
 
 FAKE = 0x10000  # 16-byte aligned, never dereferenced: every call below fails validation
@@ -142,3 +142,17 @@ def _epi(res=FAKE, rrs=16, outer=None, ors=0, idx=None, rows=8):
 def test_fwd_fused_checks_its_epilogue(lib, epi, want):
     # -3: the epilogue passed every check and the launch failed (no device)
     assert fwd_fused(lib, _epi(**epi)) == want
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(pool=_pool(cap=65)), -1), (dict(W=5), -2), (dict(num=0), 0), (dict(x=FAKE + 4), -1),
+    (dict(rows=3, idx=None), -1), (dict(), -3)])
+@no_gpu
+def test_checkpoint_export_validation(lib, kw, want):
+    a = dict(x=FAKE, pool=_pool(cap=9), num=2, rows=8, idx=FAKE, W=4, D=3)
+    a.update(kw)
+    P = lambda v: None if v is None else ctypes.c_void_p(v)
+    rc = lib.cconv_checkpoint_export(P(a["x"]), 16, a["pool"], P(FAKE), P(FAKE), P(FAKE),
+                                     a["num"], P(FAKE), 2, 8, P(a["idx"]), a["rows"], 16,
+                                     a["W"], a["D"], 1, None, None)
+    assert rc == want

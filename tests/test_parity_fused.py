@@ -189,3 +189,57 @@ def test_bad_row_index_sets_flag_and_skips():
     torch.cuda.synchronize()
     assert int(err.item()) & ops.DERR_ROW_INDEX
     assert torch.equal(got_u[2 * q:3 * q], res_u[2 * q:3 * q])
+
+
+# ---- prefill checkpoint export ------------------------------------------------
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("layout", ["DS", "SD", "wide"])
+@pytest.mark.parametrize("W,D", [(4, 3), (2, 1), (3, 4)])
+def test_checkpoint_export(dtype, layout, W, D):
+    S = (W - 1) * D
+    lens = [3 * S + 5, S, 2 * S, 200]
+    kw = dict(lens=lens, C=520 if dtype == torch.float32 else 1040, width=W, dilation=D, act=1,
+              dtype=dtype, w_std=0.5, num_slots=40)
+    if layout == "wide":
+        case = synth.depthwise_case(900 + W * 10 + D, DEV, cap=S + 4, **kw)
+        case.pool = case.pool[:, :, 2:]
+    else:
+        case = synth.depthwise_case(900 + W * 10 + D, DEV, layout=layout, **kw)
+    T = case.num_tokens
+    R = T + 9
+    gc = torch.Generator(device="cpu").manual_seed(10)
+    perm = torch.randperm(R, generator=gc)[:T].to(torch.int32).to(DEV)
+    x_phys = physical(case.x, perm, R)
+    ck_seq = torch.tensor([0, 0, 1, 2, 3, 3], dtype=torch.int32, device=DEV)
+    ck_off = torch.tensor([S, 3 * S, S, 2 * S, 64, 200], dtype=torch.int32, device=DEV)
+    ck_slot = torch.tensor([30, 31, 32, 33, 34, 35], dtype=torch.int32, device=DEV)
+    want = pool_np(case.pool.clone())
+    oracle.cconv_checkpoint_export(to_np(x_phys), want, to_np(ck_seq), to_np(ck_off),
+                                   to_np(ck_slot), to_np(case.cu_seqlens), W, D, to_np(perm))
+    pool = case.pool.clone()
+    err = new_err()
+    ops.cconv_checkpoint_export(x_phys, pool, ck_seq, ck_off, ck_slot, case.cu_seqlens, W, D,
+                                perm, dev_err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert_bits_equal(pool_np(pool), want)
+
+
+def test_checkpoint_export_bad_entries_are_flagged_and_skipped():
+    W, D, S = 4, 1, 3
+    case = synth.depthwise_case(950, DEV, lens=[10, 5], C=256, width=W, dilation=D, act=1,
+                                dtype=torch.bfloat16, w_std=0.5, num_slots=8)
+    ck_seq = torch.tensor([0, 2, 1, 1], dtype=torch.int32, device=DEV)    # request 2: none
+    ck_off = torch.tensor([4, 3, 2, 5], dtype=torch.int32, device=DEV)    # 2 < S
+    ck_slot = torch.tensor([5, 6, 7, 8], dtype=torch.int32, device=DEV)   # slot 8 == num_slots
+    pool = case.pool.clone()
+    err = new_err()
+    ops.cconv_checkpoint_export(case.x, pool, ck_seq, ck_off, ck_slot, case.cu_seqlens, W, D,
+                                dev_err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & ops.DERR_CHECKPOINT
+    want = pool_np(case.pool.clone())
+    oracle.cconv_checkpoint_export(to_np(case.x), want, [0], [4], [5], to_np(case.cu_seqlens),
+                                   W, D)
+    assert_bits_equal(pool_np(pool), want)
