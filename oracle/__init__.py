@@ -77,6 +77,9 @@ def _load():
                 P, I64, P, I64, I64, I64, I32, I32, P, P, P, I32, P, I32, P, I32, I32, I32, I32,
                 I32]
             lib.oracle_cconv_checkpoint_export.restype = ctypes.c_int
+            lib.oracle_cca_project_epilogue.argtypes = [
+                P, I64, P, I64, P, I64, P, I64, I32, I32, I32, I32, I32, P, I64]
+            lib.oracle_cca_project_epilogue.restype = ctypes.c_int
             lib.oracle_f32_to_bf16.argtypes = [ctypes.c_float]
             lib.oracle_f32_to_bf16.restype = ctypes.c_uint16
             lib.oracle_bf16_to_f32.argtypes = [ctypes.c_uint16]
@@ -299,3 +302,19 @@ def cca_qk_conv(qk, w_dw, b_dw, w_gr, b_gr, groups, t0, t1, delayed, delayed_ini
 
 def oracle_f32_to_bf16_scalar(v: float) -> int:
     return int(_load().oracle_f32_to_bf16(ctypes.c_float(v)))
+
+
+def cca_project_epilogue(qk, conv, v_current, delayed_prev, num_q_heads, num_kv_heads, out):
+    """The q/k residual mix and value assembly of "vllm.model_executor.models.zaya"
+    ZayaCCA.project after the conv: out = [conv_q + q_res | conv_k + k_res |
+    v_current | delayed_prev] per token (head_dim = qk channels / heads)."""
+    lib = _load()
+    dt = _dtype_code(qk)
+    hd = qk.shape[1] // (num_q_heads + num_kv_heads)
+    rc = lib.oracle_cca_project_epilogue(
+        _ptr(qk), _rows(qk), _ptr(conv), _rows(conv), _ptr(v_current), _rows(v_current),
+        _ptr(delayed_prev), _rows(delayed_prev), qk.shape[0], num_q_heads, num_kv_heads, hd, dt,
+        _ptr(out), _rows(out))
+    if rc != 0:
+        raise ValueError(f"oracle_cca_project_epilogue rejected its arguments ({rc})")
+

@@ -511,3 +511,59 @@ int oracle_cca_qk_conv(const void* qk, int64_t qk_rs, const void* w_dw, const vo
 float oracle_bf16_to_f32(uint16_t h) { return orc_bf16_to_f32(h); }
 uint16_t oracle_f32_to_bf16(float f) { return orc_f32_to_bf16(f); }
 size_t oracle_esize(int dtype) { return orc_esize(dtype); }
+
+
+/* ---- Zaya q/k residual mix and value assembly ------------------------------ */
+
+static float orc_round(float v, int dtype) {
+  return dtype == ORC_F32 ? v : orc_bf16_to_f32(orc_f32_to_bf16(v));
+}
+
+/*
+ * [Z] ZayaCCA.project after _mix_with_state, written with torch tensors of the
+ * module dtype (every elementwise result rounded to it; 0.5 * v is exact):
+ *   qres[t][h][d] = 0.5 * round(q[t][h][d] + k[t][h / kvg][d])     (repeat_interleave)
+ *   kres[t][j][d] = round(mean_{g < kvg} qres[t][j*kvg + g][d])      (mean in fp32)
+ *   out[t] = [ round(conv_q[t][h][d] + qres[t][h][d])  for h < Hq,
+ *              round(conv_k[t][j][d] + kres[t][j][d])  for j < Hkv,
+ *              v_current[t] (Hkv*hd/2 values), delayed_prev[t] (Hkv*hd/2 values) ]
+ * with q = qk[:, :Hq*hd], k = qk[:, Hq*hd:], kvg = Hq / Hkv, conv the grouped
+ * conv output and delayed_prev the delayed half of v of oracle_cca_qk_conv.
+ */
+int oracle_cca_project_epilogue(const void* qk, int64_t qk_rs, const void* conv,
+                                int64_t conv_rs, const void* v_cur, int64_t vc_rs,
+                                const void* dprev, int64_t dp_rs, int32_t T, int32_t Hq,
+                                int32_t Hkv, int32_t hd, int32_t dtype, void* out,
+                                int64_t out_rs) {
+  if (Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || hd % 2 != 0) return -1;
+  const int kvg = Hq / Hkv;
+  const int64_t qdim = (int64_t)Hq * hd, kvdim = (int64_t)Hkv * hd;
+  float* qres = (float*)malloc(sizeof(float) * (size_t)qdim);
+  for (int64_t t = 0; t < T; ++t) {
+    for (int h = 0; h < Hq; ++h)
+      for (int d = 0; d < hd; ++d) {
+        const float q = orc_get(qk, t * qk_rs + (int64_t)h * hd + d, dtype);
+        const float k = orc_get(qk, t * qk_rs + qdim + (int64_t)(h / kvg) * hd + d, dtype);
+        qres[(int64_t)h * hd + d] = 0.5f * orc_round(q + k, dtype);
+        const float c = orc_get(conv, t * conv_rs + (int64_t)h * hd + d, dtype);
+        orc_put(out, t * out_rs + (int64_t)h * hd + d, dtype, c + qres[(int64_t)h * hd + d]);
+      }
+    for (int j = 0; j < Hkv; ++j)
+      for (int d = 0; d < hd; ++d) {
+        float sum = 0.0f;
+        for (int g = 0; g < kvg; ++g) sum += qres[(int64_t)(j * kvg + g) * hd + d];
+        const float kres = orc_round(sum / (float)kvg, dtype);
+        const float c = orc_get(conv, t * conv_rs + qdim + (int64_t)j * hd + d, dtype);
+        orc_put(out, t * out_rs + qdim + (int64_t)j * hd + d, dtype, c + kres);
+      }
+    for (int64_t i = 0; i < kvdim / 2; ++i) {
+      orc_put_raw(out, t * out_rs + qdim + kvdim + i, dtype,
+                  orc_get_raw(v_cur, t * vc_rs + i, dtype));
+      orc_put_raw(out, t * out_rs + qdim + kvdim + kvdim / 2 + i, dtype,
+                  orc_get_raw(dprev, t * dp_rs + i, dtype));
+    }
+  }
+  free(qres);
+  return 0;
+}
+

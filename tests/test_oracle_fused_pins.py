@@ -227,3 +227,63 @@ def test_checkpoint_follows_token_indices_and_rejects_bad_offsets():
         with pytest.raises(ValueError):
             oracle.cconv_checkpoint_export(to_np(case.x), pool_np(case.pool.clone()), bad[0],
                                            bad[1], bad[2], cu, W, D)
+
+
+# ---- Zaya q/k residual mix and value assembly -------------------------------
+
+def _torch_project_tail(qk, conv, v_cur, dprev, Hq, Hkv):
+    """The tail of ZayaCCA.project on the Zaya page, run with torch's own ops in
+    the tensors' dtype (an implementation independent of the oracle's C)."""
+    T = qk.shape[0]
+    hd = qk.shape[1] // (Hq + Hkv)
+    qdim, kvg = Hq * hd, Hq // Hkv
+    heads = (T, -1, hd)
+    queries, keys = qk[:, :qdim], qk[:, qdim:]
+    query_residual = 0.5 * (queries.reshape(heads)
+                            + keys.reshape(heads).repeat_interleave(kvg, dim=1))
+    key_residual = query_residual.reshape(T, -1, kvg, hd).mean(dim=2)
+    query = conv[:, :qdim].reshape(heads) + query_residual
+    key = conv[:, qdim:].reshape(heads) + key_residual
+    value = torch.cat([v_cur, dprev], dim=-1)
+    return torch.cat([query, key, value.reshape(heads)], dim=1).flatten(1)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("Hq,Hkv", [(4, 2), (3, 1), (2, 2)])
+def test_cca_project_tail_matches_torch(dtype, Hq, Hkv):
+    hd, T = 16, 11
+    g = torch.Generator().manual_seed(Hq * 10 + Hkv)
+    C = (Hq + Hkv) * hd
+    qk = torch.randn(T, C, generator=g).to(dtype)
+    conv = torch.randn(T, C, generator=g).to(dtype)
+    v_cur = torch.randn(T, Hkv * hd // 2, generator=g).to(dtype)
+    dprev = torch.randn(T, Hkv * hd // 2, generator=g).to(dtype)
+    want = _torch_project_tail(qk, conv, v_cur, dprev, Hq, Hkv)
+    out = np.zeros((T, Hq * hd + 2 * Hkv * hd), dtype=to_np(qk).dtype)
+    oracle.cca_project_epilogue(to_np(qk), to_np(conv), to_np(v_cur), to_np(dprev), Hq, Hkv,
+                                out)
+    got, ref = _f64(out), _f64(to_np(want))
+    if dtype == torch.float32:
+        assert np.abs(got - ref).max() <= 1e-6
+    else:
+        # bf16 results agree except where the fp32 mean's summation order flips a rounding
+        ulp = np.abs(ref) * 2.0 ** -7 + 1e-30
+        assert np.all(np.abs(got - ref) <= ulp)
+    vcols = slice(Hq * hd + Hkv * hd, None)
+    assert np.array_equal(out[:, vcols], to_np(torch.cat([v_cur, dprev], dim=-1)))
+
+
+def test_cca_project_tail_one_query_head_per_kv_head():
+    """With one query head per kv head the key residual is the query residual of
+    the same head: key = conv_k + 0.5 * (q + k) as well."""
+    Hq = Hkv = 3
+    hd, T = 8, 5
+    g = torch.Generator().manual_seed(3)
+    qk = torch.randn(T, 2 * Hq * hd, generator=g)
+    conv = torch.randn(T, 2 * Hq * hd, generator=g)
+    v = torch.zeros(T, Hkv * hd // 2)
+    out = np.zeros((T, 3 * Hq * hd), np.float32)
+    oracle.cca_project_epilogue(to_np(qk), to_np(conv), to_np(v), to_np(v), Hq, Hkv, out)
+    res = 0.5 * (qk[:, :Hq * hd] + qk[:, Hq * hd:])
+    assert np.allclose(out[:, :Hq * hd], to_np(conv[:, :Hq * hd] + res), atol=1e-6)
+    assert np.allclose(out[:, Hq * hd:2 * Hq * hd], to_np(conv[:, Hq * hd:] + res), atol=1e-6)
