@@ -168,6 +168,32 @@ def cca_calls(name, cc, dev_err):
                  h2d=[cc.qk, cc.delayed], d2h=[out, dprev])]
 
 
+def cca_fused_calls(name, cc, Hq, dev_err):
+    """cca_qk_conv_fused: the conv plus ZayaCCA.project's residual mix and value
+    assembly into the [query | key | value] output rows."""
+    from state_cached_causal_gb300 import ops
+    e, T, Cqk, Dv, n = _e(cc.qk), int(cc.qk.shape[0]), cc.Cqk, cc.Dv, cc.meta["n"]
+    v_cur = torch.randn(T, Dv, device=cc.qk.device).to(cc.qk.dtype)
+    out = torch.empty(T, Cqk + 2 * Dv, device=cc.qk.device, dtype=cc.qk.dtype)
+    hi = cc.has_init.to(torch.int64).cpu()
+    valid = (cc.state_idx.cpu() >= 0).to(torch.int64)
+    nread, nwrite = int((hi * valid).sum()), int(valid.sum())
+    wbytes = sum(_e(t) * t.numel() for t in (cc.w_dw, cc.b_dw, cc.w_gr, cc.b_gr)
+                 if t is not None)
+    # qk, delayed and v_current read once; the [query | key | value] rows written once
+    nbytes = (T * Cqk * e + 2 * T * Dv * e + T * (Cqk + 2 * Dv) * e + wbytes + Dv * e
+              + (nread + nwrite) * (n * Cqk * e + Dv * e))
+    flops = 2.0 * T * Cqk * (Cqk // cc.groups) * cc.t1 + 2.0 * (T + 1) * Cqk * cc.t0
+
+    def f(cc=cc):
+        ops.cca_qk_conv_fused(cc.qk, cc.w_dw, cc.b_dw, cc.w_gr, cc.b_gr, cc.groups, Hq, cc.t0,
+                              cc.t1, cc.delayed, cc.delayed_init, v_cur, cc.pool,
+                              cc.delayed_state, cc.state_idx, cc.cu_seqlens, cc.has_init, out,
+                              dev_err=dev_err)
+    return [Call(f"{name}.cca_qk_conv_fused", "cca_qk_conv_fused", f, T * Cqk, nbytes, flops,
+                 h2d=[cc.qk, cc.delayed, v_cur], d2h=[out])]
+
+
 def build_workload(name, dev, dev_err):
     from state_cached_causal_gb300 import synth
     if name == "hybrid_step":
@@ -204,6 +230,10 @@ def build_workload(name, dev, dev_err):
         return cca_calls("cca_small", cc, dev_err), "zaya cca 256 decodes + 2x4096"
     if name == "zaya_cca":
         return cca_calls("zaya_cca", synth.zaya_cca(dev), dev_err), "zaya_cca"
+    if name == "zaya_fused":
+        return cca_fused_calls("zaya_fused", synth.zaya_cca(dev), 16, dev_err), (
+            "zaya_fused: the zaya_cca batch through cca_qk_conv_fused (conv + q/k residual "
+            "mix + [query | key | value] assembly, 16 q + 4 kv heads)")
     if name == "ple_fused_small":
         case = synth.depthwise_case(2004, dev, lens=[2048] * 8, C=16384, width=4, dilation=3,
                                     act=1, dtype=torch.bfloat16, w_std=0.1, num_slots=256,
@@ -292,7 +322,8 @@ class ClockSampler:
 KERNEL_SOURCES = {
     "cconv_fwd_varlen": ["depthwise.cuh", "depthwise.cu", "common.cuh", "update.cuh"],
     "cconv_update": ["update_bulk.cu", "update.cuh", "async.cuh", "common.cuh"],
-    "cca_qk_conv": ["cca_qk_conv.cu", "async.cuh", "common.cuh"],
+    "cca_qk_conv": ["cca.cuh", "cca_qk_conv.cu", "async.cuh", "common.cuh"],
+    "cca_qk_conv_fused": ["cca.cuh", "cca_fused.cu", "async.cuh", "common.cuh"],
     "cconv_fwd_varlen_fused": ["depthwise.cuh", "depthwise_fused.cu", "common.cuh"],
     "cconv_update_fused": ["update_bulk.cu", "update.cuh", "async.cuh", "common.cuh"],
 }

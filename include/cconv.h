@@ -309,6 +309,40 @@ int cca_qk_conv(const void* qk, int64_t qk_row_stride, const void* w_dw, const v
                 int64_t out_delayed_prev_row_stride, int32_t* dev_err,
                 cconv_stream_t stream);
 
+/*
+ * cca_qk_conv_fused -- cca_qk_conv with the rest of ZayaCCA.project fused into
+ * its epilogue, writing the layer's [query | key | value] rows directly.
+ *
+ * Defined by: "vllm.model_executor.models.zaya" ZayaCCA.project (after
+ * _mix_with_state): query_residual = 0.5 * (queries + keys repeated over the
+ * kv group), key_residual = its mean over the kv group, query = conv_q +
+ * query_residual, key = conv_k + key_residual, value = [v_proj_current,
+ * delayed_prev], output = [query, key, value] per token.
+ *
+ * Per token t (computed in bf16 as the page's torch code: each sum rounded):
+ *   out[t][h*128 + d]     = conv_q + 0.5 * bf16(q[t][h][d] + k[t][h / kvg][d]),  h < num_q_heads
+ *   out[t][qdim + j*128 + d] = conv_k + bf16(mean over the kv group of those),   j < kv heads
+ *   out[t][Cqk + i]       = v_current[t][i],  out[t][Cqk + Dv + i] = delayed_prev[t][i]
+ * with q = qk[:, :qdim], k = qk[:, qdim:], qdim = num_q_heads * 128, kv heads =
+ * groups - num_q_heads, kvg = num_q_heads / kv heads, conv the grouped conv of
+ * cca_qk_conv and delayed_prev its out_delayed_prev rows. State updates as
+ * cca_qk_conv.
+ *
+ *   v_current   [num_tokens, Dv] with row stride; Dv = kv heads * 128 / 2
+ *   out         [num_tokens, Cqk + 2*Dv] with row stride out_row_stride >= Cqk + 2*Dv
+ *   other arguments as cca_qk_conv (bf16 only)
+ */
+int cca_qk_conv_fused(const void* qk, int64_t qk_row_stride, const void* w_dw,
+                      const void* b_dw, const void* w_gr, const void* b_gr, int32_t groups,
+                      int32_t num_q_heads, int32_t t0, int32_t t1, const void* delayed,
+                      int64_t delayed_row_stride, const void* delayed_init, int32_t Dv,
+                      const void* v_current, int64_t v_current_row_stride,
+                      cconv_pool_t conv_state, void* delayed_state,
+                      int64_t delayed_state_row_stride, const int32_t* state_idx,
+                      const int32_t* cu_seqlens, const uint8_t* has_init, int32_t num_seqs,
+                      int32_t num_tokens, int32_t Cqk, int32_t dtype, void* out,
+                      int64_t out_row_stride, int32_t* dev_err, cconv_stream_t stream);
+
 /* Static English text for a status code. */
 const char* cconv_status_string(int status);
 

@@ -1,0 +1,26 @@
+// Entry point cca_qk_conv_fused: cca_qk_conv with the rest of ZayaCCA.project
+// fused into the epilogue (kernel in cca.cuh, instantiated with FUSED = true).
+#include "cca.cuh"
+
+using namespace cca;
+
+extern "C" int cca_qk_conv_fused(const void* qk, int64_t qk_row_stride, const void* w_dw,
+                                 const void* b_dw, const void* w_gr, const void* b_gr,
+                                 int32_t groups, int32_t num_q_heads, int32_t t0, int32_t t1,
+                                 const void* delayed, int64_t delayed_row_stride,
+                                 const void* delayed_init, int32_t Dv,
+                                 const void* v_current, int64_t v_current_row_stride,
+                                 cconv_pool_t conv_state, void* delayed_state,
+                                 int64_t delayed_state_row_stride, const int32_t* state_idx,
+                                 const int32_t* cu_seqlens, const uint8_t* has_init,
+                                 int32_t num_seqs, int32_t num_tokens, int32_t Cqk,
+                                 int32_t dtype, void* out, int64_t out_row_stride,
+                                 int32_t* dev_err, cconv_stream_t stream) {
+  // the delayed half of v lands in the last Dv columns of each output row
+  char* dprev = out ? static_cast<char*>(out) + (int64_t)(Cqk + Dv) * 2 : nullptr;
+  return cca_entry<true>(qk, qk_row_stride, w_dw, b_dw, w_gr, b_gr, groups, t0, t1, delayed,
+                         delayed_row_stride, delayed_init, Dv, conv_state, delayed_state,
+                         delayed_state_row_stride, state_idx, cu_seqlens, has_init, num_seqs,
+                         num_tokens, Cqk, dtype, out, out_row_stride, dprev, out_row_stride,
+                         num_q_heads, v_current, v_current_row_stride, dev_err, stream);
+}

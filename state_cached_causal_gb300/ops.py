@@ -77,6 +77,10 @@ def load():
         lib.cca_qk_conv.argtypes = [P, I64, P, P, P, P, I32, I32, I32, P, I64, P, I32, Pool, P,
                                     I64, P, P, P, I32, I32, I32, I32, P, I64, P, I64, P, P]
         lib.cca_qk_conv.restype = ctypes.c_int
+        lib.cca_qk_conv_fused.argtypes = [P, I64, P, P, P, P, I32, I32, I32, I32, P, I64, P, I32,
+                                          P, I64, Pool, P, I64, P, P, P, I32, I32, I32, I32, P,
+                                          I64, P, P]
+        lib.cca_qk_conv_fused.restype = ctypes.c_int
         lib.cconv_status_string.argtypes = [ctypes.c_int]
         lib.cconv_status_string.restype = ctypes.c_char_p
         lib.cconv_abi_version.argtypes = []
@@ -269,3 +273,23 @@ def cca_qk_conv(qk, w_dw, b_dw, w_gr, b_gr, groups, t0, t1, delayed, delayed_ini
         int(qk.shape[1]), _dtype_code(qk), _ptr(out_qk), _rows(out_qk),
         _ptr(out_delayed_prev), _rows(out_delayed_prev), _ptr(dev_err), _stream(stream))
     _check("cca_qk_conv", rc)
+
+
+def cca_qk_conv_fused(qk, w_dw, b_dw, w_gr, b_gr, groups, num_q_heads, t0, t1, delayed,
+                      delayed_init, v_current, conv_state, delayed_state, state_idx, cu_seqlens,
+                      has_init, out, dev_err=None, stream=None, num_tokens=None):
+    """cca_qk_conv with ZayaCCA.project's residual mix and value assembly (see
+    cca_qk_conv_fused in cconv.h); out: [T, Cqk + 2*Dv] = [query | key | value]."""
+    _i32(state_idx, "state_idx")
+    _i32(cu_seqlens, "cu_seqlens")
+    _u8(has_init, "has_init")
+    T = int(qk.shape[0]) if num_tokens is None else int(num_tokens)
+    rc = load().cca_qk_conv_fused(
+        _ptr(qk), _rows(qk), _ptr(w_dw), _ptr(b_dw), _ptr(w_gr), _ptr(b_gr), int(groups),
+        int(num_q_heads), int(t0), int(t1), _ptr(delayed), _rows(delayed), _ptr(delayed_init),
+        int(delayed.shape[1]), _ptr(v_current), _rows(v_current), _pool(conv_state),
+        _ptr(delayed_state), _rows(delayed_state), _ptr(state_idx), _ptr(cu_seqlens),
+        _ptr(has_init), int(state_idx.shape[0]), T, int(qk.shape[1]), _dtype_code(qk),
+        _ptr(out), _rows(out), _ptr(dev_err), _stream(stream))
+    _check("cca_qk_conv_fused", rc)
+

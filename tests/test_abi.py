@@ -48,7 +48,7 @@ def test_status_strings(lib):
     for s in (-1, -2, -3):
         assert ops.status_string(s) not in ("ok", "unknown status")
     assert ops.status_string(17) == "unknown status"
-    assert ops.abi_version() == 3
+    assert ops.abi_version() == 4
 
 
 FAKE = 0x10000  # 16-byte aligned, never dereferenced: every call below fails validation

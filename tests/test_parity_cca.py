@@ -164,3 +164,34 @@ def test_cca_rejects_unsupported():
 def test_zaya_cca_full_sampled():
     case = synth.zaya_cca(DEV)
     check(case, groups=[0, 19])
+
+
+# ---- the fused tail of ZayaCCA.project ----------------------------------------
+
+@pytest.mark.parametrize("Hq,Hkv,t0,t1", [(4, 2, 2, 2), (16, 4, 2, 2), (2, 2, 3, 1),
+                                          (6, 2, 1, 2)])
+def test_cca_fused_project_tail(Hq, Hkv, t0, t1):
+    case = synth.cca_case(460 + Hq + t0, DEV, lens=LENS, decode_prefix=3, Hq=Hq, Hkv=Hkv,
+                          t0=t0, t1=t1, padding_every=6)
+    T = int(case.qk.shape[0])
+    g = torch.Generator(device=DEV).manual_seed(11)
+    v_cur = torch.randn(T, case.Dv, generator=g, device=DEV).to(torch.bfloat16)
+    out = torch.full((T, case.Cqk + 2 * case.Dv + 8), 9.0, device=DEV, dtype=torch.bfloat16)
+    pool = case.pool.clone()
+    dstate = case.delayed_state.clone()
+    err = new_err()
+    ops.cca_qk_conv_fused(case.qk, case.w_dw, case.b_dw, case.w_gr, case.b_gr, case.groups, Hq,
+                          t0, t1, case.delayed, case.delayed_init, v_cur, pool, dstate,
+                          case.state_idx, case.cu_seqlens, case.has_init,
+                          out[:, :case.Cqk + 2 * case.Dv], dev_err=err)
+    chans, w_conv, w_dprev, w_pool, w_dstate = oracle_cca(case)
+    want = np.zeros((T, case.Cqk + 2 * case.Dv), dtype=np.uint16)
+    oracle.cca_project_epilogue(to_np(case.qk), w_conv, to_np(v_cur), w_dprev, Hq, Hkv, want)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    got = to_np(out)
+    assert_out_close(got[:, :case.Cqk], want[:, :case.Cqk], torch.bfloat16, "query|key")
+    assert_bits_equal(got[:, case.Cqk:case.Cqk + 2 * case.Dv], want[:, case.Cqk:], "value")
+    assert bool((out[:, case.Cqk + 2 * case.Dv:] == 9.0).all())
+    assert_bits_equal(pool_np(pool), w_pool, "conv_state")
+    assert_bits_equal(to_np(dstate), w_dstate, "delayed_state")
