@@ -744,9 +744,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int c0 = g * kGS + kc * 8;
       if (g != cur_g) {
         // B operand of group g: B[tap][k-chunk][n] = w_gr[g*128 + n][k-chunk*8 + e][tap]
-        // (unrolled so that several rows' loads are in flight at once)
+        // (unrolled by two: a second row's loads in flight, little code)
         constexpr int kBIter = kGS * (kGS / 8) / (kProdWarps * 32);
-#pragma unroll 8
+#pragma unroll 2
         for (int it = 0; it < kBIter; ++it) {
           const int pr = p + it * (kProdWarps * 32);
           const int o = pr & (kGS - 1), bkc = pr >> 7;
@@ -927,7 +927,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int m = 1; m <= NH; ++m)
           cconv::unpack16<__nv_bfloat16>(
               *reinterpret_cast<const uint4*>(xst + (rs0 + NH - m) * kXRowBytes + kc * 16), xw[m]);
-#pragma unroll
+        // (not unrolled: the code stays small for the instruction cache, the
+        // fast path above being the one that runs on most tiles)
+#pragma unroll 1
         for (int rr = 0; rr < 8; ++rr) {
           const int r = rs0 + rr;
           const uint4 cur = *reinterpret_cast<const uint4*>(xst + (r + NH) * kXRowBytes + kc * 16);
