@@ -68,6 +68,13 @@
 extern "C" {
 #endif
 
+/* Symbols of the C ABI (the library builds with hidden visibility otherwise). */
+#if defined(__GNUC__)
+#define CCONV_API __attribute__((visibility("default")))
+#else
+#define CCONV_API
+#endif
+
 /* Same type as cudaStream_t; NULL is the legacy default stream. */
 typedef struct CUstream_st* cconv_stream_t;
 
@@ -137,7 +144,7 @@ typedef struct cconv_pool {
  *   out          [num_tokens, C], row stride out_row_stride; must not alias x.
  *                Rows outside every sequence are not written.
  */
-int cconv_fwd_varlen(const void* x, int64_t x_row_stride, const void* w, const void* bias,
+CCONV_API int cconv_fwd_varlen(const void* x, int64_t x_row_stride, const void* w, const void* bias,
                      cconv_pool_t conv_states, const int32_t* state_idx,
                      const int32_t* cu_seqlens, const uint8_t* has_init, int32_t num_seqs,
                      int32_t num_tokens, int32_t C, int32_t width, int32_t dilation,
@@ -166,7 +173,7 @@ int cconv_fwd_varlen(const void* x, int64_t x_row_stride, const void* w, const v
  *   has_init     uint8 [num_seqs] or NULL (all true)
  *   n_spec       0..7;  cap >= S + n_spec;  width 2..4; dilation 1..4
  */
-int cconv_update(const void* x, int64_t x_row_stride, cconv_pool_t conv_states,
+CCONV_API int cconv_update(const void* x, int64_t x_row_stride, cconv_pool_t conv_states,
                  const void* w, const void* bias, const int32_t* state_idx,
                  int32_t num_seqs, int32_t n_spec, const int32_t* num_accepted,
                  const uint8_t* has_init, int32_t C, int32_t width, int32_t dilation,
@@ -213,7 +220,7 @@ typedef struct cconv_epilogue {
  * of (out, out_row_stride). State handling, arguments and errors are those of
  * cconv_fwd_varlen; num_tokens counts logical rows.
  */
-int cconv_fwd_varlen_fused(const void* x, int64_t x_row_stride, const void* w,
+CCONV_API int cconv_fwd_varlen_fused(const void* x, int64_t x_row_stride, const void* w,
                            const void* bias, cconv_pool_t conv_states,
                            const int32_t* state_idx, const int32_t* cu_seqlens,
                            const uint8_t* has_init, int32_t num_seqs, int32_t num_tokens,
@@ -225,7 +232,7 @@ int cconv_fwd_varlen_fused(const void* x, int64_t x_row_stride, const void* w,
  * cconv_update_fused -- cconv_update with the epilogue above in place of
  * (out, out_row_stride): request s owns logical rows [s*q, s*q+q).
  */
-int cconv_update_fused(const void* x, int64_t x_row_stride, cconv_pool_t conv_states,
+CCONV_API int cconv_update_fused(const void* x, int64_t x_row_stride, cconv_pool_t conv_states,
                        const void* w, const void* bias, const int32_t* state_idx,
                        int32_t num_seqs, int32_t n_spec, const int32_t* num_accepted,
                        const uint8_t* has_init, int32_t C, int32_t width, int32_t dilation,
@@ -261,7 +268,7 @@ int cconv_update_fused(const void* x, int64_t x_row_stride, cconv_pool_t conv_st
  * CCONV_DERR_CHECKPOINT (a row outside num_rows CCONV_DERR_ROW_INDEX) and is
  * skipped.
  */
-int cconv_checkpoint_export(const void* x, int64_t x_row_stride, cconv_pool_t conv_states,
+CCONV_API int cconv_checkpoint_export(const void* x, int64_t x_row_stride, cconv_pool_t conv_states,
                             const int32_t* ckpt_seq, const int32_t* ckpt_offset,
                             const int32_t* ckpt_slot, int32_t num_ckpt,
                             const int32_t* cu_seqlens, int32_t num_seqs, int32_t num_tokens,
@@ -298,7 +305,7 @@ int cconv_checkpoint_export(const void* x, int64_t x_row_stride, cconv_pool_t co
  *                     with row stride delayed_state_row_stride
  *   t0 1..4, t1 1..2, dtype CCONV_DTYPE_BF16 (fp32 returns -2), Dv % 8 == 0
  */
-int cca_qk_conv(const void* qk, int64_t qk_row_stride, const void* w_dw, const void* b_dw,
+CCONV_API int cca_qk_conv(const void* qk, int64_t qk_row_stride, const void* w_dw, const void* b_dw,
                 const void* w_gr, const void* b_gr, int32_t groups, int32_t t0, int32_t t1,
                 const void* delayed, int64_t delayed_row_stride, const void* delayed_init,
                 int32_t Dv, cconv_pool_t conv_state, void* delayed_state,
@@ -332,7 +339,7 @@ int cca_qk_conv(const void* qk, int64_t qk_row_stride, const void* w_dw, const v
  *   out         [num_tokens, Cqk + 2*Dv] with row stride out_row_stride >= Cqk + 2*Dv
  *   other arguments as cca_qk_conv (bf16 only)
  */
-int cca_qk_conv_fused(const void* qk, int64_t qk_row_stride, const void* w_dw,
+CCONV_API int cca_qk_conv_fused(const void* qk, int64_t qk_row_stride, const void* w_dw,
                       const void* b_dw, const void* w_gr, const void* b_gr, int32_t groups,
                       int32_t num_q_heads, int32_t t0, int32_t t1, const void* delayed,
                       int64_t delayed_row_stride, const void* delayed_init, int32_t Dv,
@@ -344,10 +351,10 @@ int cca_qk_conv_fused(const void* qk, int64_t qk_row_stride, const void* w_dw,
                       int64_t out_row_stride, int32_t* dev_err, cconv_stream_t stream);
 
 /* Static English text for a status code. */
-const char* cconv_status_string(int status);
+CCONV_API const char* cconv_status_string(int status);
 
 /* ABI version of this header (increments on any signature change). */
-int cconv_abi_version(void);
+CCONV_API int cconv_abi_version(void);
 
 #ifdef __cplusplus
 }

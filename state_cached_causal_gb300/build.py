@@ -22,6 +22,7 @@ LIB = os.path.join(PKG, "libcconv.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
+                 "-Xcompiler", "-fvisibility=hidden",
                  "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC]
 
 

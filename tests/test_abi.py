@@ -27,7 +27,8 @@ def declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     text = re.sub(r"//[^\n]*", "", text)
-    names = re.findall(r"^\s*(?:const\s+)?\w+\s*\**\s*(\w+)\s*\(", text, flags=re.M)
+    names = re.findall(r"^\s*(?:CCONV_API\s+)?(?:const\s+)?\w+\s*\**\s*(\w+)\s*\(", text,
+                       flags=re.M)
     return sorted(set(n for n in names if n not in ("if", "while", "for")))
 
 
@@ -41,6 +42,15 @@ def test_header_declares_the_three_operations():
 def test_library_exports_every_declared_symbol(lib):
     for n in declared_functions():
         assert hasattr(lib, n), n
+
+
+def test_library_exports_nothing_else():
+    """Only the C ABI is visible: internal kernels and helpers stay hidden."""
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", cbuild.build()], capture_output=True,
+                         text=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    assert exported == set(declared_functions())
 
 
 def test_status_strings(lib):
