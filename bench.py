@@ -356,7 +356,7 @@ def recorded_traffic(kernel):
 
 # channels (groups for CCA) of each workload in the oracle sample: about 10 s of
 # single-core work on the GPU host; `light` is the reference arm's per-step sample
-SAMPLE_CHANNELS = {"gdn_decode": 8192, "gdn_mixed": 4096, "zaya_cca": 20, "ple_spec": 8192}
+SAMPLE_CHANNELS = {"gdn_decode": 8192, "gdn_mixed": 8192, "zaya_cca": 20, "ple_spec": 12288}
 LIGHT_CHANNELS = {"gdn_decode": 512, "gdn_mixed": 64, "zaya_cca": 1, "ple_spec": 64}
 
 
