@@ -21,9 +21,19 @@
  *           library keeps no pointer after a call returns and allocates no
  *           memory. Tensors are row-major; a "row stride" is in elements.
  * Types.    dtype CCONV_DTYPE_F32 or CCONV_DTYPE_BF16 names the storage type
- *           of activations, weights, biases, outputs and state pools of one
- *           call (they share it). Arithmetic accumulates in fp32; outputs are
- *           rounded to nearest-even into the storage type.
+ *           of activations, weights, biases and outputs of one call (they
+ *           share it). Arithmetic accumulates in fp32; outputs are rounded to
+ *           nearest-even into the storage type.
+ * State type. A pool carries its own storage type (cconv_pool_t.dtype), which
+ *           may differ from the call's (the PLE page's get_state_dtype takes it
+ *           from mamba_cache_dtype). History read from a pool is converted to
+ *           the call's type, and values written to a pool are converted to the
+ *           pool's type (the Zaya page's conv_state[slot].to(qk.dtype) and
+ *           new_history.to(conv_state.dtype)): bf16 -> fp32 is exact, fp32 ->
+ *           bf16 rounds to nearest even. Columns a call rewrites pass through
+ *           the call's type, also those it only moves; columns it does not
+ *           rewrite keep their bits. Pools of the other type than the call
+ *           are accessed element by element.
  * Tap order. PyTorch cross-correlation with left history: weight column
  *           width-1 multiplies the current token, column k the input
  *           (width-1-k)*dilation tokens earlier.
@@ -109,6 +119,8 @@ typedef struct cconv_pool {
   int64_t s_col;     /* element stride between columns                  */
   int32_t num_slots; /* slots in the pool                               */
   int32_t cap;       /* columns in the view                             */
+  int32_t dtype;     /* storage type of the pool: CCONV_DTYPE_F32 or
+                        CCONV_DTYPE_BF16 (p aligned to its element size) */
 } cconv_pool_t;
 
 /*
@@ -302,7 +314,10 @@ CCONV_API int cconv_checkpoint_export(const void* x, int64_t x_row_stride, cconv
  *   w_dw [Cqk, t0], b_dw [Cqk] or NULL; w_gr [Cqk, 128, t1], b_gr [Cqk] or NULL
  *   delayed, out_delayed_prev [num_tokens, Dv] with row strides; delayed_init [Dv]
  *   conv_state        pool view with cap >= n; delayed_state [num_slots, Dv]
- *                     with row stride delayed_state_row_stride
+ *                     with row stride delayed_state_row_stride, of the pool's
+ *                     storage type (bf16, or fp32 with the conversions of
+ *                     "State type"; an fp32 delayed state left as it is by an
+ *                     empty request with has_init keeps its bits)
  *   t0 1..4, t1 1..2, dtype CCONV_DTYPE_BF16 (fp32 returns -2), Dv % 8 == 0
  */
 CCONV_API int cca_qk_conv(const void* qk, int64_t qk_row_stride, const void* w_dw, const void* b_dw,

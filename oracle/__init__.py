@@ -54,28 +54,28 @@ def _load():
             lib = ctypes.CDLL(build())
             P, I64, I32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32
             lib.oracle_cconv_fwd_varlen.argtypes = [
-                P, I64, P, P, P, I64, I64, I64, I32, I32, P, P, P, I32, I32, I32, I32,
+                P, I64, P, P, P, I64, I64, I64, I32, I32, I32, P, P, P, I32, I32, I32, I32,
                 I32, I32, P, I64]
             lib.oracle_cconv_fwd_varlen.restype = ctypes.c_int
             lib.oracle_cconv_update.argtypes = [
-                P, I64, P, I64, I64, I64, I32, I32, P, P, P, I32, I32, P, P, I32, I32,
+                P, I64, P, I64, I64, I64, I32, I32, I32, P, P, P, I32, I32, P, P, I32, I32,
                 I32, I32, I32, P, I64]
             lib.oracle_cconv_update.restype = ctypes.c_int
             lib.oracle_cca_qk_conv.argtypes = [
                 P, I64, P, P, P, P, I32, I32, I32, P, I64, P, I32, P, I64, I64, I64,
-                I32, I32, P, I64, P, P, P, I32, I32, I32, P, I64, P, I64]
+                I32, I32, I32, P, I64, P, P, P, I32, I32, I32, P, I64, P, I64]
             lib.oracle_cca_qk_conv.restype = ctypes.c_int
             lib.oracle_cconv_fwd_varlen_fused.argtypes = [
-                P, I64, P, P, P, I64, I64, I64, I32, I32, P, P, P, I32, I32, I32, I32,
+                P, I64, P, P, P, I64, I64, I64, I32, I32, I32, P, P, P, I32, I32, I32, I32,
                 I32, I32, P, I32, P, I64, P, I64]
             lib.oracle_cconv_fwd_varlen_fused.restype = ctypes.c_int
             lib.oracle_cconv_update_fused.argtypes = [
-                P, I64, P, I64, I64, I64, I32, I32, P, P, P, I32, I32, P, P, I32, I32,
+                P, I64, P, I64, I64, I64, I32, I32, I32, P, P, P, I32, I32, P, P, I32, I32,
                 I32, I32, I32, P, I32, P, I64, P, I64]
             lib.oracle_cconv_update_fused.restype = ctypes.c_int
             lib.oracle_cconv_checkpoint_export.argtypes = [
-                P, I64, P, I64, I64, I64, I32, I32, P, P, P, I32, P, I32, P, I32, I32, I32, I32,
-                I32]
+                P, I64, P, I64, I64, I64, I32, I32, I32, P, P, P, I32, P, I32, P, I32, I32, I32,
+                I32, I32]
             lib.oracle_cconv_checkpoint_export.restype = ctypes.c_int
             lib.oracle_cca_project_epilogue.argtypes = [
                 P, I64, P, I64, P, I64, P, I64, I32, I32, I32, I32, I32, P, I64]
@@ -160,7 +160,8 @@ def cconv_fwd_varlen(x, w, bias, pool, state_idx, cu_seqlens, has_init, width, d
     B = int(state_idx.shape[0])
     rc = lib.oracle_cconv_fwd_varlen(
         _ptr(x), _rows(x), _ptr(w), _ptr(bias), _pool_base(pool), ss, sc, scol,
-        pool.shape[0], pool.shape[2], _ptr(state_idx), _ptr(cu_seqlens), _ptr(has_init),
+        pool.shape[0], pool.shape[2], _dtype_code(pool),
+        _ptr(state_idx), _ptr(cu_seqlens), _ptr(has_init),
         B, x.shape[1], width, dilation, act, dt, _ptr(out), _rows(out))
     if rc != 0:
         raise ValueError(f"oracle_cconv_fwd_varlen rejected its arguments ({rc})")
@@ -188,6 +189,7 @@ def cconv_update(x, pool, w, bias, state_idx, n_spec, num_accepted, has_init, wi
     B = int(state_idx.shape[0])
     rc = lib.oracle_cconv_update(
         _ptr(x), _rows(x), _pool_base(pool), ss, sc, scol, pool.shape[0], pool.shape[2],
+        _dtype_code(pool),
         _ptr(w), _ptr(bias), _ptr(state_idx), B, n_spec, _ptr(num_accepted),
         _ptr(has_init), x.shape[1], width, dilation, act, dt, _ptr(out), _rows(out))
     if rc != 0:
@@ -214,7 +216,8 @@ def cconv_fwd_varlen_fused(x, w, bias, pool, state_idx, cu_seqlens, has_init, wi
     B = int(state_idx.shape[0])
     rc = lib.oracle_cconv_fwd_varlen_fused(
         _ptr(x), _rows(x), _ptr(w), _ptr(bias), _pool_base(pool), ss, sc, scol,
-        pool.shape[0], pool.shape[2], _ptr(state_idx), _ptr(cu_seqlens), _ptr(has_init),
+        pool.shape[0], pool.shape[2], _dtype_code(pool),
+        _ptr(state_idx), _ptr(cu_seqlens), _ptr(has_init),
         B, x.shape[1], width, dilation, act, dt, _ptr(token_indices), x.shape[0],
         _ptr(residual), _rows(residual), _ptr(outer), _rows(outer) if outer is not None else 0)
     if rc != 0:
@@ -237,6 +240,7 @@ def cconv_update_fused(x, pool, w, bias, state_idx, n_spec, num_accepted, has_in
     B = int(state_idx.shape[0])
     rc = lib.oracle_cconv_update_fused(
         _ptr(x), _rows(x), _pool_base(pool), ss, sc, scol, pool.shape[0], pool.shape[2],
+        _dtype_code(pool),
         _ptr(w), _ptr(bias), _ptr(state_idx), B, n_spec, _ptr(num_accepted),
         _ptr(has_init), x.shape[1], width, dilation, act, dt, _ptr(token_indices),
         x.shape[0], _ptr(residual), _rows(residual), _ptr(outer),
@@ -261,6 +265,7 @@ def cconv_checkpoint_export(x, pool, ck_seq, ck_off, ck_slot, cu_seqlens, width,
     ss, sc, scol = _pool_strides(pool)
     rc = lib.oracle_cconv_checkpoint_export(
         _ptr(x), _rows(x), _pool_base(pool), ss, sc, scol, pool.shape[0], pool.shape[2],
+        _dtype_code(pool),
         _ptr(ck_seq), _ptr(ck_off), _ptr(ck_slot), int(ck_seq.shape[0]), _ptr(cu_seqlens),
         int(cu_seqlens.shape[0]) - 1, _ptr(token_indices), x.shape[0], x.shape[1], width,
         dilation, dt)
@@ -292,7 +297,8 @@ def cca_qk_conv(qk, w_dw, b_dw, w_gr, b_gr, groups, t0, t1, delayed, delayed_ini
     rc = lib.oracle_cca_qk_conv(
         _ptr(qk), _rows(qk), _ptr(w_dw), _ptr(b_dw), _ptr(w_gr), _ptr(b_gr), groups, t0,
         t1, _ptr(delayed), _rows(delayed), _ptr(delayed_init), delayed.shape[1],
-        _pool_base(pool), ss, sc, scol, pool.shape[0], pool.shape[2], _ptr(delayed_state),
+        _pool_base(pool), ss, sc, scol, pool.shape[0], pool.shape[2], _dtype_code(pool),
+        _ptr(delayed_state),
         _rows(delayed_state), _ptr(state_idx), _ptr(cu_seqlens), _ptr(has_init), B,
         qk.shape[1], dt, _ptr(out_qk), _rows(out_qk), _ptr(out_delayed_prev),
         _rows(out_delayed_prev))

@@ -93,6 +93,35 @@ static float orc_raw_to_f32(orc_raw r, int dtype) {
   return orc_bf16_to_f32((uint16_t)r);
 }
 
+/*
+ * Conv-state pools have their own storage type sdtype, which may differ from
+ * the activations' dtype ([P] get_state_dtype: the mamba_cache_dtype of the
+ * cache config). [Z] _mix_with_state converts on both sides: the history it
+ * reads is conv_state[slot].to(qk.dtype), and what it writes back is
+ * new_history.to(conv_state.dtype). So a state element enters the conv as the
+ * activation type, and an element of the new state (a token, or a history
+ * column carried over) is converted to the state type. bf16 -> fp32 is exact;
+ * fp32 -> bf16 rounds to nearest even. With one type, both are bit copies.
+ */
+static orc_raw orc_convert(orc_raw r, int from, int to) {
+  if (from == to) return r;
+  const float v = orc_raw_to_f32(r, from);
+  if (to == ORC_F32) {
+    uint32_t u;
+    memcpy(&u, &v, 4);
+    return u;
+  }
+  return orc_f32_to_bf16(v);
+}
+
+static orc_raw orc_state_get(const void* pool, int64_t i, int sdtype, int dtype) {
+  return orc_convert(orc_get_raw(pool, i, sdtype), sdtype, dtype);
+}
+
+static void orc_state_put(void* pool, int64_t i, int sdtype, int dtype, orc_raw r) {
+  orc_put_raw(pool, i, sdtype, orc_convert(r, dtype, sdtype));
+}
+
 /* SiLU in fp32: v * sigmoid(v) = v / (1 + exp(-v)) ([G] activation "silu",
  * [P] self.activation = "silu"). */
 static float orc_act(float v, int act) {
@@ -139,7 +168,8 @@ static void orc_depthwise_channel(const orc_raw* xt, int S, int L, const void* w
  */
 int oracle_cconv_fwd_varlen(const void* x, int64_t x_rs, const void* w, const void* bias,
                             void* pool, int64_t s_slot, int64_t s_chan, int64_t s_col,
-                            int32_t num_slots, int32_t cap, const int32_t* state_idx,
+                            int32_t num_slots, int32_t cap, int32_t sdtype,
+                            const int32_t* state_idx,
                             const int32_t* cu_seqlens, const uint8_t* has_init,
                             int32_t num_seqs, int32_t C, int32_t W, int32_t D, int32_t act,
                             int32_t dtype, void* out, int64_t out_rs) {
@@ -154,13 +184,13 @@ int oracle_cconv_fwd_varlen(const void* x, int64_t x_rs, const void* w, const vo
     orc_raw* xt = (orc_raw*)malloc(sizeof(orc_raw) * (size_t)(S + L + 1));
     for (int64_t c = 0; c < C; ++c) {
       for (int i = 0; i < S; ++i)
-        xt[i] = h ? orc_get_raw(pool, slot * s_slot + c * s_chan + i * s_col, dtype) : 0u;
+        xt[i] = h ? orc_state_get(pool, slot * s_slot + c * s_chan + i * s_col, sdtype, dtype) : 0u;
       for (int i = 0; i < L; ++i) xt[S + i] = orc_get_raw(x, (start + i) * x_rs + c, dtype);
       orc_depthwise_channel(xt, S, L, w, c * W, bias, c, W, D, act, dtype, out,
                             start * out_rs + c, out_rs);
       if (slot >= 0)
         for (int i = 0; i < S; ++i)
-          orc_put_raw(pool, slot * s_slot + c * s_chan + i * s_col, dtype, xt[L + i]);
+          orc_state_put(pool, slot * s_slot + c * s_chan + i * s_col, sdtype, dtype, xt[L + i]);
     }
     free(xt);
   }
@@ -183,6 +213,7 @@ int oracle_cconv_fwd_varlen(const void* x, int64_t x_rs, const void* w, const vo
  */
 int oracle_cconv_update(const void* x, int64_t x_rs, void* pool, int64_t s_slot,
                         int64_t s_chan, int64_t s_col, int32_t num_slots, int32_t cap,
+                        int32_t sdtype,
                         const void* w, const void* bias, const int32_t* state_idx,
                         int32_t num_seqs, int32_t n_spec, const int32_t* num_accepted,
                         const uint8_t* has_init, int32_t C, int32_t W, int32_t D, int32_t act,
@@ -210,7 +241,7 @@ int oracle_cconv_update(const void* x, int64_t x_rs, void* pool, int64_t s_slot,
     for (int64_t c = 0; c < C; ++c) {
       const int ncols = n_spec > 0 ? cap : S;
       for (int i = 0; i < ncols; ++i)
-        Bc[i] = h ? orc_get_raw(pool, slot * s_slot + c * s_chan + i * s_col, dtype) : 0u;
+        Bc[i] = h ? orc_state_get(pool, slot * s_slot + c * s_chan + i * s_col, sdtype, dtype) : 0u;
       for (int i = 0; i < S; ++i) xt[i] = Bc[off + i];
       for (int i = 0; i < q; ++i) xt[S + i] = orc_get_raw(x, (row0 + i) * x_rs + c, dtype);
       orc_depthwise_channel(xt, S, q, w, c * W, bias, c, W, D, act, dtype, out,
@@ -218,11 +249,11 @@ int oracle_cconv_update(const void* x, int64_t x_rs, void* pool, int64_t s_slot,
       if (slot < 0) continue;
       if (n_spec == 0) {
         for (int i = 0; i < S; ++i)
-          orc_put_raw(pool, slot * s_slot + c * s_chan + i * s_col, dtype, xt[1 + i]);
+          orc_state_put(pool, slot * s_slot + c * s_chan + i * s_col, sdtype, dtype, xt[1 + i]);
       } else {
         for (int i = 0; i < cap; ++i) {
           orc_raw v = (i < cap - q) ? Bc[off + 1 + i] : xt[S + (i - (cap - q))];
-          orc_put_raw(pool, slot * s_slot + c * s_chan + i * s_col, dtype, v);
+          orc_state_put(pool, slot * s_slot + c * s_chan + i * s_col, sdtype, dtype, v);
         }
       }
     }
@@ -271,7 +302,7 @@ static void orc_depthwise_channel_res(const orc_raw* xt, int S, int L, const voi
  * outside [0, num_rows). */
 int oracle_cconv_fwd_varlen_fused(const void* x, int64_t x_rs, const void* w,
                                   const void* bias, void* pool, int64_t s_slot, int64_t s_chan,
-                                  int64_t s_col, int32_t num_slots, int32_t cap,
+                                  int64_t s_col, int32_t num_slots, int32_t cap, int32_t sdtype,
                                   const int32_t* state_idx, const int32_t* cu_seqlens,
                                   const uint8_t* has_init, int32_t num_seqs, int32_t C,
                                   int32_t W, int32_t D, int32_t act, int32_t dtype,
@@ -296,13 +327,13 @@ int oracle_cconv_fwd_varlen_fused(const void* x, int64_t x_rs, const void* w,
     orc_raw* xt = (orc_raw*)malloc(sizeof(orc_raw) * (size_t)(S + L + 1));
     for (int64_t c = 0; c < C; ++c) {
       for (int i = 0; i < S; ++i)
-        xt[i] = h ? orc_get_raw(pool, slot * s_slot + c * s_chan + i * s_col, dtype) : 0u;
+        xt[i] = h ? orc_state_get(pool, slot * s_slot + c * s_chan + i * s_col, sdtype, dtype) : 0u;
       for (int i = 0; i < L; ++i) xt[S + i] = orc_get_raw(x, prow[i] * x_rs + c, dtype);
       orc_depthwise_channel_res(xt, S, L, w, c * W, bias, c, W, D, act, dtype, prow, res,
                                 res_rs, outer, outer_rs);
       if (slot >= 0)
         for (int i = 0; i < S; ++i)
-          orc_put_raw(pool, slot * s_slot + c * s_chan + i * s_col, dtype, xt[L + i]);
+          orc_state_put(pool, slot * s_slot + c * s_chan + i * s_col, sdtype, dtype, xt[L + i]);
     }
     free(xt);
     free(prow);
@@ -314,6 +345,7 @@ int oracle_cconv_fwd_varlen_fused(const void* x, int64_t x_rs, const void* w,
  * [s*q, s*q + q). -2 if a logical row maps outside [0, num_rows). */
 int oracle_cconv_update_fused(const void* x, int64_t x_rs, void* pool, int64_t s_slot,
                               int64_t s_chan, int64_t s_col, int32_t num_slots, int32_t cap,
+                        int32_t sdtype,
                               const void* w, const void* bias, const int32_t* state_idx,
                               int32_t num_seqs, int32_t n_spec, const int32_t* num_accepted,
                               const uint8_t* has_init, int32_t C, int32_t W, int32_t D,
@@ -348,7 +380,7 @@ int oracle_cconv_update_fused(const void* x, int64_t x_rs, void* pool, int64_t s
     for (int64_t c = 0; c < C; ++c) {
       const int ncols = n_spec > 0 ? cap : S;
       for (int i = 0; i < ncols; ++i)
-        Bc[i] = h ? orc_get_raw(pool, slot * s_slot + c * s_chan + i * s_col, dtype) : 0u;
+        Bc[i] = h ? orc_state_get(pool, slot * s_slot + c * s_chan + i * s_col, sdtype, dtype) : 0u;
       for (int i = 0; i < S; ++i) xt[i] = Bc[off + i];
       for (int i = 0; i < q; ++i) xt[S + i] = orc_get_raw(x, prow[i] * x_rs + c, dtype);
       orc_depthwise_channel_res(xt, S, q, w, c * W, bias, c, W, D, act, dtype, prow, res,
@@ -356,11 +388,11 @@ int oracle_cconv_update_fused(const void* x, int64_t x_rs, void* pool, int64_t s
       if (slot < 0) continue;
       if (n_spec == 0) {
         for (int i = 0; i < S; ++i)
-          orc_put_raw(pool, slot * s_slot + c * s_chan + i * s_col, dtype, xt[1 + i]);
+          orc_state_put(pool, slot * s_slot + c * s_chan + i * s_col, sdtype, dtype, xt[1 + i]);
       } else {
         for (int i = 0; i < cap; ++i) {
           orc_raw v = (i < cap - q) ? Bc[off + 1 + i] : xt[S + (i - (cap - q))];
-          orc_put_raw(pool, slot * s_slot + c * s_chan + i * s_col, dtype, v);
+          orc_state_put(pool, slot * s_slot + c * s_chan + i * s_col, sdtype, dtype, v);
         }
       }
     }
@@ -382,11 +414,13 @@ int oracle_cconv_update_fused(const void* x, int64_t x_rs, void* pool, int64_t s
  * inputs"). Checkpoint k names request ck_seq[k], a token offset
  * ck_off[k] in [S, L] of that request and a destination slot ck_slot[k]:
  *   pool[ck_slot[k]][c][i] = x[p(cu[s] + ck_off[k] - S + i)][c],  i < S
- * (a bit copy; p = token_indices or the identity). Columns >= S of the slot
- * are untouched. Returns -2 on a checkpoint outside these ranges.
+ * (a bit copy when the pool has x's type, else converted to the pool's type;
+ * p = token_indices or the identity). Columns >= S of the slot are untouched.
+ * Returns -2 on a checkpoint outside these ranges.
  */
 int oracle_cconv_checkpoint_export(const void* x, int64_t x_rs, void* pool, int64_t s_slot,
                                    int64_t s_chan, int64_t s_col, int32_t num_slots, int32_t cap,
+                        int32_t sdtype,
                                    const int32_t* ck_seq, const int32_t* ck_off,
                                    const int32_t* ck_slot, int32_t num_ckpt,
                                    const int32_t* cu_seqlens, int32_t num_seqs,
@@ -404,7 +438,7 @@ int oracle_cconv_checkpoint_export(const void* x, int64_t x_rs, void* pool, int6
       const int64_t p = tidx ? tidx[li] : li;
       if (p < 0 || p >= num_rows) return -2;
       for (int64_t c = 0; c < C; ++c)
-        orc_put_raw(pool, slot * s_slot + c * s_chan + i * s_col, dtype,
+        orc_state_put(pool, slot * s_slot + c * s_chan + i * s_col, sdtype, dtype,
                     orc_get_raw(x, p * x_rs + c, dtype));
     }
   }
@@ -427,14 +461,16 @@ int oracle_cconv_checkpoint_export(const void* x, int64_t x_rs, void* pool, int6
  *   out_delayed_prev[start + j] = delayed[start + j - 1]       (j >= 1)
  *   conv_state[slot][c][i]      = xt[c][L + i]                 (i < n)
  *   delayed_state[slot]         = L > 0 ? delayed[start + L - 1]
- *                                       : (h ? delayed_state[slot] : delayed_init)
+ *                                       : (h ? left as it is : delayed_init)
  * A slot < 0 is a padding row: zero history, initial delayed value, no write.
+ * conv_state and delayed_state have the storage type sdtype (converted as
+ * orc_state_get / orc_state_put say).
  */
 int oracle_cca_qk_conv(const void* qk, int64_t qk_rs, const void* w_dw, const void* b_dw,
                        const void* w_gr, const void* b_gr, int32_t G, int32_t T0, int32_t T1,
                        const void* delayed, int64_t delayed_rs, const void* delayed_init,
                        int32_t Dv, void* pool, int64_t s_slot, int64_t s_chan, int64_t s_col,
-                       int32_t num_slots, int32_t cap, void* delayed_state,
+                       int32_t num_slots, int32_t cap, int32_t sdtype, void* delayed_state,
                        int64_t dstate_rs, const int32_t* state_idx,
                        const int32_t* cu_seqlens, const uint8_t* has_init, int32_t num_seqs,
                        int32_t Cqk, int32_t dtype, void* out_qk, int64_t out_rs,
@@ -454,7 +490,7 @@ int oracle_cca_qk_conv(const void* qk, int64_t qk_rs, const void* w_dw, const vo
     for (int64_t c = 0; c < Cqk; ++c) {
       orc_raw* xc = xt + c * (n + L);
       for (int i = 0; i < n; ++i)
-        xc[i] = h ? orc_get_raw(pool, slot * s_slot + c * s_chan + i * s_col, dtype) : 0u;
+        xc[i] = h ? orc_state_get(pool, slot * s_slot + c * s_chan + i * s_col, sdtype, dtype) : 0u;
       for (int i = 0; i < L; ++i) xc[n + i] = orc_get_raw(qk, (start + i) * qk_rs + c, dtype);
       for (int m = 0; m < nu; ++m) {
         const int p = m - (T1 - 1);
@@ -484,22 +520,22 @@ int oracle_cca_qk_conv(const void* qk, int64_t qk_rs, const void* w_dw, const vo
       }
     }
     for (int64_t c = 0; c < Dv; ++c) {
-      orc_raw first = h ? orc_get_raw(delayed_state, slot * dstate_rs + c, dtype)
+      orc_raw first = h ? orc_state_get(delayed_state, slot * dstate_rs + c, sdtype, dtype)
                         : orc_get_raw(delayed_init, c, dtype);
       if (L > 0) orc_put_raw(out_dprev, start * dprev_rs + c, dtype, first);
       for (int j = 1; j < L; ++j)
         orc_put_raw(out_dprev, (start + j) * dprev_rs + c, dtype,
                     orc_get_raw(delayed, (start + j - 1) * delayed_rs + c, dtype));
-      if (slot >= 0) {
+      if (slot >= 0 && (L > 0 || !h)) {
         orc_raw last = L > 0 ? orc_get_raw(delayed, (start + L - 1) * delayed_rs + c, dtype)
                              : first;
-        orc_put_raw(delayed_state, slot * dstate_rs + c, dtype, last);
+        orc_state_put(delayed_state, slot * dstate_rs + c, sdtype, dtype, last);
       }
     }
     if (slot >= 0)
       for (int64_t c = 0; c < Cqk; ++c)
         for (int i = 0; i < n; ++i)
-          orc_put_raw(pool, slot * s_slot + c * s_chan + i * s_col, dtype,
+          orc_state_put(pool, slot * s_slot + c * s_chan + i * s_col, sdtype, dtype,
                       xt[c * (n + L) + L + i]);
     free(xt);
     free(u);

@@ -16,4 +16,4 @@ extern "C" const char* cconv_status_string(int status) {
   }
 }
 
-extern "C" int cconv_abi_version(void) { return 4; }
+extern "C" int cconv_abi_version(void) { return 5; }

@@ -255,6 +255,29 @@ __device__ __forceinline__ uint4 pick(const uint4 (&h)[N], int idx) {
   return r;
 }
 
+// Eight delayed-state values of `slot` (unit k) as bf16, and back: an fp32
+// delayed state (the pool's type) is rounded on load and widened on store.
+__device__ __forceinline__ uint4 dstate_load(const Args& a, int slot, int k) {
+  if (!a.pool.mixed)
+    return *reinterpret_cast<const uint4*>(a.dstate + ((int64_t)slot * a.dstate_rs + k * 8) * 2);
+  const float4* p =
+      reinterpret_cast<const float4*>(a.dstate + ((int64_t)slot * a.dstate_rs + k * 8) * 4);
+  const float4 lo = p[0], hi = p[1];
+  return make_uint4(cconv::pack_bf16x2(lo.x, lo.y), cconv::pack_bf16x2(lo.z, lo.w),
+                    cconv::pack_bf16x2(hi.x, hi.y), cconv::pack_bf16x2(hi.z, hi.w));
+}
+__device__ __forceinline__ void dstate_store(const Args& a, int slot, int k, const uint4& v) {
+  if (!a.pool.mixed) {
+    *reinterpret_cast<uint4*>(a.dstate + ((int64_t)slot * a.dstate_rs + k * 8) * 2) = v;
+    return;
+  }
+  float f[8];
+  cconv::unpack16<__nv_bfloat16>(v, f);
+  float4* p = reinterpret_cast<float4*>(a.dstate + ((int64_t)slot * a.dstate_rs + k * 8) * 4);
+  p[0] = make_float4(f[0], f[1], f[2], f[3]);
+  p[1] = make_float4(f[4], f[5], f[6], f[7]);
+}
+
 // The NH columns of 8 channels from their channel-first words (channel v,
 // column col at 16-bit element v * NH + col).
 template <int NH>
@@ -293,11 +316,16 @@ __device__ __forceinline__ void hist_load_all(const Pool& P, int slot, int c0, u
     if (P.mode == cconv::kPoolSD) {
       h[col] = *reinterpret_cast<const uint4*>(base + ((int64_t)col * P.s_col + c0) * 2);
     } else {
+      // element by element; an fp32 pool is rounded to the bf16 activations
+      const int SE = P.mixed ? 4 : 2;
+      const char* sb = P.p + (int64_t)slot * P.s_slot * SE;
       uint32_t e[8];
 #pragma unroll
-      for (int v = 0; v < 8; ++v)
-        e[v] = *reinterpret_cast<const uint16_t*>(
-            base + ((int64_t)(c0 + v) * P.s_chan + (int64_t)col * P.s_col) * 2);
+      for (int v = 0; v < 8; ++v) {
+        const uint32_t b = cconv::load_bits(
+            sb + ((int64_t)(c0 + v) * P.s_chan + (int64_t)col * P.s_col) * SE, SE);
+        e[v] = P.mixed ? cconv::state_to_act<__nv_bfloat16>(b) : b;
+      }
       h[col] = make_uint4(e[0] | (e[1] << 16), e[2] | (e[3] << 16), e[4] | (e[5] << 16),
                           e[6] | (e[7] << 16));
     }
@@ -328,12 +356,16 @@ __device__ __forceinline__ void hist_store_all(const Pool& P, int slot, int c0,
     if (P.mode == cconv::kPoolSD) {
       *reinterpret_cast<uint4*>(base + ((int64_t)col * P.s_col + c0) * 2) = h[col];
     } else {
+      // element by element; an fp32 pool takes the bf16 values widened
+      const int SE = P.mixed ? 4 : 2;
+      char* sb = P.p + (int64_t)slot * P.s_slot * SE;
       const uint32_t wd[4] = {h[col].x, h[col].y, h[col].z, h[col].w};
 #pragma unroll
-      for (int v = 0; v < 8; ++v)
-        *reinterpret_cast<uint16_t*>(base + ((int64_t)(c0 + v) * P.s_chan +
-                                             (int64_t)col * P.s_col) * 2) =
-            static_cast<uint16_t>(wd[v >> 1] >> ((v & 1) * 16));
+      for (int v = 0; v < 8; ++v) {
+        const uint32_t b = (wd[v >> 1] >> ((v & 1) * 16)) & 0xffffu;
+        cconv::store_bits(sb + ((int64_t)(c0 + v) * P.s_chan + (int64_t)col * P.s_col) * SE,
+                          SE, P.mixed ? cconv::act_to_state<__nv_bfloat16>(b) : b);
+      }
     }
   }
 }
@@ -1054,15 +1086,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (slot >= a.pool.num_slots) continue;
         const bool h = slot >= 0 && (hini == nullptr || hini[s] != 0);
         for (int k = lane; k < dunits; k += 32) {
-          const uint4 first =
-              h ? *reinterpret_cast<const uint4*>(a.dstate + ((int64_t)slot * a.dstate_rs + k * 8) * 2)
-                : cconv::ldg16(a.delayed_init + k * 16);
+          const uint4 first = h ? dstate_load(a, slot, k) : cconv::ldg16(a.delayed_init + k * 16);
           const uint4 last =
               en > st ? cconv::ldg16(a.delayed + ((int64_t)(en - 1) * a.delayed_rs + k * 8) * 2)
                       : first;
           if (en > st) cconv::stg16(a.dprev + ((int64_t)st * a.dprev_rs + k * 8) * 2, first);
-          if (slot >= 0)
-            *reinterpret_cast<uint4*>(a.dstate + ((int64_t)slot * a.dstate_rs + k * 8) * 2) = last;
+          // (an empty request with history leaves its delayed state as it is)
+          if (slot >= 0 && (en > st || !h)) dstate_store(a, slot, k, last);
         }
       }
       // Raw-history state of owned requests of two or more tokens, once every
@@ -1184,6 +1214,9 @@ static int cca_entry(const void* qk, int64_t qk_row_stride, const void* w_dw, co
   if (!w_dw || !w_gr || !delayed_init || !conv_state.p || !delayed_state ||
       (num_seqs > 0 && (!state_idx || !cu_seqlens)))
     return CCONV_ERR_INVALID;
+  if (conv_state.dtype != CCONV_DTYPE_BF16 && conv_state.dtype != CCONV_DTYPE_F32)
+    return CCONV_ERR_INVALID;
+  const int sesize = conv_state.dtype == CCONV_DTYPE_F32 ? 4 : 2;
   if (num_tokens > 0 && (!qk || !delayed || !out_qk || !out_delayed_prev))
     return CCONV_ERR_INVALID;
   if (num_seqs < 0 || num_tokens < 0 || groups <= 0 || Cqk <= 0 || Dv <= 0 || t0 < 1 || t1 < 1)
@@ -1193,7 +1226,8 @@ static int cca_entry(const void* qk, int64_t qk_row_stride, const void* w_dw, co
   if (Cqk / groups != kGS || t0 > 4 || t1 > 2) return CCONV_ERR_UNSUPPORTED;
   const int n = t0 + t1 - 2;
   if (conv_state.cap < n || conv_state.num_slots <= 0 || conv_state.s_slot <= 0 ||
-      conv_state.s_chan <= 0 || conv_state.s_col <= 0)
+      conv_state.s_chan <= 0 || conv_state.s_col <= 0 ||
+      reinterpret_cast<uintptr_t>(conv_state.p) % sesize != 0)
     return CCONV_ERR_INVALID;
   if (!al16(w_gr) || (b_gr && !al16(b_gr))) return CCONV_ERR_INVALID;
   if (Dv % 8 != 0 || !al16(delayed_init) || !al16(delayed_state) ||
@@ -1227,8 +1261,12 @@ static int cca_entry(const void* qk, int64_t qk_row_stride, const void* w_dw, co
   a.pool.num_slots = conv_state.num_slots;
   a.pool.cap = conv_state.cap;
   // channel-first with exactly n columns: a channel chunk's history is n
-  // contiguous 16-byte units; column-first: one unit per column
-  if (n > 0 && conv_state.s_col == 1 && conv_state.s_chan == n && conv_state.cap == n &&
+  // contiguous 16-byte units; column-first: one unit per column; an fp32
+  // pool (and delayed state) element by element, converted
+  a.pool.mixed = conv_state.dtype != CCONV_DTYPE_BF16;
+  if (a.pool.mixed)
+    a.pool.mode = cconv::kPoolGeneric;
+  else if (n > 0 && conv_state.s_col == 1 && conv_state.s_chan == n && conv_state.cap == n &&
       al16(conv_state.p) && conv_state.s_slot % 8 == 0)
     a.pool.mode = cconv::kPoolDS;
   else if (conv_state.s_chan == 1 && al16(conv_state.p) && conv_state.s_col % 8 == 0 &&

@@ -96,23 +96,19 @@ extern "C" int cconv_checkpoint_export(const void* x, int64_t x_row_stride,
   const int esize = dtype == CCONV_DTYPE_F32 ? 4 : 2, V = 16 / esize;
   if (num_ckpt < 0 || num_seqs < 0 || num_tokens < 0 || num_rows < 0) return CCONV_ERR_INVALID;
   if (num_ckpt == 0) return CCONV_OK;
-  if (!x || !conv_states.p || !ckpt_seq || !ckpt_offset || !ckpt_slot || !cu_seqlens)
-    return CCONV_ERR_INVALID;
+  if (!x || !ckpt_seq || !ckpt_offset || !ckpt_slot || !cu_seqlens) return CCONV_ERR_INVALID;
+  if (check_pool(conv_states) != CCONV_OK) return CCONV_ERR_INVALID;
   if (C <= 0 || C % V != 0 || !aligned16(x) || x_row_stride < C || x_row_stride % V != 0)
     return CCONV_ERR_INVALID;
   if (width < 1 || dilation < 1) return CCONV_ERR_INVALID;
   if (width < 2 || width > 4 || dilation > 4) return CCONV_ERR_UNSUPPORTED;
   if (!token_indices && num_rows < num_tokens) return CCONV_ERR_INVALID;
-  if (conv_states.num_slots <= 0 || conv_states.cap <= 0 || conv_states.cap > kMaxCap ||
-      conv_states.s_slot <= 0 ||
-      conv_states.s_chan <= 0 || conv_states.s_col <= 0)
-    return CCONV_ERR_INVALID;
   const int S = (width - 1) * dilation;
   if (conv_states.cap < S) return CCONV_ERR_INVALID;
   CkptArgs a;
   a.x = static_cast<const char*>(x);
   a.x_rs = x_row_stride;
-  a.pool = make_pool(conv_states, esize, V);
+  a.pool = make_pool(conv_states, dtype);
   a.ck_seq = ckpt_seq;
   a.ck_off = ckpt_offset;
   a.ck_slot = ckpt_slot;
@@ -130,7 +126,8 @@ extern "C" int cconv_checkpoint_export(const void* x, int64_t x_row_stride,
   const dim3 grid((unsigned)ctiles, (unsigned)num_ckpt);
   const size_t smem = (size_t)nt * conv_states.cap * 16;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  const cudaError_t e = dtype == CCONV_DTYPE_F32 ? launch_ckpt<float>(S, grid, nt, smem, st, a)
-                                                 : launch_ckpt<__nv_bfloat16>(S, grid, nt, smem, st, a);
+  const cudaError_t e = dtype == CCONV_DTYPE_F32
+                            ? launch_ckpt<float>(S, grid, nt, smem, st, a)
+                            : launch_ckpt<__nv_bfloat16>(S, grid, nt, smem, st, a);
   return e == cudaSuccess ? CCONV_OK : CCONV_ERR_LAUNCH;
 }

@@ -166,7 +166,42 @@ struct Pool {
   int64_t s_slot, s_chan, s_col;   // element strides
   int32_t num_slots, cap;
   int32_t mode;
+  int32_t mixed;   // 1: the pool holds the other storage type than the call
 };
+
+// A pool of the other storage type than the activations ("mixed"): history
+// read from it is converted to the activation type, values written to it are
+// converted to the pool's type (bf16 -> fp32 is exact, fp32 -> bf16 rounds to
+// nearest even). Such pools are always accessed element by element (mode
+// kPoolGeneric); the element size is then the other type's.
+template <typename T>
+__device__ __forceinline__ uint32_t state_to_act(uint32_t sbits) {
+  if constexpr (sizeof(T) == 4)
+    return sbits << 16;                        // bf16 pool, fp32 activations
+  else
+    return f32_to_raw<T>(__uint_as_float(sbits));   // fp32 pool, bf16 activations
+}
+template <typename T>
+__device__ __forceinline__ uint32_t act_to_state(uint32_t abits) {
+  if constexpr (sizeof(T) == 4)
+    return f32_to_raw<__nv_bfloat16>(__uint_as_float(abits));
+  else
+    return abits << 16;
+}
+template <typename T>
+__device__ __forceinline__ int state_bytes(const Pool& P) {
+  return P.mixed ? 6 - Elem<T>::bytes : Elem<T>::bytes;
+}
+__device__ __forceinline__ uint32_t load_bits(const char* p, int bytes) {
+  return bytes == 4 ? *reinterpret_cast<const uint32_t*>(p)
+                    : (uint32_t)*reinterpret_cast<const uint16_t*>(p);
+}
+__device__ __forceinline__ void store_bits(char* p, int bytes, uint32_t bits) {
+  if (bytes == 4)
+    *reinterpret_cast<uint32_t*>(p) = bits;
+  else
+    *reinterpret_cast<uint16_t*>(p) = static_cast<uint16_t>(bits);
+}
 
 // A thread's pool block lives in shared memory as `cap` 16-byte columns,
 // column `col` at blk[col * nt] (threads interleaved so that a column access
@@ -213,15 +248,14 @@ __device__ void pool_load(const Pool& P, int slot, int c0, int ncols, uint4* blk
       }
     }
   } else {
+    const int SE = state_bytes<T>(P);
+    const char* sb = P.p + (int64_t)slot * P.s_slot * SE;
     for (int col = 0; col < ncols; ++col) {
 #pragma unroll
       for (int v = 0; v < V; ++v) {
-        const int64_t off = ((int64_t)(c0 + v) * P.s_chan + (int64_t)col * P.s_col) * E;
-        uint32_t bits;
-        if (E == 4)
-          bits = *reinterpret_cast<const uint32_t*>(base + off);
-        else
-          bits = *reinterpret_cast<const uint16_t*>(base + off);
+        const int64_t off = ((int64_t)(c0 + v) * P.s_chan + (int64_t)col * P.s_col) * SE;
+        uint32_t bits = load_bits(sb + off, SE);
+        if (P.mixed) bits = state_to_act<T>(bits);
         set_elem<T>(blk + col * nt, v, bits);
       }
     }
@@ -257,15 +291,15 @@ __device__ void pool_store(const Pool& P, int slot, int c0, int ncols, const uin
       dst[k] = make_uint4(wd[0], wd[1], wd[2], wd[3]);
     }
   } else {
+    const int SE = state_bytes<T>(P);
+    char* sb = P.p + (int64_t)slot * P.s_slot * SE;
     for (int col = 0; col < ncols; ++col) {
 #pragma unroll
       for (int v = 0; v < V; ++v) {
-        const int64_t off = ((int64_t)(c0 + v) * P.s_chan + (int64_t)col * P.s_col) * E;
-        const uint32_t bits = get_elem<T>(blk + col * nt, v);
-        if (E == 4)
-          *reinterpret_cast<uint32_t*>(base + off) = bits;
-        else
-          *reinterpret_cast<uint16_t*>(base + off) = static_cast<uint16_t>(bits);
+        const int64_t off = ((int64_t)(c0 + v) * P.s_chan + (int64_t)col * P.s_col) * SE;
+        uint32_t bits = get_elem<T>(blk + col * nt, v);
+        if (P.mixed) bits = act_to_state<T>(bits);
+        store_bits(sb + off, SE, bits);
       }
     }
   }

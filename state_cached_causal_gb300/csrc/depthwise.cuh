@@ -373,10 +373,14 @@ __global__ void __launch_bounds__(256) update_kernel(const UpdArgs a) {
             a.pool.p + (elem0 + (int64_t)col * a.pool.s_col + cb) * E + k * 16);
       }
     } else {
+      const int SE = state_bytes<T>(a.pool);
       for (int c = tid; c < nch; c += nt)
-        for (int col = 0; col < cap; ++col)
-          st_s[col * nb + c] = *reinterpret_cast<const R*>(
-              a.pool.p + (elem0 + (int64_t)(cb + c) * a.pool.s_chan + (int64_t)col * a.pool.s_col) * E);
+        for (int col = 0; col < cap; ++col) {
+          const int64_t e = elem0 + (int64_t)(cb + c) * a.pool.s_chan + (int64_t)col * a.pool.s_col;
+          uint32_t bits = load_bits(a.pool.p + e * SE, SE);
+          if (a.pool.mixed) bits = state_to_act<T>(bits);
+          st_s[col * nb + c] = static_cast<R>(bits);
+        }
     }
   }
   {
@@ -480,10 +484,15 @@ __global__ void __launch_bounds__(256) update_kernel(const UpdArgs a) {
                                   k * 16) = reinterpret_cast<const uint4*>(st_s + col * nb)[k];
       }
     } else {
+      const int SE = state_bytes<T>(a.pool);
       for (int c = tid; c < nch; c += nt)
-        for (int col = 0; col < ncols; ++col)
-          *reinterpret_cast<R*>(a.pool.p + (elem0 + (int64_t)(cb + c) * a.pool.s_chan +
-                                            (int64_t)col * a.pool.s_col) * E) = st_s[col * nb + c];
+        for (int col = 0; col < ncols; ++col) {
+          uint32_t bits = st_s[col * nb + c];
+          if (a.pool.mixed) bits = act_to_state<T>(bits);
+          store_bits(a.pool.p + (elem0 + (int64_t)(cb + c) * a.pool.s_chan +
+                                 (int64_t)col * a.pool.s_col) * SE,
+                     SE, bits);
+        }
     }
   }
 }
@@ -492,7 +501,11 @@ __global__ void __launch_bounds__(256) update_kernel(const UpdArgs a) {
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-static int pool_mode(const cconv_pool_t& pv, int esize, int V) {
+// The 16-byte fast paths need a pool of the call's own type; a pool of the
+// other type is read and written element by element, with conversion.
+static int pool_mode(const cconv_pool_t& pv, int dtype) {
+  if (pv.dtype != dtype) return kPoolGeneric;
+  const int esize = dtype == CCONV_DTYPE_F32 ? 4 : 2, V = 16 / esize;
   const bool base_ok = aligned16(pv.p);
   if (pv.s_col == 1 && pv.s_chan == pv.cap && base_ok && (pv.s_slot * esize) % 16 == 0)
     return kPoolDS;
@@ -500,7 +513,7 @@ static int pool_mode(const cconv_pool_t& pv, int esize, int V) {
   return kPoolGeneric;
 }
 
-static Pool make_pool(const cconv_pool_t& pv, int esize, int V) {
+static Pool make_pool(const cconv_pool_t& pv, int dtype) {
   Pool P;
   P.p = static_cast<char*>(pv.p);
   P.s_slot = pv.s_slot;
@@ -508,8 +521,19 @@ static Pool make_pool(const cconv_pool_t& pv, int esize, int V) {
   P.s_col = pv.s_col;
   P.num_slots = pv.num_slots;
   P.cap = pv.cap;
-  P.mode = pool_mode(pv, esize, V);
+  P.mode = pool_mode(pv, dtype);
+  P.mixed = pv.dtype != dtype;
   return P;
+}
+
+// A pool view: its storage type, sizes, strides and element alignment.
+static int check_pool(const cconv_pool_t& pv) {
+  if (pv.dtype != CCONV_DTYPE_F32 && pv.dtype != CCONV_DTYPE_BF16) return CCONV_ERR_INVALID;
+  const int sesize = pv.dtype == CCONV_DTYPE_F32 ? 4 : 2;
+  if (!pv.p || (reinterpret_cast<uintptr_t>(pv.p) % sesize) != 0) return CCONV_ERR_INVALID;
+  if (pv.num_slots <= 0 || pv.cap <= 0 || pv.cap > kMaxCap) return CCONV_ERR_INVALID;
+  if (pv.s_slot <= 0 || pv.s_chan <= 0 || pv.s_col <= 0) return CCONV_ERR_INVALID;
+  return CCONV_OK;
 }
 
 // Threads per block: up to 128 channel units, fewer when the per-thread
@@ -531,7 +555,8 @@ static int check_common(const void* x, int64_t x_rs, const void* w, const cconv_
   if (dtype != CCONV_DTYPE_F32 && dtype != CCONV_DTYPE_BF16) return CCONV_ERR_INVALID;
   *esize = dtype == CCONV_DTYPE_F32 ? 4 : 2;
   *V = 16 / *esize;
-  if (!w || !pv.p || (num_seqs > 0 && !state_idx)) return CCONV_ERR_INVALID;
+  if (!w || (num_seqs > 0 && !state_idx)) return CCONV_ERR_INVALID;
+  if (check_pool(pv) != CCONV_OK) return CCONV_ERR_INVALID;
   if (rows > 0 && (!x || !out)) return CCONV_ERR_INVALID;
   if (C <= 0 || C % *V != 0) return CCONV_ERR_INVALID;
   if (width < 1 || dilation < 1) return CCONV_ERR_INVALID;
@@ -539,8 +564,6 @@ static int check_common(const void* x, int64_t x_rs, const void* w, const cconv_
   if (act != CCONV_ACT_NONE && act != CCONV_ACT_SILU) return CCONV_ERR_INVALID;
   if (!aligned16(x) || !aligned16(out)) return CCONV_ERR_INVALID;
   if (x_rs < C || out_rs < C || x_rs % *V != 0 || out_rs % *V != 0) return CCONV_ERR_INVALID;
-  if (pv.num_slots <= 0 || pv.cap <= 0 || pv.cap > kMaxCap) return CCONV_ERR_INVALID;
-  if (pv.s_slot <= 0 || pv.s_chan <= 0 || pv.s_col <= 0) return CCONV_ERR_INVALID;
   return CCONV_OK;
 }
 
@@ -617,7 +640,7 @@ static int fwd_entry(const void* x, int64_t x_row_stride, const void* w, const v
   a.x_rs = x_row_stride;
   a.w = static_cast<const char*>(w);
   a.bias = static_cast<const char*>(bias);
-  a.pool = make_pool(conv_states, esize, V);
+  a.pool = make_pool(conv_states, dtype);
   a.state_idx = state_idx;
   a.cu = cu_seqlens;
   a.has_init = has_init;
@@ -689,7 +712,7 @@ static int upd_entry(const void* x, int64_t x_row_stride, cconv_pool_t conv_stat
   UpdArgs a;
   a.x = static_cast<const char*>(x);
   a.x_rs = x_row_stride;
-  a.pool = make_pool(conv_states, esize, V);
+  a.pool = make_pool(conv_states, dtype);
   a.w = static_cast<const char*>(w);
   a.bias = static_cast<const char*>(bias);
   a.state_idx = state_idx;

@@ -39,7 +39,8 @@ class Pool(ctypes.Structure):
     """cconv_pool_t: [slot, channel, column] view of a conv-state pool."""
     _fields_ = [("p", ctypes.c_void_p), ("s_slot", ctypes.c_int64),
                 ("s_chan", ctypes.c_int64), ("s_col", ctypes.c_int64),
-                ("num_slots", ctypes.c_int32), ("cap", ctypes.c_int32)]
+                ("num_slots", ctypes.c_int32), ("cap", ctypes.c_int32),
+                ("dtype", ctypes.c_int32)]
 
 
 class CConvError(RuntimeError):
@@ -126,7 +127,12 @@ def _pool(view: torch.Tensor) -> Pool:
         raise ValueError("pool view must be [slot, channel, column]")
     s = view.stride()
     return Pool(ctypes.c_void_p(view.data_ptr()), s[0], s[1], s[2], view.shape[0],
-                view.shape[2])
+                view.shape[2], _dtype_code(view))
+
+
+def _same_state_dtype(conv_state, delayed_state):
+    if delayed_state.dtype != conv_state.dtype:
+        raise TypeError("delayed_state must have the conv-state pool's dtype")
 
 
 def _stream(stream):
@@ -159,7 +165,8 @@ def cconv_fwd_varlen(x, w, bias, conv_states, state_idx, cu_seqlens, has_init, w
     """Varlen causal depthwise conv with state (see cconv_fwd_varlen in cconv.h).
 
     x, out: [T, C]; w: [C, width]; bias: [C] or None; conv_states: [slot, C, cap]
-    view; state_idx/cu_seqlens: int32; has_init: uint8/bool or None.
+    view (fp32 or bf16, whatever x's dtype); state_idx/cu_seqlens: int32;
+    has_init: uint8/bool or None.
     """
     _i32(state_idx, "state_idx")
     _i32(cu_seqlens, "cu_seqlens")
@@ -261,6 +268,7 @@ def cca_qk_conv(qk, w_dw, b_dw, w_gr, b_gr, groups, t0, t1, delayed, delayed_ini
                 conv_state, delayed_state, state_idx, cu_seqlens, has_init, out_qk,
                 out_delayed_prev, dev_err=None, stream=None, num_tokens=None):
     """Zaya CCA two-stage q/k conv + delayed-v shift (see cca_qk_conv in cconv.h)."""
+    _same_state_dtype(conv_state, delayed_state)
     _i32(state_idx, "state_idx")
     _i32(cu_seqlens, "cu_seqlens")
     _u8(has_init, "has_init")
@@ -280,6 +288,7 @@ def cca_qk_conv_fused(qk, w_dw, b_dw, w_gr, b_gr, groups, num_q_heads, t0, t1, d
                       has_init, out, dev_err=None, stream=None, num_tokens=None):
     """cca_qk_conv with ZayaCCA.project's residual mix and value assembly (see
     cca_qk_conv_fused in cconv.h); out: [T, Cqk + 2*Dv] = [query | key | value]."""
+    _same_state_dtype(conv_state, delayed_state)
     _i32(state_idx, "state_idx")
     _i32(cu_seqlens, "cu_seqlens")
     _u8(has_init, "has_init")

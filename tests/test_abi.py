@@ -58,7 +58,7 @@ def test_status_strings(lib):
     for s in (-1, -2, -3):
         assert ops.status_string(s) not in ("ok", "unknown status")
     assert ops.status_string(17) == "unknown status"
-    assert ops.abi_version() == 4
+    assert ops.abi_version() == 5
 
 
 FAKE = 0x10000  # 16-byte aligned, never dereferenced: every call below fails validation
@@ -68,10 +68,10 @@ FAKE = 0x10000  # 16-byte aligned, never dereferenced: every call below fails va
 no_gpu = pytest.mark.skipif(torch.cuda.is_available(), reason="fake pointers: CPU-only")
 
 
-def _pool(num_slots=4, C=16, cap=3, layout="DS"):
+def _pool(num_slots=4, C=16, cap=3, layout="DS", dtype=1, base=FAKE):
     if layout == "DS":
-        return ops.Pool(ctypes.c_void_p(FAKE), C * cap, cap, 1, num_slots, cap)
-    return ops.Pool(ctypes.c_void_p(FAKE), C * cap, 1, C, num_slots, cap)
+        return ops.Pool(ctypes.c_void_p(base), C * cap, cap, 1, num_slots, cap, dtype)
+    return ops.Pool(ctypes.c_void_p(base), C * cap, 1, C, num_slots, cap, dtype)
 
 
 def fwd(lib, **kw):
@@ -101,7 +101,8 @@ def upd(lib, **kw):
     (dict(out=FAKE + 8), -1), (dict(xrs=8), -1), (dict(ors=20), -1), (dict(dt=5), -1),
     (dict(act=7), -1), (dict(W=0), -1), (dict(W=5), -2), (dict(D=5), -2), (dict(D=0), -1),
     (dict(pool=_pool(cap=2)), -1), (dict(B=-1), -1), (dict(T=-1), -1),
-    (dict(pool=_pool(num_slots=0)), -1)])
+    (dict(pool=_pool(num_slots=0)), -1), (dict(pool=_pool(dtype=2)), -1),
+    (dict(pool=_pool(dtype=0, base=FAKE + 2)), -1), (dict(pool=_pool(base=FAKE + 1)), -1)])
 @no_gpu
 def test_fwd_varlen_rejects_bad_arguments(lib, kw, want):
     assert fwd(lib, **kw) == want
@@ -119,6 +120,17 @@ def test_fwd_varlen_empty_batch_is_a_noop(lib):
 @no_gpu
 def test_update_rejects_bad_arguments(lib, kw, want):
     assert upd(lib, **kw) == want
+
+
+@pytest.mark.parametrize("pool_dtype,dt", [(0, 1), (1, 0), (0, 0), (1, 1)])
+@no_gpu
+def test_state_dtype_may_differ_from_the_call(lib, pool_dtype, dt):
+    # every (activation, pool) type pair passes validation (-3: no device);
+    # a bf16 pool needs only 2-byte alignment on the element-wise path
+    assert fwd(lib, dt=dt, pool=_pool(dtype=pool_dtype)) == -3
+    assert upd(lib, dt=dt, pool=_pool(cap=6, dtype=pool_dtype)) == -3
+    if pool_dtype == 1 and dt == 0:
+        assert fwd(lib, dt=dt, pool=_pool(dtype=1, base=FAKE + 2)) == -3
 
 
 @no_gpu
@@ -156,7 +168,8 @@ def test_fwd_fused_checks_its_epilogue(lib, epi, want):
 
 @pytest.mark.parametrize("kw,want", [
     (dict(pool=_pool(cap=65)), -1), (dict(W=5), -2), (dict(num=0), 0), (dict(x=FAKE + 4), -1),
-    (dict(rows=3, idx=None), -1), (dict(), -3)])
+    (dict(rows=3, idx=None), -1), (dict(), -3), (dict(pool=_pool(cap=9, dtype=0)), -3),
+    (dict(pool=_pool(cap=9, dtype=3)), -1)])
 @no_gpu
 def test_checkpoint_export_validation(lib, kw, want):
     a = dict(x=FAKE, pool=_pool(cap=9), num=2, rows=8, idx=FAKE, W=4, D=3)
