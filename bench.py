@@ -60,6 +60,7 @@ def depthwise_calls(name, case, dev_err):
     from state_cached_causal_gb300 import ops
     calls = []
     e, C, W, S = _e(case.w), case.C, case.width, case.meta["S"]
+    es = _e(case.pool)                                # the pool's own storage type
     wbytes = C * W * e + (C * e if case.bias is not None else 0)
     if case.x is not None:
         out = torch.empty_like(case.x)
@@ -68,7 +69,7 @@ def depthwise_calls(name, case, dev_err):
         nread = int((hi * valid).sum())
         nwrite = int(valid.sum())
         T = case.num_tokens
-        nbytes = 2 * T * C * e + wbytes + C * e * S * (nread + nwrite)
+        nbytes = 2 * T * C * e + wbytes + C * es * S * (nread + nwrite)
 
         def f(case=case, out=out):
             ops.cconv_fwd_varlen(case.x, case.w, case.bias, case.pool, case.state_idx,
@@ -81,7 +82,7 @@ def depthwise_calls(name, case, dev_err):
         R = int(case.spec_state_idx.numel())
         q = 1 + case.n_spec
         cols_w = case.meta["cap"] if case.n_spec else S
-        nbytes = 2 * R * q * C * e + wbytes + R * C * e * (S + cols_w)
+        nbytes = 2 * R * q * C * e + wbytes + R * C * es * (S + cols_w)
         na = case.num_accepted if case.n_spec else None
 
         def g(case=case, out=out, na=na):
@@ -151,13 +152,14 @@ def cca_calls(name, cc, dev_err):
     out = torch.empty_like(cc.qk)
     dprev = torch.empty_like(cc.delayed)
     e, T, Cqk, Dv, n = _e(cc.qk), int(cc.qk.shape[0]), cc.Cqk, cc.Dv, cc.meta["n"]
+    es = _e(cc.pool)
     hi = cc.has_init.to(torch.int64).cpu()
     valid = (cc.state_idx.cpu() >= 0).to(torch.int64)
     nread, nwrite = int((hi * valid).sum()), int(valid.sum())
     wbytes = sum(_e(t) * t.numel() for t in (cc.w_dw, cc.b_dw, cc.w_gr, cc.b_gr)
                  if t is not None)
     nbytes = (2 * T * Cqk * e + 2 * T * Dv * e + wbytes + Dv * e
-              + (nread + nwrite) * (n * Cqk * e + Dv * e))
+              + (nread + nwrite) * (n * Cqk * es + Dv * es))
     flops = 2.0 * T * Cqk * (Cqk // cc.groups) * cc.t1 + 2.0 * (T + 1) * Cqk * cc.t0
 
     def f(cc=cc, out=out, dprev=dprev):
@@ -208,6 +210,24 @@ def build_workload(name, dev, dev_err):
                 "(cca_qk_conv) + ple_spec 32x2048 prefill + 512x(1+3) spec x 16384 ch, "
                 "width 4 dilation 3 (cconv_fwd_varlen + cconv_update)")
         return calls, desc
+    if name == "hybrid_step_f32state":
+        # the same step with fp32 conv-state pools (and CCA delayed state) under
+        # the bf16 activations: random fp32 state, so both conversions are live
+        def f32(case, seed):
+            g = torch.Generator(device=dev).manual_seed(seed)
+            case.pool = torch.randn(case.pool.shape, generator=g, device=dev)
+            if hasattr(case, "delayed_state"):
+                case.delayed_state = torch.randn(case.delayed_state.shape, generator=g,
+                                                 device=dev)
+            return case
+        calls = []
+        calls += depthwise_calls("gdn_decode", f32(synth.gdn_decode(dev), 1), dev_err)
+        calls += depthwise_calls("gdn_mixed", f32(synth.gdn_mixed(dev), 2), dev_err)
+        calls += cca_calls("zaya_cca", f32(synth.zaya_cca(dev), 3), dev_err)
+        calls += depthwise_calls("ple_spec", f32(synth.ple_spec(dev), 4), dev_err)
+        return calls, ("hybrid_step_f32state: the hybrid_step batches with fp32 conv-state "
+                       "pools (channel-first) and fp32 CCA delayed state under bf16 "
+                       "activations")
     # small single-kernel cases for profiling (a few GB at most, > L2)
     if name == "ple_prefill_small":
         case = synth.depthwise_case(2001, dev, lens=[2048] * 8, C=16384, width=4, dilation=3,

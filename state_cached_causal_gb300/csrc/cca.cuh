@@ -298,6 +298,28 @@ __device__ __forceinline__ void hist_from_words(const uint32_t (&w)[4 * NH], uin
 template <int NH>
 __device__ __forceinline__ void hist_load_all(const Pool& P, int slot, int c0, uint4 (&h)[NH]) {
   const char* base = P.p + (int64_t)slot * P.s_slot * 2;
+  if (P.mode == cconv::kPoolDSWide) {
+    // fp32 channel-first: channel v, column col at float v * NH + col
+    const uint4* src =
+        reinterpret_cast<const uint4*>(P.p + ((int64_t)slot * P.s_slot + (int64_t)c0 * NH) * 4);
+    uint32_t f[8 * NH];
+#pragma unroll
+    for (int k = 0; k < 2 * NH; ++k) {
+      const uint4 r = src[k];
+      f[4 * k] = r.x;
+      f[4 * k + 1] = r.y;
+      f[4 * k + 2] = r.z;
+      f[4 * k + 3] = r.w;
+    }
+    auto el = [&](int v, int col) {
+      return cconv::state_to_act<__nv_bfloat16>(f[v * NH + col]);
+    };
+#pragma unroll
+    for (int col = 0; col < NH; ++col)
+      h[col] = make_uint4(el(0, col) | (el(1, col) << 16), el(2, col) | (el(3, col) << 16),
+                          el(4, col) | (el(5, col) << 16), el(6, col) | (el(7, col) << 16));
+    return;
+  }
   if (P.mode == cconv::kPoolDS) {
     uint32_t w[4 * NH];
 #pragma unroll
@@ -336,6 +358,22 @@ template <int NH>
 __device__ __forceinline__ void hist_store_all(const Pool& P, int slot, int c0,
                                                const uint4 (&h)[NH]) {
   char* base = P.p + (int64_t)slot * P.s_slot * 2;
+  if (P.mode == cconv::kPoolDSWide) {
+    uint32_t f[8 * NH];   // f[v * NH + col]: channel v, column col, fp32 bits
+#pragma unroll
+    for (int col = 0; col < NH; ++col) {
+      const uint32_t wd[4] = {h[col].x, h[col].y, h[col].z, h[col].w};
+#pragma unroll
+      for (int v = 0; v < 8; ++v)
+        f[v * NH + col] =
+            cconv::act_to_state<__nv_bfloat16>((wd[v >> 1] >> ((v & 1) * 16)) & 0xffffu);
+    }
+    uint4* dst = reinterpret_cast<uint4*>(P.p + ((int64_t)slot * P.s_slot + (int64_t)c0 * NH) * 4);
+#pragma unroll
+    for (int k = 0; k < 2 * NH; ++k)
+      dst[k] = make_uint4(f[4 * k], f[4 * k + 1], f[4 * k + 2], f[4 * k + 3]);
+    return;
+  }
   if (P.mode == cconv::kPoolDS) {
     uint32_t e[8 * NH];   // e[v * NH + col]: channel v, column col
 #pragma unroll
@@ -876,7 +914,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // overwrite them), so a tile of one-token requests waits for one round
       // of loads; otherwise it is loaded when the row is computed.
       constexpr bool kScratch = (T1 == 2) && (NH >= 1) && (NH <= 2);
-      const bool scratch = kScratch && !single && a.pool.mode != cconv::kPoolGeneric;
+      const bool scratch = kScratch && !single &&
+                           (a.pool.mode == cconv::kPoolDS || a.pool.mode == cconv::kPoolSD);
       if (scratch) {
 #pragma unroll 1
         for (int rr = 0; rr < kProdRows; ++rr) {
@@ -1261,11 +1300,15 @@ static int cca_entry(const void* qk, int64_t qk_row_stride, const void* w_dw, co
   a.pool.num_slots = conv_state.num_slots;
   a.pool.cap = conv_state.cap;
   // channel-first with exactly n columns: a channel chunk's history is n
-  // contiguous 16-byte units; column-first: one unit per column; an fp32
-  // pool (and delayed state) element by element, converted
+  // contiguous 16-byte units; column-first: one unit per column. An fp32
+  // pool: 2n units per 8 channels when channel-first with exactly n columns,
+  // else element by element; converted either way (so is the delayed state)
   a.pool.mixed = conv_state.dtype != CCONV_DTYPE_BF16;
   if (a.pool.mixed)
-    a.pool.mode = cconv::kPoolGeneric;
+    a.pool.mode = (n > 0 && conv_state.s_col == 1 && conv_state.s_chan == n &&
+                   conv_state.cap == n && al16(conv_state.p) && conv_state.s_slot % 4 == 0)
+                      ? cconv::kPoolDSWide
+                      : cconv::kPoolGeneric;
   else if (n > 0 && conv_state.s_col == 1 && conv_state.s_chan == n && conv_state.cap == n &&
       al16(conv_state.p) && conv_state.s_slot % 8 == 0)
     a.pool.mode = cconv::kPoolDS;

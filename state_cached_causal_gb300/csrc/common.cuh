@@ -158,7 +158,9 @@ __device__ __forceinline__ void cp_async_wait() {
 enum PoolMode : int32_t {
   kPoolDS = 0,    // s_col == 1 && s_chan == cap: a unit-aligned channel-first slab
   kPoolSD = 1,    // s_chan == 1: one 16-byte unit per column
-  kPoolGeneric = 2
+  kPoolGeneric = 2,
+  kPoolDSWide = 3   // kPoolDS layout, fp32 pool under bf16 activations: a thread's
+                    // 8 channels are 2*cap contiguous 16-byte units
 };
 
 struct Pool {
@@ -172,8 +174,9 @@ struct Pool {
 // A pool of the other storage type than the activations ("mixed"): history
 // read from it is converted to the activation type, values written to it are
 // converted to the pool's type (bf16 -> fp32 is exact, fp32 -> bf16 rounds to
-// nearest even). Such pools are always accessed element by element (mode
-// kPoolGeneric); the element size is then the other type's.
+// nearest even). Such pools are accessed element by element (mode
+// kPoolGeneric, the element size being the other type's), except a dense
+// channel-first fp32 pool under bf16 activations (kPoolDSWide).
 template <typename T>
 __device__ __forceinline__ uint32_t state_to_act(uint32_t sbits) {
   if constexpr (sizeof(T) == 4)
@@ -247,6 +250,22 @@ __device__ void pool_load(const Pool& P, int slot, int c0, int ncols, uint4* blk
         }
       }
     }
+  } else if (sizeof(T) == 2 && P.mode == kPoolDSWide) {
+    const uint4* src =
+        reinterpret_cast<const uint4*>(P.p + ((int64_t)slot * P.s_slot + (int64_t)c0 * P.cap) * 4);
+    int v = 0, col = 0;
+    for (int k = 0; k < 2 * P.cap; ++k) {
+      const uint4 r = src[k];
+      const uint32_t wd[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        set_elem<T>(blk + col * nt, v, state_to_act<T>(wd[t]));
+        if (++col == P.cap) {
+          col = 0;
+          ++v;
+        }
+      }
+    }
   } else {
     const int SE = state_bytes<T>(P);
     const char* sb = P.p + (int64_t)slot * P.s_slot * SE;
@@ -262,7 +281,9 @@ __device__ void pool_load(const Pool& P, int slot, int c0, int ncols, uint4* blk
   }
 }
 
-// Store columns [0, ncols) back (the DS mode rewrites the whole slab).
+// Store columns [0, ncols) back (the DS mode rewrites the whole slab; the
+// DSWide mode too when ncols == cap, else it writes the ncols columns alone,
+// since columns it does not rewrite keep their fp32 bits).
 template <typename T>
 __device__ void pool_store(const Pool& P, int slot, int c0, int ncols, const uint4* blk,
                            int nt) {
@@ -289,6 +310,30 @@ __device__ void pool_store(const Pool& P, int slot, int c0, int ncols, const uin
         }
       }
       dst[k] = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+    }
+  } else if (sizeof(T) == 2 && P.mode == kPoolDSWide) {
+    char* slab = P.p + ((int64_t)slot * P.s_slot + (int64_t)c0 * P.cap) * 4;
+    if (ncols == P.cap) {
+      uint4* dst = reinterpret_cast<uint4*>(slab);
+      int v = 0, col = 0;
+      for (int k = 0; k < 2 * P.cap; ++k) {
+        uint32_t wd[4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          wd[t] = act_to_state<T>(get_elem<T>(blk + col * nt, v));
+          if (++col == P.cap) {
+            col = 0;
+            ++v;
+          }
+        }
+        dst[k] = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+      }
+    } else {
+      for (int col = 0; col < ncols; ++col)
+#pragma unroll
+        for (int v = 0; v < V; ++v)
+          store_bits(slab + ((int64_t)v * P.cap + col) * 4, 4,
+                     act_to_state<T>(get_elem<T>(blk + col * nt, v)));
     }
   } else {
     const int SE = state_bytes<T>(P);

@@ -501,12 +501,20 @@ __global__ void __launch_bounds__(256) update_kernel(const UpdArgs a) {
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// The 16-byte fast paths need a pool of the call's own type; a pool of the
-// other type is read and written element by element, with conversion.
+// The 16-byte fast paths need a pool of the call's own type, or a dense
+// channel-first fp32 pool under bf16 activations; other pools of the other
+// type are read and written element by element, with conversion.
 static int pool_mode(const cconv_pool_t& pv, int dtype) {
-  if (pv.dtype != dtype) return kPoolGeneric;
-  const int esize = dtype == CCONV_DTYPE_F32 ? 4 : 2, V = 16 / esize;
   const bool base_ok = aligned16(pv.p);
+  if (pv.dtype != dtype) {
+    // fp32 state under bf16 activations: the channel-first slab of 8 channels
+    // is 2*cap 16-byte units
+    if (pv.dtype == CCONV_DTYPE_F32 && pv.s_col == 1 && pv.s_chan == pv.cap && base_ok &&
+        (pv.s_slot * 4) % 16 == 0)
+      return kPoolDSWide;
+    return kPoolGeneric;
+  }
+  const int esize = dtype == CCONV_DTYPE_F32 ? 4 : 2, V = 16 / esize;
   if (pv.s_col == 1 && pv.s_chan == pv.cap && base_ok && (pv.s_slot * esize) % 16 == 0)
     return kPoolDS;
   if (pv.s_chan == 1 && base_ok && pv.s_col % V == 0 && pv.s_slot % V == 0) return kPoolSD;
@@ -745,7 +753,7 @@ static int upd_entry(const void* x, int64_t x_row_stride, cconv_pool_t conv_stat
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   // A channel-first pool whose slot slabs start on 16 bytes streams through
   // the bulk-copy pipeline; anything else takes the block-per-request kernel.
-  if (a.pool.mode == kPoolDS) {
+  if (a.pool.mode == kPoolDS || a.pool.mode == kPoolDSWide) {
     const cudaError_t eb = launch_update_bulk(a, width, dilation, dtype, esize, FUSED, st);
     if (eb != cudaErrorNotSupported) return eb == cudaSuccess ? CCONV_OK : CCONV_ERR_LAUNCH;
     a.pool.mode = kPoolGeneric;

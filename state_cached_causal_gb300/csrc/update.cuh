@@ -30,10 +30,14 @@ struct UpdArgs {
 };
 
 // Launches the persistent bulk-copy pipeline for a channel-first pool whose
-// per-slot slabs start on 16 bytes (Pool::mode == kPoolDS). Returns
-// cudaErrorNotSupported when the shapes do not fit it (the caller then uses
-// the block-per-request kernel).
+// per-slot slabs start on 16 bytes (Pool::mode == kPoolDS, or kPoolDSWide for
+// an fp32 pool under bf16 activations). Returns cudaErrorNotSupported when
+// the shapes do not fit it (the caller then uses the block-per-request
+// kernel).
 cudaError_t launch_update_bulk(UpdArgs a, int width, int dilation, int dtype, int esize,
                                bool fused, cudaStream_t st);
+// The kPoolDSWide instantiations (their own translation unit).
+cudaError_t launch_update_bulk_wide(UpdArgs a, int width, int dilation, bool fused,
+                                    cudaStream_t st);
 
 }  // namespace cconv

@@ -1,0 +1,434 @@
+// Decode / speculative decode (cconv_update) over a channel-first conv-state
+// pool [slot, channel, column], as a persistent bulk-copy pipeline (the kernel
+// template; update_bulk.cu and update_bulk_wide.cu instantiate it).
+//
+// Pages: "vllm.model_executor.layers.mamba.ops.cpu.gdn_attention"
+// (_spec_forward: the rolling buffer read at num_accepted - 1 and rewritten
+// as the kept columns followed by the new tokens; _spec_aware_nonspec: the
+// one-token decode) and "Qwen4ExpPLELayer" (_short_conv_dilated_dispatch:
+// the spec branch with dilation).
+//
+// GB300 design. A work item is one request x one tile of up to 512 channels:
+// its slab of the pool (tile channels x cap columns, contiguous in a
+// channel-first pool) and its q token rows. Both move as whole bulk copies
+// (TMA engine, cp.async.bulk) into a 4-deep ring of shared-memory stages, so
+// the loads of the next three items are in flight while eight compute warps
+// work on the current one. The compute warps roll each channel's buffer in
+// place and overwrite the token rows with the outputs; the copy thread then
+// writes the stage back with bulk stores (the new slab and q output rows) and
+// refills it once the stores have read it. Items are split into one
+// contiguous range per CTA, channel-tile-major, so a CTA reloads its weights
+// only when its range crosses into the next channel tile. Every wait is
+// bounded; a timeout sets an error bit, and the copy thread waits for its
+// copies in flight before the CTA exits.
+#pragma once
+
+#include <algorithm>
+#include <mutex>
+#include <type_traits>
+
+#include "async.cuh"
+#include "common.cuh"
+#include "update.cuh"
+
+namespace cconv {
+namespace {
+
+constexpr int kStages = 4;
+constexpr int kComputeThreads = 256;                 // 8 compute warps
+constexpr int kThreads = kComputeThreads + 32;       // + the copy warp
+constexpr int kTileMax = 512;                        // channels per work item
+constexpr int kMinCtasPerSm = 3;
+constexpr size_t kStageBudget = 72 * 1024;           // stages of one CTA
+constexpr long long kWaitCycles = 2000000000LL;      // ~1 s at 2 GHz
+
+enum : int32_t { kSkip = 1, kHist = 2, kOwn = 4, kLoadState = 8 };
+
+struct Meta {
+  int32_t s, ct, off, flags, slot;
+  int32_t prow[kMaxSpec + 1];   // physical row of the request's token r
+};
+
+struct Ctl {
+  uint64_t full[kStages];   // copy thread's arrival + the stage's load bytes
+  uint64_t done[kStages];   // every compute thread, after its last write
+  Meta meta[kStages];
+  volatile int abort;
+};
+constexpr int kCtlBytes = (sizeof(Ctl) + 127) / 128 * 128;
+
+struct BulkArgs {
+  int32_t tile;          // channels per work item (multiple of 8)
+  int32_t stage_bytes;   // bytes per stage (multiple of 128)
+  int32_t xs_off;        // byte offset of the token rows within a stage
+  int32_t rs_off;        // fused: byte offset of the residual rows
+  int32_t os_off;        // fused: byte offset of the outer residual rows
+  int64_t items;         // B * ctiles
+};
+
+__device__ bool wait_bounded(Ctl* ctl, uint64_t* bar, uint32_t parity, int32_t* dev_err) {
+  const long long t0 = clock64();
+  for (uint32_t it = 0;; ++it) {
+    if (mbar_try(bar, parity)) return true;
+    if ((it & 63u) == 63u) {
+      if (ctl->abort) return false;
+      if (clock64() - t0 > kWaitCycles) {
+        ctl->abort = 1;
+        flag_error(dev_err, CCONV_DERR_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
+// Request metadata of one item, validated: a slot beyond the pool, a
+// num_accepted outside [1, q] or (fused) a token row outside the physical rows
+// flags the error and skips the item.
+template <bool FUSED>
+__device__ Meta item_meta(const UpdArgs& a, int64_t item, int S) {
+  Meta m;
+  m.s = (int32_t)(item % a.B);
+  m.ct = (int32_t)(item / a.B);
+  m.off = 0;
+  m.flags = 0;
+  const int slot = a.state_idx[m.s];
+  m.slot = slot;
+  if (slot >= a.pool.num_slots) {
+    flag_error(a.dev_err, CCONV_DERR_SLOT_RANGE);
+    m.flags = kSkip;
+    return m;
+  }
+  if (a.n_spec > 0) {
+    m.off = a.num_accepted[m.s] - 1;
+    if (m.off < 0 || m.off > a.n_spec) {
+      flag_error(a.dev_err, CCONV_DERR_NUM_ACCEPTED);
+      m.flags = kSkip;
+      return m;
+    }
+  }
+  if (FUSED) {
+    const int q = 1 + a.n_spec;
+    for (int r = 0; r < q; ++r) {
+      const int64_t li = (int64_t)m.s * q + r;
+      const int p = a.tidx ? a.tidx[li] : (int)li;
+      if (p < 0 || p >= a.num_rows) {
+        flag_error(a.dev_err, CCONV_DERR_ROW_INDEX);
+        m.flags = kSkip;
+        return m;
+      }
+      m.prow[r] = p;
+    }
+  }
+  const bool hs = slot >= 0 && (a.has_init == nullptr || a.has_init[m.s] != 0);
+  if (hs) m.flags |= kHist;
+  if (slot >= 0) {
+    m.flags |= kOwn;
+    // Without history every column the call writes is recomputed; columns it
+    // leaves alone (decode of a wider buffer) must come back unchanged.
+    const int ncols = a.n_spec > 0 ? a.pool.cap : S;
+    if (hs || ncols < a.pool.cap) m.flags |= kLoadState;
+  }
+  return m;
+}
+
+// State elements of type TS as raw activation bits of type T, and back (the
+// identity for one type; see state_to_act / act_to_state).
+template <typename T, typename TS>
+__device__ __forceinline__ uint32_t bulk_in(uint32_t sbits) {
+  if constexpr (std::is_same<T, TS>::value)
+    return sbits;
+  else
+    return state_to_act<T>(sbits);
+}
+template <typename T, typename TS>
+__device__ __forceinline__ uint32_t bulk_out(uint32_t abits) {
+  if constexpr (std::is_same<T, TS>::value)
+    return abits;
+  else
+    return act_to_state<T>(abits);
+}
+
+// T: activations; TS: the pool (T, or fp32 under bf16 activations). A stage
+// holds the slab in the pool's own type, so columns the call leaves alone go
+// back with their bits.
+template <typename T, typename TS, int W, int D, bool FUSED>
+__global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
+    update_bulk_kernel(const UpdArgs a, const BulkArgs b) {
+  constexpr int S = (W - 1) * D;
+  constexpr int E = Elem<T>::bytes, ES = Elem<TS>::bytes, QM = kMaxSpec + 1;
+  using R = typename std::conditional<E == 4, uint32_t, uint16_t>::type;    // raw element
+  using RS = typename std::conditional<ES == 4, uint32_t, uint16_t>::type;  // raw state element
+  extern __shared__ __align__(128) unsigned char bsm[];
+  Ctl* ctl = reinterpret_cast<Ctl*>(bsm);
+  unsigned char* stage0 = bsm + kCtlBytes;
+  const int tid = threadIdx.x;
+  const int64_t i0 = (int64_t)blockIdx.x * b.items / gridDim.x;
+  const int n = (int)((int64_t)(blockIdx.x + 1) * b.items / gridDim.x - i0);
+  const int q = 1 + a.n_spec, cap = a.pool.cap;
+  const int tile = b.tile;
+
+  if (tid == 0) {
+    for (int k = 0; k < kStages; ++k) {
+      mbar_init(&ctl->full[k], 1);
+      mbar_init(&ctl->done[k], kComputeThreads);
+    }
+    ctl->abort = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (tid >= kComputeThreads) {
+    // ---- copy thread: bulk loads ahead, bulk stores behind -------------
+    if (tid != kComputeThreads) return;
+    auto issue_load = [&](int j, const Meta& m) {
+      const int st = j % kStages;
+      unsigned char* sb = stage0 + (size_t)st * b.stage_bytes;
+      ctl->meta[st] = m;
+      if (m.flags & kSkip) {
+        mbar_arrive(&ctl->full[st]);
+        return;
+      }
+      const int cb = m.ct * tile, nch = min(tile, a.C - cb);
+      const uint32_t row_bytes = (uint32_t)nch * E;
+      const uint32_t slab_bytes = (uint32_t)nch * cap * ES;
+      const int rows_per_token = FUSED ? (a.outer ? 3 : 2) : 1;
+      mbar_arrive_tx(&ctl->full[st], q * rows_per_token * row_bytes +
+                                         ((m.flags & kLoadState) ? slab_bytes : 0u));
+      for (int r = 0; r < q; ++r) {
+        const int64_t p = FUSED ? (int64_t)m.prow[r] : (int64_t)m.s * q + r;
+        bulk_load(sb + b.xs_off + (size_t)r * tile * E, a.x + (p * a.x_rs + cb) * E, row_bytes,
+                  &ctl->full[st]);
+        if (FUSED) {
+          bulk_load(sb + b.rs_off + (size_t)r * tile * E, a.out + (p * a.out_rs + cb) * E,
+                    row_bytes, &ctl->full[st]);
+          if (a.outer)
+            bulk_load(sb + b.os_off + (size_t)r * tile * E, a.outer + (p * a.outer_rs + cb) * E,
+                      row_bytes, &ctl->full[st]);
+        }
+      }
+      if (m.flags & kLoadState)
+        bulk_load(sb, a.pool.p + ((int64_t)m.slot * a.pool.s_slot + (int64_t)cb * cap) * ES,
+                  slab_bytes, &ctl->full[st]);
+    };
+    int issued = 0;
+    for (; issued < min(n, kStages); ++issued)
+      issue_load(issued, item_meta<FUSED>(a, i0 + issued, S));
+    Meta next{};
+    if (issued < n) next = item_meta<FUSED>(a, i0 + issued, S);   // one item ahead
+    int j = 0;
+    for (; j < n; ++j) {
+      const int st = j % kStages;
+      if (!wait_bounded(ctl, &ctl->done[st], (uint32_t)(j / kStages) & 1u, a.dev_err)) break;
+      const Meta m = ctl->meta[st];
+      if (!(m.flags & kSkip)) {
+        unsigned char* sb = stage0 + (size_t)st * b.stage_bytes;
+        const int cb = m.ct * tile, nch = min(tile, a.C - cb);
+        const uint32_t row_bytes = (uint32_t)nch * E;
+        for (int r = 0; r < q; ++r)
+          bulk_store(a.out + ((FUSED ? (int64_t)m.prow[r] : (int64_t)m.s * q + r) * a.out_rs +
+                              cb) * E,
+                     sb + b.xs_off + (size_t)r * tile * E, row_bytes);
+        if (m.flags & kOwn) {
+          bulk_store(a.pool.p + ((int64_t)m.slot * a.pool.s_slot + (int64_t)cb * cap) * ES, sb,
+                     (uint32_t)nch * cap * ES);
+        }
+      }
+      bulk_commit();
+      if (issued < n) {
+        bulk_wait_read<0>();   // the stage's stores have read it
+        issue_load(issued, next);
+        ++issued;
+        if (issued < n) next = item_meta<FUSED>(a, i0 + issued, S);
+      }
+    }
+    if (j < n) {
+      // aborting: wait for the loads still in flight into this CTA's stages
+      for (int k = j; k < issued; ++k) {
+        const long long t0 = clock64();
+        while (!mbar_try(&ctl->full[k % kStages], (uint32_t)(k / kStages) & 1u))
+          if (clock64() - t0 > kWaitCycles) break;
+      }
+    }
+    bulk_wait<0>();
+    return;
+  }
+
+  // ---- compute warps: two channels per thread ---------------------------
+  const bool silu_on = a.act == CCONV_ACT_SILU;
+  const int ncols = a.n_spec > 0 ? cap : S;
+  const int keep = ncols - q;   // spec: kept columns B[off+1, off+1+keep), keep >= S-1
+  float wk[2][W], bv[2];
+  int cur_ct = -1;
+  for (int j = 0; j < n; ++j) {
+    const int st = j % kStages;
+    if (!wait_bounded(ctl, &ctl->full[st], (uint32_t)(j / kStages) & 1u, a.dev_err)) break;
+    const Meta m = ctl->meta[st];
+    if (!(m.flags & kSkip)) {
+      const int cb = m.ct * tile, nch = min(tile, a.C - cb);
+      if (m.ct != cur_ct) {
+        cur_ct = m.ct;
+#pragma unroll
+        for (int kc = 0; kc < 2; ++kc) {
+          const int c = min(tid + kc * kComputeThreads, nch - 1);
+#pragma unroll
+          for (int k = 0; k < W; ++k) wk[kc][k] = load_f32<T>(a.w, (int64_t)(cb + c) * W + k);
+          bv[kc] = a.bias ? load_f32<T>(a.bias, cb + c) : 0.0f;
+        }
+      }
+      unsigned char* sb = stage0 + (size_t)st * b.stage_bytes;
+      RS* slab = reinterpret_cast<RS*>(sb);
+      R* xs = reinterpret_cast<R*>(sb + b.xs_off);
+      const R* rs = reinterpret_cast<const R*>(sb + b.rs_off);
+      const R* os = reinterpret_cast<const R*>(sb + b.os_off);
+      const bool has_outer = a.outer != nullptr;
+      const bool hs = m.flags & kHist, own = m.flags & kOwn;
+#pragma unroll
+      for (int kc = 0; kc < 2; ++kc) {
+        const int c = tid + kc * kComputeThreads;
+        if (c >= nch) break;
+        RS* row = slab + c * cap;
+        float pr[S];
+        R pb[S];   // the prior window in the activation type
+#pragma unroll
+        for (int i = 0; i < S; ++i) {
+          pb[i] = hs ? static_cast<R>(bulk_in<T, TS>(row[m.off + i])) : R(0);
+          pr[i] = raw_to_f32<T>(pb[i]);
+        }
+        R xb[QM];
+        float xf[QM];
+#pragma unroll
+        for (int u = 0; u < QM; ++u) {
+          xb[u] = u < q ? xs[u * tile + c] : R(0);
+          xf[u] = raw_to_f32<T>(xb[u]);
+        }
+#pragma unroll
+        for (int i = 0; i < QM; ++i) {
+          if (i < q) {
+            float acc = bv[kc];
+#pragma unroll
+            for (int k = 0; k < W; ++k) {
+              const int idx = S + i - (W - 1 - k) * D;   // position in prior ++ tokens
+              acc = fmaf(wk[kc][k], idx >= S ? xf[idx - S] : pr[idx], acc);
+            }
+            float y = silu_on ? silu<T>(acc) : acc;
+            if constexpr (FUSED) {
+              y = raw_to_f32<T>(rs[i * tile + c]) + y;
+              if (has_outer) y = y + raw_to_f32<T>(os[i * tile + c]);
+            }
+            xs[i * tile + c] = f32_to_raw<T>(y);
+          }
+        }
+        if (own) {
+          // B[off+1+col] for col < S-1 is pb[col+1]; wider buffers keep more
+          // columns, each read ahead of every write
+#pragma unroll
+          for (int col = 0; col + 1 < S; ++col)
+            row[col] = static_cast<RS>(bulk_out<T, TS>(pb[col + 1]));
+          if (a.n_spec == 0) {
+            row[S - 1] = static_cast<RS>(bulk_out<T, TS>(xb[0]));
+          } else {
+            for (int col = S - 1; col < keep; ++col)
+              row[col] = hs ? static_cast<RS>(
+                                  bulk_out<T, TS>(bulk_in<T, TS>(row[m.off + 1 + col])))
+                            : RS(0);
+#pragma unroll
+            for (int u = 0; u < QM; ++u)
+              if (u < q) row[keep + u] = static_cast<RS>(bulk_out<T, TS>(xb[u]));
+          }
+        }
+      }
+      fence_proxy_async();   // the bulk stores read what this thread wrote
+    }
+    mbar_arrive(&ctl->done[st]);
+  }
+}
+
+// Per instantiation and device: the shared-memory opt-in (once) and the CTAs
+// per SM for the last stage size asked for.
+struct LaunchCache {
+  std::mutex mu;
+  uint64_t attr_set = 0;   // bit per device
+  int dev = -1;
+  size_t smem = 0;
+  int per_sm = 0;
+};
+
+template <typename T, typename TS, int W, int D, bool FUSED>
+cudaError_t launch_t(const UpdArgs& a, const BulkArgs& b, size_t smem, cudaStream_t st, int dev,
+                     int num_sms) {
+  auto k = update_bulk_kernel<T, TS, W, D, FUSED>;
+  static LaunchCache cache;
+  int per_sm = 0;
+  {
+    std::lock_guard<std::mutex> g(cache.mu);
+    if (dev < 64 && !((cache.attr_set >> dev) & 1u)) {
+      const cudaError_t e = cudaFuncSetAttribute(
+          k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)(kCtlBytes + kStageBudget));
+      if (e != cudaSuccess) return e;
+      cache.attr_set |= 1ull << dev;
+    }
+    if (cache.dev != dev || cache.smem != smem) {
+      const cudaError_t e =
+          cudaOccupancyMaxActiveBlocksPerMultiprocessor(&cache.per_sm, k, kThreads, smem);
+      if (e != cudaSuccess) return e;
+      cache.dev = dev;
+      cache.smem = smem;
+    }
+    per_sm = std::max(1, cache.per_sm);
+  }
+  const int64_t grid = std::min<int64_t>(b.items, (int64_t)per_sm * num_sms);
+  k<<<(unsigned)grid, kThreads, smem, st>>>(a, b);
+  return cudaGetLastError();
+}
+
+template <typename T, typename TS, bool FUSED>
+cudaError_t launch_wd(int W, int D, const UpdArgs& a, const BulkArgs& b, size_t smem,
+                      cudaStream_t st, int dev, int num_sms) {
+#define CCONV_BULK_CASE(w_, d_) \
+  if (W == w_ && D == d_) return launch_t<T, TS, w_, d_, FUSED>(a, b, smem, st, dev, num_sms);
+  CCONV_BULK_CASE(2, 1) CCONV_BULK_CASE(2, 2) CCONV_BULK_CASE(2, 3) CCONV_BULK_CASE(2, 4)
+  CCONV_BULK_CASE(3, 1) CCONV_BULK_CASE(3, 2) CCONV_BULK_CASE(3, 3) CCONV_BULK_CASE(3, 4)
+  CCONV_BULK_CASE(4, 1) CCONV_BULK_CASE(4, 2) CCONV_BULK_CASE(4, 3) CCONV_BULK_CASE(4, 4)
+#undef CCONV_BULK_CASE
+  return cudaErrorInvalidValue;
+}
+
+// Tile choice and launch for activations T over a pool of TS.
+template <typename T, typename TS>
+cudaError_t launch_bulk_types(UpdArgs a, int width, int dilation, bool fused, cudaStream_t st) {
+  const int q = 1 + a.n_spec, cap = a.pool.cap;
+  constexpr int esize = Elem<T>::bytes, sesize = Elem<TS>::bytes;
+  const int V = 16 / esize;
+  const int row_sets = fused ? 3 : 1;   // token rows (+ residual and outer rows)
+  // Largest channel tile (a multiple of 8 channels, so every row and slab is
+  // a multiple of 16 bytes) whose stages fit the budget.
+  int tile = kTileMax;
+  auto rows_bytes = [&](int t) { return ((size_t)q * t * esize + 127) / 128 * 128; };
+  auto stage_bytes = [&](int t) {
+    const size_t slab = ((size_t)t * cap * sesize + 127) / 128 * 128;
+    return slab + row_sets * rows_bytes(t);
+  };
+  while (tile > 8 && stage_bytes(tile) * kStages > kStageBudget) tile /= 2;
+  if (stage_bytes(tile) * kStages > kStageBudget || tile % V != 0) return cudaErrorNotSupported;
+  tile = std::min(tile, (a.C + 7) / 8 * 8);
+  BulkArgs b;
+  b.tile = tile;
+  b.stage_bytes = (int32_t)stage_bytes(tile);
+  b.xs_off = (int32_t)(((size_t)tile * cap * sesize + 127) / 128 * 128);
+  b.rs_off = b.xs_off + (int32_t)rows_bytes(tile);
+  b.os_off = b.rs_off + (int32_t)rows_bytes(tile);
+  a.ctiles = (a.C + tile - 1) / tile;
+  b.items = (int64_t)a.B * a.ctiles;
+  if (b.items <= 0) return cudaSuccess;
+  int dev = 0, num_sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 64) return cudaErrorNotSupported;
+  const size_t smem = kCtlBytes + (size_t)kStages * b.stage_bytes;
+  return fused ? launch_wd<T, TS, true>(width, dilation, a, b, smem, st, dev, num_sms)
+               : launch_wd<T, TS, false>(width, dilation, a, b, smem, st, dev, num_sms);
+}
+
+}  // namespace
+}  // namespace cconv

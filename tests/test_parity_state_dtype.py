@@ -70,6 +70,21 @@ def test_update_state_type(act, sd, layout, n_spec):
 
 
 @pytest.mark.parametrize("act,sd", MIX)
+def test_decode_on_a_widened_pool_keeps_the_other_columns(act, sd):
+    # one-token decodes on a channel-first pool with spare columns: columns
+    # >= S are not rewritten and keep their bits (an fp32 pool under bf16
+    # activations goes through the bulk-copy pipeline with fp32 stages)
+    W, D, S = 4, 1, 3
+    case = synth.depthwise_case(1325, DEV, lens=[], C=_C(act), width=W, dilation=D, act=1,
+                                dtype=act, w_std=0.5, bias_std=0.1, spec_requests=300,
+                                n_spec=0, cap=S + 5)
+    case.spec_has_init = torch.ones(300, dtype=torch.uint8, device=DEV)
+    case.spec_has_init[::4] = 0
+    case.pool = other_pool(case.pool.shape, sd, "DS", 1326)
+    check_upd(case)
+
+
+@pytest.mark.parametrize("act,sd", MIX)
 def test_fused_fwd_state_type(act, sd):
     W, D = 4, 3
     lens = [1, 1, 0, 2, 9, 10, 64, 65, 129, 200, 7]
