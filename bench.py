@@ -240,6 +240,14 @@ def build_workload(name, dev, dev_err):
                                     spec_requests=512, n_spec=3)
         return depthwise_calls("ple_spec_small", case, dev_err), \
             "ple spec 512x(1+3) tok x 16384 ch"
+    if name == "ple_spec_small_f32state":
+        case = synth.depthwise_case(2002, dev, lens=[], C=16384, width=4, dilation=3, act=1,
+                                    dtype=torch.bfloat16, w_std=0.1, num_slots=1024,
+                                    spec_requests=512, n_spec=3)
+        g = torch.Generator(device=dev).manual_seed(2005)
+        case.pool = torch.randn(case.pool.shape, generator=g, device=dev)
+        return depthwise_calls("ple_spec_small_f32state", case, dev_err), \
+            "ple spec 512x(1+3) tok x 16384 ch, fp32 conv-state pool under bf16 activations"
     if name == "gdn_mixed":
         return depthwise_calls("gdn_mixed", synth.gdn_mixed(dev), dev_err), "gdn_mixed"
     if name == "gdn_decode":

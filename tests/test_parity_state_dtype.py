@@ -146,11 +146,12 @@ def test_fused_update_state_type(act, sd, n_spec):
 
 @pytest.mark.parametrize("act,sd", MIX)
 @pytest.mark.parametrize("layout", ["DS", "SD"])
-def test_checkpoint_export_state_type(act, sd, layout):
+@pytest.mark.parametrize("spare", [0, 3])
+def test_checkpoint_export_state_type(act, sd, layout, spare):
     W, D, S = 4, 3, 9
     lens = [3 * S + 5, S, 2 * S, 200]
     case = synth.depthwise_case(1360, DEV, lens=lens, C=_C(act), width=W, dilation=D, act=1,
-                                dtype=act, w_std=0.5, num_slots=40)
+                                dtype=act, w_std=0.5, num_slots=40, cap=S + spare)
     case.pool = other_pool(case.pool.shape, sd, layout, 1361)
     T = case.num_tokens
     ck_seq = torch.tensor([0, 0, 1, 2, 3, 3], dtype=torch.int32, device=DEV)
