@@ -446,6 +446,34 @@ static __device__ int tile_edge(const Args& a, const int32_t* cu, int tau, int f
 
 // ---- the kernel ----------------------------------------------------------------
 
+// Unit u -> (group g, token tile tau). The plain kernel walks the units
+// group-major (one group's B operand for many tiles). The fused kernel's
+// residuals read other groups' rows of the same tokens (a query head the key
+// rows of its kv head, a key head the rows of its kvg query heads), so it
+// walks each kv group in blocks of kFusedTileBlock tiles, the kvg query heads
+// and then the key head taking the block's tiles one after another: the rows
+// their residuals read were loaded a few units earlier and are still in L2.
+constexpr int kFusedTileBlock = 8;
+template <bool FUSED>
+__device__ __forceinline__ void unit_to_gt(const Args& a, int u, int& g, int& tau) {
+  if (!FUSED) {
+    g = u / a.num_tiles;
+    tau = u - g * a.num_tiles;
+    return;
+  }
+  const int m5 = a.kvg + 1, per = m5 * a.num_tiles;
+  const int j = u / per, r = u - j * per;
+  const int tb = r / (m5 * kFusedTileBlock);
+  const int t0 = tb * kFusedTileBlock;
+  const int nt = min(kFusedTileBlock, a.num_tiles - t0);
+  const int rr = r - tb * m5 * kFusedTileBlock;
+  const int m = rr / nt;
+  tau = t0 + (rr - m * nt);
+  g = m < a.kvg ? j * a.kvg + m : a.Hq + j;
+}
+
+
+
 // Work counters of the dynamic part of the split, one slot per launch in
 // flight (a launch takes slot epoch % kEpochs; its last CTA clears it).
 constexpr int kEpochs = 64;
@@ -454,43 +482,77 @@ constexpr int kStaticPercent = 90;           // share of the units split statica
 static __device__ unsigned int g_work_next[kEpochs];
 static __device__ unsigned int g_work_done[kEpochs];
 
-// The tail of ZayaCCA.project for 8 channels (cc .. cc+7 of head g, token t)
-// of the conv output `conv`, in the module's bf16 as the page's torch code
+// The tail of ZayaCCA.project, in the module's bf16 as the page's torch code
 // computes it: a query head h adds 0.5 * bf16(q_h + k_{h/kvg}); a key head j
-// adds bf16(mean over its kv group of those); each sum is rounded to bf16.
-__device__ __forceinline__ uint4 add_residual(const Args& a, int t, int g, int cc, uint4 conv) {
-  const char* row = a.qk + (int64_t)t * a.qk_rs * 2;
+// adds bf16(mean over its kv group of those). residual4 gathers, for channels
+// cc .. cc+7 of head g and the four tokens t[k] (ok[k]: a stored row), the
+// rounded term before the halving for a query head (bf16(q + k), exact in
+// bf16) and the key residual itself for a key head, as packed bf16 -- all loads
+// of a step in flight together, ahead of the accumulator; add_residual then
+// adds it to a conv output.
+__device__ __forceinline__ void residual4(const Args& a, const int64_t (&t)[4],
+                                          const bool (&ok)[4], int g, int cc, uint4 (&res)[4]) {
   const int qdim = a.Hq * kGS;
-  float cv[8], res[8];
-  cconv::unpack16<__nv_bfloat16>(conv, cv);
-  auto qres = [&](int h, const float (&kf)[8], float (&r)[8]) {
-    float qf[8];
-    cconv::unpack16<__nv_bfloat16>(cconv::ldg16(row + ((int64_t)h * kGS + cc) * 2), qf);
-#pragma unroll
-    for (int e = 0; e < 8; ++e) r[e] = 0.5f * __bfloat162float(__float2bfloat16_rn(qf[e] + kf[e]));
-  };
+  auto row = [&](int k) { return a.qk + t[k] * a.qk_rs * 2; };
+  const uint4 z = make_uint4(0u, 0u, 0u, 0u);
   if (g < a.Hq) {
-    float kf[8];
-    cconv::unpack16<__nv_bfloat16>(
-        cconv::ldg16(row + ((int64_t)qdim + (g / a.kvg) * kGS + cc) * 2), kf);
-    qres(g, kf, res);
-  } else {
-    const int j = g - a.Hq;
-    float kf[8], sum[8], r[8];
-    cconv::unpack16<__nv_bfloat16>(cconv::ldg16(row + ((int64_t)qdim + j * kGS + cc) * 2), kf);
+    uint4 qv[4], kv[4];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) sum[e] = 0.0f;
-    for (int gg = 0; gg < a.kvg; ++gg) {
-      qres(j * a.kvg + gg, kf, r);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) sum[e] += r[e];
+    for (int k = 0; k < 4; ++k) {
+      qv[k] = ok[k] ? cconv::ldg16(row(k) + ((int64_t)g * kGS + cc) * 2) : z;
+      kv[k] = ok[k] ? cconv::ldg16(row(k) + ((int64_t)qdim + (g / a.kvg) * kGS + cc) * 2) : z;
     }
 #pragma unroll
-    for (int e = 0; e < 8; ++e)
-      res[e] = __bfloat162float(__float2bfloat16_rn(sum[e] / (float)a.kvg));
+    for (int k = 0; k < 4; ++k) {
+      float qf[8], kf[8];
+      cconv::unpack16<__nv_bfloat16>(qv[k], qf);
+      cconv::unpack16<__nv_bfloat16>(kv[k], kf);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) qf[e] += kf[e];
+      res[k] = cconv::pack16<__nv_bfloat16>(qf);   // bf16(q + k)
+    }
+    return;
+  }
+  const int j = g - a.Hq;
+  uint4 kv[4];
+  float sum[4][8];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    kv[k] = ok[k] ? cconv::ldg16(row(k) + ((int64_t)qdim + j * kGS + cc) * 2) : z;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) sum[k][e] = 0.0f;
+  }
+#pragma unroll 1
+  for (int gg = 0; gg < a.kvg; ++gg) {
+    uint4 qv[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      qv[k] = ok[k] ? cconv::ldg16(row(k) + ((int64_t)(j * a.kvg + gg) * kGS + cc) * 2) : z;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      float qf[8], kf[8];
+      cconv::unpack16<__nv_bfloat16>(qv[k], qf);
+      cconv::unpack16<__nv_bfloat16>(kv[k], kf);
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+        sum[k][e] += 0.5f * __bfloat162float(__float2bfloat16_rn(qf[e] + kf[e]));
+    }
   }
 #pragma unroll
-  for (int e = 0; e < 8; ++e) cv[e] = cv[e] + res[e];
+  for (int k = 0; k < 4; ++k) {
+    float m[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) m[e] = sum[k][e] / (float)a.kvg;
+    res[k] = cconv::pack16<__nv_bfloat16>(m);      // bf16(mean)
+  }
+}
+
+__device__ __forceinline__ uint4 add_residual(bool query, const uint4& pre, const uint4& conv) {
+  float cv[8], rf[8];
+  cconv::unpack16<__nv_bfloat16>(conv, cv);
+  cconv::unpack16<__nv_bfloat16>(pre, rf);
+#pragma unroll
+  for (int e = 0; e < 8; ++e) cv[e] = cv[e] + (query ? 0.5f * rf[e] : rf[e]);
   return cconv::pack16<__nv_bfloat16>(cv);
 }
 
@@ -593,7 +655,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       const int u = cur++;
-      const int g = u / a.num_tiles, tau = u - g * a.num_tiles;
+      int g, tau;
+      unit_to_gt<FUSED>(a, u, g, tau);
       const bool cont = (g == prev_g && tau == prev_tau + 1);
       const int lo = cont ? hi_prev : tile_edge(a, cu, tau, 0);
       const int own_lo = cont ? own_hi_prev : count_le(cu, a.B, lo, true, 0);
@@ -740,6 +803,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                                      half * kEpiCols + k)
                           : 0.0f;
 
+      // FUSED: this lane's residual terms (rows q*32 + k*8 + lane/4, channel
+      // chunks c), gathered while the tile's MMA runs
+      uint4 resid[kEpiCols / 32][4];
+      if constexpr (FUSED) {
+        int64_t tt[4];
+        bool okr[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int tr = q * 32 + k * 8 + (lane >> 2);
+          okr[k] = tr < len && M.rowj[tr] >= 0;
+          tt[k] = lo + tr;
+        }
+#pragma unroll
+        for (int c = 0; c < kEpiCols / 32; ++c)
+          residual4(a, tt, okr, g, half * kEpiCols + c * 32 + (lane & 3) * 8, resid[c]);
+      }
+
       // q/k outputs: TMEM -> +bias -> bf16 -> shared-memory transpose -> global,
       // 32 columns at a time (the next 32 columns' TMEM load in flight), so that
       // a store instruction covers 8 rows x 64 contiguous bytes.
@@ -775,7 +855,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint4 v = *reinterpret_cast<const uint4*>(stage + rr * kOutRowPitch + seg * 16);
           if (tr < len && M.rowj[tr] >= 0) {
             const int cc = half * kEpiCols + c * 32 + seg * 8;   // channel within the head
-            if constexpr (FUSED) v = add_residual(a, lo + tr, g, cc, v);
+            if constexpr (FUSED) v = add_residual(g < a.Hq, resid[c][k], v);
             cconv::stg16(a.out + ((int64_t)(lo + tr) * a.out_rs + (int64_t)g * kGS + cc) * 2, v);
           }
         }
