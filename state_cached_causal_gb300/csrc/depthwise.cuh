@@ -497,6 +497,116 @@ __global__ void __launch_bounds__(256) update_kernel(const UpdArgs a) {
   }
 }
 
+// One-token decodes (n_spec == 0) on a dense channel-first pool of the call's
+// type with exactly S columns (weights and biases 16-byte aligned, as their
+// W and 1 units per thread are vector loads): a thread takes one request x one 16-byte
+// channel unit, reads the unit's S history units (contiguous: channel v's
+// columns are elements v*S .. v*S+S-1) and its token in one round trip, and
+// writes the output and the shifted state. No staging and no pipeline: a
+// decode batch is one short wave.
+template <typename T, int W, int D>
+__global__ void __launch_bounds__(256) decode_kernel(const UpdArgs a) {
+  constexpr int S = (W - 1) * D, V = Elem<T>::V, E = Elem<T>::bytes;
+  constexpr int NW = S * 4;                            // 32-bit words of the slab
+  const int units = a.C / V;
+  const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (gid >= (int64_t)a.B * units) return;
+  const int s = (int)(gid / units), u = (int)(gid - (int64_t)s * units), c0 = u * V;
+  // every load that does not need the slot is issued before its use: the
+  // metadata, the token, the unit's W x V weights (W units) and biases
+  const int slot = a.state_idx[s];
+  const bool hi = a.has_init == nullptr || a.has_init[s] != 0;
+  const uint4 xr = ldg16(a.x + ((int64_t)s * a.x_rs + c0) * E);
+  uint32_t ww[W * 4];
+#pragma unroll
+  for (int k = 0; k < W; ++k) {
+    const uint4 r = ldg16(a.w + ((int64_t)c0 * W + k * V) * E);
+    ww[4 * k] = r.x;
+    ww[4 * k + 1] = r.y;
+    ww[4 * k + 2] = r.z;
+    ww[4 * k + 3] = r.w;
+  }
+  const uint4 br = a.bias ? ldg16(a.bias + (int64_t)c0 * E) : make_uint4(0u, 0u, 0u, 0u);
+  const uint32_t bw[4] = {br.x, br.y, br.z, br.w};
+  if (slot >= a.pool.num_slots) {
+    if (u == 0) flag_error(a.dev_err, CCONV_DERR_SLOT_RANGE);
+    return;
+  }
+  const bool hs = slot >= 0 && hi;
+  uint4* slab = reinterpret_cast<uint4*>(
+      a.pool.p + ((int64_t)(slot >= 0 ? slot : 0) * a.pool.s_slot + (int64_t)c0 * S) * E);
+  uint32_t wd[NW];
+#pragma unroll
+  for (int k = 0; k < S; ++k) {
+    const uint4 r = hs ? slab[k] : make_uint4(0u, 0u, 0u, 0u);
+    wd[4 * k] = r.x;
+    wd[4 * k + 1] = r.y;
+    wd[4 * k + 2] = r.z;
+    wd[4 * k + 3] = r.w;
+  }
+  const uint32_t xw[4] = {xr.x, xr.y, xr.z, xr.w};
+  // raw element i of the slab / element v of the token / element i of the
+  // unit's weights (channel c0 + i / W, tap i % W) and biases
+  auto hel = [&](int i) -> uint32_t {
+    if constexpr (E == 4)
+      return wd[i];
+    else
+      return (wd[i >> 1] >> ((i & 1) * 16)) & 0xffffu;
+  };
+  auto xel = [&](int v) -> uint32_t {
+    if constexpr (E == 4)
+      return xw[v];
+    else
+      return (xw[v >> 1] >> ((v & 1) * 16)) & 0xffffu;
+  };
+  auto wel = [&](int i) -> uint32_t {
+    if constexpr (E == 4)
+      return ww[i];
+    else
+      return (ww[i >> 1] >> ((i & 1) * 16)) & 0xffffu;
+  };
+  auto bel = [&](int v) -> uint32_t {
+    if constexpr (E == 4)
+      return bw[v];
+    else
+      return (bw[v >> 1] >> ((v & 1) * 16)) & 0xffffu;
+  };
+  const bool silu_on = a.act == CCONV_ACT_SILU;
+  float y[V];
+#pragma unroll
+  for (int v = 0; v < V; ++v) {
+    float acc = raw_to_f32<T>(bel(v));
+#pragma unroll
+    for (int k = 0; k < W; ++k) {
+      const int idx = S - (W - 1 - k) * D;             // position in history ++ token
+      const uint32_t b = idx >= S ? xel(v) : hel(v * S + idx);
+      acc = fmaf(raw_to_f32<T>(wel(v * W + k)), raw_to_f32<T>(b), acc);
+    }
+    y[v] = silu_on ? silu<T>(acc) : acc;
+  }
+  stg16(a.out + ((int64_t)s * a.out_rs + c0) * E, pack16<T>(y));
+  if (slot < 0) return;
+  // new state: columns 0 .. S-2 are the old 1 .. S-1, column S-1 the token
+  uint32_t nw[NW];
+#pragma unroll
+  for (int i = 0; i < NW; ++i) nw[i] = 0u;
+#pragma unroll
+  for (int v = 0; v < V; ++v) {
+#pragma unroll
+    for (int col = 0; col < S; ++col) {
+      const int i = v * S + col;
+      const uint32_t b = col + 1 < S ? hel(i + 1) : xel(v);
+      if constexpr (E == 4)
+        nw[i] = b;
+      else
+        nw[i >> 1] |= b << ((i & 1) * 16);
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < S; ++k)
+    slab[k] = make_uint4(nw[4 * k], nw[4 * k + 1], nw[4 * k + 2], nw[4 * k + 3]);
+}
+
 // ---- host side -----------------------------------------------------------
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -602,6 +712,21 @@ static cudaError_t launch_upd(int W, int D, dim3 grid, int nt, size_t smem,
   CCONV_UPD_CASE(3, 1) CCONV_UPD_CASE(3, 2) CCONV_UPD_CASE(3, 3) CCONV_UPD_CASE(3, 4)
   CCONV_UPD_CASE(4, 1) CCONV_UPD_CASE(4, 2) CCONV_UPD_CASE(4, 3) CCONV_UPD_CASE(4, 4)
 #undef CCONV_UPD_CASE
+  return cudaErrorInvalidValue;
+}
+
+template <typename T>
+static cudaError_t launch_dec(int W, int D, dim3 grid, int nt, cudaStream_t st,
+                             const UpdArgs& a) {
+#define CCONV_DEC_CASE(w_, d_)                                              \
+  if (W == w_ && D == d_) {                                                 \
+    decode_kernel<T, w_, d_><<<grid, nt, 0, st>>>(a);                       \
+    return cudaGetLastError();                                              \
+  }
+  CCONV_DEC_CASE(2, 1) CCONV_DEC_CASE(2, 2) CCONV_DEC_CASE(2, 3) CCONV_DEC_CASE(2, 4)
+  CCONV_DEC_CASE(3, 1) CCONV_DEC_CASE(3, 2) CCONV_DEC_CASE(3, 3) CCONV_DEC_CASE(3, 4)
+  CCONV_DEC_CASE(4, 1) CCONV_DEC_CASE(4, 2) CCONV_DEC_CASE(4, 3) CCONV_DEC_CASE(4, 4)
+#undef CCONV_DEC_CASE
   return cudaErrorInvalidValue;
 }
 
@@ -751,10 +876,24 @@ static int upd_entry(const void* x, int64_t x_row_stride, cconv_pool_t conv_stat
   if (nblk > 0x7fffffff) return CCONV_ERR_INVALID;
   const size_t smem = smem_for(nt);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  // A channel-first pool whose slot slabs start on 16 bytes streams through
-  // the bulk-copy pipeline; anything else takes the block-per-request kernel.
+  // One-token decodes on a dense channel-first pool of exactly S columns take
+  // the one-pass decode kernel; other channel-first pools whose slot slabs
+  // start on 16 bytes stream through the bulk-copy pipeline; anything else
+  // takes the block-per-request kernel.
+  if (!FUSED && n_spec == 0 && a.pool.mode == kPoolDS && conv_states.cap == S &&
+      aligned16(w) && (!bias || aligned16(bias))) {
+    const int units = C / V;
+    const int64_t blocks = ((int64_t)num_seqs * units + 255) / 256;
+    if (blocks <= 0x7fffffff) {
+      const cudaError_t ed =
+          dtype == CCONV_DTYPE_F32
+              ? launch_dec<float>(width, dilation, dim3((unsigned)blocks), 256, st, a)
+              : launch_dec<__nv_bfloat16>(width, dilation, dim3((unsigned)blocks), 256, st, a);
+      return ed == cudaSuccess ? CCONV_OK : CCONV_ERR_LAUNCH;
+    }
+  }
   if (a.pool.mode == kPoolDS || a.pool.mode == kPoolDSWide) {
-    const cudaError_t eb = launch_update_bulk(a, width, dilation, dtype, esize, FUSED, st);
+    const cudaError_t eb = launch_update_bulk(a, width, dilation, dtype, FUSED, st);
     if (eb != cudaErrorNotSupported) return eb == cudaSuccess ? CCONV_OK : CCONV_ERR_LAUNCH;
     a.pool.mode = kPoolGeneric;
   }

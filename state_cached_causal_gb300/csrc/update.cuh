@@ -34,8 +34,8 @@ struct UpdArgs {
 // an fp32 pool under bf16 activations). Returns cudaErrorNotSupported when
 // the shapes do not fit it (the caller then uses the block-per-request
 // kernel).
-cudaError_t launch_update_bulk(UpdArgs a, int width, int dilation, int dtype, int esize,
-                               bool fused, cudaStream_t st);
+cudaError_t launch_update_bulk(UpdArgs a, int width, int dilation, int dtype, bool fused,
+                               cudaStream_t st);
 // The kPoolDSWide instantiations (their own translation unit).
 cudaError_t launch_update_bulk_wide(UpdArgs a, int width, int dilation, bool fused,
                                     cudaStream_t st);

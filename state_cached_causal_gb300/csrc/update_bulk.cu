@@ -3,9 +3,8 @@
 
 namespace cconv {
 
-cudaError_t launch_update_bulk(UpdArgs a, int width, int dilation, int dtype, int esize,
-                               bool fused, cudaStream_t st) {
-  (void)esize;
+cudaError_t launch_update_bulk(UpdArgs a, int width, int dilation, int dtype, bool fused,
+                               cudaStream_t st) {
   if (a.pool.mode == kPoolDSWide)
     return launch_update_bulk_wide(a, width, dilation, fused, st);
   return dtype == CCONV_DTYPE_F32
