@@ -503,6 +503,13 @@ def dist_env():
     return ws, rank, local
 
 
+def whole_job_value(ws, units_per_step, steps, elapsed):
+    """Replicas: every rank runs the whole step on its own GPU (weak scaling), so
+    the job processed ws * units_per_step * steps units in the slowest rank's
+    time; in G(tokens*channels)/s."""
+    return ws * units_per_step * steps / elapsed / 1e9
+
+
 def reduce_max(value, ws):
     if ws <= 1:
         return value
@@ -593,7 +600,7 @@ def arm_ours(args):
     if int(dev_err.item()) != 0:
         raise SystemExit(f"device error flag {int(dev_err.item())} in the timed region")
 
-    value = ws * units_per_step * args.steps / elapsed / 1e9
+    value = whole_job_value(ws, units_per_step, args.steps, elapsed)
     hbm_peak, bf16_peak, peak_src = measured_peaks()
     dom = max(calls, key=lambda c: per_call[c.name])
     t_dom = per_call[dom.name]
