@@ -243,6 +243,49 @@ def test_bad_slot_sets_flag_and_skips_only_that_sequence():
     assert_out_close(got[cu[2]:cu[3]], want_out[cu[2]:cu[3]], torch.bfloat16)
 
 
+def test_decode_bad_slot_sets_flag_and_skips_only_that_request():
+    # one-token decodes on a dense channel-first pool of S columns (the one-pass
+    # decode kernel): the bad request's output row and every slot stay as they were
+    case = synth.depthwise_case(306, DEV, lens=[], C=1040, width=4, dilation=1, act=1,
+                                dtype=torch.bfloat16, w_std=0.5, bias_std=0.1, num_slots=12,
+                                spec_requests=5, n_spec=0)
+    case.spec_state_idx[2] = 12                # == num_slots
+    err = new_err()
+    pool = case.pool.clone()
+    out = torch.full_like(case.x_spec, 3.0)
+    ops.cconv_update(case.x_spec, pool, case.w, case.bias, case.spec_state_idx, 0, None, None,
+                     4, 1, 1, out, dev_err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & ops.DERR_SLOT_RANGE
+    assert bool((out[2] == 3.0).all())
+    keep = [0, 1, 3, 4]
+    x = to_np(case.x_spec)[keep]
+    ref_pool = pool_np(case.pool.clone())
+    ref_out = np.zeros_like(x)
+    oracle.cconv_update(x, ref_pool, to_np(case.w), to_np(case.bias),
+                        to_np(case.spec_state_idx)[keep], 0, None, None, 4, 1, 1, ref_out)
+    assert_out_close(to_np(out)[keep], ref_out, torch.bfloat16)
+    assert_bits_equal(pool_np(pool), ref_pool)
+
+
+@pytest.mark.parametrize("what", ["w", "bias"])
+def test_decode_with_unaligned_weights(what):
+    # weights or biases that do not start on 16 bytes cannot take the decode
+    # kernel's vector loads; the call still computes the same result
+    case = synth.depthwise_case(307, DEV, lens=[], C=1040, width=4, dilation=1, act=1,
+                                dtype=torch.bfloat16, w_std=0.5, bias_std=0.1,
+                                spec_requests=9, n_spec=0)
+    if what == "w":
+        buf = torch.zeros(case.w.numel() + 1, dtype=case.w.dtype, device=DEV)
+        buf[1:] = case.w.reshape(-1)
+        case.w = buf[1:].view(case.w.shape)
+    else:
+        buf = torch.zeros(case.bias.numel() + 3, dtype=case.bias.dtype, device=DEV)
+        buf[3:] = case.bias
+        case.bias = buf[3:]
+    check_upd(case)
+
+
 def test_bad_cu_seqlens_sets_flag():
     case = synth.depthwise_case(306, DEV, lens=[4, 5, 6], C=256, width=4, dilation=1, act=1,
                                 dtype=torch.bfloat16, w_std=0.5)
