@@ -1,8 +1,8 @@
 """GPU parity: cconv_fwd_varlen / cconv_update (through the C ABI) vs the oracle.
 
 State write-back is compared bit for bit; outputs within max|err| <= 1e-5
-(fp32) or |err| <= 2e-2 + 2e-2*|ref| (bf16), the tolerance of the north-star
-contract, element by element on the same seeded inputs.
+(fp32) or |err| <= 2e-2 + 2e-2*|ref| (bf16), element by element on the same
+seeded inputs.
 """
 import numpy as np
 import pytest
