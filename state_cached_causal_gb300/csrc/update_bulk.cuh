@@ -11,9 +11,10 @@
 // GB300 design. A work item is one request x one tile of up to 512 channels:
 // its slab of the pool (tile channels x cap columns, contiguous in a
 // channel-first pool) and its q token rows. Both move as whole bulk copies
-// (TMA engine, cp.async.bulk) into a 4-deep ring of shared-memory stages, so
-// the loads of the next three items are in flight while eight compute warps
-// work on the current one. The compute warps roll each channel's buffer in
+// (TMA engine, cp.async.bulk) into a 4-deep ring of shared-memory stages (3
+// for the fused entry point, whose stages also carry residual and outer rows),
+// so the loads of the next items are in flight while eight compute warps work
+// on the current one. The compute warps roll each channel's buffer in
 // place and overwrite the token rows with the outputs; the copy thread then
 // writes the stage back with bulk stores (the new slab and q output rows) and
 // refills it once the stores have read it. Items are split into one
@@ -34,7 +35,11 @@
 namespace cconv {
 namespace {
 
-constexpr int kStages = 4;
+constexpr int kStages = 4;                           // ring depth (plain), Ctl extent
+constexpr int kStagesFused = 3;                      // fused: 3 stages of a 512-channel tile
+                                                     // beat 4 of a 256-channel one
+template <bool FUSED>
+constexpr int stages_of() { return FUSED ? kStagesFused : kStages; }
 constexpr int kComputeThreads = 256;                 // 8 compute warps
 constexpr int kThreads = kComputeThreads + 32;       // + the copy warp
 constexpr int kTileMax = 512;                        // channels per work item
@@ -154,6 +159,7 @@ __device__ __forceinline__ uint32_t bulk_out(uint32_t abits) {
 template <typename T, typename TS, int W, int D, bool FUSED>
 __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
     update_bulk_kernel(const UpdArgs a, const BulkArgs b) {
+  constexpr int NS = stages_of<FUSED>();
   constexpr int S = (W - 1) * D;
   constexpr int E = Elem<T>::bytes, ES = Elem<TS>::bytes, QM = kMaxSpec + 1;
   using R = typename std::conditional<E == 4, uint32_t, uint16_t>::type;    // raw element
@@ -168,7 +174,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
   const int tile = b.tile;
 
   if (tid == 0) {
-    for (int k = 0; k < kStages; ++k) {
+    for (int k = 0; k < NS; ++k) {
       mbar_init(&ctl->full[k], 1);
       mbar_init(&ctl->done[k], kComputeThreads);
     }
@@ -181,7 +187,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
     // ---- copy thread: bulk loads ahead, bulk stores behind -------------
     if (tid != kComputeThreads) return;
     auto issue_load = [&](int j, const Meta& m) {
-      const int st = j % kStages;
+      const int st = j % NS;
       unsigned char* sb = stage0 + (size_t)st * b.stage_bytes;
       ctl->meta[st] = m;
       if (m.flags & kSkip) {
@@ -211,14 +217,14 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
                   slab_bytes, &ctl->full[st]);
     };
     int issued = 0;
-    for (; issued < min(n, kStages); ++issued)
+    for (; issued < min(n, NS); ++issued)
       issue_load(issued, item_meta<FUSED>(a, i0 + issued, S));
     Meta next{};
     if (issued < n) next = item_meta<FUSED>(a, i0 + issued, S);   // one item ahead
     int j = 0;
     for (; j < n; ++j) {
-      const int st = j % kStages;
-      if (!wait_bounded(ctl, &ctl->done[st], (uint32_t)(j / kStages) & 1u, a.dev_err)) break;
+      const int st = j % NS;
+      if (!wait_bounded(ctl, &ctl->done[st], (uint32_t)(j / NS) & 1u, a.dev_err)) break;
       const Meta m = ctl->meta[st];
       if (!(m.flags & kSkip)) {
         unsigned char* sb = stage0 + (size_t)st * b.stage_bytes;
@@ -245,7 +251,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
       // aborting: wait for the loads still in flight into this CTA's stages
       for (int k = j; k < issued; ++k) {
         const long long t0 = clock64();
-        while (!mbar_try(&ctl->full[k % kStages], (uint32_t)(k / kStages) & 1u))
+        while (!mbar_try(&ctl->full[k % NS], (uint32_t)(k / NS) & 1u))
           if (clock64() - t0 > kWaitCycles) break;
       }
     }
@@ -260,8 +266,8 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
   float wk[2][W], bv[2];
   int cur_ct = -1;
   for (int j = 0; j < n; ++j) {
-    const int st = j % kStages;
-    if (!wait_bounded(ctl, &ctl->full[st], (uint32_t)(j / kStages) & 1u, a.dev_err)) break;
+    const int st = j % NS;
+    if (!wait_bounded(ctl, &ctl->full[st], (uint32_t)(j / NS) & 1u, a.dev_err)) break;
     const Meta m = ctl->meta[st];
     if (!(m.flags & kSkip)) {
       const int cb = m.ct * tile, nch = min(tile, a.C - cb);
@@ -408,8 +414,9 @@ cudaError_t launch_bulk_types(UpdArgs a, int width, int dilation, bool fused, cu
     const size_t slab = ((size_t)t * cap * sesize + 127) / 128 * 128;
     return slab + row_sets * rows_bytes(t);
   };
-  while (tile > 8 && stage_bytes(tile) * kStages > kStageBudget) tile /= 2;
-  if (stage_bytes(tile) * kStages > kStageBudget || tile % V != 0) return cudaErrorNotSupported;
+  const int ns = fused ? kStagesFused : kStages;
+  while (tile > 8 && stage_bytes(tile) * ns > kStageBudget) tile /= 2;
+  if (stage_bytes(tile) * ns > kStageBudget || tile % V != 0) return cudaErrorNotSupported;
   tile = std::min(tile, (a.C + 7) / 8 * 8);
   BulkArgs b;
   b.tile = tile;
@@ -425,7 +432,7 @@ cudaError_t launch_bulk_types(UpdArgs a, int width, int dilation, bool fused, cu
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
   if (dev >= 64) return cudaErrorNotSupported;
-  const size_t smem = kCtlBytes + (size_t)kStages * b.stage_bytes;
+  const size_t smem = kCtlBytes + (size_t)ns * b.stage_bytes;
   return fused ? launch_wd<T, TS, true>(width, dilation, a, b, smem, st, dev, num_sms)
                : launch_wd<T, TS, false>(width, dilation, a, b, smem, st, dev, num_sms);
 }
