@@ -38,6 +38,7 @@ sys.path.insert(0, ROOT)
 METRIC = ("causal-conv G(tokens·channels)/s and achieved HBM GB/s vs GB300 peak, 1 GPU")
 UNIT = "G(tokens*channels)/s"
 FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 7900.0    # GB300 HBM3e data-sheet bandwidth (context beside the measured peak)
 
 
 # ---- workloads ---------------------------------------------------------------
@@ -614,7 +615,8 @@ def arm_ours(args):
     for c in calls:
         t = per_call[c.name]
         d = {"ms": t * 1e3, "Gtokch_per_s": c.units / t / 1e9, "GB_per_s": c.bytes / t / 1e9,
-             "hbm_frac": c.bytes / t / 1e9 / hbm_peak, "bytes": c.bytes}
+             "hbm_frac": c.bytes / t / 1e9 / hbm_peak,
+             "hbm_frac_of_nominal": c.bytes / t / 1e9 / NOMINAL_HBM_GBS, "bytes": c.bytes}
         if c.flops:
             d["TFLOP_per_s"] = c.flops / t / 1e12
             d["tensor_frac_of_bf16_peak"] = c.flops / t / 1e12 / bf16_peak
