@@ -155,13 +155,16 @@ __device__ __forceinline__ uint32_t bulk_out(uint32_t abits) {
 
 // T: activations; TS: the pool (T, or fp32 under bf16 activations). A stage
 // holds the slab in the pool's own type, so columns the call leaves alone go
-// back with their bits.
-template <typename T, typename TS, int W, int D, bool FUSED>
+// back with their bits. QM bounds the tokens per request (q <= QM): the
+// per-channel token loops are unrolled to QM, so a fused call with q <= 4 takes
+// the QM = 4 instantiation instead of predicating away half of an 8-token loop.
+template <typename T, typename TS, int W, int D, bool FUSED, int QM>
 __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
     update_bulk_kernel(const UpdArgs a, const BulkArgs b) {
   constexpr int NS = stages_of<FUSED>();
   constexpr int S = (W - 1) * D;
-  constexpr int E = Elem<T>::bytes, ES = Elem<TS>::bytes, QM = kMaxSpec + 1;
+  constexpr int E = Elem<T>::bytes, ES = Elem<TS>::bytes;
+  static_assert(QM >= 1 && QM <= kMaxSpec + 1, "tokens per request");
   using R = typename std::conditional<E == 4, uint32_t, uint16_t>::type;    // raw element
   using RS = typename std::conditional<ES == 4, uint32_t, uint16_t>::type;  // raw state element
   extern __shared__ __align__(128) unsigned char bsm[];
@@ -359,10 +362,10 @@ struct LaunchCache {
   int per_sm = 0;
 };
 
-template <typename T, typename TS, int W, int D, bool FUSED>
+template <typename T, typename TS, int W, int D, bool FUSED, int QM>
 cudaError_t launch_t(const UpdArgs& a, const BulkArgs& b, size_t smem, cudaStream_t st, int dev,
                      int num_sms) {
-  auto k = update_bulk_kernel<T, TS, W, D, FUSED>;
+  auto k = update_bulk_kernel<T, TS, W, D, FUSED, QM>;
   static LaunchCache cache;
   int per_sm = 0;
   {
@@ -390,8 +393,14 @@ cudaError_t launch_t(const UpdArgs& a, const BulkArgs& b, size_t smem, cudaStrea
 template <typename T, typename TS, bool FUSED>
 cudaError_t launch_wd(int W, int D, const UpdArgs& a, const BulkArgs& b, size_t smem,
                       cudaStream_t st, int dev, int num_sms) {
-#define CCONV_BULK_CASE(w_, d_) \
-  if (W == w_ && D == d_) return launch_t<T, TS, w_, d_, FUSED>(a, b, smem, st, dev, num_sms);
+  // fused bf16 calls of at most 4 tokens per request take the QM = 4 kernels
+  // (measured faster there; the plain path keeps one instantiation per shape)
+  constexpr int kQ4 = (FUSED && sizeof(T) == 2) ? 4 : kMaxSpec + 1;
+  const bool q4 = kQ4 == 4 && 1 + a.n_spec <= 4;
+#define CCONV_BULK_CASE(w_, d_)                                                         \
+  if (W == w_ && D == d_)                                                               \
+    return q4 ? launch_t<T, TS, w_, d_, FUSED, kQ4>(a, b, smem, st, dev, num_sms)       \
+              : launch_t<T, TS, w_, d_, FUSED, kMaxSpec + 1>(a, b, smem, st, dev, num_sms);
   CCONV_BULK_CASE(2, 1) CCONV_BULK_CASE(2, 2) CCONV_BULK_CASE(2, 3) CCONV_BULK_CASE(2, 4)
   CCONV_BULK_CASE(3, 1) CCONV_BULK_CASE(3, 2) CCONV_BULK_CASE(3, 3) CCONV_BULK_CASE(3, 4)
   CCONV_BULK_CASE(4, 1) CCONV_BULK_CASE(4, 2) CCONV_BULK_CASE(4, 3) CCONV_BULK_CASE(4, 4)
