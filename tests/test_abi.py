@@ -179,3 +179,47 @@ def test_checkpoint_export_validation(lib, kw, want):
                                      a["num"], P(FAKE), 2, 8, P(a["idx"]), a["rows"], 16,
                                      a["W"], a["D"], 1, None, None)
     assert rc == want
+
+
+def cca(lib, fused=False, **kw):
+    # Zaya shapes: 16 q + 4 kv heads of 128 (20 groups), Dv = 256, history n = 2
+    a = dict(qk=FAKE, qrs=2560, w_dw=FAKE, b_dw=None, w_gr=FAKE, b_gr=None, G=20, Hq=16, t0=2,
+             t1=2, dl=FAKE, drs=256, dinit=FAKE, Dv=256, vc=FAKE, vcrs=256,
+             pool=_pool(C=2560, cap=2), ds=FAKE, dsrs=256, sidx=FAKE, cu=FAKE, hi=None, B=2,
+             T=8, C=2560, dt=1, out=FAKE, ors=2560 + 512, dp=FAKE, dprs=256)
+    a.update(kw)
+    P = lambda v: None if v is None else ctypes.c_void_p(v)
+    if fused:
+        return lib.cca_qk_conv_fused(P(a["qk"]), a["qrs"], P(a["w_dw"]), P(a["b_dw"]),
+                                     P(a["w_gr"]), P(a["b_gr"]), a["G"], a["Hq"], a["t0"],
+                                     a["t1"], P(a["dl"]), a["drs"], P(a["dinit"]), a["Dv"],
+                                     P(a["vc"]), a["vcrs"], a["pool"], P(a["ds"]), a["dsrs"],
+                                     P(a["sidx"]), P(a["cu"]), P(a["hi"]), a["B"], a["T"],
+                                     a["C"], a["dt"], P(a["out"]), a["ors"], None, None)
+    return lib.cca_qk_conv(P(a["qk"]), a["qrs"], P(a["w_dw"]), P(a["b_dw"]), P(a["w_gr"]),
+                           P(a["b_gr"]), a["G"], a["t0"], a["t1"], P(a["dl"]), a["drs"],
+                           P(a["dinit"]), a["Dv"], a["pool"], P(a["ds"]), a["dsrs"],
+                           P(a["sidx"]), P(a["cu"]), P(a["hi"]), a["B"], a["T"], a["C"], a["dt"],
+                           P(a["out"]), 2560, P(a["dp"]), a["dprs"], None, None)
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(), -3), (dict(dt=0), -2), (dict(dt=5), -1), (dict(w_gr=None), -1),
+    (dict(C=2570), -1), (dict(C=2500), -2), (dict(G=40), -2), (dict(t0=5), -2), (dict(t1=3), -2), (dict(t0=0), -1),
+    (dict(pool=_pool(C=2560, cap=1)), -1), (dict(pool=_pool(C=2560, cap=2, dtype=4)), -1),
+    (dict(pool=_pool(C=2560, cap=2, dtype=0)), -3), (dict(ds=FAKE + 8), -1),
+    (dict(dsrs=100), -1), (dict(Dv=250), -1), (dict(qk=FAKE + 2), -1), (dict(qrs=2500), -1),
+    (dict(B=0), 0), (dict(T=-1), -1)])
+@no_gpu
+def test_cca_validation(lib, kw, want):
+    assert cca(lib, **kw) == want
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(), -3), (dict(Hq=15), -1), (dict(Hq=20), -1), (dict(Dv=128, dsrs=128, drs=128), -1),
+    (dict(vc=None), -1), (dict(vc=FAKE + 4), -1), (dict(vcrs=200), -1), (dict(ors=2560), -1)])
+@no_gpu
+def test_cca_fused_validation(lib, kw, want):
+    # the fused form also checks the head split (Hq q heads over groups - Hq kv
+    # heads, Dv = kv heads * 64), v_current and the [query | key | value] rows
+    assert cca(lib, fused=True, **kw) == want
