@@ -47,44 +47,48 @@ def build(force: bool = False) -> str:
     return _LIB_PATH
 
 
+def _configure(lib):
+    """Declare the C signatures on a loaded oracle library."""
+    P, I64, I32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32
+    lib.oracle_cconv_fwd_varlen.argtypes = [
+        P, I64, P, P, P, I64, I64, I64, I32, I32, I32, P, P, P, I32, I32, I32, I32,
+        I32, I32, P, I64]
+    lib.oracle_cconv_fwd_varlen.restype = ctypes.c_int
+    lib.oracle_cconv_update.argtypes = [
+        P, I64, P, I64, I64, I64, I32, I32, I32, P, P, P, I32, I32, P, P, I32, I32,
+        I32, I32, I32, P, I64]
+    lib.oracle_cconv_update.restype = ctypes.c_int
+    lib.oracle_cca_qk_conv.argtypes = [
+        P, I64, P, P, P, P, I32, I32, I32, P, I64, P, I32, P, I64, I64, I64,
+        I32, I32, I32, P, I64, P, P, P, I32, I32, I32, P, I64, P, I64]
+    lib.oracle_cca_qk_conv.restype = ctypes.c_int
+    lib.oracle_cconv_fwd_varlen_fused.argtypes = [
+        P, I64, P, P, P, I64, I64, I64, I32, I32, I32, P, P, P, I32, I32, I32, I32,
+        I32, I32, P, I32, P, I64, P, I64]
+    lib.oracle_cconv_fwd_varlen_fused.restype = ctypes.c_int
+    lib.oracle_cconv_update_fused.argtypes = [
+        P, I64, P, I64, I64, I64, I32, I32, I32, P, P, P, I32, I32, P, P, I32, I32,
+        I32, I32, I32, P, I32, P, I64, P, I64]
+    lib.oracle_cconv_update_fused.restype = ctypes.c_int
+    lib.oracle_cconv_checkpoint_export.argtypes = [
+        P, I64, P, I64, I64, I64, I32, I32, I32, P, P, P, I32, P, I32, P, I32, I32, I32,
+        I32, I32]
+    lib.oracle_cconv_checkpoint_export.restype = ctypes.c_int
+    lib.oracle_cca_project_epilogue.argtypes = [
+        P, I64, P, I64, P, I64, P, I64, I32, I32, I32, I32, I32, P, I64]
+    lib.oracle_cca_project_epilogue.restype = ctypes.c_int
+    lib.oracle_f32_to_bf16.argtypes = [ctypes.c_float]
+    lib.oracle_f32_to_bf16.restype = ctypes.c_uint16
+    lib.oracle_bf16_to_f32.argtypes = [ctypes.c_uint16]
+    lib.oracle_bf16_to_f32.restype = ctypes.c_float
+    return lib
+
+
 def _load():
     global _lib
     with _lock:
         if _lib is None:
-            lib = ctypes.CDLL(build())
-            P, I64, I32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32
-            lib.oracle_cconv_fwd_varlen.argtypes = [
-                P, I64, P, P, P, I64, I64, I64, I32, I32, I32, P, P, P, I32, I32, I32, I32,
-                I32, I32, P, I64]
-            lib.oracle_cconv_fwd_varlen.restype = ctypes.c_int
-            lib.oracle_cconv_update.argtypes = [
-                P, I64, P, I64, I64, I64, I32, I32, I32, P, P, P, I32, I32, P, P, I32, I32,
-                I32, I32, I32, P, I64]
-            lib.oracle_cconv_update.restype = ctypes.c_int
-            lib.oracle_cca_qk_conv.argtypes = [
-                P, I64, P, P, P, P, I32, I32, I32, P, I64, P, I32, P, I64, I64, I64,
-                I32, I32, I32, P, I64, P, P, P, I32, I32, I32, P, I64, P, I64]
-            lib.oracle_cca_qk_conv.restype = ctypes.c_int
-            lib.oracle_cconv_fwd_varlen_fused.argtypes = [
-                P, I64, P, P, P, I64, I64, I64, I32, I32, I32, P, P, P, I32, I32, I32, I32,
-                I32, I32, P, I32, P, I64, P, I64]
-            lib.oracle_cconv_fwd_varlen_fused.restype = ctypes.c_int
-            lib.oracle_cconv_update_fused.argtypes = [
-                P, I64, P, I64, I64, I64, I32, I32, I32, P, P, P, I32, I32, P, P, I32, I32,
-                I32, I32, I32, P, I32, P, I64, P, I64]
-            lib.oracle_cconv_update_fused.restype = ctypes.c_int
-            lib.oracle_cconv_checkpoint_export.argtypes = [
-                P, I64, P, I64, I64, I64, I32, I32, I32, P, P, P, I32, P, I32, P, I32, I32, I32,
-                I32, I32]
-            lib.oracle_cconv_checkpoint_export.restype = ctypes.c_int
-            lib.oracle_cca_project_epilogue.argtypes = [
-                P, I64, P, I64, P, I64, P, I64, I32, I32, I32, I32, I32, P, I64]
-            lib.oracle_cca_project_epilogue.restype = ctypes.c_int
-            lib.oracle_f32_to_bf16.argtypes = [ctypes.c_float]
-            lib.oracle_f32_to_bf16.restype = ctypes.c_uint16
-            lib.oracle_bf16_to_f32.argtypes = [ctypes.c_uint16]
-            lib.oracle_bf16_to_f32.restype = ctypes.c_float
-            _lib = lib
+            _lib = _configure(ctypes.CDLL(build()))
     return _lib
 
 
