@@ -92,7 +92,9 @@ enum {
   CCONV_OK = 0,
   CCONV_ERR_INVALID = -1,
   CCONV_ERR_UNSUPPORTED = -2,
-  CCONV_ERR_LAUNCH = -3
+  CCONV_ERR_LAUNCH = -3,
+  CCONV_ERR_TOO_LARGE = -4   /* cca_qk_conv_noalloc: more work than its fixed
+                                scratch can count                       */
 };
 
 enum { CCONV_DTYPE_F32 = 0, CCONV_DTYPE_BF16 = 1 };
@@ -364,6 +366,50 @@ CCONV_API int cca_qk_conv_fused(const void* qk, int64_t qk_row_stride, const voi
                       const int32_t* cu_seqlens, const uint8_t* has_init, int32_t num_seqs,
                       int32_t num_tokens, int32_t Cqk, int32_t dtype, void* out,
                       int64_t out_row_stride, int32_t* dev_err, cconv_stream_t stream);
+
+/*
+ * cca_qk_conv_noalloc -- cca_qk_conv for callers that cannot allocate device
+ * memory, with the kernel's scratch in a fixed array inside the library.
+ *
+ * No page has a counterpart: this is a calling convention of this library,
+ * not a step of the method. Arguments, results, state updates and errors are
+ * exactly those of cca_qk_conv, plus CCONV_ERR_TOO_LARGE below.
+ *
+ * Who needs it. Some callers may not call cudaMalloc (or anything that does):
+ * a host framework that owns all device memory and gives its kernels only
+ * their inputs and outputs (an inference engine's plugin, say, whose enqueue
+ * step must not allocate); code recording a CUDA graph, where an allocation
+ * would break the capture; and latency-critical serving loops, where an
+ * allocation can wait for the whole device. The kernel needs a little scratch
+ * memory besides its inputs and outputs -- the two counters of its dynamic
+ * work split -- and this entry point keeps it in a 256-byte array the library
+ * declares at file scope, so the call allocates nothing, ever.
+ *
+ * Limits and sharing.
+ *   - Every GPU that loads the library holds the 256 bytes until the process
+ *     exits. A call's work units (token tiles of at most 128 rows, times
+ *     groups) must not exceed 2^30, so that the counters cannot wrap; a larger
+ *     call returns CCONV_ERR_TOO_LARGE and enqueues nothing.
+ *   - Every call on a device shares the one array. The call clears the
+ *     counters on `stream` before its kernel starts, so a call never depends
+ *     on what an earlier call left there; but two calls whose kernels overlap
+ *     on the GPU (different streams, no ordering between them) race on the
+ *     counters and may skip or repeat work without any error. Order such
+ *     calls, e.g. on one stream.
+ *   - The first call on each device looks up the array's device address (with
+ *     that device current) and keeps it; make that first call before any
+ *     stream capture begins.
+ */
+CCONV_API int cca_qk_conv_noalloc(const void* qk, int64_t qk_row_stride, const void* w_dw,
+                        const void* b_dw, const void* w_gr, const void* b_gr, int32_t groups,
+                        int32_t t0, int32_t t1, const void* delayed, int64_t delayed_row_stride,
+                        const void* delayed_init, int32_t Dv, cconv_pool_t conv_state,
+                        void* delayed_state, int64_t delayed_state_row_stride,
+                        const int32_t* state_idx, const int32_t* cu_seqlens,
+                        const uint8_t* has_init, int32_t num_seqs, int32_t num_tokens,
+                        int32_t Cqk, int32_t dtype, void* out_qk, int64_t out_qk_row_stride,
+                        void* out_delayed_prev, int64_t out_delayed_prev_row_stride,
+                        int32_t* dev_err, cconv_stream_t stream);
 
 /* Static English text for a status code. */
 CCONV_API const char* cconv_status_string(int status);

@@ -11,9 +11,11 @@ extern "C" const char* cconv_status_string(int status) {
       return "unsupported combination (no kernel for these sizes or this dtype)";
     case CCONV_ERR_LAUNCH:
       return "CUDA launch failed";
+    case CCONV_ERR_TOO_LARGE:
+      return "too much work for the fixed scratch of cca_qk_conv_noalloc (at most 2^30 units)";
     default:
       return "unknown status";
   }
 }
 
-extern "C" int cconv_abi_version(void) { return 5; }
+extern "C" int cconv_abi_version(void) { return 6; }

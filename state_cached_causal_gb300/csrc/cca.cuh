@@ -108,6 +108,7 @@ struct Args {
   int32_t num_tiles, tile_pitch, units;
   int32_t static_units;   // units per CTA in the static part of the split
   int32_t epoch;          // this launch's slot of the work counters
+  unsigned int* work;     // or, when not null, the counters [next, done] themselves
   char* out;
   int64_t out_rs;
   char* dprev;
@@ -479,6 +480,9 @@ __device__ __forceinline__ void unit_to_gt(const Args& a, int u, int& g, int& ta
 constexpr int kEpochs = 64;
 constexpr int kDynChunk = 2;                 // units per dynamic grab
 constexpr int kStaticPercent = 90;           // share of the units split statically
+// Work units a launch may have when its two counters come from the caller's
+// fixed scratch (cca_qk_conv_noalloc): the counters never pass 2^31.
+constexpr int64_t kStaticScratchMaxUnits = int64_t(1) << 30;
 static __device__ unsigned int g_work_next[kEpochs];
 static __device__ unsigned int g_work_done[kEpochs];
 
@@ -641,7 +645,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!W.wait(&ctl->meta_empty[ms], ((i / kMetaStages) & 1) ^ 1)) break;
       if (cur >= end) {
         int got = 0;
-        if (lane == 0) got = (int)atomicAdd(&g_work_next[a.epoch], (unsigned)kDynChunk);
+        if (lane == 0)
+          got = (int)atomicAdd(a.work ? a.work : &g_work_next[a.epoch], (unsigned)kDynChunk);
         got = __shfl_sync(0xffffffffu, got, 0);
         cur = dyn0 + got;
         end = min(cur + kDynChunk, a.units);
@@ -1266,10 +1271,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   // The last CTA out (all others have stopped taking units) clears this
   // launch's counters for the next launch that gets the same slot.
   if (threadIdx.x == 0) {
+    unsigned int* next = a.work ? a.work : &g_work_next[a.epoch];
+    unsigned int* done = a.work ? a.work + 1 : &g_work_done[a.epoch];
     __threadfence();
-    if (atomicAdd(&g_work_done[a.epoch], 1u) == gridDim.x - 1) {
-      atomicExch(&g_work_next[a.epoch], 0u);
-      atomicExch(&g_work_done[a.epoch], 0u);
+    if (atomicAdd(done, 1u) == gridDim.x - 1) {
+      atomicExch(next, 0u);
+      atomicExch(done, 0u);
     }
   }
 }
@@ -1306,6 +1313,9 @@ static cudaError_t launch(const CUtensorMap& map, const Args& a, int grid, cudaS
   cudaError_t e = cudaFuncSetAttribute(cca_kernel<T0, T1, FUSED>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
+  // counters passed in (the static-scratch entry point) start at zero
+  if (a.work && (e = cudaMemsetAsync(a.work, 0, 2 * sizeof(unsigned int), st)) != cudaSuccess)
+    return e;
   cca_kernel<T0, T1, FUSED><<<grid, kThreads, smem, st>>>(map, a);
   return cudaGetLastError();
 }
@@ -1328,7 +1338,8 @@ static int cca_entry(const void* qk, int64_t qk_row_stride, const void* w_dw, co
                      int32_t Cqk, int32_t dtype, void* out_qk, int64_t out_qk_row_stride,
                      void* out_delayed_prev, int64_t out_delayed_prev_row_stride,
                      int32_t num_q_heads, const void* v_current, int64_t v_current_row_stride,
-                     int32_t* dev_err, cconv_stream_t stream) {
+                     int32_t* dev_err, cconv_stream_t stream,
+                     int (*static_scratch)(unsigned int**) = nullptr) {
   if (dtype != CCONV_DTYPE_BF16 && dtype != CCONV_DTYPE_F32) return CCONV_ERR_INVALID;
   if (!w_dw || !w_gr || !delayed_init || !conv_state.p || !delayed_state ||
       (num_seqs > 0 && (!state_idx || !cu_seqlens)))
@@ -1409,6 +1420,10 @@ static int cca_entry(const void* qk, int64_t qk_row_stride, const void* w_dw, co
   a.n = n;
   a.tile_pitch = kRows - std::max(n - 1, 0);
   a.num_tiles = std::max(1, (num_tokens + a.tile_pitch - 1) / a.tile_pitch);
+  // The static-scratch entry point's counters count at most
+  // kStaticScratchMaxUnits units.
+  if (static_scratch && (int64_t)a.num_tiles * groups > kStaticScratchMaxUnits)
+    return CCONV_ERR_TOO_LARGE;
   a.units = a.num_tiles * groups;
   a.out = static_cast<char*>(out_qk);
   a.out_rs = out_qk_row_stride;
@@ -1437,6 +1452,7 @@ static int cca_entry(const void* qk, int64_t qk_row_stride, const void* w_dw, co
   a.static_units = (int)((int64_t)a.units * kStaticPercent / 100 / grid);
   static std::atomic<unsigned> launches{0};
   a.epoch = (int)(launches.fetch_add(1u) % kEpochs);
+  a.work = nullptr;
 
   CUtensorMap map;
   memset(&map, 0, sizeof(map));
@@ -1452,6 +1468,11 @@ static int cca_entry(const void* qk, int64_t qk_row_stride, const void* w_dw, co
                      CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return CCONV_ERR_INVALID;
+  }
+  // (looked up only for a call that passed every check)
+  if (static_scratch) {
+    const int rc = static_scratch(&a.work);
+    if (rc != CCONV_OK) return rc;
   }
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = cudaErrorInvalidValue;

@@ -17,7 +17,7 @@ import torch
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libcconv.so")
 
-OK, ERR_INVALID, ERR_UNSUPPORTED, ERR_LAUNCH = 0, -1, -2, -3
+OK, ERR_INVALID, ERR_UNSUPPORTED, ERR_LAUNCH, ERR_TOO_LARGE = 0, -1, -2, -3, -4
 DTYPE_F32, DTYPE_BF16 = 0, 1
 ACT_NONE, ACT_SILU = 0, 1
 DERR_SLOT_RANGE, DERR_CU_SEQLENS, DERR_NUM_ACCEPTED, DERR_TIMEOUT = 1, 2, 4, 8
@@ -78,6 +78,8 @@ def load():
         lib.cca_qk_conv.argtypes = [P, I64, P, P, P, P, I32, I32, I32, P, I64, P, I32, Pool, P,
                                     I64, P, P, P, I32, I32, I32, I32, P, I64, P, I64, P, P]
         lib.cca_qk_conv.restype = ctypes.c_int
+        lib.cca_qk_conv_noalloc.argtypes = lib.cca_qk_conv.argtypes
+        lib.cca_qk_conv_noalloc.restype = ctypes.c_int
         lib.cca_qk_conv_fused.argtypes = [P, I64, P, P, P, P, I32, I32, I32, I32, P, I64, P, I32,
                                           P, I64, Pool, P, I64, P, P, P, I32, I32, I32, I32, P,
                                           I64, P, P]
@@ -268,19 +270,38 @@ def cca_qk_conv(qk, w_dw, b_dw, w_gr, b_gr, groups, t0, t1, delayed, delayed_ini
                 conv_state, delayed_state, state_idx, cu_seqlens, has_init, out_qk,
                 out_delayed_prev, dev_err=None, stream=None, num_tokens=None):
     """Zaya CCA two-stage q/k conv + delayed-v shift (see cca_qk_conv in cconv.h)."""
+    _cca_call("cca_qk_conv", qk, w_dw, b_dw, w_gr, b_gr, groups, t0, t1, delayed,
+              delayed_init, conv_state, delayed_state, state_idx, cu_seqlens, has_init, out_qk,
+              out_delayed_prev, dev_err, stream, num_tokens)
+
+
+def cca_qk_conv_noalloc(qk, w_dw, b_dw, w_gr, b_gr, groups, t0, t1, delayed, delayed_init,
+                        conv_state, delayed_state, state_idx, cu_seqlens, has_init, out_qk,
+                        out_delayed_prev, dev_err=None, stream=None, num_tokens=None):
+    """cca_qk_conv whose kernel scratch lives in a fixed array inside the library,
+    for callers that must not allocate (see cca_qk_conv_noalloc in cconv.h). Calls
+    whose kernels overlap on the GPU share that scratch and race."""
+    _cca_call("cca_qk_conv_noalloc", qk, w_dw, b_dw, w_gr, b_gr, groups, t0, t1, delayed,
+              delayed_init, conv_state, delayed_state, state_idx, cu_seqlens, has_init, out_qk,
+              out_delayed_prev, dev_err, stream, num_tokens)
+
+
+def _cca_call(fn, qk, w_dw, b_dw, w_gr, b_gr, groups, t0, t1, delayed, delayed_init,
+              conv_state, delayed_state, state_idx, cu_seqlens, has_init, out_qk,
+              out_delayed_prev, dev_err, stream, num_tokens):
     _same_state_dtype(conv_state, delayed_state)
     _i32(state_idx, "state_idx")
     _i32(cu_seqlens, "cu_seqlens")
     _u8(has_init, "has_init")
     T = int(qk.shape[0]) if num_tokens is None else int(num_tokens)
-    rc = load().cca_qk_conv(
+    rc = getattr(load(), fn)(
         _ptr(qk), _rows(qk), _ptr(w_dw), _ptr(b_dw), _ptr(w_gr), _ptr(b_gr), int(groups),
         int(t0), int(t1), _ptr(delayed), _rows(delayed), _ptr(delayed_init),
         int(delayed.shape[1]), _pool(conv_state), _ptr(delayed_state), _rows(delayed_state),
         _ptr(state_idx), _ptr(cu_seqlens), _ptr(has_init), int(state_idx.shape[0]), T,
         int(qk.shape[1]), _dtype_code(qk), _ptr(out_qk), _rows(out_qk),
         _ptr(out_delayed_prev), _rows(out_delayed_prev), _ptr(dev_err), _stream(stream))
-    _check("cca_qk_conv", rc)
+    _check(fn, rc)
 
 
 def cca_qk_conv_fused(qk, w_dw, b_dw, w_gr, b_gr, groups, num_q_heads, t0, t1, delayed,

@@ -55,10 +55,10 @@ def test_library_exports_nothing_else():
 
 def test_status_strings(lib):
     assert ops.status_string(0) == "ok"
-    for s in (-1, -2, -3):
+    for s in (-1, -2, -3, -4):
         assert ops.status_string(s) not in ("ok", "unknown status")
     assert ops.status_string(17) == "unknown status"
-    assert ops.abi_version() == 5
+    assert ops.abi_version() == 6
 
 
 FAKE = 0x10000  # 16-byte aligned, never dereferenced: every call below fails validation
@@ -181,7 +181,7 @@ def test_checkpoint_export_validation(lib, kw, want):
     assert rc == want
 
 
-def cca(lib, fused=False, **kw):
+def cca(lib, fused=False, noalloc=False, **kw):
     # Zaya shapes: 16 q + 4 kv heads of 128 (20 groups), Dv = 256, history n = 2
     a = dict(qk=FAKE, qrs=2560, w_dw=FAKE, b_dw=None, w_gr=FAKE, b_gr=None, G=20, Hq=16, t0=2,
              t1=2, dl=FAKE, drs=256, dinit=FAKE, Dv=256, vc=FAKE, vcrs=256,
@@ -196,11 +196,12 @@ def cca(lib, fused=False, **kw):
                                      P(a["vc"]), a["vcrs"], a["pool"], P(a["ds"]), a["dsrs"],
                                      P(a["sidx"]), P(a["cu"]), P(a["hi"]), a["B"], a["T"],
                                      a["C"], a["dt"], P(a["out"]), a["ors"], None, None)
-    return lib.cca_qk_conv(P(a["qk"]), a["qrs"], P(a["w_dw"]), P(a["b_dw"]), P(a["w_gr"]),
+    fn = lib.cca_qk_conv_noalloc if noalloc else lib.cca_qk_conv
+    return fn(P(a["qk"]), a["qrs"], P(a["w_dw"]), P(a["b_dw"]), P(a["w_gr"]),
                            P(a["b_gr"]), a["G"], a["t0"], a["t1"], P(a["dl"]), a["drs"],
                            P(a["dinit"]), a["Dv"], a["pool"], P(a["ds"]), a["dsrs"],
                            P(a["sidx"]), P(a["cu"]), P(a["hi"]), a["B"], a["T"], a["C"], a["dt"],
-                           P(a["out"]), 2560, P(a["dp"]), a["dprs"], None, None)
+                           P(a["out"]), a.get("oqrs", 2560), P(a["dp"]), a["dprs"], None, None)
 
 
 @pytest.mark.parametrize("kw,want", [
@@ -213,6 +214,19 @@ def cca(lib, fused=False, **kw):
 @no_gpu
 def test_cca_validation(lib, kw, want):
     assert cca(lib, **kw) == want
+    # the no-allocation form checks its arguments exactly as cca_qk_conv does
+    assert cca(lib, noalloc=True, **kw) == want
+
+
+@no_gpu
+def test_cca_noalloc_rejects_more_work_than_its_scratch_counts(lib):
+    # 2^30 tokens in tiles of 127 rows, times 600 groups: about 5.1e9
+    # units, more than the 2^30 its fixed counters may count; cca_qk_conv
+    # itself takes the call to the launch (-3: no device here)
+    big = dict(T=2**30, G=600, C=600 * 128, qrs=600 * 128, oqrs=600 * 128,
+               pool=_pool(C=600 * 128, cap=2))
+    assert cca(lib, noalloc=True, **big) == ops.ERR_TOO_LARGE
+    assert cca(lib, noalloc=False, **big) == -3
 
 
 @pytest.mark.parametrize("kw,want", [
