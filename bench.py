@@ -349,15 +349,18 @@ class ClockSampler:
 # Sources that make up each entry point's kernels (a recorded DRAM traffic
 # figure stays valid while these files are unchanged).
 KERNEL_SOURCES = {
-    "cconv_fwd_varlen": ["depthwise.cuh", "depthwise.cu", "common.cuh", "update.cuh"],
-    "cconv_update": ["depthwise.cuh", "depthwise.cu", "update_bulk.cuh", "update_bulk.cu",
-                     "update_bulk_wide.cu", "update.cuh", "async.cuh", "common.cuh"],
+    "cconv_fwd_varlen": ["depthwise.cuh", "depthwise.cu", "depthwise_wide.cu", "common.cuh",
+                         "update.cuh"],
+    "cconv_update": ["depthwise.cuh", "depthwise.cu", "depthwise_wide.cu", "update_bulk.cuh",
+                     "update_bulk.cu", "update_bulk_f32.cu", "update_bulk_wide.cu", "update.cuh",
+                     "async.cuh", "common.cuh"],
     "cca_qk_conv": ["cca.cuh", "cca_qk_conv.cu", "async.cuh", "common.cuh"],
     "cca_qk_conv_fused": ["cca.cuh", "cca_fused.cu", "async.cuh", "common.cuh"],
-    "cconv_fwd_varlen_fused": ["depthwise.cuh", "depthwise_fused.cu", "common.cuh"],
-    "cconv_update_fused": ["depthwise.cuh", "depthwise_fused.cu", "update_bulk.cuh",
-                           "update_bulk.cu", "update_bulk_wide.cu", "update.cuh", "async.cuh",
-                           "common.cuh"],
+    "cconv_fwd_varlen_fused": ["depthwise.cuh", "depthwise_fused.cu", "depthwise_wide.cu",
+                               "common.cuh"],
+    "cconv_update_fused": ["depthwise.cuh", "depthwise_fused.cu", "depthwise_wide.cu",
+                           "update_bulk.cuh", "update_bulk.cu", "update_bulk_f32.cu",
+                           "update_bulk_wide.cu", "update.cuh", "async.cuh", "common.cuh"],
 }
 
 

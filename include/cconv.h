@@ -154,7 +154,8 @@ typedef struct cconv_pool {
  *                non-decreasing, cu[num_seqs] <= num_tokens)
  *   has_init     uint8 [num_seqs] or NULL
  *   C            multiple of 8 (bf16) or 4 (fp32)
- *   width        2..4;  dilation 1..4;  act CCONV_ACT_*
+ *   width        2..8;  dilation 1..8 (others return CCONV_ERR_INVALID);
+ *                act CCONV_ACT_*
  *   out          [num_tokens, C], row stride out_row_stride; must not alias x.
  *                Rows outside every sequence are not written.
  */
@@ -185,7 +186,7 @@ CCONV_API int cconv_fwd_varlen(const void* x, int64_t x_row_stride, const void* 
  *   x, out       [num_seqs*q, C] with row strides as for cconv_fwd_varlen
  *   num_accepted int32 [num_seqs], required when n_spec > 0, else ignored
  *   has_init     uint8 [num_seqs] or NULL (all true)
- *   n_spec       0..7;  cap >= S + n_spec;  width 2..4; dilation 1..4
+ *   n_spec       0..7;  cap >= S + n_spec;  width 2..8; dilation 1..8
  */
 CCONV_API int cconv_update(const void* x, int64_t x_row_stride, cconv_pool_t conv_states,
                  const void* w, const void* bias, const int32_t* state_idx,
@@ -277,7 +278,7 @@ CCONV_API int cconv_update_fused(const void* x, int64_t x_row_stride, cconv_pool
  *   x            [num_rows, C] with row stride (as cconv_fwd_varlen)
  *   ckpt_*       int32 [num_ckpt] (num_ckpt <= 65535)
  *   cu_seqlens   int32 [num_seqs+1] over num_tokens logical rows
- *   width 2..4, dilation 1..4, S in {1,2,3,4,6,8,9,12}
+ *   width 2..8, dilation 1..8 (S = (width-1)*dilation <= 56)
  * A checkpoint whose request, offset or slot is out of range sets
  * CCONV_DERR_CHECKPOINT (a row outside num_rows CCONV_DERR_ROW_INDEX) and is
  * skipped.

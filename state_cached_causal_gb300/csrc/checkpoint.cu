@@ -24,12 +24,16 @@ struct CkptArgs {
   const int32_t* cu;
   const int32_t* tidx;
   int32_t num_seqs, num_rows, C, T;
+  int32_t S;   // window rows (read by the runtime-S instantiation)
   int32_t* dev_err;
 };
 
-template <typename T, int S>
+// SC is the window S, or 0 for the instantiation that reads it at run time
+// (windows other than those of widths and dilations up to 4).
+template <typename T, int SC>
 __global__ void __launch_bounds__(128) checkpoint_kernel(const CkptArgs a) {
   constexpr int V = Elem<T>::V, E = Elem<T>::bytes;
+  const int S = SC > 0 ? SC : a.S;
   extern __shared__ uint4 dyn_smem[];
   const int nt = blockDim.x, tid = threadIdx.x;
   const int k = blockIdx.y;
@@ -44,12 +48,15 @@ __global__ void __launch_bounds__(128) checkpoint_kernel(const CkptArgs a) {
     if (blockIdx.x == 0 && tid == 0) flag_error(a.dev_err, CCONV_DERR_CHECKPOINT);
     return;
   }
-  int64_t prow[S];
-#pragma unroll
-  for (int i = 0; i < S; ++i) {
+  // physical row of window row i (every thread checks all of them, so the
+  // exit stays block-uniform)
+  auto prow = [&](int i) -> int64_t {
     const int64_t li = (int64_t)st + off - S + i;
-    prow[i] = a.tidx ? a.tidx[li] : li;
-    if (prow[i] < 0 || prow[i] >= a.num_rows) {
+    return a.tidx ? a.tidx[li] : li;
+  };
+  for (int i = 0; i < S; ++i) {
+    const int64_t p = prow(i);
+    if (p < 0 || p >= a.num_rows) {
       if (blockIdx.x == 0 && tid == 0) flag_error(a.dev_err, CCONV_DERR_ROW_INDEX);
       return;
     }
@@ -60,8 +67,8 @@ __global__ void __launch_bounds__(128) checkpoint_kernel(const CkptArgs a) {
   // so its columns >= S are read first and go back unchanged
   uint4* blk = dyn_smem + tid;
   if (a.pool.mode == kPoolDS) pool_load<T>(a.pool, slot, c0, S, blk, nt);
-#pragma unroll
-  for (int i = 0; i < S; ++i) blk[i * nt] = ldg16(a.x + (prow[i] * a.x_rs + c0) * E);
+#pragma unroll 4
+  for (int i = 0; i < S; ++i) blk[i * nt] = ldg16(a.x + (prow(i) * a.x_rs + c0) * E);
   pool_store<T>(a.pool, slot, c0, S, blk, nt);
 }
 
@@ -76,7 +83,8 @@ cudaError_t launch_ckpt(int S, dim3 grid, int nt, size_t smem, cudaStream_t st,
   CCONV_CKPT_CASE(1) CCONV_CKPT_CASE(2) CCONV_CKPT_CASE(3) CCONV_CKPT_CASE(4)
   CCONV_CKPT_CASE(6) CCONV_CKPT_CASE(8) CCONV_CKPT_CASE(9) CCONV_CKPT_CASE(12)
 #undef CCONV_CKPT_CASE
-  return cudaErrorInvalidValue;
+  checkpoint_kernel<T, 0><<<grid, nt, smem, st>>>(a);
+  return cudaGetLastError();
 }
 
 }  // namespace
@@ -100,8 +108,8 @@ extern "C" int cconv_checkpoint_export(const void* x, int64_t x_row_stride,
   if (check_pool(conv_states) != CCONV_OK) return CCONV_ERR_INVALID;
   if (C <= 0 || C % V != 0 || !aligned16(x) || x_row_stride < C || x_row_stride % V != 0)
     return CCONV_ERR_INVALID;
-  if (width < 1 || dilation < 1) return CCONV_ERR_INVALID;
-  if (width < 2 || width > 4 || dilation > 4) return CCONV_ERR_UNSUPPORTED;
+  if (width < 2 || width > kMaxWidth || dilation < 1 || dilation > kMaxDilation)
+    return CCONV_ERR_INVALID;
   if (!token_indices && num_rows < num_tokens) return CCONV_ERR_INVALID;
   const int S = (width - 1) * dilation;
   if (conv_states.cap < S) return CCONV_ERR_INVALID;
@@ -118,6 +126,7 @@ extern "C" int cconv_checkpoint_export(const void* x, int64_t x_row_stride,
   a.num_rows = num_rows;
   a.C = C;
   a.T = num_tokens;
+  a.S = S;
   a.dev_err = dev_err;
   const int units = C / V;
   const int nt = pick_threads(units, conv_states.cap);   // cap columns of 16 bytes per thread

@@ -35,6 +35,10 @@ constexpr int kUpdChan = 2;     // channels per thread of the update kernel
 // (plus its stream ring) in shared memory, within the 48 KB a block gets
 // without opting in, at 32 threads.
 constexpr int kMaxCap = 64;
+// Widths and dilations of the depthwise entry points (S = (width-1)*dilation
+// <= 56, so a 64-token varlen chunk still holds the whole window and a view
+// of S + n_spec columns fits kMaxCap).
+constexpr int kMaxWidth = 8, kMaxDilation = 8;
 
 struct FwdArgs {
   const char* x;
@@ -47,6 +51,7 @@ struct FwdArgs {
   const uint8_t* has_init;
   int32_t B, T, C;
   int32_t act;
+  int32_t dil;           // dilation (read by the runtime-dilation instantiations)
   int32_t chunk_shift;   // tokens per block = 1 << chunk_shift
   int32_t nblk;          // chunk ids of the grid
   int32_t order_lpt;     // grid = (ctiles, nblk), chunk ids in reverse
@@ -82,6 +87,11 @@ static __device__ int find_chunk_seq(const int32_t* __restrict__ cu, int B, int 
   return (max(__ldg(cu + lo), 0) >> sh) + lo <= b ? lo : -1;
 }
 
+// DC is the dilation, or 0 for the instantiations that read it at run time
+// (a.dil): widths 5..8 and dilations 5..8 take those, so that the build has
+// one kernel per width for them rather than one per (width, dilation).
+// Widths above 4 keep a longer register window and get fewer blocks per SM.
+//
 // FUSED: the epilogue of the fused entry point -- logical row r of sequence s
 // (logical row cu[s] + r of the call) lives at physical row p of x, residual
 // and outer_residual (p = token_indices[cu[s] + r], or cu[s] + r without
@@ -89,9 +99,10 @@ static __device__ int find_chunk_seq(const int32_t* __restrict__ cu, int B, int 
 // the output row. Each output row's stream entry then carries three 16-byte
 // units (x, residual, outer) and the block stages the physical rows it touches
 // in shared memory.
-template <typename T, int W, int D, bool FUSED>
-__global__ void __launch_bounds__(128, 4) fwd_varlen_kernel(const FwdArgs a) {
-  constexpr int S = (W - 1) * D;
+template <typename T, int W, int DC, bool FUSED>
+__global__ void __launch_bounds__(128, (W <= 4 ? 4 : 2)) fwd_varlen_kernel(const FwdArgs a) {
+  const int D = DC > 0 ? DC : a.dil;
+  const int S = (W - 1) * D;
   constexpr int V = Elem<T>::V, E = Elem<T>::bytes;
   constexpr int PF = FUSED ? kPrefetchFused : kPrefetch;
   constexpr int RING = FUSED ? kRingFused : kRing;
@@ -303,9 +314,11 @@ __global__ void __launch_bounds__(128, 4) fwd_varlen_kernel(const FwdArgs a) {
 // p_r = token_indices[s*q + r] (identity without them) of x, residual and
 // outer residual; residual[p_r] = round(residual + act(conv) + outer) replaces
 // the output, the residual and outer rows being staged beside the tokens.
-template <typename T, int W, int D, bool FUSED>
+template <typename T, int W, int DC, bool FUSED>
 __global__ void __launch_bounds__(256) update_kernel(const UpdArgs a) {
-  constexpr int S = (W - 1) * D;
+  const int D = DC > 0 ? DC : a.dil;   // DC == 0: the dilation is read at run time
+  const int S = (W - 1) * D;
+  constexpr int SC = (W - 1) * (DC > 0 ? DC : 1);   // register window (DC > 0)
   constexpr int E = Elem<T>::bytes, QM = kMaxSpec + 1, K = kUpdChan;
   using R = typename std::conditional<E == 4, uint32_t, uint16_t>::type;   // raw element
   extern __shared__ uint4 dyn_smem[];
@@ -417,50 +430,93 @@ __global__ void __launch_bounds__(256) update_kernel(const UpdArgs a) {
     const int c = tid + kc * nt;
     if (c >= nch) break;
     R* row = st_s + c;                                 // column col at row[col * cs]
-    float pr[S];                                        // B[off + i], zero without history
-    R pb[S];
+    if constexpr (DC == 0) {
+      // Runtime dilation: the taps read the prior window and the tokens in
+      // shared memory, and the outputs replace the tokens once all are
+      // computed; then the buffer is rolled in place (each column read ahead
+      // of its overwrite: off + 1 + col > col).
+      float y[QM];
 #pragma unroll
-    for (int i = 0; i < S; ++i) {
-      pb[i] = hs ? row[(off + i) * cs] : R(0);
-      pr[i] = raw_to_f32<T>(pb[i]);
-    }
-    R xb[QM];
-    float xf[QM];
+      for (int i = 0; i < QM; ++i) {
+        y[i] = 0.0f;
+        if (i < q) {
+          float acc = bv[kc];
 #pragma unroll
-    for (int u = 0; u < QM; ++u) {
-      xb[u] = u < q ? xs[u * nb + c] : R(0);
-      xf[u] = raw_to_f32<T>(xb[u]);
-    }
-#pragma unroll
-    for (int i = 0; i < QM; ++i) {
-      if (i < q) {
-        float acc = bv[kc];
-#pragma unroll
-        for (int k = 0; k < W; ++k) {
-          const int idx = S + i - (W - 1 - k) * D;   // position in prior ++ tokens
-          acc = fmaf(wk[kc][k], idx >= S ? xf[idx - S] : pr[idx], acc);
+          for (int k = 0; k < W; ++k) {
+            const int idx = S + i - (W - 1 - k) * D;   // position in prior ++ tokens
+            const float v = idx >= S ? raw_to_f32<T>(xs[(idx - S) * nb + c])
+                                     : (hs ? raw_to_f32<T>(row[(off + idx) * cs]) : 0.0f);
+            acc = fmaf(wk[kc][k], v, acc);
+          }
+          y[i] = silu_on ? silu<T>(acc) : acc;
+          if constexpr (FUSED)
+            y[i] = (raw_to_f32<T>(rs_s[i * nb + c]) + y[i]) + raw_to_f32<T>(os_s[i * nb + c]);
         }
-        float y = silu_on ? silu<T>(acc) : acc;
-        if constexpr (FUSED)
-          y = (raw_to_f32<T>(rs_s[i * nb + c]) + y) + raw_to_f32<T>(os_s[i * nb + c]);
-        xs[i * nb + c] = f32_to_raw<T>(y);
       }
-    }
-    if (slot >= 0) {
-      if (a.n_spec == 0) {
+      R xb[QM];
 #pragma unroll
-        for (int col = 0; col + 1 < S; ++col) row[col * cs] = pb[col + 1];
-        row[(S - 1) * cs] = xb[0];
-      } else {
-        // B[off+1+col] for col < S-1 is pb[col+1]; wider buffers keep more
-        // columns, read ahead of every write
+      for (int u = 0; u < QM; ++u) xb[u] = u < q ? xs[u * nb + c] : R(0);
 #pragma unroll
-        for (int col = 0; col + 1 < S; ++col) row[col * cs] = pb[col + 1];
-        for (int col = S - 1; col < keep; ++col)
+      for (int i = 0; i < QM; ++i)
+        if (i < q) xs[i * nb + c] = f32_to_raw<T>(y[i]);
+      if (slot >= 0) {
+        const int kept = a.n_spec == 0 ? S - 1 : keep;
+        for (int col = 0; col < kept; ++col)
           row[col * cs] = hs ? row[(off + 1 + col) * cs] : R(0);
+        if (a.n_spec == 0) {
+          row[(S - 1) * cs] = xb[0];
+        } else {
 #pragma unroll
-        for (int u = 0; u < QM; ++u)
-          if (u < q) row[(keep + u) * cs] = xb[u];
+          for (int u = 0; u < QM; ++u)
+            if (u < q) row[(keep + u) * cs] = xb[u];
+        }
+      }
+    } else {
+      float pr[SC];                                        // B[off + i], zero without history
+      R pb[SC];
+#pragma unroll
+      for (int i = 0; i < SC; ++i) {
+        pb[i] = hs ? row[(off + i) * cs] : R(0);
+        pr[i] = raw_to_f32<T>(pb[i]);
+      }
+      R xb[QM];
+      float xf[QM];
+#pragma unroll
+      for (int u = 0; u < QM; ++u) {
+        xb[u] = u < q ? xs[u * nb + c] : R(0);
+        xf[u] = raw_to_f32<T>(xb[u]);
+      }
+#pragma unroll
+      for (int i = 0; i < QM; ++i) {
+        if (i < q) {
+          float acc = bv[kc];
+#pragma unroll
+          for (int k = 0; k < W; ++k) {
+            const int idx = SC + i - (W - 1 - k) * DC;   // position in prior ++ tokens
+            acc = fmaf(wk[kc][k], idx >= SC ? xf[idx - SC] : pr[idx], acc);
+          }
+          float y = silu_on ? silu<T>(acc) : acc;
+          if constexpr (FUSED)
+            y = (raw_to_f32<T>(rs_s[i * nb + c]) + y) + raw_to_f32<T>(os_s[i * nb + c]);
+          xs[i * nb + c] = f32_to_raw<T>(y);
+        }
+      }
+      if (slot >= 0) {
+        if (a.n_spec == 0) {
+#pragma unroll
+          for (int col = 0; col + 1 < SC; ++col) row[col * cs] = pb[col + 1];
+          row[(SC - 1) * cs] = xb[0];
+        } else {
+          // B[off+1+col] for col < S-1 is pb[col+1]; wider buffers keep more
+          // columns, read ahead of every write
+#pragma unroll
+          for (int col = 0; col + 1 < SC; ++col) row[col * cs] = pb[col + 1];
+          for (int col = SC - 1; col < keep; ++col)
+            row[col * cs] = hs ? row[(off + 1 + col) * cs] : R(0);
+#pragma unroll
+          for (int u = 0; u < QM; ++u)
+            if (u < q) row[(keep + u) * cs] = xb[u];
+        }
       }
     }
   }
@@ -677,17 +733,27 @@ static int check_common(const void* x, int64_t x_rs, const void* w, const cconv_
   if (check_pool(pv) != CCONV_OK) return CCONV_ERR_INVALID;
   if (rows > 0 && (!x || !out)) return CCONV_ERR_INVALID;
   if (C <= 0 || C % *V != 0) return CCONV_ERR_INVALID;
-  if (width < 1 || dilation < 1) return CCONV_ERR_INVALID;
-  if (width < 2 || width > 4 || dilation > 4) return CCONV_ERR_UNSUPPORTED;
+  if (width < 2 || width > kMaxWidth || dilation < 1 || dilation > kMaxDilation)
+    return CCONV_ERR_INVALID;
   if (act != CCONV_ACT_NONE && act != CCONV_ACT_SILU) return CCONV_ERR_INVALID;
   if (!aligned16(x) || !aligned16(out)) return CCONV_ERR_INVALID;
   if (x_rs < C || out_rs < C || x_rs % *V != 0 || out_rs % *V != 0) return CCONV_ERR_INVALID;
   return CCONV_OK;
 }
 
+// Widths 5..8 or dilations 5..8: one runtime-dilation kernel per width
+// (depthwise_wide.cu).
+cudaError_t launch_fwd_wide(int dtype, bool fused, int W, dim3 grid, int nt, size_t smem,
+                            cudaStream_t st, const FwdArgs& a);
+cudaError_t launch_upd_wide(int dtype, bool fused, int W, dim3 grid, int nt, size_t smem,
+                            cudaStream_t st, const UpdArgs& a);
+
 template <typename T, bool FUSED>
 static cudaError_t launch_fwd(int W, int D, dim3 grid, int nt, size_t smem,
                               cudaStream_t st, const FwdArgs& a) {
+  if (W > 4 || D > 4)
+    return launch_fwd_wide(sizeof(T) == 4 ? CCONV_DTYPE_F32 : CCONV_DTYPE_BF16, FUSED, W, grid,
+                           nt, smem, st, a);
 #define CCONV_FWD_CASE(w_, d_)                                              \
   if (W == w_ && D == d_) {                                                 \
     fwd_varlen_kernel<T, w_, d_, FUSED><<<grid, nt, smem, st>>>(a);         \
@@ -703,6 +769,9 @@ static cudaError_t launch_fwd(int W, int D, dim3 grid, int nt, size_t smem,
 template <typename T, bool FUSED>
 static cudaError_t launch_upd(int W, int D, dim3 grid, int nt, size_t smem,
                               cudaStream_t st, const UpdArgs& a) {
+  if (W > 4 || D > 4)
+    return launch_upd_wide(sizeof(T) == 4 ? CCONV_DTYPE_F32 : CCONV_DTYPE_BF16, FUSED, W, grid,
+                           nt, smem, st, a);
 #define CCONV_UPD_CASE(w_, d_)                                              \
   if (W == w_ && D == d_) {                                                 \
     update_kernel<T, w_, d_, FUSED><<<grid, nt, smem, st>>>(a);             \
@@ -781,6 +850,7 @@ static int fwd_entry(const void* x, int64_t x_row_stride, const void* w, const v
   a.T = num_tokens;
   a.C = C;
   a.act = act;
+  a.dil = dilation;
   a.out = static_cast<char*>(out);
   a.out_rs = out_row_stride;
   a.outer = FUSED ? static_cast<const char*>(epi->outer_residual) : nullptr;
@@ -855,6 +925,7 @@ static int upd_entry(const void* x, int64_t x_row_stride, cconv_pool_t conv_stat
   a.has_init = has_init;
   a.C = C;
   a.act = act;
+  a.dil = dilation;
   a.out = static_cast<char*>(out);
   a.out_rs = out_row_stride;
   a.outer = FUSED ? static_cast<const char*>(epi->outer_residual) : nullptr;
@@ -880,8 +951,8 @@ static int upd_entry(const void* x, int64_t x_row_stride, cconv_pool_t conv_stat
   // the one-pass decode kernel; other channel-first pools whose slot slabs
   // start on 16 bytes stream through the bulk-copy pipeline; anything else
   // takes the block-per-request kernel.
-  if (!FUSED && n_spec == 0 && a.pool.mode == kPoolDS && conv_states.cap == S &&
-      aligned16(w) && (!bias || aligned16(bias))) {
+  if (!FUSED && n_spec == 0 && a.pool.mode == kPoolDS && conv_states.cap == S && width <= 4 &&
+      dilation <= 4 && aligned16(w) && (!bias || aligned16(bias))) {
     const int units = C / V;
     const int64_t blocks = ((int64_t)num_seqs * units + 255) / 256;
     if (blocks <= 0x7fffffff) {

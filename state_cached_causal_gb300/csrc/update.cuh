@@ -20,6 +20,7 @@ struct UpdArgs {
   const int32_t* num_accepted;
   const uint8_t* has_init;
   int32_t C, act, ctiles;
+  int32_t dil;          // dilation (read by the runtime-dilation instantiations)
   char* out;            // output rows, or the residual rows of the fused entry point
   int64_t out_rs;
   const char* outer;    // fused: outer residual rows or null
@@ -36,8 +37,11 @@ struct UpdArgs {
 // kernel).
 cudaError_t launch_update_bulk(UpdArgs a, int width, int dilation, int dtype, bool fused,
                                cudaStream_t st);
-// The kPoolDSWide instantiations (their own translation unit).
+// The kPoolDSWide instantiations and the fp32 ones (translation units of
+// their own).
 cudaError_t launch_update_bulk_wide(UpdArgs a, int width, int dilation, bool fused,
                                     cudaStream_t st);
+cudaError_t launch_update_bulk_f32(UpdArgs a, int width, int dilation, bool fused,
+                                   cudaStream_t st);
 
 }  // namespace cconv

@@ -158,11 +158,17 @@ __device__ __forceinline__ uint32_t bulk_out(uint32_t abits) {
 // back with their bits. QM bounds the tokens per request (q <= QM): the
 // per-channel token loops are unrolled to QM, so a fused call with q <= 4 takes
 // the QM = 4 instantiation instead of predicating away half of an 8-token loop.
-template <typename T, typename TS, int W, int D, bool FUSED, int QM>
+//
+// DC is the dilation, or 0 for the kernels that read it at run time (widths
+// or dilations above 4): those read each channel's prior window straight from
+// its slab in shared memory instead of a register window.
+template <typename T, typename TS, int W, int DC, bool FUSED, int QM>
 __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
     update_bulk_kernel(const UpdArgs a, const BulkArgs b) {
   constexpr int NS = stages_of<FUSED>();
-  constexpr int S = (W - 1) * D;
+  const int D = DC > 0 ? DC : a.dil;
+  const int S = (W - 1) * D;
+  constexpr int SC = (W - 1) * (DC > 0 ? DC : 1);   // register window (DC > 0)
   constexpr int E = Elem<T>::bytes, ES = Elem<TS>::bytes;
   static_assert(QM >= 1 && QM <= kMaxSpec + 1, "tokens per request");
   using R = typename std::conditional<E == 4, uint32_t, uint16_t>::type;    // raw element
@@ -296,53 +302,100 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
         const int c = tid + kc * kComputeThreads;
         if (c >= nch) break;
         RS* row = slab + c * cap;
-        float pr[S];
-        R pb[S];   // the prior window in the activation type
+        if constexpr (DC == 0) {
+          // runtime dilation: taps read the slab and the token rows in place;
+          // the outputs replace the tokens once all are computed, then the
+          // buffer rolls in place (column off + 1 + col is read before col
+          // is written)
+          float y[QM];
 #pragma unroll
-        for (int i = 0; i < S; ++i) {
-          pb[i] = hs ? static_cast<R>(bulk_in<T, TS>(row[m.off + i])) : R(0);
-          pr[i] = raw_to_f32<T>(pb[i]);
-        }
-        R xb[QM];
-        float xf[QM];
+          for (int i = 0; i < QM; ++i) {
+            y[i] = 0.0f;
+            if (i < q) {
+              float acc = bv[kc];
 #pragma unroll
-        for (int u = 0; u < QM; ++u) {
-          xb[u] = u < q ? xs[u * tile + c] : R(0);
-          xf[u] = raw_to_f32<T>(xb[u]);
-        }
-#pragma unroll
-        for (int i = 0; i < QM; ++i) {
-          if (i < q) {
-            float acc = bv[kc];
-#pragma unroll
-            for (int k = 0; k < W; ++k) {
-              const int idx = S + i - (W - 1 - k) * D;   // position in prior ++ tokens
-              acc = fmaf(wk[kc][k], idx >= S ? xf[idx - S] : pr[idx], acc);
+              for (int k = 0; k < W; ++k) {
+                const int idx = S + i - (W - 1 - k) * D;   // position in prior ++ tokens
+                const float v =
+                    idx >= S ? raw_to_f32<T>(xs[(idx - S) * tile + c])
+                             : (hs ? raw_to_f32<T>(bulk_in<T, TS>(row[m.off + idx])) : 0.0f);
+                acc = fmaf(wk[kc][k], v, acc);
+              }
+              y[i] = silu_on ? silu<T>(acc) : acc;
+              if constexpr (FUSED) {
+                y[i] = raw_to_f32<T>(rs[i * tile + c]) + y[i];
+                if (has_outer) y[i] = y[i] + raw_to_f32<T>(os[i * tile + c]);
+              }
             }
-            float y = silu_on ? silu<T>(acc) : acc;
-            if constexpr (FUSED) {
-              y = raw_to_f32<T>(rs[i * tile + c]) + y;
-              if (has_outer) y = y + raw_to_f32<T>(os[i * tile + c]);
-            }
-            xs[i * tile + c] = f32_to_raw<T>(y);
           }
-        }
-        if (own) {
-          // B[off+1+col] for col < S-1 is pb[col+1]; wider buffers keep more
-          // columns, each read ahead of every write
+          R xb[QM];
 #pragma unroll
-          for (int col = 0; col + 1 < S; ++col)
-            row[col] = static_cast<RS>(bulk_out<T, TS>(pb[col + 1]));
-          if (a.n_spec == 0) {
-            row[S - 1] = static_cast<RS>(bulk_out<T, TS>(xb[0]));
-          } else {
-            for (int col = S - 1; col < keep; ++col)
-              row[col] = hs ? static_cast<RS>(
-                                  bulk_out<T, TS>(bulk_in<T, TS>(row[m.off + 1 + col])))
+          for (int u = 0; u < QM; ++u) xb[u] = u < q ? xs[u * tile + c] : R(0);
+#pragma unroll
+          for (int i = 0; i < QM; ++i)
+            if (i < q) xs[i * tile + c] = f32_to_raw<T>(y[i]);
+          if (own) {
+            const int kept = a.n_spec == 0 ? S - 1 : keep;
+            for (int col = 0; col < kept; ++col)
+              row[col] = hs ? static_cast<RS>(bulk_out<T, TS>(bulk_in<T, TS>(row[m.off + 1 + col])))
                             : RS(0);
+            if (a.n_spec == 0) {
+              row[S - 1] = static_cast<RS>(bulk_out<T, TS>(xb[0]));
+            } else {
 #pragma unroll
-            for (int u = 0; u < QM; ++u)
-              if (u < q) row[keep + u] = static_cast<RS>(bulk_out<T, TS>(xb[u]));
+              for (int u = 0; u < QM; ++u)
+                if (u < q) row[keep + u] = static_cast<RS>(bulk_out<T, TS>(xb[u]));
+            }
+          }
+        } else {
+          float pr[SC];
+          R pb[SC];   // the prior window in the activation type
+#pragma unroll
+          for (int i = 0; i < SC; ++i) {
+            pb[i] = hs ? static_cast<R>(bulk_in<T, TS>(row[m.off + i])) : R(0);
+            pr[i] = raw_to_f32<T>(pb[i]);
+          }
+          R xb[QM];
+          float xf[QM];
+#pragma unroll
+          for (int u = 0; u < QM; ++u) {
+            xb[u] = u < q ? xs[u * tile + c] : R(0);
+            xf[u] = raw_to_f32<T>(xb[u]);
+          }
+#pragma unroll
+          for (int i = 0; i < QM; ++i) {
+            if (i < q) {
+              float acc = bv[kc];
+#pragma unroll
+              for (int k = 0; k < W; ++k) {
+                const int idx = SC + i - (W - 1 - k) * DC;   // position in prior ++ tokens
+                acc = fmaf(wk[kc][k], idx >= SC ? xf[idx - SC] : pr[idx], acc);
+              }
+              float y = silu_on ? silu<T>(acc) : acc;
+              if constexpr (FUSED) {
+                y = raw_to_f32<T>(rs[i * tile + c]) + y;
+                if (has_outer) y = y + raw_to_f32<T>(os[i * tile + c]);
+              }
+              xs[i * tile + c] = f32_to_raw<T>(y);
+            }
+          }
+          if (own) {
+            // B[off+1+col] for col < S-1 is pb[col+1]; wider buffers keep more
+            // columns, each read ahead of every write
+#pragma unroll
+            for (int col = 0; col + 1 < SC; ++col)
+              row[col] = static_cast<RS>(bulk_out<T, TS>(pb[col + 1]));
+            if (a.n_spec == 0) {
+              row[SC - 1] = static_cast<RS>(bulk_out<T, TS>(xb[0]));
+            } else {
+              for (int col = SC - 1; col < keep; ++col)
+                row[col] = hs ? static_cast<RS>(
+                                    bulk_out<T, TS>(bulk_in<T, TS>(row[m.off + 1 + col])))
+                              : RS(0);
+#pragma unroll
+              for (int u = 0; u < QM; ++u)
+                if (u < q) row[keep + u] = static_cast<RS>(bulk_out<T, TS>(xb[u]));
+            }
           }
         }
       }
@@ -390,6 +443,23 @@ cudaError_t launch_t(const UpdArgs& a, const BulkArgs& b, size_t smem, cudaStrea
   return cudaGetLastError();
 }
 
+// Widths or dilations above 4: one runtime-dilation kernel per width (the
+// 4-token specialisation is left to the common shapes).
+template <typename T, typename TS, bool FUSED>
+cudaError_t launch_bulk_wide(int W, const UpdArgs& a, const BulkArgs& b, size_t smem,
+                             cudaStream_t st, int dev, int num_sms) {
+  switch (W) {
+#define CCONV_BULK_WIDE(w_) \
+  case w_:                  \
+    return launch_t<T, TS, w_, 0, FUSED, kMaxSpec + 1>(a, b, smem, st, dev, num_sms);
+    CCONV_BULK_WIDE(2) CCONV_BULK_WIDE(3) CCONV_BULK_WIDE(4) CCONV_BULK_WIDE(5)
+    CCONV_BULK_WIDE(6) CCONV_BULK_WIDE(7) CCONV_BULK_WIDE(8)
+#undef CCONV_BULK_WIDE
+    default:
+      return cudaErrorInvalidValue;
+  }
+}
+
 template <typename T, typename TS, bool FUSED>
 cudaError_t launch_wd(int W, int D, const UpdArgs& a, const BulkArgs& b, size_t smem,
                       cudaStream_t st, int dev, int num_sms) {
@@ -397,6 +467,7 @@ cudaError_t launch_wd(int W, int D, const UpdArgs& a, const BulkArgs& b, size_t 
   // (measured faster there; the plain path keeps one instantiation per shape)
   constexpr int kQ4 = (FUSED && sizeof(T) == 2) ? 4 : kMaxSpec + 1;
   const bool q4 = kQ4 == 4 && 1 + a.n_spec <= 4;
+  if (W > 4 || D > 4) return launch_bulk_wide<T, TS, FUSED>(W, a, b, smem, st, dev, num_sms);
 #define CCONV_BULK_CASE(w_, d_)                                                         \
   if (W == w_ && D == d_)                                                               \
     return q4 ? launch_t<T, TS, w_, d_, FUSED, kQ4>(a, b, smem, st, dev, num_sms)       \

@@ -99,7 +99,8 @@ def upd(lib, **kw):
     (dict(x=None), -1), (dict(x=None, out=None, T=0), -3), (dict(w=None), -1), (dict(out=None), -1), (dict(sidx=None), -1),
     (dict(cu=None), -1), (dict(C=12), -1), (dict(C=0), -1), (dict(x=FAKE + 2), -1),
     (dict(out=FAKE + 8), -1), (dict(xrs=8), -1), (dict(ors=20), -1), (dict(dt=5), -1),
-    (dict(act=7), -1), (dict(W=0), -1), (dict(W=5), -2), (dict(D=5), -2), (dict(D=0), -1),
+    (dict(act=7), -1), (dict(W=0), -1), (dict(W=1), -1), (dict(W=9), -1), (dict(D=9), -1),
+    (dict(D=0), -1), (dict(W=8, D=8, pool=_pool(cap=56)), -3), (dict(W=5, D=2, pool=_pool(cap=8)), -3),
     (dict(pool=_pool(cap=2)), -1), (dict(B=-1), -1), (dict(T=-1), -1),
     (dict(pool=_pool(num_slots=0)), -1), (dict(pool=_pool(dtype=2)), -1),
     (dict(pool=_pool(dtype=0, base=FAKE + 2)), -1), (dict(pool=_pool(base=FAKE + 1)), -1)])
@@ -116,7 +117,8 @@ def test_fwd_varlen_empty_batch_is_a_noop(lib):
 @pytest.mark.parametrize("kw,want", [
     (dict(na=None), -1), (dict(ns=8), -2), (dict(ns=-1), -1),
     (dict(pool=_pool(cap=5)), -1), (dict(C=4, dt=1), -1), (dict(x=None), -1),
-    (dict(W=5), -2)])
+    (dict(W=9), -1), (dict(D=9), -1), (dict(W=1), -1), (dict(W=8, D=8, pool=_pool(cap=59)), -3),
+    (dict(W=8, D=8, pool=_pool(cap=58)), -1)])
 @no_gpu
 def test_update_rejects_bad_arguments(lib, kw, want):
     assert upd(lib, **kw) == want
@@ -167,7 +169,8 @@ def test_fwd_fused_checks_its_epilogue(lib, epi, want):
 
 
 @pytest.mark.parametrize("kw,want", [
-    (dict(pool=_pool(cap=65)), -1), (dict(W=5), -2), (dict(num=0), 0), (dict(x=FAKE + 4), -1),
+    (dict(pool=_pool(cap=65)), -1), (dict(W=9), -1), (dict(D=9), -1), (dict(W=8, D=8), -1),
+    (dict(W=8, D=8, pool=_pool(cap=56)), -3), (dict(num=0), 0), (dict(x=FAKE + 4), -1),
     (dict(rows=3, idx=None), -1), (dict(), -3), (dict(pool=_pool(cap=9, dtype=0)), -3),
     (dict(pool=_pool(cap=9, dtype=3)), -1)])
 @no_gpu

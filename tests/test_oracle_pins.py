@@ -74,9 +74,11 @@ def test_bf16_rounding_matches_torch():
 # ---- depthwise varlen vs F.conv1d ----------------------------------------------
 
 CASES = [(w, d) for w in (2, 3, 4) for d in (1, 2, 3)]
+# widths and dilations to 8: corners and the diagonal of the accepted range
+WIDE = [(8, 1), (2, 8), (8, 8), (5, 5), (6, 3), (7, 7), (3, 6)]
 
 
-@pytest.mark.parametrize("W,D", CASES)
+@pytest.mark.parametrize("W,D", CASES + WIDE)
 @pytest.mark.parametrize("act,use_bias", [(0, False), (1, True)])
 def test_fwd_varlen_fp32_matches_conv1d(W, D, act, use_bias):
     S = (W - 1) * D

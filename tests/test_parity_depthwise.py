@@ -108,8 +108,14 @@ def check_upd(case):
 
 # ---- fuzz over width x dilation x dtype --------------------------------------
 
+# widths and dilations above 4 (one runtime-dilation kernel per width): the
+# corners and the diagonal of width 2..8 x dilation 1..8, and mixed ones
+WIDE = [(8, 1), (2, 8), (8, 8), (5, 5), (6, 6), (7, 7), (5, 1), (2, 5), (3, 6), (6, 2), (7, 8),
+        (4, 5)]
+
+
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
-@pytest.mark.parametrize("W,D", [(w, d) for w in (2, 3, 4) for d in (1, 2, 3, 4)])
+@pytest.mark.parametrize("W,D", [(w, d) for w in (2, 3, 4) for d in (1, 2, 3, 4)] + WIDE)
 def test_fwd_varlen_fuzz(W, D, dtype):
     S = (W - 1) * D
     lens = [1, 1, 1, 0, 2, max(1, S - 1), S, S + 1, 63, 64, 65, 129, 200, 7]
@@ -121,7 +127,7 @@ def test_fwd_varlen_fuzz(W, D, dtype):
 
 
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
-@pytest.mark.parametrize("W,D", [(w, d) for w in (2, 3, 4) for d in (1, 2, 3, 4)])
+@pytest.mark.parametrize("W,D", [(w, d) for w in (2, 3, 4) for d in (1, 2, 3, 4)] + WIDE)
 @pytest.mark.parametrize("n_spec", [0, 1, 3, 7])
 def test_update_fuzz(W, D, dtype, n_spec):
     case = synth.depthwise_case(200 + 10 * W + D + n_spec, DEV, lens=[], C=1040 if dtype ==

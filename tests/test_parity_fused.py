@@ -49,7 +49,7 @@ def oracle_fwd_fused(case, res, outer, perm, x_phys):
 
 
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
-@pytest.mark.parametrize("W,D", [(4, 1), (4, 3), (2, 2), (3, 4)])
+@pytest.mark.parametrize("W,D", [(4, 1), (4, 3), (2, 2), (3, 4), (8, 8), (5, 2), (2, 7)])
 @pytest.mark.parametrize("with_outer,with_perm", [(True, True), (False, False), (True, False)])
 def test_fwd_fused(dtype, W, D, with_outer, with_perm):
     S = (W - 1) * D
@@ -80,8 +80,8 @@ def test_fwd_fused(dtype, W, D, with_outer, with_perm):
 @pytest.mark.parametrize("layout", ["DS", "SD"])
 @pytest.mark.parametrize("n_spec", [0, 3])
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
-def test_update_fused(layout, n_spec, dtype):
-    W, D = 4, 3
+@pytest.mark.parametrize("W,D", [(4, 3), (7, 6)])
+def test_update_fused(layout, n_spec, dtype, W, D):
     case = synth.depthwise_case(700 + n_spec, DEV, lens=[], C=520 if dtype == torch.float32
                                 else 1040, width=W, dilation=D, act=1, dtype=dtype, w_std=0.5,
                                 bias_std=0.1, spec_requests=29, n_spec=n_spec, layout=layout)
@@ -195,7 +195,7 @@ def test_bad_row_index_sets_flag_and_skips():
 
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
 @pytest.mark.parametrize("layout", ["DS", "SD", "wide"])
-@pytest.mark.parametrize("W,D", [(4, 3), (2, 1), (3, 4)])
+@pytest.mark.parametrize("W,D", [(4, 3), (2, 1), (3, 4), (8, 8), (6, 5)])
 def test_checkpoint_export(dtype, layout, W, D):
     S = (W - 1) * D
     lens = [3 * S + 5, S, 2 * S, 200]

@@ -43,7 +43,7 @@ def _C(act):
 
 @pytest.mark.parametrize("act,sd", MIX)
 @pytest.mark.parametrize("layout", ["DS", "SD", "wide"])
-@pytest.mark.parametrize("W,D", [(4, 1), (4, 3), (2, 2), (3, 4)])
+@pytest.mark.parametrize("W,D", [(4, 1), (4, 3), (2, 2), (3, 4), (8, 8), (5, 3)])
 def test_fwd_varlen_state_type(act, sd, layout, W, D):
     S = (W - 1) * D
     lens = [1, 1, 1, 0, 2, max(1, S - 1), S, S + 1, 63, 64, 65, 129, 200, 7]
@@ -57,11 +57,12 @@ def test_fwd_varlen_state_type(act, sd, layout, W, D):
 @pytest.mark.parametrize("act,sd", MIX)
 @pytest.mark.parametrize("layout", ["DS", "SD", "wide"])
 @pytest.mark.parametrize("n_spec", [0, 1, 3])
-def test_update_state_type(act, sd, layout, n_spec):
-    W, D = 4, 3
+@pytest.mark.parametrize("W,D", [(4, 3), (6, 4)])
+def test_update_state_type(act, sd, layout, n_spec, W, D):
+    S = (W - 1) * D
     case = synth.depthwise_case(1320 + n_spec, DEV, lens=[], C=_C(act), width=W, dilation=D,
                                 act=1, dtype=act, w_std=0.5, bias_std=0.1, spec_requests=67,
-                                n_spec=n_spec, cap=9 + n_spec + (1 if layout == "wide" else 0))
+                                n_spec=n_spec, cap=S + n_spec + (1 if layout == "wide" else 0))
     g = torch.Generator(device=DEV).manual_seed(13)
     case.spec_has_init = (torch.rand(67, generator=g, device=DEV) < 0.8).to(torch.uint8)
     case.spec_state_idx[::9] = -1
