@@ -9,6 +9,7 @@ import torch
 
 import oracle
 from state_cached_causal_gb300 import ops, synth
+from tests._full import assert_blocks, count_out_of_tol, pmap
 from tests._util import pool_np, to_np
 from tests.test_parity_depthwise import assert_bits_equal, assert_out_close, new_err
 
@@ -161,9 +162,37 @@ def test_cca_rejects_unsupported():
 
 
 @pytest.mark.slow
-def test_zaya_cca_full_sampled():
+def test_zaya_cca_full():
+    """Every group of the zaya_cca launch against the oracle, one group per job
+    on all host cores (the groups are independent; each job keeps its own
+    delayed state, and the delayed half of v and the delayed state are compared
+    once, from group 0's run)."""
     case = synth.zaya_cca(DEV)
-    check(case, groups=[0, 19])
+    err = new_err()
+    out, dprev, pool, dstate = gpu_cca(case, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    qk, got, got_pool = to_np(case.qk), to_np(out), pool_np(pool)
+    w_dw, b_dw, w_gr, b_gr = (to_np(case.w_dw), to_np(case.b_dw), to_np(case.w_gr),
+                              to_np(case.b_gr))
+    want, want_pool = np.zeros_like(got), pool_np(case.pool.clone())
+    delayed, dinit, ds0 = to_np(case.delayed), to_np(case.delayed_init), to_np(case.delayed_state)
+    meta = (to_np(case.state_idx), to_np(case.cu_seqlens), to_np(case.has_init))
+    gs = case.Cqk // case.groups
+    opt = lambda a, sl: None if a is None else a[sl]
+
+    def group(g):
+        sl = slice(g * gs, (g + 1) * gs)
+        ds, dp = ds0.copy(), np.zeros_like(delayed)
+        oracle.cca_qk_conv(qk[:, sl], w_dw[sl], opt(b_dw, sl), w_gr[sl], opt(b_gr, sl), 1,
+                           case.t0, case.t1, delayed, dinit, want_pool[:, sl, :], ds, *meta,
+                           want[:, sl], dp)
+        n, e = count_out_of_tol(got[:, sl], want[:, sl], True)
+        return sl, n, e, int((got_pool[:, sl, :] != want_pool[:, sl, :]).sum()), dp, ds
+    res = pmap(group, range(case.groups))
+    assert_blocks([r[:4] for r in res], "zaya_cca")
+    assert_bits_equal(to_np(dprev), res[0][4], "delayed_prev")
+    assert_bits_equal(to_np(dstate), res[0][5], "delayed_state")
 
 
 # ---- the fused tail of ZayaCCA.project ----------------------------------------

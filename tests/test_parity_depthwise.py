@@ -10,6 +10,7 @@ import torch
 
 import oracle
 from state_cached_causal_gb300 import ops, synth
+from tests._full import assert_blocks, channel_blocks, count_out_of_tol, pmap
 from tests._util import np_to_f64, pool_np, to_np
 
 pytestmark = pytest.mark.gpu
@@ -349,33 +350,60 @@ def _slices(C):
     return [slice(0, 64), slice(C // 2 - 40, C // 2 + 24), slice(C - 64, C)]
 
 
+def check_full(case, out=None, out_s=None, pool=None, what=""):
+    """Every channel of a full-size launch against the oracle: the varlen outputs
+    (out), then the update outputs (out_s) on the pool the varlen call left, both
+    within the tolerance, and the whole pool -- used and unused slots -- bit for
+    bit. The oracle runs on channel blocks on all host cores."""
+    bf16 = case.dtype == torch.bfloat16
+    w = to_np(case.w)
+    b = None if case.bias is None else to_np(case.bias)
+    want_pool = pool_np(case.pool.clone())
+    got_pool = pool_np(pool)
+    jobs = []
+    if out is not None:
+        x, got = to_np(case.x), to_np(out)
+        want = np.zeros_like(got)
+        meta = (to_np(case.state_idx), to_np(case.cu_seqlens), to_np(case.has_init))
+        jobs.append(lambda sl: (oracle.cconv_fwd_varlen(
+            x[:, sl], w[sl], None if b is None else b[sl], want_pool[:, sl, :], *meta,
+            case.width, case.dilation, case.act, want[:, sl]), (got, want))[1])
+    if out_s is not None:
+        xs, got_s = to_np(case.x_spec), to_np(out_s)
+        want_s = np.zeros_like(got_s)
+        na = to_np(case.num_accepted) if case.n_spec else None
+        sidx, shi = to_np(case.spec_state_idx), to_np(case.spec_has_init)
+        jobs.append(lambda sl: (oracle.cconv_update(
+            xs[:, sl], want_pool[:, sl, :], w[sl], None if b is None else b[sl], sidx,
+            case.n_spec, na, shi, case.width, case.dilation, case.act, want_s[:, sl]),
+            (got_s, want_s))[1])
+
+    def block(sl):
+        bad, worst = 0, 0.0
+        for job in jobs:                       # varlen first, then the update
+            g, wnt = job(sl)
+            n, e = count_out_of_tol(g[:, sl], wnt[:, sl], bf16)
+            bad, worst = bad + n, max(worst, e)
+        return sl, bad, worst, int((got_pool[:, sl, :] != want_pool[:, sl, :]).sum())
+    assert_blocks(pmap(block, channel_blocks(case.C)), what)
+
+
 @pytest.mark.slow
-def test_gdn_mixed_full_sampled():
+def test_gdn_mixed_full():
     case = synth.gdn_mixed(DEV)
     err = new_err()
     out, pool = gpu_fwd(case, err=err)
     torch.cuda.synchronize()
     assert int(err.item()) == 0
-    for sl in _slices(case.C):
-        want_out, want_pool = oracle_fwd(case, chans=sl)
-        assert_out_close(to_np(out)[:, sl], want_out, case.dtype)
-        assert_bits_equal(pool_np(pool)[:, sl, :], want_pool)
-    used = set(case.state_idx.tolist())
-    unused = torch.tensor([s for s in range(pool.shape[0]) if s not in used], device=DEV)
-    assert torch.equal(pool[unused], case.pool[unused])
+    check_full(case, out=out, pool=pool, what="gdn_mixed")
 
 
 @pytest.mark.slow
-def test_ple_spec_full_sampled():
+def test_ple_spec_full():
     case = synth.ple_spec(DEV)
     err = new_err()
     out, pool = gpu_fwd(case, err=err)
     out_s, pool = gpu_upd(case, pool=pool, err=err)
     torch.cuda.synchronize()
     assert int(err.item()) == 0
-    for sl in _slices(case.C):
-        want_out, want_pool = oracle_fwd(case, chans=sl)
-        want_s, want_pool = oracle_upd(case, pool_np_in=want_pool, chans=sl)
-        assert_out_close(to_np(out)[:, sl], want_out, case.dtype)
-        assert_out_close(to_np(out_s)[:, sl], want_s, case.dtype, "spec out")
-        assert_bits_equal(pool_np(pool)[:, sl, :], want_pool)
+    check_full(case, out=out, out_s=out_s, pool=pool, what="ple_spec")

@@ -1,10 +1,10 @@
 """GPU parity at full size for the paths bench.py times beyond the hybrid step:
 the fused PLE dispatch (spec + prefill rows in one physical tensor, random
 request order), the fused Zaya tail, and fp32 conv-state pools under bf16
-activations. The library runs the whole launch; the oracle checks sampled
-channel slices (each channel is independent in the depthwise conv) or one kv
-group (the fused CCA couples a kv group's query and key heads), whose values it
-computes exactly.
+activations. The library runs the whole launch; the oracle checks every
+channel (each depthwise channel is independent: channel blocks on all host
+cores) and every kv group of the fused CCA (a kv group's query and key heads
+are coupled: one job per kv group).
 """
 import numpy as np
 import pytest
@@ -13,8 +13,9 @@ import torch
 import oracle
 from state_cached_causal_gb300 import ops, synth
 from tests._util import pool_np, to_np
-from tests.test_parity_depthwise import (_slices, assert_bits_equal, assert_out_close, gpu_fwd,
-                                         gpu_upd, new_err, oracle_fwd, oracle_upd)
+from tests._full import assert_blocks, channel_blocks, count_out_of_tol, pmap
+from tests.test_parity_depthwise import (assert_bits_equal, check_full, gpu_fwd, gpu_upd,
+                                         new_err)
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 DEV = torch.device("cuda")
@@ -26,34 +27,26 @@ def _f32_pool(case, seed):
     return case
 
 
-def test_gdn_mixed_fp32_state_full_sampled():
+def test_gdn_mixed_fp32_state_full():
     case = _f32_pool(synth.gdn_mixed(DEV), 3001)
     err = new_err()
     out, pool = gpu_fwd(case, err=err)
     torch.cuda.synchronize()
     assert int(err.item()) == 0
-    for sl in _slices(case.C):
-        want_out, want_pool = oracle_fwd(case, chans=sl)
-        assert_out_close(to_np(out)[:, sl], want_out, case.dtype)
-        assert_bits_equal(pool_np(pool)[:, sl, :], want_pool)
+    check_full(case, out=out, pool=pool, what="gdn_mixed, fp32 state")
 
 
-def test_ple_spec_fp32_state_full_sampled():
+def test_ple_spec_fp32_state_full():
     case = _f32_pool(synth.ple_spec(DEV), 3002)
     err = new_err()
     out, pool = gpu_fwd(case, err=err)
     out_s, pool = gpu_upd(case, pool=pool, err=err)
     torch.cuda.synchronize()
     assert int(err.item()) == 0
-    for sl in _slices(case.C):
-        want_out, want_pool = oracle_fwd(case, chans=sl)
-        want_s, want_pool = oracle_upd(case, pool_np_in=want_pool, chans=sl)
-        assert_out_close(to_np(out)[:, sl], want_out, case.dtype)
-        assert_out_close(to_np(out_s)[:, sl], want_s, case.dtype, "spec out")
-        assert_bits_equal(pool_np(pool)[:, sl, :], want_pool)
+    check_full(case, out=out, out_s=out_s, pool=pool, what="ple_spec, fp32 state")
 
 
-def test_ple_fused_full_sampled():
+def test_ple_fused_full():
     # the ple_spec batch with every request's rows at a random place of one
     # physical tensor: spec requests through cconv_update_fused, prefills
     # through cconv_fwd_varlen_fused, residual += conv + outer residual
@@ -81,25 +74,30 @@ def test_ple_fused_full_sampled():
                                idx_p, dev_err=err)
     torch.cuda.synchronize()
     assert int(err.item()) == 0
-    for sl in _slices(C):
-        sub = lambda t: np.ascontiguousarray(to_np(t)[:, sl])
-        want = sub(res)
-        want_pool = pool_np(case.pool)[:, sl, :].copy()
-        w = np.ascontiguousarray(to_np(case.w)[sl])
-        oracle.cconv_update_fused(sub(x), want_pool, w, None, to_np(case.spec_state_idx),
-                                  case.n_spec, to_np(case.num_accepted), None, case.width,
-                                  case.dilation, case.act, want, sub(outer), to_np(idx_s))
-        oracle.cconv_fwd_varlen_fused(sub(x), w, None, want_pool, to_np(case.state_idx),
-                                      to_np(case.cu_seqlens), to_np(case.has_init), case.width,
-                                      case.dilation, case.act, want, sub(outer), to_np(idx_p))
-        assert_out_close(to_np(got)[:, sl], want, case.dtype, "residual")
-        assert_bits_equal(pool_np(pool)[:, sl, :], want_pool)
+    xn, resn, outern, gotn = to_np(x), to_np(res), to_np(outer), to_np(got)
+    want, want_pool, got_pool = resn.copy(), pool_np(case.pool.clone()), pool_np(pool)
+    wn = to_np(case.w)
+    sidx, na, ip = to_np(case.spec_state_idx), to_np(case.num_accepted), to_np(idx_s)
+    meta, ipp = (to_np(case.state_idx), to_np(case.cu_seqlens), to_np(case.has_init)), to_np(idx_p)
+
+    def block(sl):
+        oracle.cconv_update_fused(xn[:, sl], want_pool[:, sl, :], wn[sl], None, sidx,
+                                  case.n_spec, na, None, case.width, case.dilation, case.act,
+                                  want[:, sl], outern[:, sl], ip)
+        oracle.cconv_fwd_varlen_fused(xn[:, sl], wn[sl], None, want_pool[:, sl, :], *meta,
+                                      case.width, case.dilation, case.act, want[:, sl],
+                                      outern[:, sl], ipp)
+        n, e = count_out_of_tol(gotn[:, sl], want[:, sl], True)
+        return sl, n, e, int((got_pool[:, sl, :] != want_pool[:, sl, :]).sum())
+    assert_blocks(pmap(block, channel_blocks(C)), "ple_fused")
 
 
-def test_zaya_fused_full_one_kv_group():
-    # 16 query + 4 key heads; kv group j = 1 is query heads 4..7 and key head 1
+def test_zaya_fused_full():
+    # 16 query + 4 key heads: kv group j is query heads 4j .. 4j+3 and key head j;
+    # one oracle job per kv group on the host cores, the value half once
     cc = synth.zaya_cca(DEV)
     Hq, Hkv, hd = 16, 4, 128
+    kvg = Hq // Hkv
     T = int(cc.qk.shape[0])
     g = torch.Generator(device=DEV).manual_seed(3005)
     v_cur = torch.randn(T, cc.Dv, generator=g, device=DEV).to(torch.bfloat16)
@@ -111,23 +109,29 @@ def test_zaya_fused_full_one_kv_group():
                           cc.cu_seqlens, cc.has_init, out, dev_err=err)
     torch.cuda.synchronize()
     assert int(err.item()) == 0
-    heads = [4, 5, 6, 7, Hq + 1]
-    chans = np.concatenate([np.arange(h * hd, (h + 1) * hd) for h in heads])
-    sub = lambda a: None if a is None else np.ascontiguousarray(a[chans])
-    qk = np.ascontiguousarray(to_np(cc.qk)[:, chans])
-    p = pool_np(cc.pool)[:, chans, :].copy()
-    ds = to_np(cc.delayed_state).copy()
-    conv = np.zeros_like(qk)
-    dprev = np.zeros_like(to_np(cc.delayed))
-    oracle.cca_qk_conv(qk, sub(to_np(cc.w_dw)), sub(to_np(cc.b_dw)), sub(to_np(cc.w_gr)),
-                       sub(to_np(cc.b_gr)), len(heads), cc.t0, cc.t1, to_np(cc.delayed),
-                       to_np(cc.delayed_init), p, ds, to_np(cc.state_idx),
-                       to_np(cc.cu_seqlens), to_np(cc.has_init), conv, dprev)
-    want = np.zeros((T, len(heads) * hd + 2 * (hd // 2)), dtype=np.uint16)
-    oracle.cca_project_epilogue(qk, conv, to_np(v_cur), dprev, 4, 1, want)
-    got = to_np(out)
-    assert_out_close(got[:, chans], want[:, :len(heads) * hd], torch.bfloat16, "query|key")
-    assert_bits_equal(got[:, cc.Cqk:cc.Cqk + cc.Dv], to_np(v_cur), "v_current")
-    assert_bits_equal(got[:, cc.Cqk + cc.Dv:], dprev, "delayed_prev")
-    assert_bits_equal(pool_np(pool)[:, chans, :], p, "conv_state")
-    assert_bits_equal(to_np(dstate), ds, "delayed_state")
+    got, got_pool = to_np(out), pool_np(pool)
+    qk_all, pool0, ds0 = to_np(cc.qk), pool_np(cc.pool), to_np(cc.delayed_state)
+    w_dw, b_dw, w_gr, b_gr = (to_np(t) for t in (cc.w_dw, cc.b_dw, cc.w_gr, cc.b_gr))
+    delayed, dinit, vc = to_np(cc.delayed), to_np(cc.delayed_init), to_np(v_cur)
+    meta = (to_np(cc.state_idx), to_np(cc.cu_seqlens), to_np(cc.has_init))
+
+    def kv_group(j):
+        heads = list(range(j * kvg, (j + 1) * kvg)) + [Hq + j]
+        chans = np.concatenate([np.arange(h * hd, (h + 1) * hd) for h in heads])
+        sub = lambda a: None if a is None else np.ascontiguousarray(a[chans])
+        qk = np.ascontiguousarray(qk_all[:, chans])
+        p = pool0[:, chans, :].copy()
+        ds = ds0.copy()
+        conv, dprev = np.zeros_like(qk), np.zeros_like(delayed)
+        oracle.cca_qk_conv(qk, sub(w_dw), sub(b_dw), sub(w_gr), sub(b_gr), len(heads), cc.t0,
+                           cc.t1, delayed, dinit, p, ds, *meta, conv, dprev)
+        want = np.zeros((T, len(heads) * hd + 2 * (hd // 2)), dtype=np.uint16)
+        oracle.cca_project_epilogue(qk, conv, vc, dprev, kvg, 1, want)
+        n, e = count_out_of_tol(got[:, chans], want[:, :len(heads) * hd], True)
+        neq = int((got_pool[:, chans, :] != p).sum())
+        return chans, n, e, neq, dprev, ds
+    res = pmap(kv_group, range(Hkv))
+    assert_blocks([r[:4] for r in res], "zaya fused query|key")
+    assert_bits_equal(got[:, cc.Cqk:cc.Cqk + cc.Dv], vc, "v_current")
+    assert_bits_equal(got[:, cc.Cqk + cc.Dv:], res[0][4], "delayed_prev")
+    assert_bits_equal(to_np(dstate), res[0][5], "delayed_state")
