@@ -73,10 +73,13 @@ constexpr int kAccCols = 128;                          // fp32 accumulator colum
 constexpr int kTmemCols = 2 * kAccCols;
 constexpr long long kWaitCycles = 2000000000LL;        // ~1 s at GB300 clocks
 constexpr int kDerrTimeout = CCONV_DERR_TIMEOUT;
-constexpr int kOutRowPitch = 80;                       // 64 bytes of a row + 16 (no bank conflicts)
+constexpr int kOutRowPitch = 64;                       // 64 bytes of a row, 16-byte chunks swizzled
 constexpr int kEpiCols = kGS / (kEpiWarps / 4);       // accumulator columns per epilogue warp
 constexpr int kProdRows = kRows / (kProdWarps * 2);    // rows per producer thread (16 per chunk)
 constexpr int kOutStageBytes = 32 * kOutRowPitch + kEpiCols * 4;   // per epilogue warp, + bias
+
+// Requests whose metadata the kernel copies into shared memory (9 bytes each).
+constexpr int kSmemRequests = 352;
 
 struct Meta {
   int lo, len, g, own_lo, own_hi;
@@ -587,6 +590,25 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
+  // A batch of at most kSmemRequests requests keeps its cu_seqlens, state_idx
+  // and has_init in shared memory: the scheduler and the aux warps read them
+  // several times per tile, and global reads of them wait on L2.
+  if (a.B <= kSmemRequests) {
+    int32_t* s_cu = reinterpret_cast<int32_t*>(ctl + 1);
+    int32_t* s_sidx = s_cu + a.B + 1;
+    uint8_t* s_hini = reinterpret_cast<uint8_t*>(s_sidx + a.B);
+    for (int k = threadIdx.x; k <= a.B; k += blockDim.x) {
+      s_cu[k] = a.cu[k];
+      if (k < a.B) {
+        s_sidx[k] = a.state_idx[k];
+        if (hini) s_hini[k] = hini[k];
+      }
+    }
+    cu = s_cu;
+    sidx = s_sidx;
+    if (hini) hini = s_hini;
+  }
+
   if (threadIdx.x == 0) {
     for (int i = 0; i < kMetaStages; ++i) {
       mbar_init(&ctl->meta_full[i], 1);
@@ -664,6 +686,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       unit_to_gt<FUSED>(a, u, g, tau);
       const bool cont = (g == prev_g && tau == prev_tau + 1);
       const int lo = cont ? hi_prev : tile_edge(a, cu, tau, 0);
+      // x rows [lo - n, lo - n + kXBoxRows) of the group's channels: issued
+      // first, so that the load runs while the rest of the metadata is found
+      if (!W.wait(&ctl->x_empty[xs], ((i / kXStages) & 1) ^ 1)) break;
+      if (lane == 0) {
+        if (a.T > 0) {
+          mbar_arrive_tx(&ctl->x_full[xs], kXStageBytes);
+          tma_load_2d(sX + xs * kXStageBytes, &xmap, g * kGS, lo - a.n, &ctl->x_full[xs]);
+        } else {
+          mbar_arrive(&ctl->x_full[xs]);
+        }
+      }
+      __syncwarp();
+      ++issued;
       const int own_lo = cont ? own_hi_prev : count_le(cu, a.B, lo, true, 0);
       const int nle_lo = count_le(cu, a.B, lo, false, own_lo);   // requests with cu <= lo
       const int hi = tile_edge(a, cu, tau + 1, nle_lo);
@@ -690,13 +725,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         single = ok ? 1 : 0;
       } else {
+        // Rows of several requests: row r's request is the last s with
+        // cu[s] <= its token, found for 32 rows at once against windows of 32
+        // cu values (every row's token compared with every value of the
+        // window); the next 32 rows start from the last row's request.
         for (int r0 = 0; r0 < kRows; r0 += 32) {
           const int r = r0 + lane;
-          const int t = lo + r;
+          const int t = lo + min(r, max(len - 1, 0));   // rows past the tile repeat the last
+          int sr = sc, wb = sc;
+          bool found = false;
+          for (;;) {
+            const int idx = wb + 1 + lane;
+            const int v = idx < a.B ? cu[idx] : 0x7fffffff;
+            int cnt = 0;
+#pragma unroll 8
+            for (int k = 0; k < 32; ++k) {
+              const int tk = __shfl_sync(0xffffffffu, t, k);
+              const unsigned m = __ballot_sync(0xffffffffu, v <= tk);
+              if (lane == k) cnt = __popc(m);
+            }
+            if (!found) {
+              sr = wb + cnt;
+              found = cnt < 32;
+            }
+            if (__all_sync(0xffffffffu, found)) break;
+            wb += 32;
+          }
           int j = -1, slot = -1, wr = -1;
           if (r < len) {
-            int sr = sc;
-            while (sr + 1 < a.B && cu[sr + 1] <= t) ++sr;
             const int st = cu[sr], en = cu[sr + 1];
             if (st >= 0 && st <= t && t < en && en <= a.T) {
               const int sl = sidx[sr];
@@ -711,8 +767,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           M.rowj[r] = j;
           M.rowslot[r] = slot;
           M.rowwr[r] = wr;
-          const int last = min(lo + r0 + 31, hi - 1);   // same walk on every lane
-          while (sc + 1 < a.B && cu[sc + 1] <= last) ++sc;
+          sc = __shfl_sync(0xffffffffu, sr, 31);
         }
       }
       if (lane == 0) {
@@ -725,18 +780,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&ctl->meta_full[ms]);
-      // x rows [lo - n, lo - n + kXBoxRows) of the group's channels
-      if (!W.wait(&ctl->x_empty[xs], ((i / kXStages) & 1) ^ 1)) break;
-      if (lane == 0) {
-        if (a.T > 0) {
-          mbar_arrive_tx(&ctl->x_full[xs], kXStageBytes);
-          tma_load_2d(sX + xs * kXStageBytes, &xmap, g * kGS, lo - a.n, &ctl->x_full[xs]);
-        } else {
-          mbar_arrive(&ctl->x_full[xs]);
-        }
-      }
-      __syncwarp();
-      ++issued;
       prev_g = g;
       prev_tau = tau;
       hi_prev = hi;
@@ -795,18 +838,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3;
     const int ew = warp - kWarpEpi0;
     const int half = ew >> 2;                    // which kEpiCols columns
-    unsigned char* stage = sOut + ew * kOutStageBytes;   // 32 rows x 64 bytes, padded
+    // 32 rows x 64 bytes: chunk c of row r sits at chunk c ^ ((r >> 1) & 3), so
+    // that both the row-per-lane writes and the 8-rows-by-64-bytes reads
+    // below touch eight different 16-byte bank groups per quarter warp
+    unsigned char* stage = sOut + ew * kOutStageBytes;
+    auto stage_at = [&](int r, int c) { return stage + r * kOutRowPitch + ((c ^ ((r >> 1) & 3)) << 4); };
     float* sbias = reinterpret_cast<float*>(stage + 32 * kOutRowPitch);   // this half's bias
+    int bias_g = -1;                                                     // group held in sbias
     for (int i = 0;; ++i) {
       const int ms = i % kMetaStages, ab = i & 1;
       if (!W.wait(&ctl->meta_full[ms], (i / kMetaStages) & 1)) break;
       if (meta[ms].g < 0) break;
       const Meta& M = meta[ms];
       const int g = M.g, lo = M.lo, len = M.len;
-      for (int k = lane; k < kEpiCols; k += 32)
-        sbias[k] = a.b_gr ? cconv::load_f32<__nv_bfloat16>(a.b_gr, (int64_t)g * kGS +
-                                                                     half * kEpiCols + k)
-                          : 0.0f;
+      if (g != bias_g) {   // the bias changes with the group only
+        for (int k = lane; k < kEpiCols; k += 32)
+          sbias[k] = a.b_gr ? cconv::load_f32<__nv_bfloat16>(a.b_gr, (int64_t)g * kGS +
+                                                                       half * kEpiCols + k)
+                            : 0.0f;
+        __syncwarp();
+        bias_g = g;
+      }
 
       // FUSED: this lane's residual terms (rows q*32 + k*8 + lane/4, channel
       // chunks c), gathered while the tile's MMA runs
@@ -849,15 +901,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           float hh[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e) hh[e] = __uint_as_float(cur[k + e]) + bb[e];
-          *reinterpret_cast<uint4*>(stage + lane * kOutRowPitch + k * 2) =
-              cconv::pack16<__nv_bfloat16>(hh);
+          *reinterpret_cast<uint4*>(stage_at(lane, k / 8)) = cconv::pack16<__nv_bfloat16>(hh);
         }
         __syncwarp();
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           const int rr = k * 8 + (lane >> 2);    // row within this warp's 32
           const int tr = q * 32 + rr;            // row within the tile
-          uint4 v = *reinterpret_cast<const uint4*>(stage + rr * kOutRowPitch + seg * 16);
+          uint4 v = *reinterpret_cast<const uint4*>(stage_at(rr, seg));
           if (tr < len && M.rowj[tr] >= 0) {
             const int cc = half * kEpiCols + c * 32 + seg * 8;   // channel within the head
             if constexpr (FUSED) v = add_residual(g < a.Hq, resid[c][k], v);
@@ -899,9 +950,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int c0 = g * kGS + kc * 8;
       if (g != cur_g) {
         // B operand of group g: B[tap][k-chunk][n] = w_gr[g*128 + n][k-chunk*8 + e][tap]
-        // (unrolled by two: a second row's loads in flight, little code)
+        // (unrolled by eight: eight rows' loads in flight)
         constexpr int kBIter = kGS * (kGS / 8) / (kProdWarps * 32);
-#pragma unroll 2
+#pragma unroll 8
         for (int it = 0; it < kBIter; ++it) {
           const int pr = p + it * (kProdWarps * 32);
           const int o = pr & (kGS - 1), bkc = pr >> 7;
@@ -1304,7 +1355,8 @@ static EncodeTiledFn encode_fn() {
 
 static size_t smem_bytes(int T1) {
   return 1024 + (size_t)T1 * kTapB + 2 * (size_t)kABuf + (size_t)kXStages * kXStageBytes +
-         (size_t)kEpiWarps * kOutStageBytes + kMetaStages * sizeof(Meta) + sizeof(Ctl);
+         (size_t)kEpiWarps * kOutStageBytes + kMetaStages * sizeof(Meta) + sizeof(Ctl) +
+         (size_t)kSmemRequests * 9 + 4;
 }
 
 template <int T0, int T1, bool FUSED>
