@@ -39,6 +39,7 @@ METRIC = ("causal-conv G(tokens·channels)/s and achieved HBM GB/s vs GB300 peak
 UNIT = "G(tokens*channels)/s"
 FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 7900.0    # GB300 HBM3e data-sheet bandwidth (context beside the measured peak)
+LEAD_CYCLES = 2_000_000     # device-side wait (about 1 ms) queued ahead of a timed region
 
 
 # ---- workloads ---------------------------------------------------------------
@@ -587,6 +588,10 @@ def arm_ours(args):
         dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(dev.index) as clk:
+        # a short device-side wait first, so that the host has queued the first
+        # launches when the timed region begins (the region then measures the
+        # device, not the host's first enqueue)
+        torch.cuda._sleep(LEAD_CYCLES)
         start.record(stream)
         for k in range(args.steps):
             for c, (a, b) in zip(calls, ev[k]):
@@ -712,6 +717,7 @@ def e2e_run(args, calls, stream, dev, ws):
     step()
     torch.cuda.synchronize()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda._sleep(LEAD_CYCLES)
     a.record(stream)
     s_in.wait_event(a)
     s_out.wait_event(a)

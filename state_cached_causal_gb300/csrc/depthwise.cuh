@@ -188,13 +188,61 @@ __global__ void __launch_bounds__(128, (W <= 4 ? 4 : 2)) fwd_varlen_kernel(const
       return r;
   };
 
+  uint4* blk = dyn_smem + tid;                       // pool columns (chunk 0 only)
+
+  // A one-token sequence (a decode in a mixed batch) skips the stream: its
+  // token, the unit's weights and its history are all requested at once, the
+  // output and the shifted history written back; one round trip to memory
+  // instead of the ring's fill and drain.
+  if constexpr (!FUSED) {
+    if (L == 1) {
+      const uint4 xr = ldg16(xs);
+      float wk[W][V], bv[V];
+#pragma unroll
+      for (int v = 0; v < V; ++v) {
+#pragma unroll
+        for (int k = 0; k < W; ++k) wk[k][v] = load_f32<T>(a.w, (int64_t)(c0 + v) * W + k);
+        bv[v] = a.bias ? load_f32<T>(a.bias, c0 + v) : 0.0f;
+      }
+      if (slot >= 0) pool_load<T>(a.pool, slot, c0, S, blk, nt);
+      if (!hs)
+        for (int col = 0; col < S; ++col) blk[col * nt] = make_uint4(0u, 0u, 0u, 0u);
+      float xv[V], y[V];
+      unpack16<T>(xr, xv);
+      const bool silu_on = a.act == CCONV_ACT_SILU;
+#pragma unroll
+      for (int v = 0; v < V; ++v) y[v] = bv[v];
+#pragma unroll
+      for (int k = 0; k < W; ++k) {
+        // tap k reads history column S - (W-1-k)*D, or the token for k = W-1
+        float hv[V];
+        if (k == W - 1) {
+#pragma unroll
+          for (int v = 0; v < V; ++v) hv[v] = xv[v];
+        } else {
+          unpack16<T>(blk[(S - (W - 1 - k) * D) * nt], hv);
+        }
+#pragma unroll
+        for (int v = 0; v < V; ++v) y[v] = fmaf(wk[k][v], hv[v], y[v]);
+      }
+#pragma unroll
+      for (int v = 0; v < V; ++v) y[v] = silu_on ? silu<T>(y[v]) : y[v];
+      stg16(os, pack16<T>(y));
+      if (slot >= 0) {
+        for (int i = 0; i + 1 < S; ++i) blk[i * nt] = blk[(i + 1) * nt];
+        blk[(S - 1) * nt] = xr;
+        pool_store<T>(a.pool, slot, c0, S, blk, nt);
+      }
+      return;
+    }
+  }
+
   // Token rows stream through a per-thread ring of 16-byte units in shared
   // memory, PF rows ahead of use (cp.async, no registers held while in
   // flight). Stream order = the order of use: dilation class rho = 0..D-1,
   // and within a class its W-1 window rows before the chunk (rows before the
   // sequence come from the state instead: their entries load nothing), then
   // rows r0+rho, r0+rho+D, ...
-  uint4* blk = dyn_smem + tid;                       // pool columns (chunk 0 only)
   uint4* ring = dyn_smem + a.pool.cap * nt + tid;    // RING stream slots of NU units
   const uint32_t ring0 = smem_addr(ring);
   const uint32_t unit_bytes = nt * 16, slot_bytes = NU * unit_bytes;
