@@ -181,6 +181,13 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
   const int n = (int)((int64_t)(blockIdx.x + 1) * b.items / gridDim.x - i0);
   const int q = 1 + a.n_spec, cap = a.pool.cap;
   const int tile = b.tile;
+  // bf16 slabs whose cap columns are whole 8-byte words (cap a multiple of 4,
+  // at most 16) and exactly S + n_spec, with n_spec <= 3, are read and written
+  // as words: the per-column 2-byte accesses of the roll were the kernel's
+  // busiest unit
+  constexpr bool kPackable = sizeof(T) == 2 && sizeof(TS) == 2 && DC > 0 && SC <= 16;
+  const bool packed = kPackable && (cap & 3) == 0 && cap <= 16 && cap == S + a.n_spec &&
+                      a.n_spec <= 3;
 
   if (tid == 0) {
     for (int k = 0; k < NS; ++k) {
@@ -350,11 +357,29 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
         } else {
           float pr[SC];
           R pb[SC];   // the prior window in the activation type
+          if (kPackable && packed) {
+            // the cap columns as cap/4 8-byte words; the window starts 16*off
+            // bits in (off <= 3)
+            uint64_t pw[4] = {0ull, 0ull, 0ull, 0ull};
+            const uint64_t* rw = reinterpret_cast<const uint64_t*>(row);
 #pragma unroll
-          for (int i = 0; i < SC; ++i) {
-            pb[i] = hs ? static_cast<R>(bulk_in<T, TS>(row[m.off + i])) : R(0);
-            pr[i] = raw_to_f32<T>(pb[i]);
+            for (int k = 0; k < 4; ++k)
+              if (hs && k < cap / 4) pw[k] = rw[k];
+            const int sh = 16 * m.off;
+            uint64_t sw[4];
+#pragma unroll
+            for (int k = 0; k < 3; ++k) sw[k] = sh ? (pw[k] >> sh) | (pw[k + 1] << (64 - sh)) : pw[k];
+            sw[3] = pw[3] >> sh;
+#pragma unroll
+            for (int i = 0; i < SC; ++i)
+              pb[i] = static_cast<R>((sw[(i >> 2) & 3] >> (16 * (i & 3))) & 0xffffu);
+          } else {
+#pragma unroll
+            for (int i = 0; i < SC; ++i)
+              pb[i] = hs ? static_cast<R>(bulk_in<T, TS>(row[m.off + i])) : R(0);
           }
+#pragma unroll
+          for (int i = 0; i < SC; ++i) pr[i] = raw_to_f32<T>(pb[i]);
           R xb[QM];
           float xf[QM];
 #pragma unroll
@@ -379,7 +404,24 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
               xs[i * tile + c] = f32_to_raw<T>(y);
             }
           }
-          if (own) {
+          if (own && kPackable && packed) {
+            // the new buffer, prior[1, S) ++ tokens (cap = S - 1 + q columns),
+            // written back as cap/4 8-byte words
+            uint64_t nw[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              uint64_t v = 0ull;
+              if (e + 1 < SC)
+                v = pb[(e + 1) % SC];
+              else if (e - (SC - 1) < QM)
+                v = xb[(e - (SC - 1)) % QM];
+              nw[e >> 2] |= v << (16 * (e & 3));
+            }
+            uint64_t* ww = reinterpret_cast<uint64_t*>(row);
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              if (k < cap / 4) ww[k] = nw[k];
+          } else if (own) {
             // B[off+1+col] for col < S-1 is pb[col+1]; wider buffers keep more
             // columns, each read ahead of every write
 #pragma unroll
