@@ -322,6 +322,15 @@ CCONV_API int cconv_checkpoint_export(const void* x, int64_t x_row_stride, cconv
  *                     "State type"; an fp32 delayed state left as it is by an
  *                     empty request with has_init keeps its bits)
  *   t0 1..4, t1 1..2, dtype CCONV_DTYPE_BF16 (fp32 returns -2), Dv % 8 == 0
+ *
+ * Launches in flight. The kernel balances its work with two counters in one
+ * of 64 slots inside the library, taken in turn by successive calls (of this
+ * entry point and of cca_qk_conv_fused); the last CTA of a launch clears its
+ * slot. At most 64 launches may therefore run at the same time: a 65th
+ * overlapping one, or a replay of a captured CUDA graph (which keeps the slot
+ * it was captured with) running beside a later call that drew the same slot,
+ * shares the counters and may skip or repeat work without an error.
+ * cca_qk_conv_noalloc keeps its counters in one array of its own instead.
  */
 CCONV_API int cca_qk_conv(const void* qk, int64_t qk_row_stride, const void* w_dw, const void* b_dw,
                 const void* w_gr, const void* b_gr, int32_t groups, int32_t t0, int32_t t1,

@@ -100,5 +100,28 @@ def build(verbose: bool = False, extra_flags=None, jobs: int | None = None) -> s
     return LIB
 
 
+def build_cca_variant(out_dir: str, extra_flags) -> str:
+    """The CCA entry points alone (``cca_qk_conv.cu`` and the status strings),
+    compiled with extra nvcc flags into ``out_dir/libcconv_cca.so``: the tests
+    build one with a short pipeline-wait limit (``-DCCA_WAIT_CYCLES=...``) to
+    run the kernel's timeout path."""
+    os.makedirs(out_dir, exist_ok=True)
+    nvcc = _nvcc()
+    objs = []
+    for name in ("cca_qk_conv.cu", "abi.cu"):
+        obj = os.path.join(out_dir, name + ".o")
+        cmd = [nvcc] + CFLAGS + list(extra_flags) + ["-c", os.path.join(CSRC, name), "-o", obj]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"nvcc failed on {name}:\n{r.stdout}\n{r.stderr}")
+        objs.append(obj)
+    lib = os.path.join(out_dir, "libcconv_cca.so")
+    r = subprocess.run([nvcc] + ARCH + ["-shared", "-o", lib] + objs, capture_output=True,
+                       text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
+    return lib
+
+
 if __name__ == "__main__":
     print(build(verbose=True))

@@ -71,7 +71,16 @@ constexpr int kLboB = kGS * 16;                        // k-chunk stride of B: 2
 constexpr int kTapB = (kGS / 8) * kLboB;               // one tap of B: 32768 B
 constexpr int kAccCols = 128;                          // fp32 accumulator columns
 constexpr int kTmemCols = 2 * kAccCols;
-constexpr long long kWaitCycles = 2000000000LL;        // ~1 s at GB300 clocks
+// Limit of a pipeline wait (~1 s at GB300 clocks). A separate test build sets
+// it to zero and CCA_WAIT_POLL_NS to a few nanoseconds (each poll returns
+// almost at once and the limit is checked after every poll), so that the
+// waits run out and the abort path runs; the drain of copies and MMAs in
+// flight keeps its own, normal limit.
+#ifndef CCA_WAIT_CYCLES
+#define CCA_WAIT_CYCLES 2000000000LL
+#endif
+constexpr long long kWaitCycles = CCA_WAIT_CYCLES;
+constexpr long long kDrainCycles = 2000000000LL;
 constexpr int kDerrTimeout = CCONV_DERR_TIMEOUT;
 constexpr int kOutRowPitch = 64;                       // 64 bytes of a row, 16-byte chunks swizzled
 constexpr int kEpiCols = kGS / (kEpiWarps / 4);       // accumulator columns per epilogue warp
@@ -209,20 +218,44 @@ struct Ctl {
   volatile int abort;
 };
 
+// mbarrier try_wait with an explicit suspend-time limit in nanoseconds.
+__device__ __forceinline__ bool mbar_try_for(uint64_t* b, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(b)), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
+
 struct Waiter {
   Ctl* ctl;
   int32_t* dev_err;
   // Bounded wait: false when the kernel is aborting (this or another wait
-  // timed out); never spins forever.
+  // timed out); never spins forever. Every caller is a whole warp, and the
+  // warp decides together (a phase seen complete by one lane is complete for
+  // all), so that its lanes never split between going on and giving up.
   __device__ bool wait(uint64_t* bar, uint32_t parity) const {
     const long long t0 = clock64();
+#ifdef CCA_WAIT_POLL_NS
+    constexpr uint32_t kCheckMask = 0u;
+#else
+    constexpr uint32_t kCheckMask = 63u;
+#endif
     for (uint32_t it = 0;; ++it) {
-      if (mbar_try(bar, parity)) return true;
-      if ((it & 63u) == 63u) {
-        if (ctl->abort) return false;
-        if (clock64() - t0 > kWaitCycles) {
+#ifdef CCA_WAIT_POLL_NS
+      const bool done = mbar_try_for(bar, parity, CCA_WAIT_POLL_NS);
+#else
+      const bool done = mbar_try(bar, parity);
+#endif
+      if (__any_sync(0xffffffffu, done)) return true;
+      if ((it & kCheckMask) == kCheckMask) {
+        if (__any_sync(0xffffffffu, ctl->abort != 0)) return false;
+        if (__any_sync(0xffffffffu, clock64() - t0 > kWaitCycles)) {
           ctl->abort = 1;
-          cconv::flag_error(dev_err, kDerrTimeout);
+          if ((threadIdx.x & 31) == 0) cconv::flag_error(dev_err, kDerrTimeout);
           return false;
         }
       }
@@ -233,7 +266,7 @@ struct Waiter {
   __device__ void drain(uint64_t* bar, uint32_t parity) const {
     const long long t0 = clock64();
     while (!mbar_try(bar, parity))
-      if (clock64() - t0 > kWaitCycles) {
+      if (clock64() - t0 > kDrainCycles) {
         cconv::flag_error(dev_err, kDerrTimeout);
         return;
       }
