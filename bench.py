@@ -252,6 +252,8 @@ def build_workload(name, dev, dev_err):
             "ple spec 512x(1+3) tok x 16384 ch, fp32 conv-state pool under bf16 activations"
     if name == "gdn_mixed":
         return depthwise_calls("gdn_mixed", synth.gdn_mixed(dev), dev_err), "gdn_mixed"
+    if name == "ple_spec":
+        return depthwise_calls("ple_spec", synth.ple_spec(dev), dev_err), "ple_spec"
     if name == "gdn_decode":
         return depthwise_calls("gdn_decode", synth.gdn_decode(dev), dev_err), "gdn_decode"
     if name == "cca_small":
