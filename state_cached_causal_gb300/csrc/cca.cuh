@@ -515,7 +515,7 @@ __device__ __forceinline__ void unit_to_gt(const Args& a, int u, int& g, int& ta
 // flight (a launch takes slot epoch % kEpochs; its last CTA clears it).
 constexpr int kEpochs = 64;
 constexpr int kDynChunk = 2;                 // units per dynamic grab
-constexpr int kStaticPercent = 90;           // share of the units split statically
+constexpr int kStaticPercent = 95;           // share of the units split statically
 // Work units a launch may have when its two counters come from the caller's
 // fixed scratch (cca_qk_conv_noalloc): the counters never pass 2^31.
 constexpr int64_t kStaticScratchMaxUnits = int64_t(1) << 30;
