@@ -10,9 +10,11 @@ shape, all through the C ABI of libcconv.so:
               and cconv_update with 3 speculative tokens)
 Every input is seeded and synthetic and resident in HBM before timing; the
 step moves about 5.7 GB, far more than the 129 MB L2, so no flush is needed.
-`value` is tokens*channels processed per second (whole job), `e2e` the same
-metric with the inputs copied from pinned host memory and the outputs copied
-back inside the timed region. `roofline` reports the dominant kernel's
+`value` is tokens*channels processed per second (whole job) over K replays of
+the step captured as one CUDA graph (the same launches as the stream path),
+`per_call` the per-launch times from a second pass launched on the stream with
+events around every launch, `e2e` the same metric with the inputs copied from
+pinned host memory and the outputs copied back inside the timed region. `roofline` reports the dominant kernel's
 achieved HBM bandwidth (algorithmic bytes / CUDA-event duration) against the
 measured copy bandwidth. `cpu_baseline` times the plain-C oracle on a bounded
 channel/request sample of the same step on the host cores.
@@ -510,6 +512,25 @@ def dist_env():
     return ws, rank, local
 
 
+def capture_step(step, stream, dev):
+    """One step captured as a CUDA graph, or None when capture is not possible."""
+    try:
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            step()
+        stream.wait_stream(side)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            step()
+        torch.cuda.synchronize()
+        return g
+    except Exception:
+        torch.cuda.synchronize()
+        return None
+
+
 def whole_job_value(ws, units_per_step, steps, elapsed):
     """Replicas: every rank runs the whole step on its own GPU (weak scaling), so
     the job processed ws * units_per_step * steps units in the slowest rank's
@@ -581,9 +602,17 @@ def arm_ours(args):
     if int(dev_err.item()) != 0:
         raise SystemExit(f"device error flag {int(dev_err.item())} during warm-up")
 
-    # timed region: K steps, events per launch on the launching stream
-    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in calls] for _ in range(args.steps)]
+    # The step's launches captured once as a CUDA graph: the timed region replays
+    # it K times (the same kernels and arguments, without the host's per-launch
+    # overhead); if capture fails, the timed region launches the calls on the
+    # stream instead.
+    graph = capture_step(step, stream, dev)
+    if graph is not None:
+        for _ in range(3):
+            graph.replay()
+        torch.cuda.synchronize()
+
+    # timed region: K steps between two events on the launching stream
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if ws > 1:
         import torch.distributed as dist
@@ -596,15 +625,28 @@ def arm_ours(args):
         torch.cuda._sleep(LEAD_CYCLES)
         start.record(stream)
         for k in range(args.steps):
-            for c, (a, b) in zip(calls, ev[k]):
-                a.record(stream)
-                c.fn()
-                b.record(stream)
+            if graph is not None:
+                graph.replay()
+            else:
+                step()
         stop.record(stream)
         torch.cuda.synchronize()
     if ws > 1:
         dist.barrier()
     elapsed = start.elapsed_time(stop) / 1e3
+
+    # per-launch breakdown: a second pass of K steps launched on the stream
+    # with events around every launch (the events add about 2 us per launch)
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in calls] for _ in range(args.steps)]
+    torch.cuda._sleep(LEAD_CYCLES)
+    for k in range(args.steps):
+        for c, (a, b) in zip(calls, ev[k]):
+            a.record(stream)
+            c.fn()
+            b.record(stream)
+    torch.cuda.synchronize()
+    events_step_ms = ev[0][0][0].elapsed_time(ev[-1][-1][1]) / args.steps
     elapsed = reduce_max(elapsed, ws)
     per_call = {c.name: sum(ev[k][i][0].elapsed_time(ev[k][i][1]) for k in range(args.steps))
                 / args.steps / 1e3 for i, c in enumerate(calls)}
@@ -642,6 +684,9 @@ def arm_ours(args):
                    "parallelism": "replicas" if ws > 1 else "1 GPU"},
         "hbm_GBps": bytes_per_step * args.steps / elapsed / 1e9,
         "gpu_launches": len(calls) * args.steps,
+        "launch": ("one CUDA graph of the step's %d launches per step" % len(calls)
+                   if graph is not None else "stream launches"),
+        "ms_per_step_stream_with_call_events": events_step_ms,
         "roofline": roofline,
         "clocks": clk.summary(),
         "per_call": breakdown,
