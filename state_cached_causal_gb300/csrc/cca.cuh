@@ -237,7 +237,7 @@ struct Waiter {
   // timed out); never spins forever. Every caller is a whole warp, and the
   // warp decides together (a phase seen complete by one lane is complete for
   // all), so that its lanes never split between going on and giving up.
-  __device__ bool wait(uint64_t* bar, uint32_t parity) const {
+  __device__ __noinline__ bool wait(uint64_t* bar, uint32_t parity) const {
     const long long t0 = clock64();
 #ifdef CCA_WAIT_POLL_NS
     constexpr uint32_t kCheckMask = 0u;
@@ -263,7 +263,7 @@ struct Waiter {
   }
   // Drain wait before exit: bounded by time only, so that an async copy or
   // MMA still in flight is waited for even while aborting.
-  __device__ void drain(uint64_t* bar, uint32_t parity) const {
+  __device__ __noinline__ void drain(uint64_t* bar, uint32_t parity) const {
     const long long t0 = clock64();
     while (!mbar_try(bar, parity))
       if (clock64() - t0 > kDrainCycles) {
@@ -333,7 +333,7 @@ __device__ __forceinline__ void hist_from_words(const uint32_t (&w)[4 * NH], uin
 // contiguous units, interleaved by channel; column-first pools hold one unit
 // per column; any other stride goes element by element.
 template <int NH>
-__device__ __forceinline__ void hist_load_all(const Pool& P, int slot, int c0, uint4 (&h)[NH]) {
+__device__ __noinline__ void hist_load_all(const Pool P, int slot, int c0, uint4 (&h)[NH]) {
   const char* base = P.p + (int64_t)slot * P.s_slot * 2;
   if (P.mode == cconv::kPoolDSWide) {
     // fp32 channel-first: channel v, column col at float v * NH + col
@@ -392,8 +392,8 @@ __device__ __forceinline__ void hist_load_all(const Pool& P, int slot, int c0, u
 }
 
 template <int NH>
-__device__ __forceinline__ void hist_store_all(const Pool& P, int slot, int c0,
-                                               const uint4 (&h)[NH]) {
+__device__ __noinline__ void hist_store_all(const Pool P, int slot, int c0,
+                                            const uint4 (&h)[NH]) {
   char* base = P.p + (int64_t)slot * P.s_slot * 2;
   if (P.mode == cconv::kPoolDSWide) {
     uint32_t f[8 * NH];   // f[v * NH + col]: channel v, column col, fp32 bits
@@ -594,6 +594,245 @@ __device__ __forceinline__ uint4 add_residual(bool query, const uint4& pre, cons
 #pragma unroll
   for (int e = 0; e < 8; ++e) cv[e] = cv[e] + (query ? 0.5f * rf[e] : rf[e]);
   return cconv::pack16<__nv_bfloat16>(cv);
+}
+
+// ---- the depthwise stage (producer warps) -----------------------------------
+// The plain path (rows that are consecutive tokens of one request past its
+// history) stays in the kernel's loop; everything else is out of line, so that
+// the loop the warp runs on almost every tile stays small for the instruction
+// cache. The out-of-line parts reload the taps they need from global memory
+// (L1/L2 hits) instead of taking the caller's registers by address.
+
+// Depthwise taps and bias of channels c0 .. c0+7 in fp32.
+template <int T0>
+__device__ __forceinline__ void load_taps(const char* w_dw, const char* b_dw, int c0,
+                                          float (&w0)[T0][8], float (&b0)[8]) {
+#pragma unroll
+  for (int v = 0; v < 8; ++v) {
+#pragma unroll
+    for (int k = 0; k < T0; ++k)
+      w0[k][v] = cconv::load_f32<__nv_bfloat16>(w_dw, (int64_t)(c0 + v) * T0 + k);
+    b0[v] = b_dw ? cconv::load_f32<__nv_bfloat16>(b_dw, c0 + v) : 0.0f;
+  }
+}
+
+// Row r of the A operand from its window xw[m] = x~[j - m]: u(j) at Au + r*16
+// and, in a two-buffer tile, u(j-1) at Ap + r*16 (fp32 sums from the bias, tap
+// by tap, one bf16 rounding).
+template <int T0, int T1, int NW>
+__device__ __forceinline__ void put_row(const float (&w0)[T0][8], const float (&b0)[8],
+                                        const float (&xw)[NW][8], unsigned char* Au,
+                                        unsigned char* Ap, int r, bool single) {
+  float uu[8];
+#pragma unroll
+  for (int v = 0; v < 8; ++v) {
+    float acc = b0[v];
+#pragma unroll
+    for (int k = 0; k < T0; ++k) acc = fmaf(w0[k][v], xw[T0 - 1 - k][v], acc);
+    uu[v] = acc;
+  }
+  *reinterpret_cast<uint4*>(Au + r * 16) = cconv::pack16<__nv_bfloat16>(uu);
+  if (T1 == 2 && !single) {
+#pragma unroll
+    for (int v = 0; v < 8; ++v) {
+      float acc = b0[v];
+#pragma unroll
+      for (int k = 0; k < T0; ++k) acc = fmaf(w0[k][v], xw[(T0 - k) % NW][v], acc);
+      uu[v] = acc;
+    }
+    *reinterpret_cast<uint4*>(Ap + r * 16) = cconv::pack16<__nv_bfloat16>(uu);
+  }
+}
+
+// B operand of group g: B[tap][k-chunk][n] = w_gr[g*128 + n][k-chunk*8 + e][tap],
+// 16 bytes per (k-chunk, n); thread p of the producers takes every
+// (kProdWarps*32)-th pair, eight pairs' loads in flight.
+template <int T1>
+__device__ __noinline__ void load_b_operand(const char* w_gr, unsigned char* sB, int g, int p) {
+  constexpr int kBIter = kGS * (kGS / 8) / (kProdWarps * 32);
+#pragma unroll 8
+  for (int it = 0; it < kBIter; ++it) {
+    const int pr = p + it * (kProdWarps * 32);
+    const int o = pr & (kGS - 1), bkc = pr >> 7;
+    const char* src = w_gr + ((int64_t)(g * kGS + o) * kGS + bkc * 8) * T1 * 2;
+    uint32_t e[8 * T1];
+#pragma unroll
+    for (int v = 0; v < T1; ++v) {
+      const uint4 r = cconv::ldg16(src + v * 16);
+      e[v * 8 + 0] = r.x & 0xffffu;
+      e[v * 8 + 1] = r.x >> 16;
+      e[v * 8 + 2] = r.y & 0xffffu;
+      e[v * 8 + 3] = r.y >> 16;
+      e[v * 8 + 4] = r.z & 0xffffu;
+      e[v * 8 + 5] = r.z >> 16;
+      e[v * 8 + 6] = r.w & 0xffffu;
+      e[v * 8 + 7] = r.w >> 16;
+    }
+#pragma unroll
+    for (int kt = 0; kt < T1; ++kt) {
+      uint32_t h[8];
+#pragma unroll
+      for (int ee = 0; ee < 8; ++ee) h[ee] = e[ee * T1 + kt];
+      *reinterpret_cast<uint4*>(sB + kt * kTapB + bkc * kLboB + o * 16) =
+          make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16),
+                     h[6] | (h[7] << 16));
+    }
+  }
+}
+
+// Row -1 of a single-buffer tile whose row 0 reads history (j < n): u at the
+// token before row 0, from the x stage and the request's history columns.
+template <int T0, int T1>
+__device__ __noinline__ void row_before_hist(const Pool P, const char* w_dw, const char* b_dw,
+                                             const Meta* M, const unsigned char* xst,
+                                             unsigned char* Au, int c0, int kc) {
+  constexpr int NH = T0 + T1 - 2, NHH = NH > 0 ? NH : 1;
+  float w0[T0][8], b0[8];
+  load_taps<T0>(w_dw, b_dw, c0, w0, b0);
+  const int j = M->rowj[0] - 1;
+  uint4 h1[NHH];
+  const int hslot = M->rowslot[0];
+  if (NH > 0 && j < T0 - 1 && hslot >= 0) {
+    hist_load_all<NHH>(P, hslot, c0, h1);
+  } else {
+#pragma unroll
+    for (int c = 0; c < NHH; ++c) h1[c] = make_uint4(0u, 0u, 0u, 0u);
+  }
+  float uu[8];
+#pragma unroll
+  for (int v = 0; v < 8; ++v) uu[v] = b0[v];
+#pragma unroll
+  for (int k = 0; k < T0; ++k) {
+    const int m = T0 - 1 - k;   // x~[j - m]; stage row of token j - m is NH - 1 - m
+    const uint4 raw = j - m >= 0
+                          ? *reinterpret_cast<const uint4*>(xst + (NH - 1 - m) * kXRowBytes + kc * 16)
+                          : pick<NHH>(h1, NH + j - m);
+    float xv[8];
+    cconv::unpack16<__nv_bfloat16>(raw, xv);
+#pragma unroll
+    for (int v = 0; v < 8; ++v) uu[v] = fmaf(w0[k][v], xv[v], uu[v]);
+  }
+  *reinterpret_cast<uint4*>(Au - 16) = cconv::pack16<__nv_bfloat16>(uu);
+}
+
+// History of the rows r0 .. r0+kProdRows-1 that read it (j < n, with a slot),
+// by cp.async into the rows' own 16-byte slots of both A buffers (free until
+// the rows' A values overwrite them): two-tap tiles with n <= 2 on a
+// channel-first or column-first pool.
+template <int NH>
+__device__ __noinline__ void prefetch_history(const Pool P, const Meta* M, unsigned char* Au,
+                                              unsigned char* Ap, int r0, int len, int c0) {
+#pragma unroll 1
+  for (int rr = 0; rr < kProdRows; ++rr) {
+    const int r = r0 + rr;
+    const int j = r < len ? M->rowj[r] : -1;
+    const int hslot = M->rowslot[r];
+    if (j >= 0 && j < NH && hslot >= 0) {
+      const char* hb = P.p + (int64_t)hslot * P.s_slot * 2;
+      const char* s0 = P.mode == cconv::kPoolDS ? hb + (int64_t)c0 * NH * 2 : hb + (int64_t)c0 * 2;
+      const char* s1 = P.mode == cconv::kPoolDS ? s0 + 16 : hb + (P.s_col + c0) * 2;
+      cconv::cp_async16(smem_u32(Au + r * 16), s0, true);
+      if (NH == 2) cconv::cp_async16(smem_u32(Ap + r * 16), s1, true);
+    }
+  }
+  cconv::cp_async_commit();
+  cconv::cp_async_wait<0>();
+}
+
+// Eight rows rs0 .. rs0+7 that are not a plain run of one request's tokens
+// past its history: the same window as the plain path, with the inputs before
+// a request's start taken from its history (prefetched into the row's A slots
+// when `scratch`) and zeros for rows outside every request; a one-token
+// request's row also writes the request's new state.
+template <int T0, int T1>
+__device__ __noinline__ void mixed_rows(const Pool P, const char* w_dw, const char* b_dw,
+                                        const Meta* M, const unsigned char* xst,
+                                        unsigned char* Au, unsigned char* Ap, int rs0, int len,
+                                        int c0, int kc, bool single, bool scratch) {
+  constexpr int NH = T0 + T1 - 2, NHH = NH > 0 ? NH : 1, NW = T0 + T1 - 1;
+  constexpr bool kScratch = (T1 == 2) && (NH >= 1) && (NH <= 2);
+  float w0[T0][8], b0[8];
+  load_taps<T0>(w_dw, b_dw, c0, w0, b0);
+  // the history columns of row r
+  auto hist_of = [&](int r, int hslot, uint4 (&h)[NHH]) {
+    if (kScratch && scratch) {
+      const uint4 s0 = *reinterpret_cast<const uint4*>(Au + r * 16);
+      const uint4 s1 = NH == 2 ? *reinterpret_cast<const uint4*>(Ap + r * 16) : s0;
+      if (P.mode == cconv::kPoolDS) {
+        uint32_t w[4 * NHH];
+        w[0] = s0.x;
+        w[1] = s0.y;
+        w[2] = s0.z;
+        w[3] = s0.w;
+        if (NH == 2) {
+          w[(4 % (4 * NHH))] = s1.x;
+          w[(5 % (4 * NHH))] = s1.y;
+          w[(6 % (4 * NHH))] = s1.z;
+          w[(7 % (4 * NHH))] = s1.w;
+        }
+        hist_from_words<NHH>(w, h);
+      } else {
+        h[0] = s0;
+        if (NH == 2) h[1 % NHH] = s1;
+      }
+    } else {
+      hist_load_all<NHH>(P, hslot, c0, h);
+    }
+  };
+  float xw[NW][8];
+#pragma unroll
+  for (int m = 1; m <= NH; ++m)
+    cconv::unpack16<__nv_bfloat16>(
+        *reinterpret_cast<const uint4*>(xst + (rs0 + NH - m) * kXRowBytes + kc * 16), xw[m]);
+#pragma unroll 1
+  for (int rr = 0; rr < 8; ++rr) {
+    const int r = rs0 + rr;
+    const uint4 cur = *reinterpret_cast<const uint4*>(xst + (r + NH) * kXRowBytes + kc * 16);
+    cconv::unpack16<__nv_bfloat16>(cur, xw[0]);
+    const int j = r < len ? M->rowj[r] : -1;
+    if (j < 0) {
+      const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+      *reinterpret_cast<uint4*>(Au + r * 16) = z;
+      if (T1 == 2 && !single) *reinterpret_cast<uint4*>(Ap + r * 16) = z;
+    } else if (j >= NH) {
+      put_row<T0, T1>(w0, b0, xw, Au, Ap, r, single);
+    } else {
+      uint4 hh[NHH];
+      const int hslot = M->rowslot[r];
+      if (hslot >= 0) {
+        hist_of(r, hslot, hh);
+      } else {
+#pragma unroll
+        for (int c = 0; c < NHH; ++c) hh[c] = make_uint4(0u, 0u, 0u, 0u);
+      }
+      float xv[NW][8];
+#pragma unroll
+      for (int v = 0; v < 8; ++v) xv[0][v] = xw[0][v];
+#pragma unroll
+      for (int m = 1; m < NW; ++m) {
+        if (m <= j) {
+#pragma unroll
+          for (int v = 0; v < 8; ++v) xv[m][v] = xw[m][v];
+        } else {
+          cconv::unpack16<__nv_bfloat16>(pick<NHH>(hh, NH + j - m), xv[m]);
+        }
+      }
+      put_row<T0, T1>(w0, b0, xv, Au, Ap, r, single);
+      // A one-token request's history is read by this row alone: its new
+      // state (history columns 1 .. n-1, then the token) is written here.
+      const int wr = M->rowwr[r];
+      if (NH > 0 && wr >= 0) {
+        uint4 ns[NHH];
+#pragma unroll
+        for (int c = 0; c < NHH; ++c) ns[c] = c + 1 < NH ? hh[(c + 1) % NHH] : cur;
+        hist_store_all<NHH>(P, wr, c0, ns);
+      }
+    }
+#pragma unroll
+    for (int m = NH; m >= 1; --m)
+#pragma unroll
+      for (int v = 0; v < 8; ++v) xw[m][v] = xw[m - 1][v];
+  }
 }
 
 // FUSED: the tail of ZayaCCA.project in the epilogue -- each conv output gets
@@ -982,101 +1221,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       const int c0 = g * kGS + kc * 8;
       if (g != cur_g) {
-        // B operand of group g: B[tap][k-chunk][n] = w_gr[g*128 + n][k-chunk*8 + e][tap]
-        // (unrolled by eight: eight rows' loads in flight)
-        constexpr int kBIter = kGS * (kGS / 8) / (kProdWarps * 32);
-#pragma unroll 8
-        for (int it = 0; it < kBIter; ++it) {
-          const int pr = p + it * (kProdWarps * 32);
-          const int o = pr & (kGS - 1), bkc = pr >> 7;
-          const char* src = a.w_gr + ((int64_t)(g * kGS + o) * kGS + bkc * 8) * T1 * 2;
-          uint32_t e[8 * T1];
-#pragma unroll
-          for (int v = 0; v < T1; ++v) {
-            const uint4 r = cconv::ldg16(src + v * 16);
-            e[v * 8 + 0] = r.x & 0xffffu;
-            e[v * 8 + 1] = r.x >> 16;
-            e[v * 8 + 2] = r.y & 0xffffu;
-            e[v * 8 + 3] = r.y >> 16;
-            e[v * 8 + 4] = r.z & 0xffffu;
-            e[v * 8 + 5] = r.z >> 16;
-            e[v * 8 + 6] = r.w & 0xffffu;
-            e[v * 8 + 7] = r.w >> 16;
-          }
-#pragma unroll
-          for (int kt = 0; kt < T1; ++kt) {
-            uint32_t h[8];
-#pragma unroll
-            for (int ee = 0; ee < 8; ++ee) h[ee] = e[ee * T1 + kt];
-            *reinterpret_cast<uint4*>(sB + kt * kTapB + bkc * kLboB + o * 16) =
-                make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16),
-                           h[6] | (h[7] << 16));
-          }
-        }
-#pragma unroll
-        for (int v = 0; v < 8; ++v) {
-#pragma unroll
-          for (int k = 0; k < T0; ++k)
-            w0[k][v] = cconv::load_f32<__nv_bfloat16>(a.w_dw, (int64_t)(c0 + v) * T0 + k);
-          b0[v] = a.b_dw ? cconv::load_f32<__nv_bfloat16>(a.b_dw, c0 + v) : 0.0f;
-        }
+        load_b_operand<T1>(a.w_gr, sB, g, p);
+        load_taps<T0>(a.w_dw, a.b_dw, c0, w0, b0);
         cur_g = g;
       }
       // u(j) of row r goes to Au + r*16; two-tap tiles put u(j-1) at Ap + r*16.
       unsigned char* Au = sA + (abuf & 1) * kABuf + kc * kLboA + 16;
       unsigned char* Ap = sA + ((abuf + 1) & 1) * kABuf + kc * kLboA + 16;
       const unsigned char* xst = sX + xs * kXStageBytes;
-      // xw[m] = x~[j - m] of the row -> its u(j) (and u(j-1))
-      auto put = [&](int r, const float (&xw)[NW][8]) {
-        float uu[8];
-#pragma unroll
-        for (int v = 0; v < 8; ++v) {
-          float acc = b0[v];
-#pragma unroll
-          for (int k = 0; k < T0; ++k) acc = fmaf(w0[k][v], xw[T0 - 1 - k][v], acc);
-          uu[v] = acc;
-        }
-        *reinterpret_cast<uint4*>(Au + r * 16) = cconv::pack16<__nv_bfloat16>(uu);
-        if (T1 == 2 && !single) {
-#pragma unroll
-          for (int v = 0; v < 8; ++v) {
-            float acc = b0[v];
-#pragma unroll
-            for (int k = 0; k < T0; ++k) acc = fmaf(w0[k][v], xw[(T0 - k) % NW][v], acc);
-            uu[v] = acc;
-          }
-          *reinterpret_cast<uint4*>(Ap + r * 16) = cconv::pack16<__nv_bfloat16>(uu);
-        }
-      };
-      // Row -1 of a single-buffer tile: u at the token before row 0. (Before
-      // the rows: a one-token request's row rewrites the history it reads.)
-      if (T1 == 2 && single && strip == 0 && len > 0 && M.rowj[0] >= 0) {
-        const int j = M.rowj[0] - 1;
-        uint4 h1[NHH];
-        const int hslot = M.rowslot[0];
-        if (NH > 0 && j < T0 - 1 && hslot >= 0) {
-          hist_load_all<NHH>(a.pool, hslot, c0, h1);
-        } else {
-#pragma unroll
-          for (int c = 0; c < NHH; ++c) h1[c] = make_uint4(0u, 0u, 0u, 0u);
-        }
-        float uu[8];
-#pragma unroll
-        for (int v = 0; v < 8; ++v) uu[v] = b0[v];
-#pragma unroll
-        for (int k = 0; k < T0; ++k) {
-          const int m = T0 - 1 - k;   // x~[j - m]; stage row of token j - m is NH - 1 - m
-          const uint4 raw =
-              j - m >= 0
-                  ? *reinterpret_cast<const uint4*>(xst + (NH - 1 - m) * kXRowBytes + kc * 16)
-                  : pick<NHH>(h1, NH + j - m);
-          float xv[8];
-          cconv::unpack16<__nv_bfloat16>(raw, xv);
-#pragma unroll
-          for (int v = 0; v < 8; ++v) uu[v] = fmaf(w0[k][v], xv[v], uu[v]);
-        }
-        *reinterpret_cast<uint4*>(Au - 16) = cconv::pack16<__nv_bfloat16>(uu);
-      }
+      // Row -1 of a single-buffer tile: u at the token before row 0, here when
+      // it reads history (row 0 at j < n; otherwise the first rows' fast path
+      // below computes it from the x stage). (Before the rows: a one-token
+      // request's row rewrites the history it reads.)
+      if (T1 == 2 && single && strip == 0 && len > 0 && M.rowj[0] >= 0 && M.rowj[0] < NH)
+        row_before_hist<T0, T1>(a.pool, a.w_dw, a.b_dw, &M, xst, Au, c0, kc);
       // History of the rows that read it (j < n, with a slot): in two-tap
       // tiles with n <= 2 it is prefetched with cp.async into the row's own
       // 16-byte slots of both A buffers (free until the row's A values
@@ -1085,51 +1243,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr bool kScratch = (T1 == 2) && (NH >= 1) && (NH <= 2);
       const bool scratch = kScratch && !single &&
                            (a.pool.mode == cconv::kPoolDS || a.pool.mode == cconv::kPoolSD);
-      if (scratch) {
-#pragma unroll 1
-        for (int rr = 0; rr < kProdRows; ++rr) {
-          const int r = strip * kProdRows + rr;
-          const int j = r < len ? M.rowj[r] : -1;
-          const int hslot = M.rowslot[r];
-          if (j >= 0 && j < NH && hslot >= 0) {
-            const char* hb = a.pool.p + (int64_t)hslot * a.pool.s_slot * 2;
-            const char* s0 = a.pool.mode == cconv::kPoolDS ? hb + (int64_t)c0 * NH * 2
-                                                           : hb + (int64_t)c0 * 2;
-            const char* s1 = a.pool.mode == cconv::kPoolDS ? s0 + 16
-                                                           : hb + (a.pool.s_col + c0) * 2;
-            cconv::cp_async16(smem_u32(Au + r * 16), s0, true);
-            if (NH == 2) cconv::cp_async16(smem_u32(Ap + r * 16), s1, true);
-          }
-        }
-        cconv::cp_async_commit();
-        cconv::cp_async_wait<0>();
+      if constexpr (kScratch) {
+        if (scratch) prefetch_history<NH>(a.pool, &M, Au, Ap, strip * kProdRows, len, c0);
       }
-      // the history columns of row r
-      auto hist_of = [&](int r, int hslot, uint4 (&h)[NHH]) {
-        if (kScratch && scratch) {
-          const uint4 s0 = *reinterpret_cast<const uint4*>(Au + r * 16);
-          const uint4 s1 = NH == 2 ? *reinterpret_cast<const uint4*>(Ap + r * 16) : s0;
-          if (a.pool.mode == cconv::kPoolDS) {
-            uint32_t w[4 * NHH];
-            w[0] = s0.x;
-            w[1] = s0.y;
-            w[2] = s0.z;
-            w[3] = s0.w;
-            if (NH == 2) {
-              w[(4 % (4 * NHH))] = s1.x;
-              w[(5 % (4 * NHH))] = s1.y;
-              w[(6 % (4 * NHH))] = s1.z;
-              w[(7 % (4 * NHH))] = s1.w;
-            }
-            hist_from_words<NHH>(w, h);
-          } else {
-            h[0] = s0;
-            if (NH == 2) h[1 % NHH] = s1;
-          }
-        } else {
-          hist_load_all<NHH>(a.pool, hslot, c0, h);
-        }
-      };
 #pragma unroll 1
       for (int sub = 0; sub < kProdRows / 8; ++sub) {
         const int rs0 = strip * kProdRows + sub * 8;
@@ -1148,10 +1264,24 @@ __global__ void __launch_bounds__(kThreads, 1)
           float xw[NW][8];
 #pragma unroll
           for (int m = 1; m <= NH; ++m) cconv::unpack16<__nv_bfloat16>(raw[NH - m], xw[m]);
+          if constexpr (T1 == 2) {
+            if (rs0 == 0 && M.single) {
+              // row -1 of a single-buffer tile: its window x~[j - 1 - m] is xw[m + 1]
+              float uu[8];
+#pragma unroll
+              for (int v = 0; v < 8; ++v) {
+                float acc = b0[v];
+#pragma unroll
+                for (int k = 0; k < T0; ++k) acc = fmaf(w0[k][v], xw[T0 - k][v], acc);
+                uu[v] = acc;
+              }
+              *reinterpret_cast<uint4*>(Au - 16) = cconv::pack16<__nv_bfloat16>(uu);
+            }
+          }
 #pragma unroll
           for (int rr = 0; rr < 8; ++rr) {
             cconv::unpack16<__nv_bfloat16>(raw[rr + NH], xw[0]);
-            put(rs0 + rr, xw);
+            put_row<T0, T1>(w0, b0, xw, Au, Ap, rs0 + rr, single);
 #pragma unroll
             for (int m = NH; m >= 1; --m)
 #pragma unroll
@@ -1159,65 +1289,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           continue;
         }
-        // Mixed rows: the same window, with the inputs before a request's
-        // start taken from its history and zeros for rows outside every
-        // request.
-        float xw[NW][8];
-#pragma unroll
-        for (int m = 1; m <= NH; ++m)
-          cconv::unpack16<__nv_bfloat16>(
-              *reinterpret_cast<const uint4*>(xst + (rs0 + NH - m) * kXRowBytes + kc * 16), xw[m]);
-        // (not unrolled: the code stays small for the instruction cache, the
-        // fast path above being the one that runs on most tiles)
-#pragma unroll 1
-        for (int rr = 0; rr < 8; ++rr) {
-          const int r = rs0 + rr;
-          const uint4 cur = *reinterpret_cast<const uint4*>(xst + (r + NH) * kXRowBytes + kc * 16);
-          cconv::unpack16<__nv_bfloat16>(cur, xw[0]);
-          const int j = r < len ? M.rowj[r] : -1;
-          if (j < 0) {
-            const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-            *reinterpret_cast<uint4*>(Au + r * 16) = z;
-            if (T1 == 2 && !single) *reinterpret_cast<uint4*>(Ap + r * 16) = z;
-          } else if (j >= NH) {
-            put(r, xw);
-          } else {
-            uint4 hh[NHH];
-            const int hslot = M.rowslot[r];
-            if (hslot >= 0) {
-              hist_of(r, hslot, hh);
-            } else {
-#pragma unroll
-              for (int c = 0; c < NHH; ++c) hh[c] = make_uint4(0u, 0u, 0u, 0u);
-            }
-            float xv[NW][8];
-#pragma unroll
-            for (int v = 0; v < 8; ++v) xv[0][v] = xw[0][v];
-#pragma unroll
-            for (int m = 1; m < NW; ++m) {
-              if (m <= j) {
-#pragma unroll
-                for (int v = 0; v < 8; ++v) xv[m][v] = xw[m][v];
-              } else {
-                cconv::unpack16<__nv_bfloat16>(pick<NHH>(hh, NH + j - m), xv[m]);
-              }
-            }
-            put(r, xv);
-            // A one-token request's history is read by this row alone: its new
-            // state (history columns 1 .. n-1, then the token) is written here.
-            const int wr = M.rowwr[r];
-            if (NH > 0 && wr >= 0) {
-              uint4 ns[NHH];
-#pragma unroll
-              for (int c = 0; c < NHH; ++c) ns[c] = c + 1 < NH ? hh[(c + 1) % NHH] : cur;
-              hist_store_all<NHH>(a.pool, wr, c0, ns);
-            }
-          }
-#pragma unroll
-          for (int m = NH; m >= 1; --m)
-#pragma unroll
-            for (int v = 0; v < 8; ++v) xw[m][v] = xw[m - 1][v];
-        }
+        mixed_rows<T0, T1>(a.pool, a.w_dw, a.b_dw, &M, xst, Au, Ap, rs0, len, c0, kc, single,
+                           scratch);
       }
       fence_proxy_async();
       __syncwarp();
