@@ -483,6 +483,45 @@ static __device__ int tile_edge(const Args& a, const int32_t* cu, int tau, int f
 
 // ---- the kernel ----------------------------------------------------------------
 
+// Row -> request for a tile of rows of several requests: row r's request is
+// the last s with cu[s] <= its token, found by each lane for its row with a
+// binary search over cu[sc .. B) (sc: a request at or before the tile's first
+// row; the next 32 rows start from the last row's request). cu is
+// non-decreasing for valid input; the search stays in bounds either way.
+// Out of line: most tiles hold one request.
+static __device__ __noinline__ void map_rows(const int32_t* cu, const int32_t* sidx,
+                                             const uint8_t* hini, int B, int T, int num_slots,
+                                             Meta* M, int lo, int len, int sc) {
+  const int lane = threadIdx.x & 31;
+  for (int r0 = 0; r0 < kRows; r0 += 32) {
+    const int r = r0 + lane;
+    const int t = lo + min(r, max(len - 1, 0));   // rows past the tile repeat the last
+    int sl_ = sc, sh_ = B;                        // answer in [sl_, sh_)
+    while (sh_ - sl_ > 1) {                       // the same count on every lane
+      const int mid = (sl_ + sh_) >> 1;
+      if (cu[mid] <= t) sl_ = mid; else sh_ = mid;
+    }
+    const int sr = sl_;
+    int j = -1, slot = -1, wr = -1;
+    if (r < len && sr < B) {
+      const int st = cu[sr], en = cu[sr + 1];
+      if (st >= 0 && st <= t && t < en && en <= T) {
+        const int sl = sidx[sr];
+        const bool h = (hini == nullptr || hini[sr] != 0);
+        if (sl < num_slots) {   // out-of-range slots are skipped and reported
+          j = t - st;
+          slot = (h && sl >= 0) ? sl : -1;
+          wr = (en - st == 1 && sl >= 0) ? sl : -1;
+        }
+      }
+    }
+    M->rowj[r] = j;
+    M->rowslot[r] = slot;
+    M->rowwr[r] = wr;
+    sc = __shfl_sync(0xffffffffu, sr, 31);
+  }
+}
+
 // Unit u -> (group g, token tile tau). The plain kernel walks the units
 // group-major (one group's B operand for many tiles). The fused kernel's
 // residuals read other groups' rows of the same tokens (a query head the key
@@ -835,15 +874,173 @@ __device__ __noinline__ void mixed_rows(const Pool P, const char* w_dw, const ch
   }
 }
 
+// Eight rows rs0 .. rs0+7 of a two-tap tile in which every row of the tile
+// is the first token of its request (j = 0), the history prefetched into the
+// rows' A slots (n <= 2, a bf16 channel-first or column-first pool): u(0) and
+// u(-1) from the token and the history columns (zeros without history), and
+// a one-token request's new state (history columns 1 .. n-1, then the token).
+// The same arithmetic as mixed_rows for such rows, in a loop small enough for
+// the instruction cache.
+template <int T0, int T1>
+__device__ __noinline__ void decode_rows(const Pool P, const char* w_dw, const char* b_dw,
+                                         const Meta* M, const unsigned char* xst,
+                                         unsigned char* Au, unsigned char* Ap, int rs0, int len,
+                                         int c0, int kc) {
+  constexpr int NH = T0 + T1 - 2, NW = T0 + T1 - 1;
+  static_assert(T1 == 2 && NH >= 1 && NH <= 2, "two-tap tiles with n <= 2");
+  float w0[T0][8], b0[8];
+  load_taps<T0>(w_dw, b_dw, c0, w0, b0);
+  const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll 1
+  for (int rr = 0; rr < 8; ++rr) {
+    const int r = rs0 + rr;
+    uint4* au = reinterpret_cast<uint4*>(Au + r * 16);
+    uint4* ap = reinterpret_cast<uint4*>(Ap + r * 16);
+    if (r >= len) {   // rows past the tile
+      *au = z;
+      *ap = z;
+      continue;
+    }
+    const uint4 cur = *reinterpret_cast<const uint4*>(xst + (r + NH) * kXRowBytes + kc * 16);
+    const uint4 s0 = *au, s1 = *ap;
+    uint4 h[NH];
+    if (P.mode == cconv::kPoolDS) {
+      uint32_t w[4 * NH];
+      w[0] = s0.x;
+      w[1] = s0.y;
+      w[2] = s0.z;
+      w[3] = s0.w;
+      if constexpr (NH == 2) {
+        w[4] = s1.x;
+        w[5] = s1.y;
+        w[6] = s1.z;
+        w[7] = s1.w;
+      }
+      hist_from_words<NH>(w, h);
+    } else {
+      h[0] = s0;
+      if constexpr (NH == 2) h[1] = s1;
+    }
+    if (M->rowslot[r] < 0) {
+#pragma unroll
+      for (int c = 0; c < NH; ++c) h[c] = z;
+    }
+    float xv[NW][8];
+    cconv::unpack16<__nv_bfloat16>(cur, xv[0]);
+#pragma unroll
+    for (int m = 1; m <= NH; ++m) cconv::unpack16<__nv_bfloat16>(h[NH - m], xv[m]);
+    put_row<T0, T1>(w0, b0, xv, Au, Ap, r, false);
+    const int wr = M->rowwr[r];
+    if (wr >= 0) {
+      uint4 ns[NH];
+#pragma unroll
+      for (int c = 0; c < NH; ++c) ns[c] = c + 1 < NH ? h[(c + 1) % NH] : cur;
+      char* base = P.p + (int64_t)wr * P.s_slot * 2;
+      if (P.mode == cconv::kPoolDS) {
+        uint32_t e[8 * NH];   // e[v * NH + col]: channel v, column col
+#pragma unroll
+        for (int col = 0; col < NH; ++col) {
+          const uint32_t wd[4] = {ns[col].x, ns[col].y, ns[col].z, ns[col].w};
+#pragma unroll
+          for (int v = 0; v < 8; ++v) e[v * NH + col] = (wd[v >> 1] >> ((v & 1) * 16)) & 0xffffu;
+        }
+#pragma unroll
+        for (int k = 0; k < NH; ++k)
+          *reinterpret_cast<uint4*>(base + (int64_t)c0 * NH * 2 + k * 16) =
+              make_uint4(e[8 * k] | (e[8 * k + 1] << 16), e[8 * k + 2] | (e[8 * k + 3] << 16),
+                         e[8 * k + 4] | (e[8 * k + 5] << 16), e[8 * k + 6] | (e[8 * k + 7] << 16));
+      } else {
+#pragma unroll
+        for (int col = 0; col < NH; ++col)
+          *reinterpret_cast<uint4*>(base + ((int64_t)col * P.s_col + c0) * 2) = ns[col];
+      }
+    }
+  }
+}
+
+// Aux warps, owned requests s with s % G == g (warp aw of kAuxWarps takes
+// every kAuxWarps-th): the first delayed value of the request (its delayed
+// state, or delayed_init without history) and its new delayed state (the
+// delayed value of its last token). Out of line: most tiles own no request.
+static __device__ __noinline__ void aux_owned(const Args& a, const int32_t* cu, const int32_t* sidx,
+                                       const uint8_t* hini, int own_lo, int own_hi, int g,
+                                       int aw) {
+  const int lane = threadIdx.x & 31;
+  const int dunits = a.Dv / 8;
+  for (int s = own_lo + ((g - own_lo % a.G) % a.G + a.G) % a.G + aw * a.G;
+       s < own_hi; s += kAuxWarps * a.G) {
+    const int st = cu[s], en = cu[s + 1];
+    const int slot = sidx[s];
+    if (st < 0 || en < st || en > a.T) {
+      if (lane == 0) cconv::flag_error(a.dev_err, CCONV_DERR_CU_SEQLENS);
+      continue;
+    }
+    if (slot >= a.pool.num_slots) continue;
+    const bool h = slot >= 0 && (hini == nullptr || hini[s] != 0);
+    for (int k = lane; k < dunits; k += 32) {
+      const uint4 first = h ? dstate_load(a, slot, k) : cconv::ldg16(a.delayed_init + k * 16);
+      const uint4 last =
+          en > st ? cconv::ldg16(a.delayed + ((int64_t)(en - 1) * a.delayed_rs + k * 8) * 2)
+                  : first;
+      if (en > st) cconv::stg16(a.dprev + ((int64_t)st * a.dprev_rs + k * 8) * 2, first);
+      // (an empty request with history leaves its delayed state as it is)
+      if (slot >= 0 && (en > st || !h)) dstate_store(a, slot, k, last);
+    }
+  }
+}
+
+// Aux warps, raw-history state of the owned requests of two or more tokens
+// (one-token requests are written by the producer of their row): the last n
+// inputs of the request, from the request's own rows and, for a request
+// shorter than n, its old history. Thread pa of the aux warps takes every
+// (kAuxWarps*32)-th (request, 8-channel unit).
+template <int NH>
+__device__ __noinline__ void aux_history(const Args& a, const int32_t* cu, const int32_t* sidx,
+                                         const uint8_t* hini, int own_lo, int own_hi, int g,
+                                         int pa) {
+  constexpr int NHH = NH > 0 ? NH : 1;
+  const int nown = own_hi - own_lo;
+  for (int task = pa; task < nown * (kGS / 8); task += kAuxWarps * 32) {
+    const int s = own_lo + (task >> 4);
+    const int tc0 = g * kGS + (task & 15) * 8;
+    const int st = cu[s], en = cu[s + 1];
+    const int slot = sidx[s];
+    if (st < 0 || en < st || en > a.T) continue;
+    if (slot >= a.pool.num_slots) {
+      if ((task & 15) == 0) cconv::flag_error(a.dev_err, CCONV_DERR_SLOT_RANGE);
+      continue;
+    }
+    if (slot < 0) continue;
+    const bool h = hini == nullptr || hini[s] != 0;
+    const int L = en - st;
+    if (L == 1) continue;
+    if (NH > 0) {
+      uint4 old[NHH], ns[NHH];
+      if (h && L < NH) {
+        hist_load_all<NHH>(a.pool, slot, tc0, old);
+      } else {
+#pragma unroll
+        for (int c = 0; c < NHH; ++c) old[c] = make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int col = 0; col < NHH; ++col) {
+        const int src = L - NH + col;
+        ns[col] = src >= 0 ? cconv::ldg16(a.qk + ((int64_t)(st + src) * a.qk_rs + tc0) * 2)
+                           : pick<NHH>(old, L + col);
+      }
+      hist_store_all<NHH>(a.pool, slot, tc0, ns);
+    }
+  }
+}
+
 // FUSED: the tail of ZayaCCA.project in the epilogue -- each conv output gets
 // its query residual 0.5*(q + k of its kv head) or key residual (the mean of
 // that over the kv group) and lands in the [query | key | value] output, whose
 // value half the aux warps fill with v_current and the delayed half of v.
 template <int T0, int T1, bool FUSED>
 __global__ void __launch_bounds__(kThreads, 1)
-    cca_kernel(const __grid_constant__ CUtensorMap xmap, const Args a) {
+    cca_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ Args a) {
   constexpr int NH = T0 + T1 - 2;               // history columns
-  constexpr int NHH = NH > 0 ? NH : 1;          // array extent for NH columns
   constexpr int NW = T0 + T1 - 1;               // x~[j - m], m = 0 .. NH, per row
   extern __shared__ __align__(1024) unsigned char dsm[];
   // 1024-byte alignment as an offset on the shared pointer itself, so that every
@@ -997,50 +1194,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         single = ok ? 1 : 0;
       } else {
-        // Rows of several requests: row r's request is the last s with
-        // cu[s] <= its token, found for 32 rows at once against windows of 32
-        // cu values (every row's token compared with every value of the
-        // window); the next 32 rows start from the last row's request.
-        for (int r0 = 0; r0 < kRows; r0 += 32) {
-          const int r = r0 + lane;
-          const int t = lo + min(r, max(len - 1, 0));   // rows past the tile repeat the last
-          int sr = sc, wb = sc;
-          bool found = false;
-          for (;;) {
-            const int idx = wb + 1 + lane;
-            const int v = idx < a.B ? cu[idx] : 0x7fffffff;
-            int cnt = 0;
-#pragma unroll 8
-            for (int k = 0; k < 32; ++k) {
-              const int tk = __shfl_sync(0xffffffffu, t, k);
-              const unsigned m = __ballot_sync(0xffffffffu, v <= tk);
-              if (lane == k) cnt = __popc(m);
-            }
-            if (!found) {
-              sr = wb + cnt;
-              found = cnt < 32;
-            }
-            if (__all_sync(0xffffffffu, found)) break;
-            wb += 32;
-          }
-          int j = -1, slot = -1, wr = -1;
-          if (r < len) {
-            const int st = cu[sr], en = cu[sr + 1];
-            if (st >= 0 && st <= t && t < en && en <= a.T) {
-              const int sl = sidx[sr];
-              const bool h = (hini == nullptr || hini[sr] != 0);
-              if (sl < a.pool.num_slots) {   // out-of-range slots are skipped and reported
-                j = t - st;
-                slot = (h && sl >= 0) ? sl : -1;
-                wr = (en - st == 1 && sl >= 0) ? sl : -1;
-              }
-            }
-          }
-          M.rowj[r] = j;
-          M.rowslot[r] = slot;
-          M.rowwr[r] = wr;
-          sc = __shfl_sync(0xffffffffu, sr, 31);
-        }
+        map_rows(cu, sidx, hini, a.B, a.T, a.pool.num_slots, &M, lo, len, sc);
       }
       if (lane == 0) {
         M.lo = lo;
@@ -1254,6 +1408,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         // tile of a one-request tile are computed and never stored)
         const bool fast =
             jf >= NH && (M.single || (rs0 + 7 < len && M.rowj[rs0 + 7] == jf + 7));
+        // a sub-block of first tokens (one-token requests): the decode loop
+        bool first_only = false;
+        if constexpr (kScratch) {
+          if (scratch) {   // warp-uniform: one ballot over both strips of the warp
+            const int rc = rs0 + (kc & 7);
+            const unsigned bal = __ballot_sync(0xffffffffu, rc >= len || M.rowj[rc] == 0);
+            first_only = ((bal >> (lane & 16)) & 0xffffu) == 0xffffu;
+          }
+        }
         if (fast) {
           // all 8 + n x rows are loaded at once, then a register window
           // slides over them
@@ -1288,6 +1451,12 @@ __global__ void __launch_bounds__(kThreads, 1)
               for (int v = 0; v < 8; ++v) xw[m][v] = xw[m - 1][v];
           }
           continue;
+        }
+        if constexpr (kScratch) {
+          if (first_only) {
+            decode_rows<T0, T1>(a.pool, a.w_dw, a.b_dw, &M, xst, Au, Ap, rs0, len, c0, kc);
+            continue;
+          }
         }
         mixed_rows<T0, T1>(a.pool, a.w_dw, a.b_dw, &M, xst, Au, Ap, rs0, len, c0, kc, single,
                            scratch);
@@ -1356,62 +1525,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       // owned requests s with s % G == g: first delayed value and delayed state
-      for (int s = M.own_lo + ((g - M.own_lo % a.G) % a.G + a.G) % a.G + aw * a.G;
-           s < M.own_hi; s += kAuxWarps * a.G) {
-        const int st = cu[s], en = cu[s + 1];
-        const int slot = sidx[s];
-        if (st < 0 || en < st || en > a.T) {
-          if (lane == 0) cconv::flag_error(a.dev_err, CCONV_DERR_CU_SEQLENS);
-          continue;
-        }
-        if (slot >= a.pool.num_slots) continue;
-        const bool h = slot >= 0 && (hini == nullptr || hini[s] != 0);
-        for (int k = lane; k < dunits; k += 32) {
-          const uint4 first = h ? dstate_load(a, slot, k) : cconv::ldg16(a.delayed_init + k * 16);
-          const uint4 last =
-              en > st ? cconv::ldg16(a.delayed + ((int64_t)(en - 1) * a.delayed_rs + k * 8) * 2)
-                      : first;
-          if (en > st) cconv::stg16(a.dprev + ((int64_t)st * a.dprev_rs + k * 8) * 2, first);
-          // (an empty request with history leaves its delayed state as it is)
-          if (slot >= 0 && (en > st || !h)) dstate_store(a, slot, k, last);
-        }
-      }
+      if (M.own_hi > M.own_lo) aux_owned(a, cu, sidx, hini, M.own_lo, M.own_hi, g, aw);
       // Raw-history state of owned requests of two or more tokens, once every
       // producer has read this tile's history (one-token requests are written
       // by the producer of their row).
       if (!W.wait(&ctl->prod_done[ms], (i / kMetaStages) & 1)) break;
-      const int nown = M.own_hi - M.own_lo;
-      for (int task = pa; task < nown * (kGS / 8); task += kAuxWarps * 32) {
-        const int s = M.own_lo + (task >> 4);
-        const int tc0 = g * kGS + (task & 15) * 8;
-        const int st = cu[s], en = cu[s + 1];
-        const int slot = sidx[s];
-        if (st < 0 || en < st || en > a.T) continue;
-        if (slot >= a.pool.num_slots) {
-          if ((task & 15) == 0) cconv::flag_error(a.dev_err, CCONV_DERR_SLOT_RANGE);
-          continue;
-        }
-        if (slot < 0) continue;
-        const bool h = hini == nullptr || hini[s] != 0;
-        const int L = en - st;
-        if (L == 1) continue;
-        if (NH > 0) {
-          uint4 old[NHH], ns[NHH];
-          if (h && L < NH) {
-            hist_load_all<NHH>(a.pool, slot, tc0, old);
-          } else {
-#pragma unroll
-            for (int c = 0; c < NHH; ++c) old[c] = make_uint4(0u, 0u, 0u, 0u);
-          }
-#pragma unroll
-          for (int col = 0; col < NHH; ++col) {
-            const int src = L - NH + col;
-            ns[col] = src >= 0 ? cconv::ldg16(a.qk + ((int64_t)(st + src) * a.qk_rs + tc0) * 2)
-                               : pick<NHH>(old, L + col);
-          }
-          hist_store_all<NHH>(a.pool, slot, tc0, ns);
-        }
-      }
+      if (M.own_hi > M.own_lo) aux_history<NH>(a, cu, sidx, hini, M.own_lo, M.own_hi, g, pa);
       __syncwarp();
       if (lane == 0) mbar_arrive(&ctl->meta_empty[ms]);
     }
