@@ -522,6 +522,43 @@ static __device__ __noinline__ void map_rows(const int32_t* cu, const int32_t* s
   }
 }
 
+// Leading token tiles that own more than kHeavyRequests requests (in a
+// decode-first batch, the tiles of one-token requests: several times the work
+// of a prefill tile). The plain kernel walks them at the start of the units
+// the CTAs take from the shared counter, so that no CTA's static range holds
+// several of them and the CTAs that finish their range first take them.
+// Every lane finds its tile's edges and owned requests by binary search (the
+// same values as tile_edge and count_le); at most 32 tiles, never the last.
+constexpr int kHeavyRequests = 16;
+static __device__ int heavy_prefix(const Args& a, const int32_t* cu) {
+  const int lane = threadIdx.x & 31;
+  // number of s in [0, B) with cu[s] <= p (strict: cu[s] < p)
+  auto count = [&](int p, bool strict) {
+    int l = 0, h = a.B;
+    while (l < h) {
+      const int mid = (l + h) >> 1;
+      if (strict ? cu[mid] < p : cu[mid] <= p) l = mid + 1; else h = mid;
+    }
+    return l;
+  };
+  auto edge = [&](int tau) {
+    if (tau <= 0) return 0;
+    if (tau >= a.num_tiles) return a.T;
+    const int p = tau * a.tile_pitch;
+    const int s = count(p, false) - 1;
+    if (s >= 0 && s < a.B) {
+      const int st = cu[s], en = cu[s + 1];
+      if (p < en && p - st > 0 && p - st < a.n) return st;
+    }
+    return p;
+  };
+  bool heavy = false;
+  if (lane + 1 < a.num_tiles)
+    heavy = count(edge(lane + 1), true) - count(edge(lane), true) > kHeavyRequests;
+  const unsigned m = __ballot_sync(0xffffffffu, heavy);
+  return m == 0xffffffffu ? 32 : __ffs(~m) - 1;
+}
+
 // Unit u -> (group g, token tile tau). The plain kernel walks the units
 // group-major (one group's B operand for many tiles). The fused kernel's
 // residuals read other groups' rows of the same tokens (a query head the key
@@ -530,11 +567,22 @@ static __device__ __noinline__ void map_rows(const int32_t* cu, const int32_t* s
 // and then the key head taking the block's tiles one after another: the rows
 // their residuals read were loaded a few units earlier and are still in L2.
 constexpr int kFusedTileBlock = 8;
+// In the plain kernel the K heavy leading tiles of every group (heavy_prefix)
+// take the unit positions [hs, hs + G*K), group-major; the other tiles fill
+// the positions before and after, group-major.
 template <bool FUSED>
-__device__ __forceinline__ void unit_to_gt(const Args& a, int u, int& g, int& tau) {
+__device__ __forceinline__ void unit_to_gt(const Args& a, int u, int K, int hs, int& g,
+                                           int& tau) {
   if (!FUSED) {
-    g = u / a.num_tiles;
-    tau = u - g * a.num_tiles;
+    const int nh = a.G * K;
+    if (u >= hs && u < hs + nh) {
+      g = (u - hs) / K;
+      tau = (u - hs) - g * K;
+      return;
+    }
+    const int m = u < hs ? u : u - nh, nb = a.num_tiles - K;
+    g = m / nb;
+    tau = K + (m - g * nb);
     return;
   }
   const int m5 = a.kvg + 1, per = m5 * a.num_tiles;
@@ -961,60 +1009,100 @@ __device__ __noinline__ void decode_rows(const Pool P, const char* w_dw, const c
 // Aux warps, owned requests s with s % G == g (warp aw of kAuxWarps takes
 // every kAuxWarps-th): the first delayed value of the request (its delayed
 // state, or delayed_init without history) and its new delayed state (the
-// delayed value of its last token). Out of line: most tiles own no request.
+// delayed value of its last token). Four requests at a time, their loads in
+// flight together. Out of line: most tiles own no request.
 static __device__ __noinline__ void aux_owned(const Args& a, const int32_t* cu, const int32_t* sidx,
-                                       const uint8_t* hini, int own_lo, int own_hi, int g,
-                                       int aw) {
+                                              const uint8_t* hini, int own_lo, int own_hi, int g,
+                                              int aw) {
   const int lane = threadIdx.x & 31;
   const int dunits = a.Dv / 8;
-  for (int s = own_lo + ((g - own_lo % a.G) % a.G + a.G) % a.G + aw * a.G;
-       s < own_hi; s += kAuxWarps * a.G) {
-    const int st = cu[s], en = cu[s + 1];
-    const int slot = sidx[s];
-    if (st < 0 || en < st || en > a.T) {
-      if (lane == 0) cconv::flag_error(a.dev_err, CCONV_DERR_CU_SEQLENS);
-      continue;
+  const int step = kAuxWarps * a.G;
+  for (int s0 = own_lo + ((g - own_lo % a.G) % a.G + a.G) % a.G + aw * a.G; s0 < own_hi;
+       s0 += 4 * step) {
+    int st[4], en[4], slot[4];
+    bool ok[4], h[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int sq = s0 + q * step;
+      ok[q] = false;
+      st[q] = en[q] = slot[q] = 0;
+      h[q] = false;
+      if (sq < own_hi) {
+        st[q] = cu[sq];
+        en[q] = cu[sq + 1];
+        slot[q] = sidx[sq];
+        if (st[q] < 0 || en[q] < st[q] || en[q] > a.T) {
+          if (lane == 0) cconv::flag_error(a.dev_err, CCONV_DERR_CU_SEQLENS);
+        } else if (slot[q] < a.pool.num_slots) {
+          ok[q] = true;
+          h[q] = slot[q] >= 0 && (hini == nullptr || hini[sq] != 0);
+        }
+      }
     }
-    if (slot >= a.pool.num_slots) continue;
-    const bool h = slot >= 0 && (hini == nullptr || hini[s] != 0);
     for (int k = lane; k < dunits; k += 32) {
-      const uint4 first = h ? dstate_load(a, slot, k) : cconv::ldg16(a.delayed_init + k * 16);
-      const uint4 last =
-          en > st ? cconv::ldg16(a.delayed + ((int64_t)(en - 1) * a.delayed_rs + k * 8) * 2)
-                  : first;
-      if (en > st) cconv::stg16(a.dprev + ((int64_t)st * a.dprev_rs + k * 8) * 2, first);
-      // (an empty request with history leaves its delayed state as it is)
-      if (slot >= 0 && (en > st || !h)) dstate_store(a, slot, k, last);
+      uint4 first[4], last[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        if (!ok[q]) continue;
+        first[q] = h[q] ? dstate_load(a, slot[q], k) : cconv::ldg16(a.delayed_init + k * 16);
+        last[q] = en[q] > st[q]
+                      ? cconv::ldg16(a.delayed + ((int64_t)(en[q] - 1) * a.delayed_rs + k * 8) * 2)
+                      : first[q];
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        if (!ok[q]) continue;
+        if (en[q] > st[q])
+          cconv::stg16(a.dprev + ((int64_t)st[q] * a.dprev_rs + k * 8) * 2, first[q]);
+        // (an empty request with history leaves its delayed state as it is)
+        if (slot[q] >= 0 && (en[q] > st[q] || !h[q])) dstate_store(a, slot[q], k, last[q]);
+      }
     }
   }
 }
 
-// Aux warps, raw-history state of the owned requests of two or more tokens
-// (one-token requests are written by the producer of their row): the last n
-// inputs of the request, from the request's own rows and, for a request
-// shorter than n, its old history. Thread pa of the aux warps takes every
-// (kAuxWarps*32)-th (request, 8-channel unit).
+// Aux warps, raw-history state of the owned requests other than one-token
+// ones (those are written by the producer of their row): the last n inputs of
+// the request, from the request's own rows and, for a request shorter than n,
+// its old history (zeros without history). Warp aw of kAuxWarps looks at 32 owned
+// requests at a time (a ballot keeps those that need it) and writes two
+// requests at a time, one 8-channel unit per lane.
 template <int NH>
 __device__ __noinline__ void aux_history(const Args& a, const int32_t* cu, const int32_t* sidx,
                                          const uint8_t* hini, int own_lo, int own_hi, int g,
-                                         int pa) {
+                                         int aw) {
   constexpr int NHH = NH > 0 ? NH : 1;
-  const int nown = own_hi - own_lo;
-  for (int task = pa; task < nown * (kGS / 8); task += kAuxWarps * 32) {
-    const int s = own_lo + (task >> 4);
-    const int tc0 = g * kGS + (task & 15) * 8;
-    const int st = cu[s], en = cu[s + 1];
-    const int slot = sidx[s];
-    if (st < 0 || en < st || en > a.T) continue;
-    if (slot >= a.pool.num_slots) {
-      if ((task & 15) == 0) cconv::flag_error(a.dev_err, CCONV_DERR_SLOT_RANGE);
-      continue;
+  const int lane = threadIdx.x & 31;
+  for (int b = own_lo + aw * 32; b < own_hi; b += kAuxWarps * 32) {
+    const int s = b + lane;
+    bool need = false;
+    if (s < own_hi) {
+      const int st = cu[s], en = cu[s + 1];
+      const int slot = sidx[s];
+      if (st >= 0 && en >= st && en <= a.T) {
+        if (slot >= a.pool.num_slots)
+          cconv::flag_error(a.dev_err, CCONV_DERR_SLOT_RANGE);
+        else
+          need = NH > 0 && slot >= 0 && en - st != 1;   // (an empty request too)
+      }
     }
-    if (slot < 0) continue;
-    const bool h = hini == nullptr || hini[s] != 0;
-    const int L = en - st;
-    if (L == 1) continue;
-    if (NH > 0) {
+    unsigned m = __ballot_sync(0xffffffffu, need);
+    while (m != 0u) {
+      const int q0 = __ffs(m) - 1;
+      m &= m - 1;
+      int q1 = -1;
+      if (m != 0u) {
+        q1 = __ffs(m) - 1;
+        m &= m - 1;
+      }
+      const int q = lane < 16 ? q0 : q1;
+      if (q < 0) continue;
+      const int sr = b + q;
+      const int tc0 = g * kGS + (lane & 15) * 8;
+      const int st = cu[sr], en = cu[sr + 1];
+      const int slot = sidx[sr];
+      const bool h = hini == nullptr || hini[sr] != 0;
+      const int L = en - st;
       uint4 old[NHH], ns[NHH];
       if (h && L < NH) {
         hist_load_all<NHH>(a.pool, slot, tc0, old);
@@ -1126,10 +1214,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Work split: units [c * S, (c + 1) * S) of CTA c first (one group's B
     // for many consecutive tiles), then chunks of the remaining units from a
     // counter shared by all CTAs, so that CTAs holding slow tiles (many
-    // requests, history reads) take fewer of them. A unit g < 0 in the meta
-    // ring tells every role to stop.
+    // requests, history reads) take fewer of them; the heavy leading tiles
+    // of every group come first among those (unit_to_gt). A unit g < 0 in
+    // the meta ring tells every role to stop.
     int cur = blockIdx.x * a.static_units, end = cur + a.static_units;
     const int dyn0 = gridDim.x * a.static_units;
+    const int K = FUSED ? 0 : heavy_prefix(a, cu);
+    const int hs = min(dyn0, a.units - a.G * K);
     int i = 0;
     for (;; ++i) {
       const int ms = i % kMetaStages, xs = i % kXStages;
@@ -1152,7 +1243,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const int u = cur++;
       int g, tau;
-      unit_to_gt<FUSED>(a, u, g, tau);
+      unit_to_gt<FUSED>(a, u, K, hs, g, tau);
       const bool cont = (g == prev_g && tau == prev_tau + 1);
       const int lo = cont ? hi_prev : tile_edge(a, cu, tau, 0);
       // x rows [lo - n, lo - n + kXBoxRows) of the group's channels: issued
@@ -1476,7 +1567,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     // The delayed half of v, the delayed state and the raw-history state of
     // owned multi-token requests: none of it feeds the MMA.
     const int aw = warp - kWarpAux0;               // 0 .. kAuxWarps-1
-    const int pa = threadIdx.x - kWarpAux0 * 32;   // 0 .. 32*kAuxWarps-1
     const int dunits = a.Dv / 8;                   // 16-byte units per delayed row
     for (int i = 0;; ++i) {
       const int ms = i % kMetaStages;
@@ -1530,7 +1620,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // producer has read this tile's history (one-token requests are written
       // by the producer of their row).
       if (!W.wait(&ctl->prod_done[ms], (i / kMetaStages) & 1)) break;
-      if (M.own_hi > M.own_lo) aux_history<NH>(a, cu, sidx, hini, M.own_lo, M.own_hi, g, pa);
+      if (M.own_hi > M.own_lo) aux_history<NH>(a, cu, sidx, hini, M.own_lo, M.own_hi, g, aw);
       __syncwarp();
       if (lane == 0) mbar_arrive(&ctl->meta_empty[ms]);
     }
