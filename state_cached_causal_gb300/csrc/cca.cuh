@@ -703,32 +703,47 @@ __device__ __forceinline__ void load_taps(const char* w_dw, const char* b_dw, in
   }
 }
 
+// Two fp32 fused multiply-adds in one instruction (each rounded to nearest
+// even, as fmaf): d = a * b + c for lanes 0 and 1.
+__device__ __forceinline__ void fma2(float& d0, float& d1, float a0, float a1, float b0,
+                                     float b1, float c0, float c1) {
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+
+// u of 8 channels from the bias and T0 taps, tap k multiplying xw[S + T0-1-k]
+// (S = 0: u(j), S = 1: u(j-1)); fp32 sums from the bias, tap by tap, two
+// channels per instruction.
+template <int T0, int S, int NW>
+__device__ __forceinline__ uint4 conv_taps(const float (&w0)[T0][8], const float (&b0)[8],
+                                           const float (&xw)[NW][8]) {
+  float uu[8];
+#pragma unroll
+  for (int v = 0; v < 8; v += 2) {
+    float a0 = b0[v], a1 = b0[v + 1];
+#pragma unroll
+    for (int k = 0; k < T0; ++k) {
+      const int m = (S + T0 - 1 - k) % NW;
+      fma2(a0, a1, w0[k][v], w0[k][v + 1], xw[m][v], xw[m][v + 1], a0, a1);
+    }
+    uu[v] = a0;
+    uu[v + 1] = a1;
+  }
+  return cconv::pack16<__nv_bfloat16>(uu);
+}
+
 // Row r of the A operand from its window xw[m] = x~[j - m]: u(j) at Au + r*16
-// and, in a two-buffer tile, u(j-1) at Ap + r*16 (fp32 sums from the bias, tap
-// by tap, one bf16 rounding).
+// and, in a two-buffer tile, u(j-1) at Ap + r*16 (one bf16 rounding each).
 template <int T0, int T1, int NW>
 __device__ __forceinline__ void put_row(const float (&w0)[T0][8], const float (&b0)[8],
                                         const float (&xw)[NW][8], unsigned char* Au,
                                         unsigned char* Ap, int r, bool single) {
-  float uu[8];
-#pragma unroll
-  for (int v = 0; v < 8; ++v) {
-    float acc = b0[v];
-#pragma unroll
-    for (int k = 0; k < T0; ++k) acc = fmaf(w0[k][v], xw[T0 - 1 - k][v], acc);
-    uu[v] = acc;
-  }
-  *reinterpret_cast<uint4*>(Au + r * 16) = cconv::pack16<__nv_bfloat16>(uu);
-  if (T1 == 2 && !single) {
-#pragma unroll
-    for (int v = 0; v < 8; ++v) {
-      float acc = b0[v];
-#pragma unroll
-      for (int k = 0; k < T0; ++k) acc = fmaf(w0[k][v], xw[(T0 - k) % NW][v], acc);
-      uu[v] = acc;
-    }
-    *reinterpret_cast<uint4*>(Ap + r * 16) = cconv::pack16<__nv_bfloat16>(uu);
-  }
+  *reinterpret_cast<uint4*>(Au + r * 16) = conv_taps<T0, 0>(w0, b0, xw);
+  if (T1 == 2 && !single)
+    *reinterpret_cast<uint4*>(Ap + r * 16) = conv_taps<T0, 1>(w0, b0, xw);
 }
 
 // B operand of group g: B[tap][k-chunk][n] = w_gr[g*128 + n][k-chunk*8 + e][tap],
@@ -1519,18 +1534,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int m = 1; m <= NH; ++m) cconv::unpack16<__nv_bfloat16>(raw[NH - m], xw[m]);
           if constexpr (T1 == 2) {
-            if (rs0 == 0 && M.single) {
-              // row -1 of a single-buffer tile: its window x~[j - 1 - m] is xw[m + 1]
-              float uu[8];
-#pragma unroll
-              for (int v = 0; v < 8; ++v) {
-                float acc = b0[v];
-#pragma unroll
-                for (int k = 0; k < T0; ++k) acc = fmaf(w0[k][v], xw[T0 - k][v], acc);
-                uu[v] = acc;
-              }
-              *reinterpret_cast<uint4*>(Au - 16) = cconv::pack16<__nv_bfloat16>(uu);
-            }
+            // row -1 of a single-buffer tile: its window x~[j - 1 - m] is xw[m + 1]
+            if (rs0 == 0 && M.single)
+              *reinterpret_cast<uint4*>(Au - 16) = conv_taps<T0, 1>(w0, b0, xw);
           }
 #pragma unroll
           for (int rr = 0; rr < 8; ++rr) {
