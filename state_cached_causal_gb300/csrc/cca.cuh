@@ -237,7 +237,18 @@ struct Waiter {
   // timed out); never spins forever. Every caller is a whole warp, and the
   // warp decides together (a phase seen complete by one lane is complete for
   // all), so that its lanes never split between going on and giving up.
-  __device__ __noinline__ bool wait(uint64_t* bar, uint32_t parity) const {
+  // The first poll is inline (a phase already complete costs no call); the
+  // polling loop is out of line.
+  __device__ __forceinline__ bool wait(uint64_t* bar, uint32_t parity) const {
+#ifdef CCA_WAIT_POLL_NS
+    const bool done = mbar_try_for(bar, parity, CCA_WAIT_POLL_NS);
+#else
+    const bool done = mbar_try(bar, parity);
+#endif
+    if (__any_sync(0xffffffffu, done)) return true;
+    return wait_loop(bar, parity);
+  }
+  __device__ __noinline__ bool wait_loop(uint64_t* bar, uint32_t parity) const {
     const long long t0 = clock64();
 #ifdef CCA_WAIT_POLL_NS
     constexpr uint32_t kCheckMask = 0u;
