@@ -187,6 +187,16 @@ CCONV_API int cconv_fwd_varlen(const void* x, int64_t x_row_stride, const void* 
  *   num_accepted int32 [num_seqs], required when n_spec > 0, else ignored
  *   has_init     uint8 [num_seqs] or NULL (all true)
  *   n_spec       0..7;  cap >= S + n_spec;  width 2..8; dilation 1..8
+ *
+ * Launches in flight. On a channel-first pool (dense [slot, channel, column])
+ * the kernel takes part of its work from a counter in one of 64 slots inside
+ * the library, drawn in turn by successive calls of this entry point and of
+ * cconv_update_fused; the last CTA of a launch clears its slot. At most 64
+ * such launches may run at the same
+ * time: a 65th overlapping one, or a replay of a captured CUDA graph (which
+ * keeps the slot it was captured with) running beside a later call that drew
+ * the same slot, shares the counter and may skip or repeat work without an
+ * error.
  */
 CCONV_API int cconv_update(const void* x, int64_t x_row_stride, cconv_pool_t conv_states,
                  const void* w, const void* bias, const int32_t* state_idx,

@@ -25,6 +25,7 @@
 #pragma once
 
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 #include <type_traits>
 
@@ -47,7 +48,21 @@ constexpr int kMinCtasPerSm = 3;
 constexpr size_t kStageBudget = 72 * 1024;           // stages of one CTA
 constexpr long long kWaitCycles = 2000000000LL;      // ~1 s at 2 GHz
 
-enum : int32_t { kSkip = 1, kHist = 2, kOwn = 4, kLoadState = 8 };
+enum : int32_t { kSkip = 1, kHist = 2, kOwn = 4, kLoadState = 8, kEnd = 16 };
+
+// Work split: a CTA first takes a contiguous range of kStaticPercent % of the
+// items (channel-tile-major: its weights change only where the range crosses a
+// tile), then kDynChunk items at a time from a counter shared by the launch's
+// CTAs, so that CTAs that run slower (the three CTAs of an SM do not get equal
+// shares of its issue slots and memory pipes) take fewer items. Counter slot
+// epoch % kEpochs per launch, cleared by the launch's last CTA: at most
+// kEpochs launches of one kernel build may be in flight at once.
+constexpr int kStaticPercent = 70;
+constexpr int kDynChunk = 2;
+constexpr int kEpochs = 64;
+__device__ unsigned int g_bulk_next[kEpochs];
+__device__ unsigned int g_bulk_done[kEpochs];
+std::atomic<unsigned> g_bulk_launches{0};   // host: slots drawn in turn by every kernel here
 
 struct Meta {
   int32_t s, ct, off, flags, slot;
@@ -68,7 +83,9 @@ struct BulkArgs {
   int32_t xs_off;        // byte offset of the token rows within a stage
   int32_t rs_off;        // fused: byte offset of the residual rows
   int32_t os_off;        // fused: byte offset of the outer residual rows
-  int64_t items;         // B * ctiles
+  int64_t items;         // B * ctiles (< 2^31)
+  int64_t static_items;  // items of each CTA's static range
+  int32_t epoch;         // this launch's counter slot
 };
 
 __device__ bool wait_bounded(Ctl* ctl, uint64_t* bar, uint32_t parity, int32_t* dev_err) {
@@ -177,8 +194,6 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
   Ctl* ctl = reinterpret_cast<Ctl*>(bsm);
   unsigned char* stage0 = bsm + kCtlBytes;
   const int tid = threadIdx.x;
-  const int64_t i0 = (int64_t)blockIdx.x * b.items / gridDim.x;
-  const int n = (int)((int64_t)(blockIdx.x + 1) * b.items / gridDim.x - i0);
   const int q = 1 + a.n_spec, cap = a.pool.cap;
   const int tile = b.tile;
   // bf16 slabs whose cap columns are whole 8-byte words (cap a multiple of 4,
@@ -232,15 +247,42 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
         bulk_load(sb, a.pool.p + ((int64_t)m.slot * a.pool.s_slot + (int64_t)cb * cap) * ES,
                   slab_bytes, &ctl->full[st]);
     };
+    // the next item: the static range first, then chunks from the counter
+    int64_t cur = (int64_t)blockIdx.x * b.static_items, end = cur + b.static_items;
+    const int64_t dyn0 = (int64_t)gridDim.x * b.static_items;
+    bool more = true;
+    auto grab = [&]() -> int64_t {
+      if (cur >= end) {
+        const unsigned got = atomicAdd(&g_bulk_next[b.epoch], (unsigned)kDynChunk);
+        cur = dyn0 + got;
+        end = min(cur + kDynChunk, b.items);
+      }
+      if (cur >= b.items) return -1;
+      return cur++;
+    };
+    // fill stage `issued % NS` with the next item, or with the end marker
+    auto fill = [&](int slot_j) {
+      const int64_t it = more ? grab() : -1;
+      if (it < 0) {
+        more = false;
+        const int st = slot_j % NS;
+        ctl->meta[st].flags = kEnd;
+        mbar_arrive(&ctl->full[st]);
+      } else {
+        issue_load(slot_j, item_meta<FUSED>(a, it, S));
+      }
+    };
     int issued = 0;
-    for (; issued < min(n, NS); ++issued)
-      issue_load(issued, item_meta<FUSED>(a, i0 + issued, S));
-    Meta next{};
-    if (issued < n) next = item_meta<FUSED>(a, i0 + issued, S);   // one item ahead
+    while (issued < NS && more) fill(issued++);
     int j = 0;
-    for (; j < n; ++j) {
+    bool aborted = false;
+    for (; j < issued; ++j) {
       const int st = j % NS;
-      if (!wait_bounded(ctl, &ctl->done[st], (uint32_t)(j / NS) & 1u, a.dev_err)) break;
+      if (ctl->meta[st].flags & kEnd) break;
+      if (!wait_bounded(ctl, &ctl->done[st], (uint32_t)(j / NS) & 1u, a.dev_err)) {
+        aborted = true;
+        break;
+      }
       const Meta m = ctl->meta[st];
       if (!(m.flags & kSkip)) {
         unsigned char* sb = stage0 + (size_t)st * b.stage_bytes;
@@ -256,20 +298,25 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
         }
       }
       bulk_commit();
-      if (issued < n) {
+      if (more) {
         bulk_wait_read<0>();   // the stage's stores have read it
-        issue_load(issued, next);
-        ++issued;
-        if (issued < n) next = item_meta<FUSED>(a, i0 + issued, S);
+        fill(issued++);
       }
     }
-    if (j < n) {
+    if (aborted) {
       // aborting: wait for the loads still in flight into this CTA's stages
       for (int k = j; k < issued; ++k) {
         const long long t0 = clock64();
         while (!mbar_try(&ctl->full[k % NS], (uint32_t)(k / NS) & 1u))
           if (clock64() - t0 > kWaitCycles) break;
       }
+    }
+    // The last CTA done with the counter clears this launch's slot (every
+    // CTA's copy thread passes here, aborting or not).
+    __threadfence();
+    if (atomicAdd(&g_bulk_done[b.epoch], 1u) == gridDim.x - 1) {
+      atomicExch(&g_bulk_next[b.epoch], 0u);
+      atomicExch(&g_bulk_done[b.epoch], 0u);
     }
     bulk_wait<0>();
     return;
@@ -281,10 +328,11 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
   const int keep = ncols - q;   // spec: kept columns B[off+1, off+1+keep), keep >= S-1
   float wk[2][W], bv[2];
   int cur_ct = -1;
-  for (int j = 0; j < n; ++j) {
+  for (int j = 0;; ++j) {
     const int st = j % NS;
     if (!wait_bounded(ctl, &ctl->full[st], (uint32_t)(j / NS) & 1u, a.dev_err)) break;
     const Meta m = ctl->meta[st];
+    if (m.flags & kEnd) break;
     if (!(m.flags & kSkip)) {
       const int cb = m.ct * tile, nch = min(tile, a.C - cb);
       if (m.ct != cur_ct) {
@@ -481,7 +529,9 @@ cudaError_t launch_t(const UpdArgs& a, const BulkArgs& b, size_t smem, cudaStrea
     per_sm = std::max(1, cache.per_sm);
   }
   const int64_t grid = std::min<int64_t>(b.items, (int64_t)per_sm * num_sms);
-  k<<<(unsigned)grid, kThreads, smem, st>>>(a, b);
+  BulkArgs bb = b;
+  bb.static_items = b.items * kStaticPercent / 100 / grid;
+  k<<<(unsigned)grid, kThreads, smem, st>>>(a, bb);
   return cudaGetLastError();
 }
 
@@ -549,6 +599,8 @@ cudaError_t launch_bulk_types(UpdArgs a, int width, int dilation, bool fused, cu
   a.ctiles = (a.C + tile - 1) / tile;
   b.items = (int64_t)a.B * a.ctiles;
   if (b.items <= 0) return cudaSuccess;
+  if (b.items >= (int64_t(1) << 31)) return cudaErrorNotSupported;
+  b.epoch = (int32_t)(g_bulk_launches.fetch_add(1u) % kEpochs);
   int dev = 0, num_sms = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);
