@@ -85,7 +85,9 @@ constexpr int kDerrTimeout = CCONV_DERR_TIMEOUT;
 constexpr int kOutRowPitch = 64;                       // 64 bytes of a row, 16-byte chunks swizzled
 constexpr int kEpiCols = kGS / (kEpiWarps / 4);       // accumulator columns per epilogue warp
 constexpr int kProdRows = kRows / (kProdWarps * 2);    // rows per producer thread (16 per chunk)
-constexpr int kOutStageBytes = 32 * kOutRowPitch + kEpiCols * 4;   // per epilogue warp, + bias
+// per epilogue warp: the 32 x 64-byte stage (512-byte aligned: the swizzle of
+// the tensor store repeats every 512 bytes) and this half's bias
+constexpr int kOutStageBytes = (32 * kOutRowPitch + kEpiCols * 4 + 511) / 512 * 512;
 
 // Requests whose metadata the kernel copies into shared memory (9 bytes each).
 constexpr int kSmemRequests = 352;
@@ -93,7 +95,8 @@ constexpr int kSmemRequests = 352;
 struct Meta {
   int lo, len, g, own_lo, own_hi;
   int single;           // rows are consecutive tokens of one request (one A buffer)
-  int pad1, pad2;
+  int tma_out;          // all 128 rows are tokens of that request: stores by the tensor map
+  int pad2;
   int rowj[kRows];      // position of the row in its request, -1 outside every request
   int rowslot[kRows];   // slot whose history the row reads, -1 for a zero history
   int rowwr[kRows];     // slot the row's producer writes at once (one-token request), else -1
@@ -156,6 +159,14 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
       " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
       : "memory");
+}
+// 2-D tensor store of a shared-memory box (bulk group of the issuing thread).
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* src, int x,
+                                             int y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(smem_u32(src)), "r"(x), "r"(y)
+               : "memory");
 }
 __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                          uint32_t idesc, uint32_t accumulate) {
@@ -1153,7 +1164,8 @@ __device__ __noinline__ void aux_history(const Args& a, const int32_t* cu, const
 // value half the aux warps fill with v_current and the delayed half of v.
 template <int T0, int T1, bool FUSED>
 __global__ void __launch_bounds__(kThreads, 1)
-    cca_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ Args a) {
+    cca_kernel(const __grid_constant__ CUtensorMap xmap, const __grid_constant__ CUtensorMap omap,
+               const __grid_constant__ Args a) {
   constexpr int NH = T0 + T1 - 2;               // history columns
   constexpr int NW = T0 + T1 - 1;               // x~[j - m], m = 0 .. NH, per row
   extern __shared__ __align__(1024) unsigned char dsm[];
@@ -1295,7 +1307,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // row -> request; sc = request holding row lo
       int sc = max(nle_lo - 1, 0);
       const int st0 = cu[sc], en0 = cu[sc + 1];
-      int single = 0;
+      int single = 0, tma_out = 0;
       if (st0 >= 0 && st0 <= lo && en0 >= hi && en0 <= a.T) {
         // the whole tile lies inside one request: row r's previous token is
         // row r - 1 (row -1 for r = 0)
@@ -1310,6 +1322,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           M.rowwr[r] = r == 0 ? wr : -1;
         }
         single = ok ? 1 : 0;
+        // rows len .. 127 are the request's next tokens, computed here as the
+        // next tile computes them (the same bits): a whole-tile store may
+        // write them too
+        tma_out = (!FUSED && ok && (int64_t)lo + kRows <= en0) ? 1 : 0;
       } else {
         map_rows(cu, sidx, hini, a.B, a.T, a.pool.num_slots, &M, lo, len, sc);
       }
@@ -1320,6 +1336,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         M.own_lo = own_lo;
         M.own_hi = own_hi;
         M.single = single;
+        M.tma_out = tma_out;
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&ctl->meta_full[ms]);
@@ -1446,6 +1463,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int e = 0; e < 8; ++e) hh[e] = __uint_as_float(cur[k + e]) + bb[e];
           *reinterpret_cast<uint4*>(stage_at(lane, k / 8)) = cconv::pack16<__nv_bfloat16>(hh);
         }
+        if (!FUSED && M.tma_out) {
+          // the stage's layout is the tensor map's 64-byte swizzle: one store
+          // of the 32 rows x 32 channels, read out before the stage is reused
+          fence_proxy_async();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&omap, stage, g * kGS + half * kEpiCols + c * 32, lo + q * 32);
+            cconv::bulk_commit();
+            cconv::bulk_wait_read<0>();
+          }
+          __syncwarp();
+          continue;
+        }
         __syncwarp();
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
@@ -1467,6 +1497,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(&ctl->meta_empty[ms]);
       }
     }
+    if (lane == 0) cconv::bulk_wait<0>();   // every tensor store has completed
   } else if (warp < kWarpAux0) {
     // ------------------------------------------------------------- producers
     // Thread p: channel chunk kc (8 channels) of rows kProdRows * strip .. + kProdRows-1.
@@ -1692,7 +1723,8 @@ static size_t smem_bytes(int T1) {
 }
 
 template <int T0, int T1, bool FUSED>
-static cudaError_t launch(const CUtensorMap& map, const Args& a, int grid, cudaStream_t st) {
+static cudaError_t launch(const CUtensorMap& map, const CUtensorMap& omap, const Args& a,
+                          int grid, cudaStream_t st) {
   const size_t smem = smem_bytes(T1);
   cudaError_t e = cudaFuncSetAttribute(cca_kernel<T0, T1, FUSED>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -1700,7 +1732,7 @@ static cudaError_t launch(const CUtensorMap& map, const Args& a, int grid, cudaS
   // counters passed in (the static-scratch entry point) start at zero
   if (a.work && (e = cudaMemsetAsync(a.work, 0, 2 * sizeof(unsigned int), st)) != cudaSuccess)
     return e;
-  cca_kernel<T0, T1, FUSED><<<grid, kThreads, smem, st>>>(map, a);
+  cca_kernel<T0, T1, FUSED><<<grid, kThreads, smem, st>>>(map, omap, a);
   return cudaGetLastError();
 }
 
@@ -1853,6 +1885,22 @@ static int cca_entry(const void* qk, int64_t qk_row_stride, const void* w_dw, co
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return CCONV_ERR_INVALID;
   }
+  // the q/k output rows as 32 x 32 boxes with the epilogue stage's 64-byte
+  // swizzle (plain entry point: whole one-request tiles are stored through it)
+  CUtensorMap omap;
+  memset(&omap, 0, sizeof(omap));
+  if (!FUSED && num_tokens > 0) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return CCONV_ERR_LAUNCH;
+    const cuuint64_t dims[2] = {(cuuint64_t)Cqk, (cuuint64_t)num_tokens};
+    const cuuint64_t strides[1] = {(cuuint64_t)out_qk_row_stride * 2};
+    const cuuint32_t box[2] = {32u, 32u};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(&omap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, out_qk, dims, strides, box,
+                     estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                     CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return CCONV_ERR_INVALID;
+  }
   // (looked up only for a call that passed every check)
   if (static_scratch) {
     const int rc = static_scratch(&a.work);
@@ -1861,7 +1909,7 @@ static int cca_entry(const void* qk, int64_t qk_row_stride, const void* w_dw, co
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = cudaErrorInvalidValue;
 #define CCA_CASE(a0, a1) \
-  if (t0 == a0 && t1 == a1) e = launch<a0, a1, FUSED>(map, a, grid, st);
+  if (t0 == a0 && t1 == a1) e = launch<a0, a1, FUSED>(map, omap, a, grid, st);
   CCA_CASE(1, 1) CCA_CASE(2, 1) CCA_CASE(3, 1) CCA_CASE(4, 1)
   CCA_CASE(1, 2) CCA_CASE(2, 2) CCA_CASE(3, 2) CCA_CASE(4, 2)
 #undef CCA_CASE
