@@ -17,12 +17,14 @@
 //               owned requests) into a 4-deep ring, and the TMA load of the
 //               tile's x rows (plus the history halo) into a 2-deep ring;
 //   warp 1      TMEM allocation and the single MMA-issuing thread;
-//   warps 2-9   epilogue: tcgen05.ld of the accumulator (two warps per TMEM
-//               lane quadrant, one half of the columns each), bias, bf16
-//               round, store;
-//   warps 10-13 producers: the depthwise stage straight into an A operand in
-//               shared memory, the group's weights into the B operand, and
-//               the new state of one-token requests;
+//   warps 2-5   epilogue: tcgen05.ld of the accumulator (one warp per TMEM
+//               lane quadrant), bias, bf16 round, and a tensor store of each
+//               32 x 32 box (the fused kernel: warps 2-9, two per quadrant,
+//               with the residual mix and per-lane stores);
+//   warps 6-13  producers (the fused kernel: 10-13): the depthwise stage
+//               straight into an A operand in shared memory, the group's
+//               weights into the B operand, and the new state of one-token
+//               requests;
 //   warps 14-15 aux: the delayed-v shift, the delayed state and the raw-history
 //               state of longer requests.
 // A tile whose rows are consecutive tokens of one request stores u once, for
@@ -55,13 +57,9 @@ constexpr int kRows = 128;        // MMA M: rows (tokens) per tile
 constexpr int kMaxN = 4;          // history columns supported (t0 + t1 - 2)
 constexpr int kXStages = 2;
 constexpr int kMetaStages = 4;
-constexpr int kProdWarps = 4;
-constexpr int kEpiWarps = 8;
 constexpr int kAuxWarps = 2;
-constexpr int kWarpSched = 0, kWarpMma = 1, kWarpEpi0 = 2, kWarpProd0 = kWarpEpi0 + kEpiWarps;
-constexpr int kWarpAux0 = kWarpProd0 + kProdWarps;
-constexpr int kWarps = kWarpAux0 + kAuxWarps;
-constexpr int kThreads = kWarps * 32;
+constexpr int kWarpSched = 0, kWarpMma = 1, kWarpEpi0 = 2;
+constexpr int kThreads = 16 * 32;
 constexpr int kXRowBytes = kGS * 2;                    // one tile row of a group: 256 B
 constexpr int kXBoxRows = kRows + kMaxN;               // rows per x stage
 constexpr int kXStageBytes = kXBoxRows * kXRowBytes;   // 33792 B
@@ -83,11 +81,24 @@ constexpr long long kWaitCycles = CCA_WAIT_CYCLES;
 constexpr long long kDrainCycles = 2000000000LL;
 constexpr int kDerrTimeout = CCONV_DERR_TIMEOUT;
 constexpr int kOutRowPitch = 64;                       // 64 bytes of a row, 16-byte chunks swizzled
-constexpr int kEpiCols = kGS / (kEpiWarps / 4);       // accumulator columns per epilogue warp
-constexpr int kProdRows = kRows / (kProdWarps * 2);    // rows per producer thread (16 per chunk)
-// per epilogue warp: the 32 x 64-byte stage (512-byte aligned: the swizzle of
-// the tensor store repeats every 512 bytes) and this half's bias
-constexpr int kOutStageBytes = (32 * kOutRowPitch + kEpiCols * 4 + 511) / 512 * 512;
+
+// Warps of a CTA: scheduler, MMA, epilogue, producers, aux (16 in all). The
+// plain kernel gives the depthwise stage eight warps and the epilogue four
+// (whole-tile tensor stores keep the epilogue light); the fused kernel's
+// epilogue adds the residual mix and keeps eight, with four producers.
+template <bool FUSED>
+struct Roles {
+  static constexpr int kProdWarps = FUSED ? 4 : 8;
+  static constexpr int kEpiWarps = FUSED ? 8 : 4;
+  static constexpr int kWarpProd0 = kWarpEpi0 + kEpiWarps;
+  static constexpr int kWarpAux0 = kWarpProd0 + kProdWarps;
+  static_assert(kWarpAux0 + kAuxWarps == kThreads / 32, "16 warps");
+  static constexpr int kEpiCols = kGS / (kEpiWarps / 4);       // accumulator columns per epilogue warp
+  static constexpr int kProdRows = kRows / (kProdWarps * 2);    // rows per producer thread
+  // per epilogue warp: the 32 x 64-byte stage (512-byte aligned: the swizzle
+  // of the tensor store repeats every 512 bytes) and its columns' bias
+  static constexpr int kOutStageBytes = (32 * kOutRowPitch + kEpiCols * 4 + 511) / 512 * 512;
+};
 
 // Requests whose metadata the kernel copies into shared memory (9 bytes each).
 constexpr int kSmemRequests = 352;
@@ -769,14 +780,14 @@ __device__ __forceinline__ void put_row(const float (&w0)[T0][8], const float (&
 }
 
 // B operand of group g: B[tap][k-chunk][n] = w_gr[g*128 + n][k-chunk*8 + e][tap],
-// 16 bytes per (k-chunk, n); thread p of the producers takes every
-// (kProdWarps*32)-th pair, eight pairs' loads in flight.
-template <int T1>
+// 16 bytes per (k-chunk, n); thread p of the NP producer threads takes every
+// NP-th pair, eight pairs' loads in flight.
+template <int T1, int NP>
 __device__ __noinline__ void load_b_operand(const char* w_gr, unsigned char* sB, int g, int p) {
-  constexpr int kBIter = kGS * (kGS / 8) / (kProdWarps * 32);
+  constexpr int kBIter = kGS * (kGS / 8) / NP;
 #pragma unroll 8
   for (int it = 0; it < kBIter; ++it) {
-    const int pr = p + it * (kProdWarps * 32);
+    const int pr = p + it * NP;
     const int o = pr & (kGS - 1), bkc = pr >> 7;
     const char* src = w_gr + ((int64_t)(g * kGS + o) * kGS + bkc * 8) * T1 * 2;
     uint32_t e[8 * T1];
@@ -839,15 +850,15 @@ __device__ __noinline__ void row_before_hist(const Pool P, const char* w_dw, con
   *reinterpret_cast<uint4*>(Au - 16) = cconv::pack16<__nv_bfloat16>(uu);
 }
 
-// History of the rows r0 .. r0+kProdRows-1 that read it (j < n, with a slot),
+// History of the rows r0 .. r0+NR-1 that read it (j < n, with a slot),
 // by cp.async into the rows' own 16-byte slots of both A buffers (free until
 // the rows' A values overwrite them): two-tap tiles with n <= 2 on a
 // channel-first or column-first pool.
-template <int NH>
+template <int NH, int NR>
 __device__ __noinline__ void prefetch_history(const Pool P, const Meta* M, unsigned char* Au,
                                               unsigned char* Ap, int r0, int len, int c0) {
 #pragma unroll 1
-  for (int rr = 0; rr < kProdRows; ++rr) {
+  for (int rr = 0; rr < NR; ++rr) {
     const int r = r0 + rr;
     const int j = r < len ? M->rowj[r] : -1;
     const int hslot = M->rowslot[r];
@@ -1168,6 +1179,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                const __grid_constant__ Args a) {
   constexpr int NH = T0 + T1 - 2;               // history columns
   constexpr int NW = T0 + T1 - 1;               // x~[j - m], m = 0 .. NH, per row
+  using R = Roles<FUSED>;
+  constexpr int kProdWarps = R::kProdWarps, kEpiWarps = R::kEpiWarps;
+  constexpr int kWarpProd0 = R::kWarpProd0, kWarpAux0 = R::kWarpAux0;
+  constexpr int kEpiCols = R::kEpiCols, kProdRows = R::kProdRows;
+  constexpr int kOutStageBytes = R::kOutStageBytes;
   extern __shared__ __align__(1024) unsigned char dsm[];
   // 1024-byte alignment as an offset on the shared pointer itself, so that every
   // pointer derived from it stays in the shared address space (a round trip
@@ -1500,7 +1516,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) cconv::bulk_wait<0>();   // every tensor store has completed
   } else if (warp < kWarpAux0) {
     // ------------------------------------------------------------- producers
-    // Thread p: channel chunk kc (8 channels) of rows kProdRows * strip .. + kProdRows-1.
+    // Thread p: channel chunk kc (8 channels) of rows kProdRows * strip .. + kProdRows-1
+    // (8 or 16 rows: one or two 8-row sub-blocks).
     const int p = threadIdx.x - kWarpProd0 * 32;   // 0 .. 32 * kProdWarps - 1
     const int kc = p & 15;
     const int strip = p >> 4;                      // 0 .. 2 * kProdWarps - 1
@@ -1523,7 +1540,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       const int c0 = g * kGS + kc * 8;
       if (g != cur_g) {
-        load_b_operand<T1>(a.w_gr, sB, g, p);
+        load_b_operand<T1, kProdWarps * 32>(a.w_gr, sB, g, p);
         load_taps<T0>(a.w_dw, a.b_dw, c0, w0, b0);
         cur_g = g;
       }
@@ -1546,7 +1563,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool scratch = kScratch && !single &&
                            (a.pool.mode == cconv::kPoolDS || a.pool.mode == cconv::kPoolSD);
       if constexpr (kScratch) {
-        if (scratch) prefetch_history<NH>(a.pool, &M, Au, Ap, strip * kProdRows, len, c0);
+        if (scratch) prefetch_history<NH, kProdRows>(a.pool, &M, Au, Ap, strip * kProdRows, len, c0);
       }
 #pragma unroll 1
       for (int sub = 0; sub < kProdRows / 8; ++sub) {
@@ -1716,16 +1733,18 @@ static EncodeTiledFn encode_fn() {
   return fn;
 }
 
+template <bool FUSED>
 static size_t smem_bytes(int T1) {
+  using R = Roles<FUSED>;
   return 1024 + (size_t)T1 * kTapB + 2 * (size_t)kABuf + (size_t)kXStages * kXStageBytes +
-         (size_t)kEpiWarps * kOutStageBytes + kMetaStages * sizeof(Meta) + sizeof(Ctl) +
+         (size_t)R::kEpiWarps * R::kOutStageBytes + kMetaStages * sizeof(Meta) + sizeof(Ctl) +
          (size_t)kSmemRequests * 9 + 4;
 }
 
 template <int T0, int T1, bool FUSED>
 static cudaError_t launch(const CUtensorMap& map, const CUtensorMap& omap, const Args& a,
                           int grid, cudaStream_t st) {
-  const size_t smem = smem_bytes(T1);
+  const size_t smem = smem_bytes<FUSED>(T1);
   cudaError_t e = cudaFuncSetAttribute(cca_kernel<T0, T1, FUSED>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
