@@ -70,10 +70,11 @@ constexpr int kTapB = (kGS / 8) * kLboB;               // one tap of B: 32768 B
 constexpr int kAccCols = 128;                          // fp32 accumulator columns
 constexpr int kTmemCols = 2 * kAccCols;
 // Limit of a pipeline wait (~1 s at GB300 clocks). A separate test build sets
-// it to zero and CCA_WAIT_POLL_NS to a few nanoseconds (each poll returns
-// almost at once and the limit is checked after every poll), so that the
-// waits run out and the abort path runs; the drain of copies and MMAs in
-// flight keeps its own, normal limit.
+// it to zero and defines CCA_WAIT_POLL_NS: every poll is then a test that
+// never suspends the thread (a try_wait's suspend-time hint alone did not
+// return soon enough on every GPU) and the limit is checked after every poll,
+// so that any wait not satisfied at once runs out and the abort path runs;
+// the drain of copies and MMAs in flight keeps its own, normal limit.
 #ifndef CCA_WAIT_CYCLES
 #define CCA_WAIT_CYCLES 2000000000LL
 #endif
@@ -240,14 +241,14 @@ struct Ctl {
   volatile int abort;
 };
 
-// mbarrier try_wait with an explicit suspend-time limit in nanoseconds.
-__device__ __forceinline__ bool mbar_try_for(uint64_t* b, uint32_t parity, uint32_t ns) {
+// mbarrier phase test that never suspends the thread (the test build's poll).
+__device__ __forceinline__ bool mbar_test(uint64_t* b, uint32_t parity) {
   uint32_t ok;
   asm volatile(
-      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(smem_u32(b)), "r"(parity), "r"(ns)
+      : "r"(smem_u32(b)), "r"(parity)
       : "memory");
   return ok != 0;
 }
@@ -263,7 +264,7 @@ struct Waiter {
   // polling loop is out of line.
   __device__ __forceinline__ bool wait(uint64_t* bar, uint32_t parity) const {
 #ifdef CCA_WAIT_POLL_NS
-    const bool done = mbar_try_for(bar, parity, CCA_WAIT_POLL_NS);
+    const bool done = mbar_test(bar, parity);
 #else
     const bool done = mbar_try(bar, parity);
 #endif
@@ -279,7 +280,7 @@ struct Waiter {
 #endif
     for (uint32_t it = 0;; ++it) {
 #ifdef CCA_WAIT_POLL_NS
-      const bool done = mbar_try_for(bar, parity, CCA_WAIT_POLL_NS);
+      const bool done = mbar_test(bar, parity);
 #else
       const bool done = mbar_try(bar, parity);
 #endif
@@ -1169,6 +1170,26 @@ __device__ __noinline__ void aux_history(const Args& a, const int32_t* cu, const
   }
 }
 
+// Plain epilogue, a box of 32 rows x 32 channels in a warp's stage (row r's
+// 16-byte chunk c at chunk c ^ ((r >> 1) & 3)) that does not leave by a
+// tensor store: each lane stores its rows' 16-byte units of the rows that hold
+// a request's token (tile rows q*32 .. +31, call rows lo + tile row). Out of
+// line: most tiles leave by the tensor store.
+static __device__ __noinline__ void epi_store_box(const unsigned char* stage, const Meta* M, int q,
+                                                  int len, int lo, char* out, int64_t out_rs,
+                                                  int col0) {
+  const int lane = threadIdx.x & 31, seg = lane & 3;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int rr = k * 8 + (lane >> 2);    // row within the warp's 32
+    const int tr = q * 32 + rr;            // row within the tile
+    const uint4 v =
+        *reinterpret_cast<const uint4*>(stage + rr * kOutRowPitch + ((seg ^ ((rr >> 1) & 3)) << 4));
+    if (tr < len && M->rowj[tr] >= 0)
+      cconv::stg16(out + ((int64_t)(lo + tr) * out_rs + col0 + seg * 8) * 2, v);
+  }
+}
+
 // FUSED: the tail of ZayaCCA.project in the epilogue -- each conv output gets
 // its query residual 0.5*(q + k of its kv head) or key residual (the mean of
 // that over the kv group) and lands in the [query | key | value] output, whose
@@ -1463,12 +1484,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem + (static_cast<uint32_t>(q * 32) << 16) + ab * kAccCols + half * kEpiCols;
       uint32_t ra[32], rb[32];
       tmem_ld32(tbase, ra);
-#pragma unroll
-      for (int c = 0; c < kEpiCols / 32; ++c) {
-        uint32_t (&cur)[32] = (c & 1) ? rb : ra;
-        uint32_t (&nxt)[32] = (c & 1) ? ra : rb;
-        tmem_wait_ld();
-        if (c + 1 < kEpiCols / 32) tmem_ld32(tbase + (c + 1) * 32, nxt);
+      // 32 accumulator columns + bias -> bf16 -> this warp's stage
+      auto to_stage = [&](const uint32_t (&cur)[32], int c) {
 #pragma unroll
         for (int k = 0; k < 32; k += 8) {
           const float4 b0v = *reinterpret_cast<const float4*>(sbias + c * 32 + k);
@@ -1479,32 +1496,63 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int e = 0; e < 8; ++e) hh[e] = __uint_as_float(cur[k + e]) + bb[e];
           *reinterpret_cast<uint4*>(stage_at(lane, k / 8)) = cconv::pack16<__nv_bfloat16>(hh);
         }
-        if (!FUSED && M.tma_out) {
-          // the stage's layout is the tensor map's 64-byte swizzle: one store
-          // of the 32 rows x 32 channels, read out before the stage is reused
-          fence_proxy_async();
-          __syncwarp();
-          if (lane == 0) {
-            tma_store_2d(&omap, stage, g * kGS + half * kEpiCols + c * 32, lo + q * 32);
-            cconv::bulk_commit();
-            cconv::bulk_wait_read<0>();
+      };
+      if constexpr (!FUSED) {
+        // the staged box leaves by one tensor store (a whole one-request tile:
+        // the stage's layout is the tensor map's 64-byte swizzle, and it is
+        // read out before the next box is staged) or by per-lane stores of
+        // its valid rows (out of line)
+        auto put_box = [&](int c) {
+          const int col0 = g * kGS + half * kEpiCols + c * 32;
+          if (M.tma_out) {
+            fence_proxy_async();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&omap, stage, col0, lo + q * 32);
+              cconv::bulk_commit();
+              cconv::bulk_wait_read<0>();
+            }
+          } else {
+            __syncwarp();
+            epi_store_box(stage, &M, q, len, lo, a.out, a.out_rs, col0);
           }
           __syncwarp();
-          continue;
+        };
+        // pairs of boxes, the second's TMEM load in flight while the first
+        // is staged (a loop over the pairs keeps the code small)
+#pragma unroll 1
+        for (int c = 0; c < kEpiCols / 32; c += 2) {
+          tmem_wait_ld();
+          tmem_ld32(tbase + (c + 1) * 32, rb);
+          to_stage(ra, c);
+          put_box(c);
+          tmem_wait_ld();
+          if (c + 2 < kEpiCols / 32) tmem_ld32(tbase + (c + 2) * 32, ra);
+          to_stage(rb, c + 1);
+          put_box(c + 1);
         }
-        __syncwarp();
+      } else {
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int rr = k * 8 + (lane >> 2);    // row within this warp's 32
-          const int tr = q * 32 + rr;            // row within the tile
-          uint4 v = *reinterpret_cast<const uint4*>(stage_at(rr, seg));
-          if (tr < len && M.rowj[tr] >= 0) {
-            const int cc = half * kEpiCols + c * 32 + seg * 8;   // channel within the head
-            if constexpr (FUSED) v = add_residual(g < a.Hq, resid[c][k], v);
-            cconv::stg16(a.out + ((int64_t)(lo + tr) * a.out_rs + (int64_t)g * kGS + cc) * 2, v);
+        for (int c = 0; c < kEpiCols / 32; ++c) {
+          uint32_t (&cur)[32] = (c & 1) ? rb : ra;
+          uint32_t (&nxt)[32] = (c & 1) ? ra : rb;
+          tmem_wait_ld();
+          if (c + 1 < kEpiCols / 32) tmem_ld32(tbase + (c + 1) * 32, nxt);
+          to_stage(cur, c);
+          __syncwarp();
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int rr = k * 8 + (lane >> 2);    // row within this warp's 32
+            const int tr = q * 32 + rr;            // row within the tile
+            uint4 v = *reinterpret_cast<const uint4*>(stage_at(rr, seg));
+            if (tr < len && M.rowj[tr] >= 0) {
+              const int cc = half * kEpiCols + c * 32 + seg * 8;   // channel within the head
+              v = add_residual(g < a.Hq, resid[c][k], v);
+              cconv::stg16(a.out + ((int64_t)(lo + tr) * a.out_rs + (int64_t)g * kGS + cc) * 2, v);
+            }
           }
+          __syncwarp();
         }
-        __syncwarp();
       }
       tc_fence_before();
       __syncwarp();

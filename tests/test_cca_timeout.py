@@ -5,8 +5,8 @@ sets CCONV_DERR_TIMEOUT, the other roles stop at their next wait, copies and
 MMAs in flight are drained, TMEM is freed and the kernel returns. With the
 normal limit (about a second) no test can make a wait run out, so this test
 builds the CCA entry point a second time with a limit of zero cycles and polls
-that return after a few nanoseconds: any wait not satisfied at its first poll
-gives up. The drain keeps its normal limit. The test checks that such a launch returns with the error bit set and
+that never suspend the thread: any wait not satisfied at its first poll gives
+up. The drain keeps its normal limit. The test checks that such a launch returns with the error bit set and
 that the same process then runs a normal call correctly.
 """
 import ctypes
