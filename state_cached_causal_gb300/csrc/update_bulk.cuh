@@ -170,6 +170,115 @@ __device__ __forceinline__ uint32_t bulk_out(uint32_t abits) {
     return act_to_state<T>(abits);
 }
 
+// Two fp32 fused multiply-adds in one instruction (each rounded to nearest
+// even, as fmaf): d = a * b + c for both lanes.
+__device__ __forceinline__ void fma2f(float& d0, float& d1, float a0, float a1, float b0,
+                                      float b1, float c0, float c1) {
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+
+// The packed bf16 case (cap a multiple of 4, at most 16, cap = S + n_spec,
+// n_spec <= 3: so cap is the one multiple of 4 in [S, S + 3]) for the two
+// adjacent channels c0, c0 + 1 of one item: their slabs (2 x cap elements,
+// contiguous) move as cap/4 16-byte words, the tokens and outputs as bf16
+// pairs, and the taps of both channels run in one packed FMA each. The
+// arithmetic per channel is that of the one-channel path.
+template <int W, int DC, int QM>
+__device__ __forceinline__ void spec_pair_packed(uint16_t* slab, uint16_t* xs, int tile, int c0,
+                                                 int q, int off, bool hs, bool own,
+                                                 bool silu_on, const float (&wk)[2][W],
+                                                 const float (&bv)[2]) {
+  constexpr int SC = (W - 1) * DC;
+  constexpr int cap = (SC + 3) / 4 * 4;
+  static_assert(cap <= 16, "packed slabs hold at most 16 columns");
+  uint4* rv = reinterpret_cast<uint4*>(slab + (int64_t)c0 * cap);
+  uint64_t w[8] = {0ull, 0ull, 0ull, 0ull, 0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    if (hs && k < cap / 4) {
+      const uint4 r = rv[k];
+      w[2 * k] = (uint64_t)r.x | ((uint64_t)r.y << 32);
+      w[2 * k + 1] = (uint64_t)r.z | ((uint64_t)r.w << 32);
+    }
+  }
+  // channel ch's words are w[ch * cap/4 + k], k < cap/4
+  uint16_t pb[2][SC];
+  const int sh = 16 * off;
+#pragma unroll
+  for (int ch = 0; ch < 2; ++ch) {
+    uint64_t pw[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int wi = ch * (cap / 4) + k;
+      pw[k] = k < cap / 4 ? w[wi] : 0ull;
+    }
+    uint64_t sw[4];
+#pragma unroll
+    for (int k = 0; k < 3; ++k) sw[k] = sh ? (pw[k] >> sh) | (pw[k + 1] << (64 - sh)) : pw[k];
+    sw[3] = pw[3] >> sh;
+#pragma unroll
+    for (int i = 0; i < SC; ++i)
+      pb[ch][i] = static_cast<uint16_t>((sw[(i >> 2) & 3] >> (16 * (i & 3))) & 0xffffu);
+  }
+  uint32_t xb[QM];
+#pragma unroll
+  for (int u = 0; u < QM; ++u)
+    xb[u] = u < q ? *reinterpret_cast<const uint32_t*>(xs + (int64_t)u * tile + c0) : 0u;
+#pragma unroll
+  for (int i = 0; i < QM; ++i) {
+    if (i < q) {
+      float a0 = bv[0], a1 = bv[1];
+#pragma unroll
+      for (int k = 0; k < W; ++k) {
+        const int idx = SC + i - (W - 1 - k) * DC;   // position in prior ++ tokens
+        float v0, v1;
+        if (idx >= SC) {
+          const uint32_t t = xb[(idx - SC) % QM];
+          v0 = __uint_as_float(t << 16);
+          v1 = __uint_as_float(t & 0xffff0000u);
+        } else {
+          v0 = __uint_as_float((uint32_t)pb[0][idx] << 16);
+          v1 = __uint_as_float((uint32_t)pb[1][idx] << 16);
+        }
+        fma2f(a0, a1, wk[0][k], wk[1][k], v0, v1, a0, a1);
+      }
+      const float y0 = silu_on ? silu<__nv_bfloat16>(a0) : a0;
+      const float y1 = silu_on ? silu<__nv_bfloat16>(a1) : a1;
+      *reinterpret_cast<uint32_t*>(xs + (int64_t)i * tile + c0) = pack_bf16x2(y0, y1);
+    }
+  }
+  if (own) {
+    // the new buffers, prior[1, S) ++ tokens (cap = S - 1 + q columns), as
+    // cap/4 8-byte words per channel, written back as cap/4 16-byte words
+    uint64_t nw[8] = {0ull, 0ull, 0ull, 0ull, 0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+    for (int ch = 0; ch < 2; ++ch) {
+      uint64_t cw[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        uint64_t v = 0ull;
+        if (e + 1 < SC)
+          v = pb[ch][(e + 1) % SC];
+        else if (e - (SC - 1) < QM)
+          v = (xb[(e - (SC - 1)) % QM] >> (16 * ch)) & 0xffffu;
+        cw[e >> 2] |= v << (16 * (e & 3));
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        if (k < cap / 4) nw[ch * (cap / 4) + k] = cw[k];
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      if (k < cap / 4)
+        rv[k] = make_uint4((uint32_t)nw[2 * k], (uint32_t)(nw[2 * k] >> 32),
+                           (uint32_t)nw[2 * k + 1], (uint32_t)(nw[2 * k + 1] >> 32));
+  }
+}
+
 // T: activations; TS: the pool (T, or fp32 under bf16 activations). A stage
 // holds the slab in the pool's own type, so columns the call leaves alone go
 // back with their bits. QM bounds the tokens per request (q <= QM): the
@@ -203,6 +312,9 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
   constexpr bool kPackable = sizeof(T) == 2 && sizeof(TS) == 2 && DC > 0 && SC <= 16;
   const bool packed = kPackable && (cap & 3) == 0 && cap <= 16 && cap == S + a.n_spec &&
                       a.n_spec <= 3;
+  // the plain kernel's packed case takes two adjacent channels per thread
+  constexpr bool kPairs = kPackable && !FUSED && (SC + 3) / 4 * 4 <= 16;
+  const bool pairs = kPairs && packed;
 
   if (tid == 0) {
     for (int k = 0; k < NS; ++k) {
@@ -339,7 +451,7 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
         cur_ct = m.ct;
 #pragma unroll
         for (int kc = 0; kc < 2; ++kc) {
-          const int c = min(tid + kc * kComputeThreads, nch - 1);
+          const int c = min(pairs ? 2 * tid + kc : tid + kc * kComputeThreads, nch - 1);
 #pragma unroll
           for (int k = 0; k < W; ++k) wk[kc][k] = load_f32<T>(a.w, (int64_t)(cb + c) * W + k);
           bv[kc] = a.bias ? load_f32<T>(a.bias, cb + c) : 0.0f;
@@ -352,6 +464,17 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
       const R* os = reinterpret_cast<const R*>(sb + b.os_off);
       const bool has_outer = a.outer != nullptr;
       const bool hs = m.flags & kHist, own = m.flags & kOwn;
+      if constexpr (kPairs) {
+        if (pairs) {
+          if (2 * tid < nch)
+            spec_pair_packed<W, (DC > 0 ? DC : 1), QM>(
+                reinterpret_cast<uint16_t*>(slab), reinterpret_cast<uint16_t*>(xs), tile, 2 * tid,
+                q, m.off, hs, own, silu_on, wk, bv);
+          fence_proxy_async();   // the bulk stores read what this thread wrote
+          mbar_arrive(&ctl->done[st]);
+          continue;
+        }
+      }
 #pragma unroll
       for (int kc = 0; kc < 2; ++kc) {
         const int c = tid + kc * kComputeThreads;
