@@ -186,11 +186,14 @@ __device__ __forceinline__ void fma2f(float& d0, float& d1, float a0, float a1, 
 // adjacent channels c0, c0 + 1 of one item: their slabs (2 x cap elements,
 // contiguous) move as cap/4 16-byte words, the tokens and outputs as bf16
 // pairs, and the taps of both channels run in one packed FMA each. The
-// arithmetic per channel is that of the one-channel path.
-template <int W, int DC, int QM>
-__device__ __forceinline__ void spec_pair_packed(uint16_t* slab, uint16_t* xs, int tile, int c0,
-                                                 int q, int off, bool hs, bool own,
-                                                 bool silu_on, const float (&wk)[2][W],
+// arithmetic per channel is that of the one-channel path. FUSED: each output
+// becomes residual + act(conv) (+ outer), the residual and outer rows read as
+// pairs from the stage (rs, os).
+template <int W, int DC, int QM, bool FUSED>
+__device__ __forceinline__ void spec_pair_packed(uint16_t* slab, uint16_t* xs, const uint16_t* rs,
+                                                 const uint16_t* os, int tile, int c0, int q,
+                                                 int off, bool hs, bool own, bool silu_on,
+                                                 bool has_outer, const float (&wk)[2][W],
                                                  const float (&bv)[2]) {
   constexpr int SC = (W - 1) * DC;
   constexpr int cap = (SC + 3) / 4 * 4;
@@ -246,8 +249,18 @@ __device__ __forceinline__ void spec_pair_packed(uint16_t* slab, uint16_t* xs, i
         }
         fma2f(a0, a1, wk[0][k], wk[1][k], v0, v1, a0, a1);
       }
-      const float y0 = silu_on ? silu<__nv_bfloat16>(a0) : a0;
-      const float y1 = silu_on ? silu<__nv_bfloat16>(a1) : a1;
+      float y0 = silu_on ? silu<__nv_bfloat16>(a0) : a0;
+      float y1 = silu_on ? silu<__nv_bfloat16>(a1) : a1;
+      if constexpr (FUSED) {
+        const uint32_t r = *reinterpret_cast<const uint32_t*>(rs + (int64_t)i * tile + c0);
+        y0 = __uint_as_float(r << 16) + y0;
+        y1 = __uint_as_float(r & 0xffff0000u) + y1;
+        if (has_outer) {
+          const uint32_t o = *reinterpret_cast<const uint32_t*>(os + (int64_t)i * tile + c0);
+          y0 = y0 + __uint_as_float(o << 16);
+          y1 = y1 + __uint_as_float(o & 0xffff0000u);
+        }
+      }
       *reinterpret_cast<uint32_t*>(xs + (int64_t)i * tile + c0) = pack_bf16x2(y0, y1);
     }
   }
@@ -312,8 +325,8 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
   constexpr bool kPackable = sizeof(T) == 2 && sizeof(TS) == 2 && DC > 0 && SC <= 16;
   const bool packed = kPackable && (cap & 3) == 0 && cap <= 16 && cap == S + a.n_spec &&
                       a.n_spec <= 3;
-  // the plain kernel's packed case takes two adjacent channels per thread
-  constexpr bool kPairs = kPackable && !FUSED && (SC + 3) / 4 * 4 <= 16;
+  // the packed case takes two adjacent channels per thread
+  constexpr bool kPairs = kPackable && (SC + 3) / 4 * 4 <= 16;
   const bool pairs = kPairs && packed;
 
   if (tid == 0) {
@@ -467,9 +480,10 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
       if constexpr (kPairs) {
         if (pairs) {
           if (2 * tid < nch)
-            spec_pair_packed<W, (DC > 0 ? DC : 1), QM>(
-                reinterpret_cast<uint16_t*>(slab), reinterpret_cast<uint16_t*>(xs), tile, 2 * tid,
-                q, m.off, hs, own, silu_on, wk, bv);
+            spec_pair_packed<W, (DC > 0 ? DC : 1), QM, FUSED>(
+                reinterpret_cast<uint16_t*>(slab), reinterpret_cast<uint16_t*>(xs),
+                reinterpret_cast<const uint16_t*>(rs), reinterpret_cast<const uint16_t*>(os), tile,
+                2 * tid, q, m.off, hs, own, silu_on, has_outer, wk, bv);
           fence_proxy_async();   // the bulk stores read what this thread wrote
           mbar_arrive(&ctl->done[st]);
           continue;
