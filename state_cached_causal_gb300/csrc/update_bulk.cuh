@@ -58,7 +58,7 @@ enum : int32_t { kSkip = 1, kHist = 2, kOwn = 4, kLoadState = 8, kEnd = 16 };
 // epoch % kEpochs per launch, cleared by the launch's last CTA: at most
 // kEpochs launches of one kernel build may be in flight at once.
 constexpr int kStaticPercent = 70;
-constexpr int kDynChunk = 2;
+constexpr int kDynChunk = 1;
 constexpr int kEpochs = 64;
 __device__ unsigned int g_bulk_next[kEpochs];
 __device__ unsigned int g_bulk_done[kEpochs];
@@ -692,9 +692,9 @@ cudaError_t launch_bulk_wide(int W, const UpdArgs& a, const BulkArgs& b, size_t 
 template <typename T, typename TS, bool FUSED>
 cudaError_t launch_wd(int W, int D, const UpdArgs& a, const BulkArgs& b, size_t smem,
                       cudaStream_t st, int dev, int num_sms) {
-  // fused bf16 calls of at most 4 tokens per request take the QM = 4 kernels
-  // (measured faster there; the plain path keeps one instantiation per shape)
-  constexpr int kQ4 = (FUSED && sizeof(T) == 2) ? 4 : kMaxSpec + 1;
+  // bf16 calls of at most 4 tokens per request take the QM = 4 kernels (their
+  // per-channel token loops are not half predicated away)
+  constexpr int kQ4 = (sizeof(T) == 2) ? 4 : kMaxSpec + 1;
   const bool q4 = kQ4 == 4 && 1 + a.n_spec <= 4;
   if (W > 4 || D > 4) return launch_bulk_wide<T, TS, FUSED>(W, a, b, smem, st, dev, num_sms);
 #define CCONV_BULK_CASE(w_, d_)                                                         \
