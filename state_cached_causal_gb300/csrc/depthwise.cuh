@@ -16,6 +16,7 @@
 #pragma once
 
 #include <algorithm>
+#include <atomic>
 #include <type_traits>
 
 #include "common.cuh"
@@ -27,7 +28,7 @@ constexpr int kChunkShiftMin = 6;   // tokens per varlen block: 64 (>= (width-1)
 constexpr int kChunkShiftMax = 7;   // ... or 128 when the call has blocks for many waves
 constexpr int kWaveBlocks = 32;     // (this many 128-token blocks per SM)
 constexpr int kPrefetch = 12;   // token rows in flight per thread (cp.async ring)
-constexpr int kRing = 16;       // ring slots per thread (> kPrefetch + 1, power of 2)
+constexpr int kRing = 14;       // ring slots per thread (>= kPrefetch + 2)
 constexpr int kPrefetchFused = 6;   // the same for the fused entry point, whose
 constexpr int kRingFused = 8;       // output-row entries are three units
 constexpr int kUpdChan = 2;     // channels per thread of the update kernel
@@ -259,7 +260,7 @@ __global__ void __launch_bounds__(128, (W <= 4 ? 4 : 2)) fwd_varlen_kernel(const
         if (r0 + pr >= r1) pr = D;   // later classes are empty too
       }
     }
-    const uint32_t dst = ring0 + (issued & (RING - 1)) * slot_bytes;
+    const uint32_t dst = ring0 + issued * slot_bytes;
     const int64_t p = ok ? prow(r) : 0;
     cp_async16(dst, ok ? xs + p * xstep : xs, ok);
     if constexpr (FUSED) {
@@ -269,7 +270,7 @@ __global__ void __launch_bounds__(128, (W <= 4 ? 4 : 2)) fwd_varlen_kernel(const
       cp_async16(dst + 2 * unit_bytes, oo ? a.outer + off + p * a.outer_rs * E : a.out, oo);
     }
     cp_async_commit();
-    ++issued;
+    issued = issued + 1 == RING ? 0 : issued + 1;   // ring slot of the next entry
   };
 #pragma unroll
   for (int i = 0; i < PF; ++i) issue();
@@ -296,8 +297,8 @@ __global__ void __launch_bounds__(128, (W <= 4 ? 4 : 2)) fwd_varlen_kernel(const
     for (int k = 0; k < W - 1; ++k) {
       const int p = r0 + rho - (W - 1 - k) * D;   // p >= -S; p < 0 only in chunk 0
       cp_async_wait<PF - 1>();
-      const uint4 r = (p >= 0) ? ring[(used & (RING - 1)) * (nt * NU)] : blk[(S + p) * nt];
-      ++used;
+      const uint4 r = (p >= 0) ? ring[used * (nt * NU)] : blk[(S + p) * nt];
+      used = used + 1 == RING ? 0 : used + 1;
       issue();
       unpack16<T>(r, win[k]);
     }
@@ -305,14 +306,14 @@ __global__ void __launch_bounds__(128, (W <= 4 ? 4 : 2)) fwd_varlen_kernel(const
     for (int r = r0 + rho; r < r1; r += D) {
       cp_async_wait<PF - 1>();
       float cur[V], y[V];
-      const uint4* e = ring + (used & (RING - 1)) * (nt * NU);
+      const uint4* e = ring + used * (nt * NU);
       unpack16<T>(e[0], cur);
       float rres[V], rout[V];
       if constexpr (FUSED) {
         unpack16<T>(e[nt], rres);
         unpack16<T>(e[2 * nt], rout);   // zeros without an outer residual
       }
-      ++used;
+      used = used + 1 == RING ? 0 : used + 1;
       issue();
 #pragma unroll
       for (int v = 0; v < V; ++v) {
@@ -761,9 +762,9 @@ static int check_pool(const cconv_pool_t& pv) {
 // Threads per block: up to 128 channel units, fewer when the per-thread
 // shared-memory columns (cols * 16 bytes) would pass the 48 KB a block gets
 // without opting in (less 1 KB for the kernels' static shared memory).
-static int pick_threads(int units, int cols) {
+static int pick_threads(int units, int cols, int budget = 47 * 1024) {
   int nt = std::min(128, ((units + 31) / 32) * 32);
-  const int by_smem = (47 * 1024) / std::max(1, cols * 16);
+  const int by_smem = budget / std::max(1, cols * 16);
   nt = std::min(nt, (by_smem / 32) * 32);
   return std::max(nt, 32);
 }
@@ -793,6 +794,27 @@ static int check_common(const void* x, int64_t x_rs, const void* w, const cconv_
 // (depthwise_wide.cu).
 cudaError_t launch_fwd_wide(int dtype, bool fused, int W, dim3 grid, int nt, size_t smem,
                             cudaStream_t st, const FwdArgs& a);
+
+// Shared memory a varlen block may take: four 128-thread blocks of a 12-column
+// pool view (12 + kRing columns of 16 bytes per thread, 53 KB) fit one SM.
+// Above 47 KB (the default 48 KB less the kernel's static shared memory) a
+// kernel opts in once per device.
+constexpr int kFwdSmemBudget = 56 * 1024;
+struct SmemOptIn {
+  std::atomic<unsigned long long> done{0};
+  cudaError_t ensure(const void* kernel, size_t smem) {
+    if (smem <= 47 * 1024) return cudaSuccess;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const unsigned long long bit = dev < 64 ? 1ull << dev : 0ull;
+    if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kFwdSmemBudget);
+    if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_release);
+    return e;
+  }
+};
 cudaError_t launch_upd_wide(int dtype, bool fused, int W, dim3 grid, int nt, size_t smem,
                             cudaStream_t st, const UpdArgs& a);
 
@@ -804,6 +826,10 @@ static cudaError_t launch_fwd(int W, int D, dim3 grid, int nt, size_t smem,
                            nt, smem, st, a);
 #define CCONV_FWD_CASE(w_, d_)                                              \
   if (W == w_ && D == d_) {                                                 \
+    static SmemOptIn opt;                                                   \
+    const cudaError_t eo =                                                  \
+        opt.ensure((const void*)fwd_varlen_kernel<T, w_, d_, FUSED>, smem); \
+    if (eo != cudaSuccess) return eo;                                       \
     fwd_varlen_kernel<T, w_, d_, FUSED><<<grid, nt, smem, st>>>(a);         \
     return cudaGetLastError();                                              \
   }
@@ -910,7 +936,8 @@ static int fwd_entry(const void* x, int64_t x_row_stride, const void* w, const v
   const int units = C / V;
   // (the fused kernel also keeps its row table, at most 128 + 2*12 ints, in
   // shared memory: 1 KB is left for it)
-  const int nt = pick_threads(units, conv_states.cap + ring_cols + (FUSED ? 4 : 0));
+  const int nt = pick_threads(units, conv_states.cap + ring_cols + (FUSED ? 4 : 0),
+                             FUSED ? 47 * 1024 : kFwdSmemBudget);
   const int ctiles = (units + nt - 1) / nt;
   // 128-token chunks halve the per-block window and setup work; 64 keeps
   // enough blocks in flight for smaller calls.

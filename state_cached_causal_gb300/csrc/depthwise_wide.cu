@@ -11,9 +11,14 @@ static cudaError_t fwd_wide_t(int W, dim3 grid, int nt, size_t smem, cudaStream_
                               const FwdArgs& a) {
   switch (W) {
 #define CCONV_FWD_WIDE(w_)                                                  \
-  case w_:                                                                  \
+  case w_: {                                                                \
+    static SmemOptIn opt;                                                   \
+    const cudaError_t eo =                                                  \
+        opt.ensure((const void*)fwd_varlen_kernel<T, w_, 0, FUSED>, smem);  \
+    if (eo != cudaSuccess) return eo;                                       \
     fwd_varlen_kernel<T, w_, 0, FUSED><<<grid, nt, smem, st>>>(a);          \
-    return cudaGetLastError();
+    return cudaGetLastError();                                              \
+  }
     CCONV_FWD_WIDE(2) CCONV_FWD_WIDE(3) CCONV_FWD_WIDE(4) CCONV_FWD_WIDE(5)
     CCONV_FWD_WIDE(6) CCONV_FWD_WIDE(7) CCONV_FWD_WIDE(8)
 #undef CCONV_FWD_WIDE
