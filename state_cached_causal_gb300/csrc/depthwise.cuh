@@ -70,22 +70,35 @@ struct FwdArgs {
 // increasing and K(s) + nchunks(s) <= K(s+1), so a grid of
 // floor(T/chunk) + B + 1 blocks covers every chunk (spare ids exit).
 // chunk = 1 << sh.
-// One warp finds max{s : K(s) <= b} with a 32-way search.
-static __device__ int find_chunk_seq(const int32_t* __restrict__ cu, int B, int b, int sh) {
+// One warp finds max{s : K(s) <= b} with a 32-way search (the answer stays in
+// [lo, hi)); its last round tests single indices and also reads cu[idx + 1],
+// so cu[s] and cu[s + 1] come back with s (two rounds of loads for B <= 1024).
+static __device__ int find_chunk_seq(const int32_t* __restrict__ cu, int B, int b, int sh,
+                                     int& cu_s, int& cu_s1) {
   const int lane = threadIdx.x & 31;
   if (B <= 0) return -1;
   int lo = 0, hi = B;
-  while (hi - lo > 1) {
+  for (;;) {
     const int step = (hi - lo + 31) / 32;
     const int idx = lo + lane * step;
+    int v0 = 0, v1 = 0;
     bool ok = false;
-    if (idx < hi) ok = (max(__ldg(cu + idx), 0) >> sh) + idx <= b;
+    if (idx < hi) {
+      v0 = __ldg(cu + idx);
+      if (step == 1) v1 = __ldg(cu + idx + 1);   // idx + 1 <= B
+      ok = (max(v0, 0) >> sh) + idx <= b;
+    }
     const unsigned m = __ballot_sync(0xffffffffu, ok);
     if (m == 0u) return -1;   // only when K(lo) > b, i.e. b before the first chunk
-    lo = lo + (31 - __clz(m)) * step;
+    const int l = 31 - __clz(m);
+    if (step == 1) {
+      cu_s = __shfl_sync(0xffffffffu, v0, l);
+      cu_s1 = __shfl_sync(0xffffffffu, v1, l);
+      return lo + l;
+    }
+    lo = lo + l * step;
     hi = min(lo + step, hi);
   }
-  return (max(__ldg(cu + lo), 0) >> sh) + lo <= b ? lo : -1;
 }
 
 // DC is the dilation, or 0 for the instantiations that read it at run time
@@ -109,7 +122,7 @@ __global__ void __launch_bounds__(128, (W <= 4 ? 4 : 2)) fwd_varlen_kernel(const
   constexpr int RING = FUSED ? kRingFused : kRing;
   constexpr int NU = FUSED ? 3 : 1;              // 16-byte units per stream entry
   extern __shared__ uint4 dyn_smem[];
-  __shared__ int sh_seq;
+  __shared__ int sh_seq, sh_start, sh_end;
   const int nt = blockDim.x, tid = threadIdx.x;
   // Chunk id b and channel tile ct. With a.order_lpt the channel tiles are
   // the fast grid dimension and chunk ids run backwards, so the blocks of the
@@ -118,22 +131,27 @@ __global__ void __launch_bounds__(128, (W <= 4 ? 4 : 2)) fwd_varlen_kernel(const
   const int b = a.order_lpt ? a.nblk - 1 - (int)blockIdx.y : (int)blockIdx.x;
   const int ct = a.order_lpt ? (int)blockIdx.x : (int)blockIdx.y;
 
+  // Sequence b's index data is checked once, by block (b, 0), beside the
+  // search (by the second warp when there is one).
+  const int checker = nt > 32 ? 32 : 0;
   if (tid < 32) {
-    const int s = find_chunk_seq(a.cu, a.B, b, a.chunk_shift);
+    int cs = 0, ce = 0;
+    const int s = find_chunk_seq(a.cu, a.B, b, a.chunk_shift, cs, ce);
     if (tid == 0) {
       sh_seq = s;
-      // Each sequence's index data is checked once, by block (s, 0).
-      if (ct == 0 && b < a.B) {
-        const int c0v = a.cu[b], c1v = a.cu[b + 1];
-        if (c0v < 0 || c1v < c0v || c1v > a.T) flag_error(a.dev_err, CCONV_DERR_CU_SEQLENS);
-        if (a.state_idx[b] >= a.pool.num_slots) flag_error(a.dev_err, CCONV_DERR_SLOT_RANGE);
-      }
+      sh_start = cs;
+      sh_end = ce;
     }
+  }
+  if (tid == checker && ct == 0 && b < a.B) {
+    const int c0v = a.cu[b], c1v = a.cu[b + 1];
+    if (c0v < 0 || c1v < c0v || c1v > a.T) flag_error(a.dev_err, CCONV_DERR_CU_SEQLENS);
+    if (a.state_idx[b] >= a.pool.num_slots) flag_error(a.dev_err, CCONV_DERR_SLOT_RANGE);
   }
   __syncthreads();
   const int s = sh_seq;
   if (s < 0) return;
-  const int start = a.cu[s], end = a.cu[s + 1];
+  const int start = sh_start, end = sh_end;
   if (start < 0 || end < start || end > a.T) return;
   const int L = end - start;
   const int sh = a.chunk_shift;
@@ -168,9 +186,6 @@ __global__ void __launch_bounds__(128, (W <= 4 ? 4 : 2)) fwd_varlen_kernel(const
   }
   const int c0 = (ct * nt + tid) * V;
   if (c0 >= a.C) return;
-  const int slot = a.state_idx[s];
-  if (slot >= a.pool.num_slots) return;
-  const bool hs = slot >= 0 && (a.has_init == nullptr || a.has_init[s] != 0);
 
   const int64_t xstep = a.x_rs * E, ostep = a.out_rs * E;
   // x row r of the sequence (r in [r0 - S, r1) or [L - S, L), r >= 0)
@@ -198,6 +213,8 @@ __global__ void __launch_bounds__(128, (W <= 4 ? 4 : 2)) fwd_varlen_kernel(const
   if constexpr (!FUSED) {
     if (L == 1) {
       const uint4 xr = ldg16(xs);
+      const int slot = a.state_idx[s];
+      const bool hi = a.has_init == nullptr || a.has_init[s] != 0;
       float wk[W][V], bv[V];
 #pragma unroll
       for (int v = 0; v < V; ++v) {
@@ -205,6 +222,8 @@ __global__ void __launch_bounds__(128, (W <= 4 ? 4 : 2)) fwd_varlen_kernel(const
         for (int k = 0; k < W; ++k) wk[k][v] = load_f32<T>(a.w, (int64_t)(c0 + v) * W + k);
         bv[v] = a.bias ? load_f32<T>(a.bias, c0 + v) : 0.0f;
       }
+      if (slot >= a.pool.num_slots) return;
+      const bool hs = slot >= 0 && hi;
       if (slot >= 0) pool_load<T>(a.pool, slot, c0, S, blk, nt);
       if (!hs)
         for (int col = 0; col < S; ++col) blk[col * nt] = make_uint4(0u, 0u, 0u, 0u);
@@ -282,6 +301,13 @@ __global__ void __launch_bounds__(128, (W <= 4 ? 4 : 2)) fwd_varlen_kernel(const
     for (int k = 0; k < W; ++k) wk[k][v] = load_f32<T>(a.w, (int64_t)(c0 + v) * W + k);
     bv[v] = a.bias ? load_f32<T>(a.bias, c0 + v) : 0.0f;
   }
+  // the slot is read after the first rows are requested
+  const int slot = a.state_idx[s];
+  if (slot >= a.pool.num_slots) {
+    cp_async_wait<0>();
+    return;
+  }
+  const bool hs = slot >= 0 && (a.has_init == nullptr || a.has_init[s] != 0);
   if (j == 0) {
     if (slot >= 0) pool_load<T>(a.pool, slot, c0, S, blk, nt);
     if (!hs)
