@@ -119,6 +119,25 @@ __device__ __forceinline__ float tanh_approx(float v) {
   return t;
 }
 
+// Two fp32 lanes in one instruction of the packed FP32 pipe; each lane rounds
+// exactly as the scalar fmaf / multiply does.
+__device__ __forceinline__ void fma_x2(float& d0, float& d1, float a0, float a1, float b0,
+                                       float b1, float c0, float c1) {
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+__device__ __forceinline__ void mul_x2(float& d0, float& d1, float a0, float a1, float b0,
+                                       float b1) {
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
 // SiLU v * sigmoid(v). fp32 storage keeps the accurate exp and division.
 // bf16 storage (8 mantissa bits) uses sigmoid(v) = (1 + tanh(v/2)) / 2 with
 // the hardware tanh (relative error about 2^-11, well under a bf16 ulp):
@@ -130,6 +149,18 @@ __device__ __forceinline__ float silu(float v) {
   } else {
     const float h = 0.5f * v;
     return fmaf(h, tanh_approx(h), h);
+  }
+}
+// silu<T> of two values (the same arithmetic, the bf16 form on the packed pipe)
+template <typename T>
+__device__ __forceinline__ void silu_x2(float& a, float& b) {
+  if constexpr (sizeof(T) == 4) {
+    a = silu<T>(a);
+    b = silu<T>(b);
+  } else {
+    float h0, h1;
+    mul_x2(h0, h1, 0.5f, 0.5f, a, b);
+    fma_x2(a, b, h0, h1, tanh_approx(h0), tanh_approx(h1), h0, h1);
   }
 }
 

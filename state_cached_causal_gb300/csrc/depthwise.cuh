@@ -328,36 +328,49 @@ __global__ void __launch_bounds__(128, (W <= 4 ? 4 : 2)) fwd_varlen_kernel(const
       issue();
       unpack16<T>(r, win[k]);
     }
-#pragma unroll 2
-    for (int r = r0 + rho; r < r1; r += D) {
-      cp_async_wait<PF - 1>();
-      float cur[V], y[V];
-      const uint4* e = ring + used * (nt * NU);
-      unpack16<T>(e[0], cur);
-      float rres[V], rout[V];
-      if constexpr (FUSED) {
-        unpack16<T>(e[nt], rres);
-        unpack16<T>(e[2 * nt], rout);   // zeros without an outer residual
+    // Rows r, r+D, ... in groups of W-1: at step i of a group win[(i+k) % (W-1)]
+    // holds row r - (W-1-k)*D and row r then replaces win[i], the oldest, so
+    // the window never moves between registers. Channel pairs go through the
+    // packed FP32 pipe (the same roundings as one channel at a time).
+#pragma unroll 1
+    for (int rg = r0 + rho; rg < r1; rg += (W - 1) * D) {
+#pragma unroll
+      for (int i = 0; i < W - 1; ++i) {
+        const int r = rg + i * D;
+        if (r < r1) {
+          cp_async_wait<PF - 1>();
+          float cur[V], y[V];
+          const uint4* e = ring + used * (nt * NU);
+          unpack16<T>(e[0], cur);
+          float rres[V], rout[V];
+          if constexpr (FUSED) {
+            unpack16<T>(e[nt], rres);
+            unpack16<T>(e[2 * nt], rout);   // zeros without an outer residual
+          }
+          used = used + 1 == RING ? 0 : used + 1;
+          issue();
+#pragma unroll
+          for (int v = 0; v < V; v += 2) {
+            float a0 = bv[v], a1 = bv[v + 1];
+#pragma unroll
+            for (int k = 0; k < W - 1; ++k) {
+              const int sl = (i + k) % (W - 1);
+              fma_x2(a0, a1, wk[k][v], wk[k][v + 1], win[sl][v], win[sl][v + 1], a0, a1);
+            }
+            fma_x2(a0, a1, wk[W - 1][v], wk[W - 1][v + 1], cur[v], cur[v + 1], a0, a1);
+            if (silu_on) silu_x2<T>(a0, a1);
+            y[v] = a0;
+            y[v + 1] = a1;
+            if constexpr (FUSED) {
+              y[v] = (rres[v] + y[v]) + rout[v];
+              y[v + 1] = (rres[v + 1] + y[v + 1]) + rout[v + 1];
+            }
+          }
+          stg16(os + prow(r) * ostep, pack16<T>(y));
+#pragma unroll
+          for (int v = 0; v < V; ++v) win[i][v] = cur[v];
+        }
       }
-      used = used + 1 == RING ? 0 : used + 1;
-      issue();
-#pragma unroll
-      for (int v = 0; v < V; ++v) {
-        float acc = bv[v];
-#pragma unroll
-        for (int k = 0; k < W - 1; ++k) acc = fmaf(wk[k][v], win[k][v], acc);
-        acc = fmaf(wk[W - 1][v], cur[v], acc);
-        y[v] = silu_on ? silu<T>(acc) : acc;
-        if constexpr (FUSED) y[v] = (rres[v] + y[v]) + rout[v];
-      }
-      stg16(os + prow(r) * ostep, pack16<T>(y));
-#pragma unroll
-      for (int k = 0; k < W - 2; ++k) {
-#pragma unroll
-        for (int v = 0; v < V; ++v) win[k][v] = win[k + 1][v];
-      }
-#pragma unroll
-      for (int v = 0; v < V; ++v) win[W - 2][v] = cur[v];
     }
   }
   cp_async_wait<0>();   // no copy may land after the thread exits
