@@ -29,6 +29,10 @@ constexpr int kChunkShiftMax = 7;   // ... or 128 when the call has blocks for m
 constexpr int kWaveBlocks = 32;     // (this many 128-token blocks per SM)
 constexpr int kPrefetch = 12;   // token rows in flight per thread (cp.async ring)
 constexpr int kRing = 14;       // ring slots per thread (>= kPrefetch + 2)
+// Undilated kernels keep fewer rows in flight: their blocks are the shortest
+// per chunk, and the batch measured faster with 10 than with 12.
+constexpr int kPrefetchD1 = 10;
+constexpr int kRingD1 = 12;
 constexpr int kPrefetchFused = 6;   // the same for the fused entry point, whose
 constexpr int kRingFused = 8;       // output-row entries are three units
 constexpr int kUpdChan = 2;     // channels per thread of the update kernel
@@ -118,8 +122,8 @@ __global__ void __launch_bounds__(128, (W <= 4 ? 4 : 2)) fwd_varlen_kernel(const
   const int D = DC > 0 ? DC : a.dil;
   const int S = (W - 1) * D;
   constexpr int V = Elem<T>::V, E = Elem<T>::bytes;
-  constexpr int PF = FUSED ? kPrefetchFused : kPrefetch;
-  constexpr int RING = FUSED ? kRingFused : kRing;
+  constexpr int PF = FUSED ? kPrefetchFused : (DC == 1 ? kPrefetchD1 : kPrefetch);
+  constexpr int RING = FUSED ? kRingFused : (DC == 1 ? kRingD1 : kRing);
   constexpr int NU = FUSED ? 3 : 1;              // 16-byte units per stream entry
   extern __shared__ uint4 dyn_smem[];
   __shared__ int sh_seq, sh_start, sh_end;
@@ -971,7 +975,8 @@ static int fwd_entry(const void* x, int64_t x_row_stride, const void* w, const v
   a.tidx = FUSED ? epi->token_indices : nullptr;
   a.num_rows = FUSED ? epi->num_rows : 0;
   a.dev_err = dev_err;
-  const int ring_cols = FUSED ? 3 * kRingFused : kRing;
+  // (the ring of the kernel launch_fwd picks: undilated widths <= 4 take kRingD1)
+  const int ring_cols = FUSED ? 3 * kRingFused : (dilation == 1 && width <= 4 ? kRingD1 : kRing);
   const int units = C / V;
   // (the fused kernel also keeps its row table, at most 128 + 2*12 ints, in
   // shared memory: 1 KB is left for it)
