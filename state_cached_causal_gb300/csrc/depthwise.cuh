@@ -76,20 +76,27 @@ struct FwdArgs {
 // chunk = 1 << sh.
 // One warp finds max{s : K(s) <= b} with a 32-way search (the answer stays in
 // [lo, hi)); its last round tests single indices and also reads cu[idx + 1],
-// so cu[s] and cu[s + 1] come back with s (two rounds of loads for B <= 1024).
-static __device__ int find_chunk_seq(const int32_t* __restrict__ cu, int B, int b, int sh,
-                                     int& cu_s, int& cu_s1) {
+// state_idx[idx] and has_init[idx], so cu[s], cu[s + 1], the slot and the
+// has_init flag come back with s (two rounds of loads for B <= 1024).
+static __device__ int find_chunk_seq(const int32_t* __restrict__ cu,
+                                     const int32_t* __restrict__ state_idx,
+                                     const uint8_t* __restrict__ has_init, int B, int b, int sh,
+                                     int& cu_s, int& cu_s1, int& slot_s, int& hi_s) {
   const int lane = threadIdx.x & 31;
   if (B <= 0) return -1;
   int lo = 0, hi = B;
   for (;;) {
     const int step = (hi - lo + 31) / 32;
     const int idx = lo + lane * step;
-    int v0 = 0, v1 = 0;
+    int v0 = 0, v1 = 0, sl = 0, hv = 1;
     bool ok = false;
     if (idx < hi) {
       v0 = __ldg(cu + idx);
-      if (step == 1) v1 = __ldg(cu + idx + 1);   // idx + 1 <= B
+      if (step == 1) {
+        v1 = __ldg(cu + idx + 1);   // idx + 1 <= B
+        sl = __ldg(state_idx + idx);
+        if (has_init) hv = __ldg(has_init + idx);
+      }
       ok = (max(v0, 0) >> sh) + idx <= b;
     }
     const unsigned m = __ballot_sync(0xffffffffu, ok);
@@ -98,6 +105,8 @@ static __device__ int find_chunk_seq(const int32_t* __restrict__ cu, int B, int 
     if (step == 1) {
       cu_s = __shfl_sync(0xffffffffu, v0, l);
       cu_s1 = __shfl_sync(0xffffffffu, v1, l);
+      slot_s = __shfl_sync(0xffffffffu, sl, l);
+      hi_s = __shfl_sync(0xffffffffu, hv, l);
       return lo + l;
     }
     lo = lo + l * step;
@@ -126,7 +135,7 @@ __global__ void __launch_bounds__(128, (W <= 4 ? 4 : 2)) fwd_varlen_kernel(const
   constexpr int RING = FUSED ? kRingFused : (DC == 1 ? kRingD1 : kRing);
   constexpr int NU = FUSED ? 3 : 1;              // 16-byte units per stream entry
   extern __shared__ uint4 dyn_smem[];
-  __shared__ int sh_seq, sh_start, sh_end;
+  __shared__ int sh_seq, sh_start, sh_end, sh_slot, sh_hi;
   const int nt = blockDim.x, tid = threadIdx.x;
   // Chunk id b and channel tile ct. With a.order_lpt the channel tiles are
   // the fast grid dimension and chunk ids run backwards, so the blocks of the
@@ -139,12 +148,15 @@ __global__ void __launch_bounds__(128, (W <= 4 ? 4 : 2)) fwd_varlen_kernel(const
   // search (by the second warp when there is one).
   const int checker = nt > 32 ? 32 : 0;
   if (tid < 32) {
-    int cs = 0, ce = 0;
-    const int s = find_chunk_seq(a.cu, a.B, b, a.chunk_shift, cs, ce);
+    int cs = 0, ce = 0, sl = 0, hv = 1;
+    const int s = find_chunk_seq(a.cu, a.state_idx, a.has_init, a.B, b, a.chunk_shift, cs, ce,
+                                 sl, hv);
     if (tid == 0) {
       sh_seq = s;
       sh_start = cs;
       sh_end = ce;
+      sh_slot = sl;
+      sh_hi = hv;
     }
   }
   if (tid == checker && ct == 0 && b < a.B) {
@@ -217,8 +229,8 @@ __global__ void __launch_bounds__(128, (W <= 4 ? 4 : 2)) fwd_varlen_kernel(const
   if constexpr (!FUSED) {
     if (L == 1) {
       const uint4 xr = ldg16(xs);
-      const int slot = a.state_idx[s];
-      const bool hi = a.has_init == nullptr || a.has_init[s] != 0;
+      const int slot = sh_slot;
+      const bool hi = sh_hi != 0;
       float wk[W][V], bv[V];
 #pragma unroll
       for (int v = 0; v < V; ++v) {
@@ -305,13 +317,12 @@ __global__ void __launch_bounds__(128, (W <= 4 ? 4 : 2)) fwd_varlen_kernel(const
     for (int k = 0; k < W; ++k) wk[k][v] = load_f32<T>(a.w, (int64_t)(c0 + v) * W + k);
     bv[v] = a.bias ? load_f32<T>(a.bias, c0 + v) : 0.0f;
   }
-  // the slot is read after the first rows are requested
-  const int slot = a.state_idx[s];
+  const int slot = sh_slot;
   if (slot >= a.pool.num_slots) {
     cp_async_wait<0>();
     return;
   }
-  const bool hs = slot >= 0 && (a.has_init == nullptr || a.has_init[s] != 0);
+  const bool hs = slot >= 0 && sh_hi != 0;
   if (j == 0) {
     if (slot >= 0) pool_load<T>(a.pool, slot, c0, S, blk, nt);
     if (!hs)
