@@ -113,7 +113,10 @@ __device__ Meta item_meta(const UpdArgs& a, int64_t item, int S) {
   m.ct = (int32_t)(item / a.B);
   m.off = 0;
   m.flags = 0;
+  // the request's index data, requested together (one round trip)
   const int slot = a.state_idx[m.s];
+  const int na = a.n_spec > 0 ? a.num_accepted[m.s] : 1;
+  const bool hi = a.has_init == nullptr || a.has_init[m.s] != 0;
   m.slot = slot;
   if (slot >= a.pool.num_slots) {
     flag_error(a.dev_err, CCONV_DERR_SLOT_RANGE);
@@ -121,7 +124,7 @@ __device__ Meta item_meta(const UpdArgs& a, int64_t item, int S) {
     return m;
   }
   if (a.n_spec > 0) {
-    m.off = a.num_accepted[m.s] - 1;
+    m.off = na - 1;
     if (m.off < 0 || m.off > a.n_spec) {
       flag_error(a.dev_err, CCONV_DERR_NUM_ACCEPTED);
       m.flags = kSkip;
@@ -141,7 +144,7 @@ __device__ Meta item_meta(const UpdArgs& a, int64_t item, int S) {
       m.prow[r] = p;
     }
   }
-  const bool hs = slot >= 0 && (a.has_init == nullptr || a.has_init[m.s] != 0);
+  const bool hs = slot >= 0 && hi;
   if (hs) m.flags |= kHist;
   if (slot >= 0) {
     m.flags |= kOwn;
@@ -424,8 +427,20 @@ __global__ void __launch_bounds__(kThreads, kMinCtasPerSm)
       }
       bulk_commit();
       if (more) {
+        // the next item's draw and index loads overlap the stores' reads of the stage
+        const int64_t it = grab();
+        Meta nm;
+        if (it >= 0) nm = item_meta<FUSED>(a, it, S);
         bulk_wait_read<0>();   // the stage's stores have read it
-        fill(issued++);
+        if (it < 0) {
+          more = false;
+          const int sn = issued % NS;
+          ctl->meta[sn].flags = kEnd;
+          mbar_arrive(&ctl->full[sn]);
+        } else {
+          issue_load(issued, nm);
+        }
+        ++issued;
       }
     }
     if (aborted) {
