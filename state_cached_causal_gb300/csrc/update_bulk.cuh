@@ -132,16 +132,20 @@ __device__ Meta item_meta(const UpdArgs& a, int64_t item, int S) {
     }
   }
   if (FUSED) {
+    // every row index requested before any is checked
     const int q = 1 + a.n_spec;
-    for (int r = 0; r < q; ++r) {
+#pragma unroll
+    for (int r = 0; r < kMaxSpec + 1; ++r) {
       const int64_t li = (int64_t)m.s * q + r;
-      const int p = a.tidx ? a.tidx[li] : (int)li;
+      if (r < q) m.prow[r] = a.tidx ? a.tidx[li] : (int)li;
+    }
+    for (int r = 0; r < q; ++r) {
+      const int p = m.prow[r];
       if (p < 0 || p >= a.num_rows) {
         flag_error(a.dev_err, CCONV_DERR_ROW_INDEX);
         m.flags = kSkip;
         return m;
       }
-      m.prow[r] = p;
     }
   }
   const bool hs = slot >= 0 && hi;
