@@ -11,8 +11,8 @@
 // the time axis; a warp moves 512 contiguous bytes per row. A dilated conv
 // with dilation d is walked as d interleaved undilated chains (rows
 // r, r+d, r+2d, ...), so the register window holds only width-1 rows
-// whatever the dilation. Eight rows are loaded before any is used to keep
-// enough bytes in flight per SM.
+// whatever the dilation. Ten to twelve rows per thread are in flight ahead of
+// use (kPrefetchD1, kPrefetch) to keep enough bytes in flight per SM.
 #pragma once
 
 #include <algorithm>
@@ -282,7 +282,7 @@ __global__ void __launch_bounds__(128, (W <= 4 ? 4 : 2)) fwd_varlen_kernel(const
   uint4* ring = dyn_smem + a.pool.cap * nt + tid;    // RING stream slots of NU units
   const uint32_t ring0 = smem_addr(ring);
   const uint32_t unit_bytes = nt * 16, slot_bytes = NU * unit_bytes;
-  int pr = r0 < r1 ? 0 : D, pm = -(W - 1), issued = 0;
+  int pr = r0 < r1 ? 0 : D, pm = -(W - 1), islot = 0;
   auto issue = [&]() {
     const int r = r0 + pr + pm * D;
     const bool ok = pr < D && r >= 0;
@@ -295,7 +295,7 @@ __global__ void __launch_bounds__(128, (W <= 4 ? 4 : 2)) fwd_varlen_kernel(const
         if (r0 + pr >= r1) pr = D;   // later classes are empty too
       }
     }
-    const uint32_t dst = ring0 + issued * slot_bytes;
+    const uint32_t dst = ring0 + islot * slot_bytes;
     const int64_t p = ok ? prow(r) : 0;
     cp_async16(dst, ok ? xs + p * xstep : xs, ok);
     if constexpr (FUSED) {
@@ -305,7 +305,7 @@ __global__ void __launch_bounds__(128, (W <= 4 ? 4 : 2)) fwd_varlen_kernel(const
       cp_async16(dst + 2 * unit_bytes, oo ? a.outer + off + p * a.outer_rs * E : a.out, oo);
     }
     cp_async_commit();
-    issued = issued + 1 == RING ? 0 : issued + 1;   // ring slot of the next entry
+    islot = islot + 1 == RING ? 0 : islot + 1;   // ring slot of the next entry issued
   };
 #pragma unroll
   for (int i = 0; i < PF; ++i) issue();
@@ -330,7 +330,7 @@ __global__ void __launch_bounds__(128, (W <= 4 ? 4 : 2)) fwd_varlen_kernel(const
   }
   const bool silu_on = a.act == CCONV_ACT_SILU;
 
-  int used = 0;
+  int uslot = 0;   // ring slot of the next entry used
 #pragma unroll 1
   for (int rho = 0; rho < D && r0 + rho < r1; ++rho) {
     float win[W - 1][V];
@@ -338,8 +338,8 @@ __global__ void __launch_bounds__(128, (W <= 4 ? 4 : 2)) fwd_varlen_kernel(const
     for (int k = 0; k < W - 1; ++k) {
       const int p = r0 + rho - (W - 1 - k) * D;   // p >= -S; p < 0 only in chunk 0
       cp_async_wait<PF - 1>();
-      const uint4 r = (p >= 0) ? ring[used * (nt * NU)] : blk[(S + p) * nt];
-      used = used + 1 == RING ? 0 : used + 1;
+      const uint4 r = (p >= 0) ? ring[uslot * (nt * NU)] : blk[(S + p) * nt];
+      uslot = uslot + 1 == RING ? 0 : uslot + 1;
       issue();
       unpack16<T>(r, win[k]);
     }
@@ -355,14 +355,14 @@ __global__ void __launch_bounds__(128, (W <= 4 ? 4 : 2)) fwd_varlen_kernel(const
         if (r < r1) {
           cp_async_wait<PF - 1>();
           float cur[V], y[V];
-          const uint4* e = ring + used * (nt * NU);
+          const uint4* e = ring + uslot * (nt * NU);
           unpack16<T>(e[0], cur);
           float rres[V], rout[V];
           if constexpr (FUSED) {
             unpack16<T>(e[nt], rres);
             unpack16<T>(e[2 * nt], rout);   // zeros without an outer residual
           }
-          used = used + 1 == RING ? 0 : used + 1;
+          uslot = uslot + 1 == RING ? 0 : uslot + 1;
           issue();
 #pragma unroll
           for (int v = 0; v < V; v += 2) {
