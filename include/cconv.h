@@ -55,7 +55,11 @@
  * Streams.  Every call only enqueues work on `stream` and returns; it never
  *           synchronises with the host (as the Zaya page's state path is
  *           written to avoid). Each call writes only its outputs and the pool slots
- *           named by state_idx.
+ *           named by state_idx. The first call that launches a given kernel on
+ *           a device also raises that kernel's dynamic shared-memory limit
+ *           (cudaFuncSetAttribute) and may query its occupancy; both are host
+ *           calls outside any stream, so make one call of each shape before
+ *           capturing a CUDA graph in a capture mode that forbids them.
  * Status.   CCONV_OK (0); CCONV_ERR_INVALID (-1: a null required pointer, a
  *           size or stride out of range, a misaligned pointer); CCONV_ERR_
  *           UNSUPPORTED (-2: a legal combination this build has no kernel
